@@ -1,0 +1,128 @@
+/*
+ * oracle/scan_ref.c -- plain, sequential CPU reference for device-wide prefix
+ * sums and order-preserving stream compaction.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the
+ * benchmark's CPU-baseline / reference leg may load this code.  It shares no
+ * code, header, table or helper with the CUDA library, and the CUDA library
+ * never calls it.
+ *
+ * Every function is the textbook definition written out as one sequential
+ * loop, with no blocking, reordering or fusion:
+ *
+ *   inclusive  y_i = sum_{j <= i} x_j      exclusive  y_i = sum_{j < i} x_j
+ *
+ * ("Prefix sum and other parallel patterns", Definitions and self-test
+ * answer 1; "CUDA prefix sum, the Hillis-Steele scan", Two scans, and which
+ * one hands you the total.)  The running-sum loop is the CPU reference the
+ * pages themselves use ("Prefix sum and other parallel patterns", scan.cu
+ * main: acc loop).
+ *
+ * Readings where the pages are silent:
+ *   - int32 sums wrap in two's complement.  The exact integer sum is carried
+ *     in 64 bits (modulo 2^64, which contains the wanted modulo 2^32) and
+ *     only the low 32 bits are stored.
+ *   - fp32 inputs are summed in float64 and returned in float64; the fp32
+ *     GPU result is compared to that with a normalised error bound.
+ *   - compaction keeps element i when flags[i] != 0, in index order; the
+ *     number kept is the count ("Prefix sum and other parallel patterns",
+ *     Stream compaction and Exercise 1: out[pos[i]] = in[i] where pos is the
+ *     exclusive scan of the flags, total = pos[n-1] + flags[n-1]).
+ *
+ * Parity pins: every function here is checked in tests/ against the pages'
+ * worked examples (tests/golden/), closed forms, invariants and brute force;
+ * see the test files for which pin covers which function.
+ */
+#include <stddef.h>
+#include <stdint.h>
+
+/* int32 scan with two's-complement wraparound. */
+void oracle_scan_i32(const int32_t *x, int32_t *y, size_t n, int inclusive)
+{
+    uint64_t acc = 0; /* exact sum modulo 2^64 */
+    for (size_t i = 0; i < n; ++i) {
+        uint64_t xi = (uint64_t)(int64_t)x[i];
+        if (inclusive) {
+            acc += xi;
+            y[i] = (int32_t)(uint32_t)acc;
+        } else {
+            y[i] = (int32_t)(uint32_t)acc;
+            acc += xi;
+        }
+    }
+}
+
+/* uint32 scan modulo 2^32. */
+void oracle_scan_u32(const uint32_t *x, uint32_t *y, size_t n, int inclusive)
+{
+    uint64_t acc = 0;
+    for (size_t i = 0; i < n; ++i) {
+        if (inclusive) {
+            acc += x[i];
+            y[i] = (uint32_t)acc;
+        } else {
+            y[i] = (uint32_t)acc;
+            acc += x[i];
+        }
+    }
+}
+
+/* fp32 inputs, float64 running sum and float64 outputs. */
+void oracle_scan_f32(const float *x, double *y, size_t n, int inclusive)
+{
+    double acc = 0.0;
+    for (size_t i = 0; i < n; ++i) {
+        if (inclusive) {
+            acc += (double)x[i];
+            y[i] = acc;
+        } else {
+            y[i] = acc;
+            acc += (double)x[i];
+        }
+    }
+}
+
+/* Error normaliser for fp32 parity: a_i = sum_{j <= i} |x_j| in float64. */
+void oracle_abs_prefix_f32(const float *x, double *y, size_t n)
+{
+    double acc = 0.0;
+    for (size_t i = 0; i < n; ++i) {
+        double v = (double)x[i];
+        acc += v < 0.0 ? -v : v;
+        y[i] = acc;
+    }
+}
+
+/*
+ * Order-preserving compaction: copy keys[i] for every i with flags[i] != 0,
+ * in index order.  Returns the number kept.  `out` must hold n elements.
+ */
+uint64_t oracle_compact_u32(const uint32_t *keys, const uint8_t *flags,
+                            uint32_t *out, size_t n)
+{
+    uint64_t count = 0;
+    for (size_t i = 0; i < n; ++i) {
+        if (flags[i] != 0) {
+            out[count] = keys[i];
+            count += 1;
+        }
+    }
+    return count;
+}
+
+/*
+ * Predicate form of the same compaction: keep keys[i] when keys[i] > 0
+ * (the predicate of "Prefix sum and other parallel patterns", compact.cu and
+ * Exercise 1), order preserved.  Returns the number kept.
+ */
+uint64_t oracle_compact_positive_f32(const float *x, float *out, size_t n)
+{
+    uint64_t count = 0;
+    for (size_t i = 0; i < n; ++i) {
+        if (x[i] > 0.0f) {
+            out[count] = x[i];
+            count += 1;
+        }
+    }
+    return count;
+}

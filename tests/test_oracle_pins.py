@@ -1,0 +1,277 @@
+"""Pins for the CPU oracle: it is checked against what the pages and plain
+mathematics fix, never against itself or the GPU.
+
+Which pin covers which oracle function:
+
+* scan_i32 / scan_u32 / scan_f32 (inclusive and exclusive):
+  worked examples (tests/golden/scan_worked_examples.txt), closed forms
+  (iota, constants, the (i % 8) + 1 and period-4 patterns), invariants
+  (inclusive - exclusive = x, last inclusive = total, exclusive[0] = 0),
+  O(n^2) brute force with Python big integers / exact fractions, and
+  wraparound through an independent uint32 running sum.
+* abs_prefix_f32: brute force with exact fractions.
+* compact_u32 / compact_positive_f32: brute-force list filter, the count
+  identity pos[n-1] + flags[n-1], subsequence check, all-zero / all-one flags.
+* the tile model: the pages' printed tables (tests/golden/).
+"""
+
+from __future__ import annotations
+
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import seeded_inputs as si
+
+M32 = 1 << 32
+
+
+def _parse_ints(field: str):
+    field = field.strip()
+    return [int(t) for t in field.split()] if field else None
+
+
+def _worked_examples(golden_dir):
+    rows = []
+    with open(os.path.join(golden_dir, "scan_worked_examples.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            name, x, inc, exc, src = [p.strip() for p in line.split("|")]
+            rows.append((name, _parse_ints(x), _parse_ints(inc), _parse_ints(exc), src))
+    return rows
+
+
+def test_worked_examples_int(golden_dir):
+    rows = _worked_examples(golden_dir)
+    assert len(rows) == 4
+    for name, x, inc, exc, _src in rows:
+        xa = np.array(x, dtype=np.int32)
+        if inc is not None:
+            assert oracle.scan_i32(xa, True).tolist() == inc, name
+            assert oracle.scan_u32(xa.astype(np.uint32), True).tolist() == inc, name
+        if exc is not None:
+            assert oracle.scan_i32(xa, False).tolist() == exc, name
+            assert oracle.scan_u32(xa.astype(np.uint32), False).tolist() == exc, name
+
+
+def test_worked_examples_f32(golden_dir):
+    for name, x, inc, exc, _src in _worked_examples(golden_dir):
+        xa = np.array(x, dtype=np.float32)
+        if inc is not None:
+            assert oracle.scan_f32(xa, True).tolist() == [float(v) for v in inc], name
+        if exc is not None:
+            assert oracle.scan_f32(xa, False).tolist() == [float(v) for v in exc], name
+
+
+@pytest.mark.parametrize("n", [1, 2, 7, 64, 4096, 100_003])
+def test_closed_form_all_ones_is_iota(n):
+    ones = np.ones(n, dtype=np.int32)
+    assert np.array_equal(oracle.scan_i32(ones, False), np.arange(n, dtype=np.int32))
+    assert np.array_equal(oracle.scan_i32(ones, True), np.arange(1, n + 1, dtype=np.int32))
+    f = np.ones(n, dtype=np.float32)
+    assert np.array_equal(oracle.scan_f32(f, True), np.arange(1, n + 1, dtype=np.float64))
+
+
+@pytest.mark.parametrize("c", [-7, 3, 1000])
+def test_closed_form_constant(c):
+    n = 5000
+    x = np.full(n, c, dtype=np.int32)
+    i = np.arange(n, dtype=np.int64)
+    assert np.array_equal(oracle.scan_i32(x, False).astype(np.int64), c * i)
+    assert np.array_equal(oracle.scan_i32(x, True).astype(np.int64), c * (i + 1))
+
+
+def test_closed_form_i_mod_8(golden_dir):
+    n = 1_049_187  # the page's element count, a partial tile at every block size
+    x = si.structured_i_mod_8(n)
+    i1 = np.arange(1, n + 1, dtype=np.int64)
+    r = i1 % 8
+    expect = 36 * (i1 // 8) + r * (r + 1) // 2
+    assert np.array_equal(oracle.scan_f32(x, True), expect.astype(np.float64))
+    # the page's tile bound: a 1024-element tile never exceeds 4608
+    assert oracle.scan_f32(x[:1024], True)[-1] == 4608.0
+
+
+def test_closed_form_period4_total():
+    n = 10_000_000
+    x = si.structured_period4(n)
+    inc = oracle.scan_f32(x, True)
+    i1 = np.arange(1, n + 1, dtype=np.int64)
+    assert np.array_equal(inc, (i1 + i1 // 4).astype(np.float64))
+    assert inc[-1] == 12_500_000.0  # total printed on the page
+    assert np.array_equal(oracle.scan_f32(x, False)[1:], inc[:-1])
+
+
+def test_structured_fixture_values(golden_dir):
+    with open(os.path.join(golden_dir, "structured_inputs.txt")) as f:
+        rows = [l.split("|") for l in f if l.strip() and not l.startswith("#")]
+    vals = {r[0].strip(): (int(r[1]), float(r[2])) for r in rows}
+    n, total = vals["period4_total"]
+    assert oracle.scan_f32(si.structured_period4(n), True)[-1] == total
+    n, peak = vals["i_mod_8_tile1024_max_prefix"]
+    assert oracle.scan_f32(si.structured_i_mod_8(n), True).max() == peak
+
+
+def _brute_force_mod32(x, inclusive):
+    out = []
+    for i in range(len(x)):
+        s = sum(int(v) for v in (x[: i + 1] if inclusive else x[:i]))
+        out.append(s % M32)
+    return out
+
+
+@pytest.mark.parametrize("n", [0, 1, 2, 3, 5, 31, 32, 33, 63, 64])
+@pytest.mark.parametrize("inclusive", [True, False])
+def test_brute_force_int_full_range(n, inclusive):
+    rng = np.random.default_rng(1000 + n)
+    x = rng.integers(-(1 << 31), 1 << 31, size=n, dtype=np.int64).astype(np.int32)
+    got_i = oracle.scan_i32(x, inclusive).astype(np.int64) % M32
+    assert got_i.tolist() == _brute_force_mod32(x, inclusive)
+    xu = rng.integers(0, 1 << 32, size=n, dtype=np.uint64).astype(np.uint32)
+    got_u = oracle.scan_u32(xu, inclusive).astype(np.int64)
+    assert got_u.tolist() == _brute_force_mod32(xu, inclusive)
+
+
+@pytest.mark.parametrize("n", [1, 2, 17, 64])
+@pytest.mark.parametrize("inclusive", [True, False])
+def test_brute_force_f32_exact_fractions(n, inclusive):
+    # Inputs of the workload's form k * 2**-24 (and signed): every partial sum
+    # of <= 64 of them is exact in float64, so the oracle must equal the exact
+    # rational prefix sum.
+    x = si.uniform_f32(n, seed=77)
+    x = np.where(np.arange(n) % 3 == 1, -x, x).astype(np.float32)
+    got = oracle.scan_f32(x, inclusive)
+    for i in range(n):
+        part = x[: i + 1] if inclusive else x[:i]
+        exact = sum((Fraction(float(v)) for v in part), Fraction(0))
+        assert Fraction(float(got[i])) == exact
+    a = oracle.abs_prefix_f32(x)
+    for i in range(n):
+        assert Fraction(float(a[i])) == sum((abs(Fraction(float(v))) for v in x[: i + 1]), Fraction(0))
+
+
+def test_wraparound_two_routes():
+    # Route 1: the oracle (64-bit exact sum, low 32 bits kept).
+    # Route 2: a uint32 running sum that wraps at every step, in numpy.
+    x = si.workload_int_pm1000(1 << 20, seed=2)
+    big = np.full(1 << 16, 2_000_000_000, dtype=np.int32)  # forces many wraps
+    for arr in (x, big, np.concatenate([big, x])):
+        acc = np.uint32(0)
+        route2 = np.empty(arr.size, dtype=np.uint32)
+        u = arr.view(np.uint32)
+        with np.errstate(over="ignore"):
+            for s in range(0, arr.size, 1 << 16):
+                blk = np.cumsum(u[s:s + (1 << 16)], dtype=np.uint32) + acc
+                route2[s:s + blk.size] = blk
+                acc = blk[-1]
+        assert np.array_equal(oracle.scan_i32(arr, True).view(np.uint32), route2)
+
+
+def test_invariants_random():
+    for seed, n in [(2, 1 << 16), (3, 100_003)]:
+        x = si.workload_int_pm1000(n, seed=seed)
+        inc = oracle.scan_i32(x, True)
+        exc = oracle.scan_i32(x, False)
+        assert exc[0] == 0
+        with np.errstate(over="ignore"):
+            assert np.array_equal((inc.view(np.uint32) - exc.view(np.uint32)), x.view(np.uint32))
+        assert int(inc[-1]) == int(np.sum(x.astype(np.int64)))  # no wrap at this size
+        assert np.array_equal(exc[1:], inc[:-1])
+    # Nonnegative counts give a monotone exclusive scan.
+    c = si.workload_poisson_counts(1 << 16, seed=4)
+    e = oracle.scan_u32(c, False)
+    assert np.all(np.diff(e.astype(np.int64)) >= 0)
+
+
+def test_fp32_integer_valued_is_exact():
+    # Integer-valued fp32 inputs with every prefix below 2**24 have a unique
+    # exact answer whatever the add order.
+    x = si.uniform_int32(200_000, 0, 9, seed=11).astype(np.float32)
+    inc = oracle.scan_f32(x, True)
+    assert inc[-1] < 2 ** 24
+    assert np.array_equal(inc, np.cumsum(x.astype(np.int64)).astype(np.float64))
+
+
+def _brute_compact(keys, flags):
+    return [int(k) for k, f in zip(keys, flags) if int(f) != 0]
+
+
+@pytest.mark.parametrize("n", [0, 1, 5, 64, 1000])
+def test_compact_brute_force(n):
+    keys = si.uniform_u32(n, seed=5)
+    flags = si.bernoulli_flags(n, 0.5, seed=6)
+    flags = np.where(np.arange(n) % 7 == 3, 200, flags).astype(np.uint8)  # any nonzero keeps
+    got = oracle.compact_u32(keys, flags)
+    assert got.tolist() == _brute_compact(keys, flags)
+
+
+def test_compact_count_identity_and_subsequence():
+    n = 1 << 16
+    for p in (0.01, 0.5, 0.99):
+        keys, flags = si.workload_compaction(n, p, seed=3)
+        got = oracle.compact_u32(keys, flags)
+        f01 = (flags != 0).astype(np.uint32)
+        pos = oracle.scan_u32(f01, False)
+        assert got.size == int(pos[-1]) + int(f01[-1])
+        # out[pos[i]] = keys[i] for kept i  (the scatter reading of the page)
+        kept = np.nonzero(f01)[0]
+        assert np.array_equal(got[pos[kept]], keys[kept])
+        # subsequence: the kept keys appear in index order
+        assert np.array_equal(got, keys[kept])
+
+
+def test_compact_degenerate():
+    n = 4099
+    keys = si.uniform_u32(n, seed=9)
+    assert oracle.compact_u32(keys, np.zeros(n, np.uint8)).size == 0
+    assert np.array_equal(oracle.compact_u32(keys, np.ones(n, np.uint8)), keys)
+
+
+def test_compact_positive_predicate():
+    x = np.array([0.5, -1.0, 0.0, 2.0, -0.0, 3.5, float("nan")], dtype=np.float32)
+    assert oracle.compact_positive_f32(x).tolist() == [0.5, 2.0, 3.5]
+
+
+def test_tile_model_against_page_tables(golden_dir):
+    levels, totals = [], {}
+    with open(os.path.join(golden_dir, "blelloch_tile_model.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            parts = line.split()
+            if parts[0] == "total":
+                totals[parts[1]] = int(parts[2])
+            else:
+                levels.append([int(p) for p in parts])
+    assert len(levels) == 12
+    tile = 4096
+    for stride, lanes, warps, plain, pad1, pad2 in levels:
+        assert tile // (2 * stride) == lanes
+        assert oracle.blelloch_level_warps(tile, stride) == warps
+        assert oracle.blelloch_level_degree(tile, stride, oracle.LAYOUT_PLAIN) == plain
+        assert oracle.blelloch_level_degree(tile, stride, oracle.LAYOUT_PAD32) == pad1
+        assert oracle.blelloch_level_degree(tile, stride, oracle.LAYOUT_PAD32_1024) == pad2
+    assert oracle.hillis_steele_adds(tile) == totals["hillis_steele_adds"]
+    assert oracle.hillis_steele_requests(tile) == totals["hillis_steele_requests"]
+    assert oracle.blelloch_adds(tile) == totals["blelloch_adds"]
+    assert oracle.blelloch_requests(tile, oracle.LAYOUT_PLAIN) == totals["blelloch_plain_requests"]
+    assert oracle.blelloch_requests(tile, oracle.LAYOUT_PAD32) == totals["blelloch_pad32_requests"]
+    assert oracle.blelloch_requests(tile, oracle.LAYOUT_PAD32_1024) == totals["blelloch_pad32_1024_requests"]
+
+
+def test_work_closed_forms(golden_dir):
+    with open(os.path.join(golden_dir, "hillis_steele_work.txt")) as f:
+        rows = [[int(v) for v in l.split()] for l in f if l.strip() and not l.startswith("#")]
+    for threads, steps, adds, seq in rows:
+        assert int(math.log2(threads)) == steps
+        assert oracle.hillis_steele_adds(threads) == adds
+        assert threads - 1 == seq
+    for k in range(1, 13):
+        n = 1 << k
+        assert oracle.hillis_steele_adds(n) == n * k - (n - 1)  # n log2 n - (n - 1)
+        assert oracle.blelloch_adds(n) == 2 * (n - 1)
