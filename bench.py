@@ -1,0 +1,462 @@
+"""Benchmark: device-wide scan throughput at n = 1e8 on one GB300.
+
+One step = four single-pass scans of 1e8 elements each: int32 exclusive and
+inclusive (uniform integers in [-1000, 1000], seed 2) and fp32 exclusive and
+inclusive (uniform [0, 1), seed 1), inputs resident in HBM.  `value` is
+elements scanned per second (G-elem/s) over all ranks; the roofline line
+converts the scan kernel's average launch time to GB/s on its algorithmic
+bytes, 2 * n * 4 bytes per launch (read once, write once).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the sequential CPU oracle on the same metric (a
+bounded sample of the same inputs per step).  Under torchrun each rank runs
+its own replica on its own GPU (independent problems, no collective on the
+data path); rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np
+
+METRIC = "scan G-elem/s & HBM GB/s vs 2n·sizeof(T) roofline, int32/fp32 at n=1e8"
+UNIT = "G-elem/s"
+N = 100_000_000
+BYTES_PER_ELEM = 8  # one 4-byte read + one 4-byte write
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+VARIANTS = [("i32", False), ("i32", True), ("f32", False), ("f32", True)]
+DATA = ("synthetic: seeded SplitMix64 counter streams; int32 uniform in [-1000, 1000] "
+        "(seed 2) and fp32 uniform in [0, 1) (seed 1)")
+WORKLOAD = ("device-wide scan, n=1e8 per launch; one step = int32 exclusive + inclusive "
+            "and fp32 exclusive + inclusive (4 launches)")
+KERNEL_SOURCES = ["stream_compaction_pass_gb300/csrc/scan.cu", "stream_compaction_pass_gb300/csrc/tile.cuh",
+                  "stream_compaction_pass_gb300/csrc/lookback.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "k_scan_lookback_n1e8.md")
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def max_over_ranks(elapsed_ms: float, device=None) -> float:
+    """Largest elapsed time over all ranks (every rank gets it)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(elapsed_ms)
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(elems_per_rank: int, world: int, max_elapsed_ms: float) -> float:
+    """Elements all ranks processed, per second, in G-elem/s."""
+    return elems_per_rank * world / (max_elapsed_ms * 1e-3) / 1e9
+
+
+def emit(obj) -> None:
+    print(json.dumps(obj), flush=True)
+
+
+# --------------------------------------------------------------------------
+# measurement helpers
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured (MEASURED_PEAKS.json hbm_gbs, burst copy)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 copy measurement)"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    try:
+        text = open(TRAFFIC_FILE).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    h = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+    if not m or not h or h.group(1) != kernel_source_hash():
+        return None
+    return int(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.proc = None
+        if gpu_id is None:
+            return
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            self.fh = os.fdopen(fd, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", gpu_id, "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        self.raw = open(self.path).read()
+        os.unlink(self.path)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.raw.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_uuid(torch, dev) -> str | None:
+    try:
+        u = torch.cuda.get_device_properties(dev).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        return None
+
+
+# --------------------------------------------------------------------------
+# CPU side: the oracle as a baseline / reference arm
+
+def oracle_step(orc, xs, xf, m: int) -> None:
+    orc.scan_i32(xs[:m], False)
+    orc.scan_i32(xs[:m], True)
+    orc.scan_f32(xf[:m], False)
+    orc.scan_f32(xf[:m], True)
+
+
+def cpu_baseline(xs, xf, budget_s: float = 10.0):
+    import oracle as orc
+    orc.load()
+    m = N
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle_step(orc, xs, xf, m)
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": 4 * m * reps / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{reps} full steps (4 sequential scans of the same 1e8-element inputs) "
+                      f"in {dt:.1f} s on one host core"}
+
+
+def run_reference(args) -> None:
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import seeded_inputs as si
+    import oracle as orc
+    orc.load()
+    budget_elems = 2.0e10  # ~20-40 s of oracle work over the whole run
+    m = int(min(N, max(100_000, budget_elems / (4 * (args.steps + args.warmup)))))
+    xs = si.workload_int_pm1000(m, seed=2)
+    xf = si.workload_f32_unit(m, seed=1)
+    for _ in range(args.warmup):
+        oracle_step(orc, xs, xf, m)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(orc, xs, xf, m)
+    dt = time.perf_counter() - t0
+    value = 4 * m * args.steps / dt / 1e9
+    sample = f"first {m} elements of the 1e8-element inputs per scan, 4 scans per step"
+    emit({"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": world,
+          "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32/fp32",
+          "data": DATA, "config": {"workload": WORKLOAD, "n": N, "sample_elems_per_scan": m},
+          "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+          "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}})
+
+
+# --------------------------------------------------------------------------
+# GPU side
+
+def time_region(torch, stream, fn, reps: int, warmup: int = 3) -> float:
+    """Mean ms per call of fn() on `stream`, CUDA events, after warm-up."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        fn()
+    b.record(stream)
+    b.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def row_rates(torch, ss, stream, dev, xs_d, xf_d, out_d):
+    """Secondary rows: every other hot-path row at its own workload, each
+    timed with CUDA events (mean of 20 after 3 warm-ups)."""
+    import seeded_inputs as si
+    rows = {}
+    peak, _ = measured_hbm_peak()
+
+    def gbs(bytes_, ms):
+        return bytes_ / (ms * 1e-3) / 1e9
+
+    # copy probe with the scan's loader: the practical roofline of this access pattern
+    ms = time_region(torch, stream, lambda: ss.ss_copy_u32(xs_d, out_d, N, stream=stream.cuda_stream), 20)
+    rows["copy_probe_u32_1e8"] = {"ms": ms, "GB/s": gbs(8 * N, ms), "frac": gbs(8 * N, ms) / peak}
+    # ablations at the same int32 workload
+    for name, algo, traffic in (("reduce_then_scan", ss.SS_ALGO_REDUCE_THEN_SCAN, 12),
+                                ("rts_blelloch_plain", ss.SS_ALGO_RTS_BLELLOCH, 12),
+                                ("rts_blelloch_pad32", ss.SS_ALGO_RTS_BLELLOCH_PAD32, 12),
+                                ("rts_blelloch_pad2", ss.SS_ALGO_RTS_BLELLOCH_PAD2, 12)):
+        ms = time_region(torch, stream, lambda a=algo: ss.ss_scan(ss.SS_I32, False, a, xs_d, out_d,
+                                                                  stream=stream.cuda_stream), 20)
+        rows[f"{name}_i32_1e8"] = {"ms": ms, "G-elem/s": N / ms / 1e6,
+                                   "GB/s_on_2n": gbs(8 * N, ms), "frac_on_2n": gbs(8 * N, ms) / peak,
+                                   "GB/s_moved": gbs(traffic * N, ms)}
+    # uint32 Poisson(8) counts, n = 2^27, in place and out of place
+    nc = 1 << 27
+    cnt = torch.from_numpy(si.workload_poisson_counts(nc, seed=4).view(np.int32)).to(dev)
+    cnt_out = torch.empty_like(cnt)
+    ms = time_region(torch, stream, lambda: ss.scan_exclusive_u32(cnt, cnt_out, stream=stream.cuda_stream), 20)
+    rows["u32_poisson_2p27_out_of_place"] = {"ms": ms, "GB/s": gbs(8 * nc, ms), "frac": gbs(8 * nc, ms) / peak}
+    ms = time_region(torch, stream, lambda: ss.scan_exclusive_u32(cnt_out, cnt_out, stream=stream.cuda_stream), 20)
+    rows["u32_poisson_2p27_in_place"] = {"ms": ms, "GB/s": gbs(8 * nc, ms), "frac": gbs(8 * nc, ms) / peak}
+    del cnt, cnt_out
+    # compaction, n = 2^28, p in {0.01, 0.5, 0.99}
+    nk = 1 << 28
+    keys = torch.from_numpy(si.uniform_u32(nk, 6).view(np.int32)).to(dev)
+    kout = torch.empty_like(keys)
+    dcount = torch.zeros(1, dtype=torch.int64, device=dev)
+    for p in (0.01, 0.5, 0.99):
+        flags_np = si.bernoulli_flags(nk, p, 7)
+        flags = torch.from_numpy(flags_np).to(dev)
+        kept = int(flags_np.sum(dtype=np.int64))
+        ms = time_region(torch, stream, lambda: ss.compact_u32(keys, flags, kout, dcount, stream=stream.cuda_stream), 20)
+        alg = nk * 5 + 4 * kept + 8
+        # key bytes a reader that skips 32-byte sectors without a kept key must fetch
+        sectors = int(np.count_nonzero(flags_np.reshape(-1, 8).any(axis=1)))
+        minimal = nk + 32 * sectors + 4 * kept + 8
+        rows[f"compact_2p28_p{p}"] = {"ms": ms, "G-elem/s": nk / ms / 1e6, "kept": kept,
+                                      "GB/s_on_5n+4k": gbs(alg, ms), "frac_on_5n+4k": gbs(alg, ms) / peak,
+                                      "GB/s_on_sector_minimum": gbs(minimal, ms),
+                                      "frac_on_sector_minimum": gbs(minimal, ms) / peak}
+        del flags
+    del keys, kout
+    # context only: torch.cumsum on the same int32 input, timed the same way
+    ms = time_region(torch, stream, lambda: torch.cumsum(xs_d, 0, out=out_d), 20)
+    rows["context_torch_cumsum_i32_1e8"] = {"ms": ms, "G-elem/s": N / ms / 1e6}
+    return rows
+
+
+def run_ours(args) -> None:
+    import torch
+    import seeded_inputs as si
+    import stream_compaction_pass_gb300 as ss
+
+    rank, world, local = dist_env()
+    assert torch.cuda.is_available(), "bench.py needs a CUDA device"
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    ss.lib()  # fail loudly if the library is missing
+    ss.ss_set_scan_config(args.config)
+
+    xs = si.workload_int_pm1000(N, seed=2)
+    xf = si.workload_f32_unit(N, seed=1)
+    stream = torch.cuda.Stream(device=dev)
+    sh = stream.cuda_stream
+    with torch.cuda.stream(stream):
+        xs_d = torch.from_numpy(xs).to(dev)
+        xf_d = torch.from_numpy(xf).to(dev)
+        out_i = torch.empty_like(xs_d)
+        out_f = torch.empty_like(xf_d)
+    torch.cuda.synchronize()
+
+    launches = [
+        lambda: ss.scan_exclusive_i32(xs_d, out_i, N, stream=sh),
+        lambda: ss.scan_inclusive_i32(xs_d, out_i, N, stream=sh),
+        lambda: ss.scan_exclusive_f32(xf_d, out_f, N, stream=sh),
+        lambda: ss.scan_inclusive_f32(xf_d, out_f, N, stream=sh),
+    ]
+
+    def step():
+        for f in launches:
+            f()
+
+    # correctness before timing: one step checked against the oracle (rank 0)
+    if rank == 0 and not args.skip_check:
+        import oracle as orc
+        launches[0]()
+        torch.cuda.synchronize()
+        assert np.array_equal(out_i.cpu().numpy(), orc.scan_i32(xs, False)), "int32 scan mismatch"
+        launches[3]()
+        torch.cuda.synchronize()
+        err = orc.fp32_normalised_error(out_f.cpu().numpy(), orc.scan_f32(xf, True), xf)
+        assert err <= 1e-4, f"fp32 scan error {err}"
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    st, _ = ss.ss_stream_status(sh)
+    assert st == ss.SS_OK
+
+    # per-launch events inside the timed region
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(launches) + 1)] for _ in range(args.steps)]
+    sampler = ClockSampler(gpu_uuid(torch, dev)) if rank == 0 else None
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for k in range(args.steps):
+        ev[k][0].record(stream)
+        for j, f in enumerate(launches):
+            f()
+            ev[k][j + 1].record(stream)
+    t_end.record(stream)
+    t_end.synchronize()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    elapsed_ms = t_start.elapsed_time(t_end)
+    launch_ms = [ev[k][j].elapsed_time(ev[k][j + 1]) for k in range(args.steps) for j in range(len(launches))]
+    st, tile = ss.ss_stream_status(sh)
+    assert st == ss.SS_OK, f"device status {st} at tile {tile}"
+
+    elapsed_ms = max_over_ranks(elapsed_ms, dev)
+    value = whole_job_rate(len(launches) * N * args.steps, world, elapsed_ms)
+    ms_per_step = elapsed_ms / args.steps
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    # roofline of the dominant kernel (the look-back scan: every launch of the step)
+    peak, peak_src = measured_hbm_peak()
+    mean_launch_ms = statistics.fmean(launch_ms)
+    achieved = BYTES_PER_ELEM * N / (mean_launch_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": recorded_traffic(), "kernel": "k_scan_lookback",
+                "bytes_per_launch": BYTES_PER_ELEM * N, "mean_launch_ms": mean_launch_ms,
+                "median_launch_ms": statistics.median(launch_ms), "peak_source": peak_src,
+                "frac_of_nominal_8TBs": achieved / 8000.0}
+
+    # end to end through the host-memory API: pinned host in, pinned host out
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    h_in_i = torch.from_numpy(xs).pin_memory()
+    h_in_f = torch.from_numpy(xf).pin_memory()
+    h_out_i = torch.empty_like(h_in_i).pin_memory()
+    h_out_f = torch.empty_like(h_in_f).pin_memory()
+
+    def e2e_step():
+        ss.ss_scan_host(ss.SS_I32, False, h_in_i, h_out_i, N, stream=sh)
+        ss.ss_scan_host(ss.SS_I32, True, h_in_i, h_out_i, N, stream=sh)
+        ss.ss_scan_host(ss.SS_F32, False, h_in_f, h_out_f, N, stream=sh)
+        ss.ss_scan_host(ss.SS_F32, True, h_in_f, h_out_f, N, stream=sh)
+
+    e2e_step()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = time.perf_counter() - t0
+    e2e = {"value": 4 * N * e2e_steps / e2e_s / 1e9, "unit": UNIT,
+           "h2d_bytes_per_step": 4 * N * 4, "d2h_bytes_per_step": 4 * N * 4,
+           "steps": e2e_steps, "api": "ss_scan_host (chunked H2D / seeded scan / D2H pipeline)"}
+
+    rows = {} if args.no_rows else row_rates(torch, ss, stream, dev, xs_d, xf_d, out_i)
+    cpu = None if args.no_cpu else cpu_baseline(xs, xf, budget_s=args.cpu_budget)
+
+    emit({"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+          "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+          "scaling": "weak", "vs_baseline": None, "dtype": "int32/fp32", "data": DATA,
+          "config": {"workload": WORKLOAD, "n": N, "elements_per_step": len(launches) * N,
+                     "l2": "inputs larger than L2 (400 MB per array vs 129 MB), no flush",
+                     "parallelism": "replicas" if world > 1 else "single GPU",
+                     "tile_elems": ss.ss_scan_tile_elems(), "scan_config": args.config},
+          "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+          "gpu_launches": len(launches) * args.steps, "clocks": clocks,
+          "GB/s": value * BYTES_PER_ELEM, "rows": rows})
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=0, help="single-pass tile configuration")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--no-rows", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--skip-check", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

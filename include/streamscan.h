@@ -1,0 +1,193 @@
+/*
+ * streamscan.h -- C ABI of libstreamscan.so: device-wide prefix sums and
+ * order-preserving stream compaction on one NVIDIA GB300 (sm_103a).
+ *
+ * Definitions ("Prefix sum and other parallel patterns", Definitions):
+ *   inclusive  out[i] = in[0] + ... + in[i]
+ *   exclusive  out[i] = in[0] + ... + in[i-1],  out[0] = 0
+ * e.g. in = [3,1,7,0,4,1,6,3] gives inclusive [3,4,11,11,15,16,22,25] and
+ * exclusive [0,3,4,11,11,15,16,22].
+ *
+ * Conventions shared by every call:
+ *   - Pointers named in/out/keys/flags/d_count/d_carry_* are DEVICE
+ *     pointers owned by the caller (e.g. from torch, cudaMalloc).  Pointers
+ *     named h_* are HOST pointers.  The library never frees caller memory.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Device
+ *     calls only enqueue work and return; results are ready when the stream
+ *     reaches them.  Calls on one stream run in order; calls on different
+ *     streams are independent (each (device, stream) pair has its own
+ *     workspace).
+ *   - int32 and uint32 sums wrap modulo 2^32 (two's complement for int32).
+ *     fp32 sums use IEEE round-to-nearest adds in an order the caller does
+ *     not control; the last bits of an fp32 result may differ from run to
+ *     run, because a tile adds its predecessors' published sums in whatever
+ *     grouping the look-back found.
+ *   - 16-byte aligned in/out take the vectorised path; any 4-byte aligned
+ *     pointers are accepted and take a slower element-wise path.
+ *   - Argument errors are found before anything is enqueued and return
+ *     SS_ERR_INVALID_ARG (ss_last_error_detail() says why).  Launch
+ *     failures return SS_ERR_CUDA.  Errors found on the device (a look-back
+ *     wait that ran out) are recorded in the stream's status word and
+ *     returned by the next ss_stream_status() call on that stream; the
+ *     outputs of the failing call are then undefined.
+ *   - n == 0 is a valid no-op (compact_u32 still writes *d_count = 0).
+ *   - The library owns a small per-(device, stream) workspace (tile
+ *     descriptors, a tile counter, the status word), about 8 bytes per 4096
+ *     elements, grown on demand with stream-ordered allocation and freed
+ *     by ss_shutdown().  Size it before capturing a stream into a CUDA
+ *     graph by making one call of the largest n on that stream first.
+ */
+#ifndef STREAMSCAN_H
+#define STREAMSCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared here so that the header needs no CUDA
+ * include. */
+typedef struct CUstream_st *ss_stream_t;
+
+typedef enum ss_status {
+    SS_OK = 0,
+    SS_ERR_INVALID_ARG = 1,      /* bad pointer, size or overlap */
+    SS_ERR_CUDA = 2,             /* a CUDA runtime call or launch failed */
+    SS_ERR_LOOKBACK_TIMEOUT = 3, /* a tile's look-back wait ran out */
+    SS_ERR_NO_MEMORY = 4,        /* workspace allocation failed */
+    SS_ERR_UNSUPPORTED = 5       /* no usable device, or bad enum value */
+} ss_status;
+
+typedef enum ss_dtype { SS_I32 = 0, SS_U32 = 1, SS_F32 = 2 } ss_dtype;
+
+/* Algorithms for ss_scan().  SS_ALGO_LOOKBACK is the product path; the
+ * others are the measured ablations. */
+typedef enum ss_algo {
+    SS_ALGO_LOOKBACK = 0,            /* single pass, decoupled look-back, 2n traffic */
+    SS_ALGO_REDUCE_THEN_SCAN = 1,    /* three kernels, 3n traffic */
+    SS_ALGO_RTS_BLELLOCH = 2,        /* same, third kernel a Blelloch tree, unpadded */
+    SS_ALGO_RTS_BLELLOCH_PAD32 = 3,  /* same, tree padded i + i/32 */
+    SS_ALGO_RTS_BLELLOCH_PAD2 = 4    /* same, tree padded i + i/32 + i/1024 */
+} ss_algo;
+
+/*
+ * Device-wide scans, single pass with decoupled look-back ("Prefix sum and
+ * other parallel patterns", A device-level scan: scan then propagate --
+ * each block looks back at the states earlier blocks published, "local sum
+ * only" or "inclusive prefix available").
+ *   in   device, n elements, read once.
+ *   out  device, n elements, written once.  out == in is allowed (in-place);
+ *        any other overlap is SS_ERR_INVALID_ARG.
+ *   n    element count, 0 <= n < 2^31 * 4096.
+ */
+ss_status scan_inclusive_i32(const int32_t *in, int32_t *out, size_t n, ss_stream_t stream);
+ss_status scan_exclusive_i32(const int32_t *in, int32_t *out, size_t n, ss_stream_t stream);
+ss_status scan_inclusive_u32(const uint32_t *in, uint32_t *out, size_t n, ss_stream_t stream);
+ss_status scan_exclusive_u32(const uint32_t *in, uint32_t *out, size_t n, ss_stream_t stream);
+ss_status scan_inclusive_f32(const float *in, float *out, size_t n, ss_stream_t stream);
+ss_status scan_exclusive_f32(const float *in, float *out, size_t n, ss_stream_t stream);
+
+/*
+ * Order-preserving stream compaction in one pass: out receives, in index
+ * order, every keys[i] whose flags[i] != 0, and *d_count the number kept
+ * ("Prefix sum and other parallel patterns", Stream compaction and
+ * Exercise 1: out[pos[i]] = in[i] with pos the exclusive scan of the 0/1
+ * keep flags, count = pos[n-1] + flags[n-1]; fused so that the flags' scan
+ * and the positions never reach device memory).
+ *   keys     device, n uint32.
+ *   flags    device, n uint8; any nonzero byte keeps the element.
+ *   out      device, room for n uint32 (only the first *d_count written);
+ *            must not overlap keys or flags.
+ *   d_count  device, one uint64, written by the call.
+ *   n        0 <= n < 2^32.
+ */
+ss_status compact_u32(const uint32_t *keys, const uint8_t *flags, uint32_t *out,
+                      uint64_t *d_count, size_t n, ss_stream_t stream);
+
+/*
+ * Generic scan entry: dtype, inclusive (0/1) and algorithm chosen at run
+ * time.  Same argument rules as the named scans.  The reduce-then-scan
+ * algorithms ("Prefix sum and other parallel patterns", three passes with
+ * scan_block_sums' carry loop; "The CUDA scan algorithm: the tree and the
+ * three kernels", Two sweeps over one tree, bank padding of "The stride
+ * doubles, and so does the conflict") also take out == in.
+ */
+ss_status ss_scan(ss_dtype dtype, int inclusive, ss_algo algo, const void *in, void *out,
+                  size_t n, ss_stream_t stream);
+
+/*
+ * Single-pass scan seeded with a carry: the prefix before in[0] is
+ * *d_carry_in (device, one element of the scan's type; NULL means 0), and
+ * the inclusive total including the seed is written to *d_carry_out (device,
+ * NULL to skip).  Scanning an array in consecutive chunks with the carry
+ * passed along gives the scan of the whole array; this is the offset step of
+ * a scan split over several calls or several devices (scan each part, scan
+ * the parts' totals, seed each part with its offset).  d_carry_out may
+ * equal d_carry_in.
+ */
+ss_status ss_scan_seeded(ss_dtype dtype, int inclusive, const void *in, void *out, size_t n,
+                         const void *d_carry_in, void *d_carry_out, ss_stream_t stream);
+
+/*
+ * Host-memory scan: h_in and h_out are HOST pointers (pinned memory gives
+ * full copy bandwidth; pageable memory works, slower).  The library copies
+ * the input to the device in chunks, scans each chunk seeded with the
+ * running carry, and copies results back, overlapping the copies of one
+ * chunk with the scan of another.  Returns when h_out holds the result
+ * (device errors are reported directly).  h_out == h_in is allowed.
+ */
+ss_status ss_scan_host(ss_dtype dtype, int inclusive, const void *h_in, void *h_out, size_t n,
+                       ss_stream_t stream);
+
+/*
+ * Bandwidth probe: copies n uint32 from in to out with the scan's loader and
+ * storer and no arithmetic ("The CUDA scan algorithm: the tree and the three
+ * kernels", Results: "copy, no scan" as the speed-of-light row).
+ */
+ss_status ss_copy_u32(const uint32_t *in, uint32_t *out, size_t n, ss_stream_t stream);
+
+/*
+ * Waits for `stream`, then returns and clears the device-side status of
+ * that stream's workspace: SS_OK, SS_ERR_LOOKBACK_TIMEOUT, or SS_ERR_CUDA if
+ * the stream itself failed.  *failing_tile (may be NULL) receives the first
+ * tile that gave up, or -1.
+ */
+ss_status ss_stream_status(ss_stream_t stream, int64_t *failing_tile);
+
+/* Static description of a status code. */
+const char *ss_status_string(ss_status status);
+
+/* Detail of the last error returned on the calling thread ("" if none). */
+const char *ss_last_error_detail(void);
+
+/* Elements per tile of the single-pass scan under the current tile
+ * configuration, and the number of configurations that can be selected. */
+size_t ss_scan_tile_elems(void);
+int ss_scan_config_count(void);
+
+/* Selects the single-pass scan's tile configuration for later calls in this
+ * process (0 = default: 256 threads x 16 elements).  Results do not depend
+ * on it, except for the rounding of fp32 sums. */
+ss_status ss_set_scan_config(int config);
+
+/* Frees every workspace the library allocated (all devices and streams).
+ * No call may be in flight. */
+void ss_shutdown(void);
+
+/*
+ * Test hook for the failure path of the look-back wait.  With tile >= 0,
+ * later single-pass calls in this process skip publishing that tile's
+ * descriptor, so its successors' waits run out after timeout_ns (their
+ * status then reads SS_ERR_LOOKBACK_TIMEOUT).  tile = -1 restores normal
+ * operation and timeout_ns = 0 restores the default limit (2 s).  No wait is
+ * ever unbounded: every wait also stops after a fixed number of polls.
+ */
+ss_status ss_debug_set_lookback_fault(int64_t tile, uint64_t timeout_ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* STREAMSCAN_H */

@@ -1,0 +1,248 @@
+"""Device-wide prefix sums and order-preserving stream compaction on one
+NVIDIA GB300 (sm_103a): a thin ctypes binding of libstreamscan.so.
+
+The functions carry the C ABI's names (include/streamscan.h) and only
+marshal arguments: device pointers, element counts and the CUDA stream.
+Every step of the computation runs in the library's CUDA kernels; there is
+no CPU fallback.  If libstreamscan.so has not been built, every call raises
+LibraryMissing (build it with ``python -m stream_compaction_pass_gb300.build``).
+
+Arguments that are arrays may be torch tensors (CUDA tensors for device
+pointers, CPU tensors or numpy arrays for host pointers) or raw integer
+addresses.  For tensors, `n` defaults to the element count and `stream` to
+torch's current stream on the tensor's device.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libstreamscan.so")
+HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "streamscan.h")
+
+SS_OK = 0
+SS_ERR_INVALID_ARG = 1
+SS_ERR_CUDA = 2
+SS_ERR_LOOKBACK_TIMEOUT = 3
+SS_ERR_NO_MEMORY = 4
+SS_ERR_UNSUPPORTED = 5
+
+SS_I32, SS_U32, SS_F32 = 0, 1, 2
+
+SS_ALGO_LOOKBACK = 0
+SS_ALGO_REDUCE_THEN_SCAN = 1
+SS_ALGO_RTS_BLELLOCH = 2
+SS_ALGO_RTS_BLELLOCH_PAD32 = 3
+SS_ALGO_RTS_BLELLOCH_PAD2 = 4
+
+
+class LibraryMissing(ImportError):
+    pass
+
+
+class StreamScanError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        super().__init__(f"{where}: status {status} ({detail})")
+        self.status = status
+        self.detail = detail
+
+
+_lib = None
+
+
+def _declare(lib):
+    P, SZ, I, U64, I64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_uint64, ctypes.c_int64
+    sigs = {
+        "scan_inclusive_i32": [P, P, SZ, P],
+        "scan_exclusive_i32": [P, P, SZ, P],
+        "scan_inclusive_u32": [P, P, SZ, P],
+        "scan_exclusive_u32": [P, P, SZ, P],
+        "scan_inclusive_f32": [P, P, SZ, P],
+        "scan_exclusive_f32": [P, P, SZ, P],
+        "compact_u32": [P, P, P, P, SZ, P],
+        "ss_scan": [I, I, I, P, P, SZ, P],
+        "ss_scan_seeded": [I, I, P, P, SZ, P, P, P],
+        "ss_scan_host": [I, I, P, P, SZ, P],
+        "ss_copy_u32": [P, P, SZ, P],
+        "ss_stream_status": [P, ctypes.POINTER(I64)],
+        "ss_set_scan_config": [I],
+        "ss_debug_set_lookback_fault": [I64, U64],
+    }
+    for name, args in sigs.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = I
+    lib.ss_status_string.argtypes = [I]
+    lib.ss_status_string.restype = ctypes.c_char_p
+    lib.ss_last_error_detail.argtypes = []
+    lib.ss_last_error_detail.restype = ctypes.c_char_p
+    lib.ss_scan_tile_elems.argtypes = []
+    lib.ss_scan_tile_elems.restype = SZ
+    lib.ss_scan_config_count.argtypes = []
+    lib.ss_scan_config_count.restype = I
+    lib.ss_shutdown.argtypes = []
+    lib.ss_shutdown.restype = None
+    return lib
+
+
+def lib():
+    """The loaded libstreamscan.so (raises LibraryMissing if not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise LibraryMissing(
+                f"{LIB_PATH} is not built; run `python -m stream_compaction_pass_gb300.build` "
+                "(needs nvcc); there is no CPU fallback")
+        _lib = _declare(ctypes.CDLL(LIB_PATH))
+    return _lib
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/streamscan.h declares."""
+    text = open(HEADER_PATH).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([A-Za-z_][A-Za-z0-9_]*)\s*\(",
+                                 text, flags=re.M)))
+
+
+def _addr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if hasattr(x, "ctypes"):
+        return x.ctypes.data
+    raise TypeError(f"cannot take the address of {type(x)!r}")
+
+
+def _numel(x) -> int:
+    if hasattr(x, "numel"):
+        return int(x.numel())
+    return int(x.size)
+
+
+def _stream(stream, *tensors) -> int:
+    if stream is not None:
+        if isinstance(stream, int):
+            return stream
+        return int(stream.cuda_stream)
+    for t in tensors:
+        if hasattr(t, "is_cuda") and t.is_cuda:
+            import torch
+            return int(torch.cuda.current_stream(t.device).cuda_stream)
+    return 0
+
+
+def _check(st: int, where: str) -> None:
+    if st != SS_OK:
+        detail = lib().ss_last_error_detail().decode() or lib().ss_status_string(st).decode()
+        raise StreamScanError(st, where, detail)
+
+
+def _scan_named(name: str, inp, out, n, stream) -> None:
+    if n is None:
+        n = _numel(inp)
+    _check(getattr(lib(), name)(_addr(inp), _addr(out), n, _stream(stream, inp, out)), name)
+
+
+def scan_inclusive_i32(inp, out, n=None, stream=None):
+    _scan_named("scan_inclusive_i32", inp, out, n, stream)
+
+
+def scan_exclusive_i32(inp, out, n=None, stream=None):
+    _scan_named("scan_exclusive_i32", inp, out, n, stream)
+
+
+def scan_inclusive_u32(inp, out, n=None, stream=None):
+    _scan_named("scan_inclusive_u32", inp, out, n, stream)
+
+
+def scan_exclusive_u32(inp, out, n=None, stream=None):
+    _scan_named("scan_exclusive_u32", inp, out, n, stream)
+
+
+def scan_inclusive_f32(inp, out, n=None, stream=None):
+    _scan_named("scan_inclusive_f32", inp, out, n, stream)
+
+
+def scan_exclusive_f32(inp, out, n=None, stream=None):
+    _scan_named("scan_exclusive_f32", inp, out, n, stream)
+
+
+def compact_u32(keys, flags, out, d_count, n=None, stream=None):
+    if n is None:
+        n = _numel(keys)
+    _check(lib().compact_u32(_addr(keys), _addr(flags), _addr(out), _addr(d_count), n,
+                             _stream(stream, keys, flags, out)), "compact_u32")
+
+
+def ss_scan(dtype: int, inclusive: bool, algo: int, inp, out, n=None, stream=None):
+    if n is None:
+        n = _numel(inp)
+    _check(lib().ss_scan(dtype, int(bool(inclusive)), algo, _addr(inp), _addr(out), n,
+                         _stream(stream, inp, out)), "ss_scan")
+
+
+def ss_scan_seeded(dtype: int, inclusive: bool, inp, out, carry_in=None, carry_out=None, n=None,
+                   stream=None):
+    if n is None:
+        n = _numel(inp)
+    _check(lib().ss_scan_seeded(dtype, int(bool(inclusive)), _addr(inp), _addr(out), n,
+                                _addr(carry_in), _addr(carry_out), _stream(stream, inp, out)),
+           "ss_scan_seeded")
+
+
+def ss_scan_host(dtype: int, inclusive: bool, h_in, h_out, n=None, stream=None):
+    if n is None:
+        n = _numel(h_in)
+    _check(lib().ss_scan_host(dtype, int(bool(inclusive)), _addr(h_in), _addr(h_out), n,
+                              _stream(stream)), "ss_scan_host")
+
+
+def ss_copy_u32(inp, out, n=None, stream=None):
+    if n is None:
+        n = _numel(inp)
+    _check(lib().ss_copy_u32(_addr(inp), _addr(out), n, _stream(stream, inp, out)), "ss_copy_u32")
+
+
+def ss_stream_status(stream=None):
+    """Waits for the stream; returns (status, failing_tile) and clears it."""
+    tile = ctypes.c_int64(-1)
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    st = lib().ss_stream_status(_stream(stream), ctypes.byref(tile))
+    return st, tile.value
+
+
+def ss_status_string(status: int) -> str:
+    return lib().ss_status_string(status).decode()
+
+
+def ss_last_error_detail() -> str:
+    return lib().ss_last_error_detail().decode()
+
+
+def ss_scan_tile_elems() -> int:
+    return int(lib().ss_scan_tile_elems())
+
+
+def ss_scan_config_count() -> int:
+    return int(lib().ss_scan_config_count())
+
+
+def ss_set_scan_config(config: int) -> None:
+    _check(lib().ss_set_scan_config(config), "ss_set_scan_config")
+
+
+def ss_shutdown() -> None:
+    lib().ss_shutdown()
+
+
+def ss_debug_set_lookback_fault(tile: int, timeout_ns: int = 0) -> None:
+    _check(lib().ss_debug_set_lookback_fault(tile, timeout_ns), "ss_debug_set_lookback_fault")

@@ -1,0 +1,475 @@
+// api.cu -- the C ABI declared in include/streamscan.h: argument checks,
+// per-(device, stream) workspaces, device status read-back and the
+// host-memory pipeline.  All arithmetic runs in the kernels of scan.cu,
+// compact.cu and ablations.cu.
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <utility>
+#include <vector>
+
+#include "../../include/streamscan.h"
+#include "internal.h"
+
+namespace {
+
+using ss::Dtype;
+
+thread_local std::string g_detail;
+
+std::atomic<int> g_config{0};
+std::atomic<int64_t> g_fault_tile{-1};
+std::atomic<uint64_t> g_timeout_ns{0};
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+
+// Descriptor epochs are 30 bits; clear the descriptors well before a tag can
+// come round again.
+constexpr uint64_t kClearEvery = 1ull << 29;
+
+constexpr size_t kHostChunk = (size_t)16 << 20;  // elements per host-pipeline chunk
+constexpr int kHostBuffers = 3;
+
+ss_status fail(ss_status st, const std::string& why) {
+    g_detail = why;
+    return st;
+}
+
+ss_status cuda_fail(cudaError_t e, const char* where) {
+    g_detail = std::string(where) + ": " + cudaGetErrorString(e);
+    return SS_ERR_CUDA;
+}
+
+struct HostPipe {
+    void* buf[kHostBuffers] = {nullptr, nullptr, nullptr};
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t ev_in[kHostBuffers] = {}, ev_scan[kHostBuffers] = {}, ev_out[kHostBuffers] = {};
+    bool ready = false;
+};
+
+struct Workspace {
+    int device = 0;
+    cudaStream_t stream = nullptr;
+    // Header: [0] tile counter (u64), [8] status words (2 x u32), [16] carry (8 B).
+    unsigned char* header = nullptr;
+    unsigned long long* desc = nullptr;
+    size_t desc_cap = 0;  // descriptors
+    void* totals = nullptr;
+    size_t totals_cap = 0;  // bytes
+    uint64_t launches_since_clear = 0;
+    HostPipe pipe;
+    std::mutex pipe_mu;  // one host pipeline at a time per workspace
+};
+
+std::mutex g_mu;
+std::map<std::pair<int, uintptr_t>, Workspace*> g_ws;
+
+unsigned long long* ws_counter(Workspace* w) { return reinterpret_cast<unsigned long long*>(w->header); }
+uint32_t* ws_status(Workspace* w) { return reinterpret_cast<uint32_t*>(w->header + 8); }
+void* ws_carry(Workspace* w) { return w->header + 16; }
+
+ss_status get_workspace(cudaStream_t s, Workspace** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto key = std::make_pair(dev, reinterpret_cast<uintptr_t>(s));
+    auto it = g_ws.find(key);
+    if (it != g_ws.end()) {
+        *out = it->second;
+        return SS_OK;
+    }
+    Workspace* w = new Workspace();
+    w->device = dev;
+    w->stream = s;
+    e = cudaMallocAsync(reinterpret_cast<void**>(&w->header), 256, s);
+    if (e != cudaSuccess) {
+        delete w;
+        return e == cudaErrorMemoryAllocation ? fail(SS_ERR_NO_MEMORY, "workspace header")
+                                              : cuda_fail(e, "cudaMallocAsync");
+    }
+    e = cudaMemsetAsync(w->header, 0, 256, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    g_ws[key] = w;
+    *out = w;
+    return SS_OK;
+}
+
+ss_status ensure_desc(Workspace* w, size_t tiles) {
+    if (tiles > w->desc_cap) {
+        size_t cap = w->desc_cap ? w->desc_cap : (size_t)1 << 16;
+        while (cap < tiles) cap *= 2;
+        if (w->desc) {
+            cudaError_t e = cudaFreeAsync(w->desc, w->stream);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync");
+            w->desc = nullptr;
+            w->desc_cap = 0;
+        }
+        cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&w->desc), cap * 8, w->stream);
+        if (e != cudaSuccess)
+            return e == cudaErrorMemoryAllocation ? fail(SS_ERR_NO_MEMORY, "descriptor array")
+                                                  : cuda_fail(e, "cudaMallocAsync");
+        e = cudaMemsetAsync(w->desc, 0, cap * 8, w->stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+        w->desc_cap = cap;
+        w->launches_since_clear = 0;
+    } else if (w->launches_since_clear >= kClearEvery) {
+        cudaError_t e = cudaMemsetAsync(w->desc, 0, w->desc_cap * 8, w->stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+        w->launches_since_clear = 0;
+    }
+    w->launches_since_clear += 1;
+    return SS_OK;
+}
+
+ss_status ensure_totals(Workspace* w, size_t bytes) {
+    if (bytes <= w->totals_cap) return SS_OK;
+    size_t cap = w->totals_cap ? w->totals_cap : (size_t)1 << 18;
+    while (cap < bytes) cap *= 2;
+    if (w->totals) {
+        cudaError_t e = cudaFreeAsync(w->totals, w->stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync");
+        w->totals = nullptr;
+        w->totals_cap = 0;
+    }
+    cudaError_t e = cudaMallocAsync(&w->totals, cap, w->stream);
+    if (e != cudaSuccess)
+        return e == cudaErrorMemoryAllocation ? fail(SS_ERR_NO_MEMORY, "totals array")
+                                              : cuda_fail(e, "cudaMallocAsync");
+    w->totals_cap = cap;
+    return SS_OK;
+}
+
+ss::LookbackWs make_ws(Workspace* w) {
+    ss::LookbackWs ws;
+    if (w) {
+        ws.desc = w->desc;
+        ws.counter = ws_counter(w);
+        ws.status = ws_status(w);
+    }
+    const uint64_t t = g_timeout_ns.load();
+    ws.timeout_ns = t ? t : kDefaultTimeoutNs;
+    ws.fault_tile = g_fault_tile.load();
+    return ws;
+}
+
+bool overlaps(const void* a, size_t abytes, const void* b, size_t bbytes) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + bbytes && y < x + abytes;
+}
+
+ss_status check_scan_args(const void* in, const void* out, size_t n, size_t tile) {
+    if (n == 0) return SS_OK;
+    if (in == nullptr || out == nullptr) return fail(SS_ERR_INVALID_ARG, "null pointer with n > 0");
+    if ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) & 3u)
+        return fail(SS_ERR_INVALID_ARG, "in/out must be 4-byte aligned");
+    if (n / tile >= ((size_t)1 << 31) - 1) return fail(SS_ERR_INVALID_ARG, "n too large");
+    if (n > (SIZE_MAX / 8)) return fail(SS_ERR_INVALID_ARG, "n too large");
+    if (in != out && overlaps(in, n * 4, out, n * 4))
+        return fail(SS_ERR_INVALID_ARG, "in and out partially overlap");
+    return SS_OK;
+}
+
+ss_status scan_lookback(Dtype dt, bool inclusive, const void* in, void* out, size_t n,
+                        const void* carry_in, void* carry_out, cudaStream_t s) {
+    const int cfg = g_config.load();
+    const size_t tile = ss::scan_config(cfg).tile();
+    ss_status st = check_scan_args(in, out, n, tile);
+    if (st != SS_OK) return st;
+    if (n == 0) return SS_OK;
+    const size_t tiles = (n + tile - 1) / tile;
+    Workspace* w = nullptr;
+    if (tiles > 1 || g_fault_tile.load() >= 0) {
+        st = get_workspace(s, &w);
+        if (st != SS_OK) return st;
+        st = ensure_desc(w, tiles);
+        if (st != SS_OK) return st;
+    }
+    cudaError_t e = ss::launch_scan_lookback(dt, inclusive, cfg, in, out, n, make_ws(w), carry_in,
+                                             carry_out, s);
+    if (e != cudaSuccess) return cuda_fail(e, "scan launch");
+    return SS_OK;
+}
+
+Dtype to_dtype(ss_dtype d) {
+    return d == SS_F32 ? Dtype::F32 : (d == SS_U32 ? Dtype::U32 : Dtype::I32);
+}
+
+bool valid_dtype(ss_dtype d) { return d == SS_I32 || d == SS_U32 || d == SS_F32; }
+
+}  // namespace
+
+extern "C" {
+
+ss_status scan_inclusive_i32(const int32_t* in, int32_t* out, size_t n, ss_stream_t stream) {
+    return scan_lookback(Dtype::I32, true, in, out, n, nullptr, nullptr, (cudaStream_t)stream);
+}
+ss_status scan_exclusive_i32(const int32_t* in, int32_t* out, size_t n, ss_stream_t stream) {
+    return scan_lookback(Dtype::I32, false, in, out, n, nullptr, nullptr, (cudaStream_t)stream);
+}
+ss_status scan_inclusive_u32(const uint32_t* in, uint32_t* out, size_t n, ss_stream_t stream) {
+    return scan_lookback(Dtype::U32, true, in, out, n, nullptr, nullptr, (cudaStream_t)stream);
+}
+ss_status scan_exclusive_u32(const uint32_t* in, uint32_t* out, size_t n, ss_stream_t stream) {
+    return scan_lookback(Dtype::U32, false, in, out, n, nullptr, nullptr, (cudaStream_t)stream);
+}
+ss_status scan_inclusive_f32(const float* in, float* out, size_t n, ss_stream_t stream) {
+    return scan_lookback(Dtype::F32, true, in, out, n, nullptr, nullptr, (cudaStream_t)stream);
+}
+ss_status scan_exclusive_f32(const float* in, float* out, size_t n, ss_stream_t stream) {
+    return scan_lookback(Dtype::F32, false, in, out, n, nullptr, nullptr, (cudaStream_t)stream);
+}
+
+ss_status ss_scan_seeded(ss_dtype dtype, int inclusive, const void* in, void* out, size_t n,
+                         const void* d_carry_in, void* d_carry_out, ss_stream_t stream) {
+    if (!valid_dtype(dtype)) return fail(SS_ERR_UNSUPPORTED, "unknown dtype");
+    if (d_carry_in && (reinterpret_cast<uintptr_t>(d_carry_in) & 3u))
+        return fail(SS_ERR_INVALID_ARG, "carry must be 4-byte aligned");
+    if (d_carry_out && (reinterpret_cast<uintptr_t>(d_carry_out) & 3u))
+        return fail(SS_ERR_INVALID_ARG, "carry must be 4-byte aligned");
+    if (n == 0) {
+        if (d_carry_out == nullptr) return SS_OK;
+        cudaStream_t s = (cudaStream_t)stream;
+        cudaError_t e = d_carry_in ? cudaMemcpyAsync(d_carry_out, d_carry_in, 4, cudaMemcpyDeviceToDevice, s)
+                                   : cudaMemsetAsync(d_carry_out, 0, 4, s);
+        return e == cudaSuccess ? SS_OK : cuda_fail(e, "carry copy");
+    }
+    return scan_lookback(to_dtype(dtype), inclusive != 0, in, out, n, d_carry_in, d_carry_out,
+                         (cudaStream_t)stream);
+}
+
+ss_status compact_u32(const uint32_t* keys, const uint8_t* flags, uint32_t* out, uint64_t* d_count,
+                      size_t n, ss_stream_t stream) {
+    cudaStream_t s = (cudaStream_t)stream;
+    if (d_count == nullptr) return fail(SS_ERR_INVALID_ARG, "d_count is null");
+    if (reinterpret_cast<uintptr_t>(d_count) & 7u)
+        return fail(SS_ERR_INVALID_ARG, "d_count must be 8-byte aligned");
+    if (n > 0) {
+        if (!keys || !flags || !out) return fail(SS_ERR_INVALID_ARG, "null pointer with n > 0");
+        if ((reinterpret_cast<uintptr_t>(keys) | reinterpret_cast<uintptr_t>(out)) & 3u)
+            return fail(SS_ERR_INVALID_ARG, "keys/out must be 4-byte aligned");
+        if (n > 0xffffffffull) return fail(SS_ERR_INVALID_ARG, "n must be < 2^32");
+        if (overlaps(out, n * 4, keys, n * 4) || overlaps(out, n * 4, flags, n))
+            return fail(SS_ERR_INVALID_ARG, "out overlaps keys or flags");
+        if (overlaps(d_count, 8, out, n * 4))
+            return fail(SS_ERR_INVALID_ARG, "d_count overlaps out");
+    }
+    if (n == 0) {
+        cudaError_t e = cudaMemsetAsync(d_count, 0, 8, s);
+        return e == cudaSuccess ? SS_OK : cuda_fail(e, "cudaMemsetAsync");
+    }
+    const size_t tiles = (n + ss::kCompactTile - 1) / ss::kCompactTile;
+    Workspace* w = nullptr;
+    if (tiles > 1 || g_fault_tile.load() >= 0) {
+        ss_status st = get_workspace(s, &w);
+        if (st != SS_OK) return st;
+        st = ensure_desc(w, tiles);
+        if (st != SS_OK) return st;
+    }
+    cudaError_t e = ss::launch_compact_u32(keys, flags, out, reinterpret_cast<unsigned long long*>(d_count),
+                                           n, make_ws(w), s);
+    return e == cudaSuccess ? SS_OK : cuda_fail(e, "compaction launch");
+}
+
+ss_status ss_scan(ss_dtype dtype, int inclusive, ss_algo algo, const void* in, void* out, size_t n,
+                  ss_stream_t stream) {
+    if (!valid_dtype(dtype)) return fail(SS_ERR_UNSUPPORTED, "unknown dtype");
+    cudaStream_t s = (cudaStream_t)stream;
+    if (algo == SS_ALGO_LOOKBACK)
+        return scan_lookback(to_dtype(dtype), inclusive != 0, in, out, n, nullptr, nullptr, s);
+    int tile_scan;
+    switch (algo) {
+        case SS_ALGO_REDUCE_THEN_SCAN: tile_scan = 0; break;
+        case SS_ALGO_RTS_BLELLOCH: tile_scan = 1; break;
+        case SS_ALGO_RTS_BLELLOCH_PAD32: tile_scan = 2; break;
+        case SS_ALGO_RTS_BLELLOCH_PAD2: tile_scan = 3; break;
+        default: return fail(SS_ERR_UNSUPPORTED, "unknown algorithm");
+    }
+    ss_status st = check_scan_args(in, out, n, ss::kRtsTile);
+    if (st != SS_OK) return st;
+    if (n == 0) return SS_OK;
+    Workspace* w = nullptr;
+    st = get_workspace(s, &w);
+    if (st != SS_OK) return st;
+    const size_t tiles = (n + ss::kRtsTile - 1) / ss::kRtsTile;
+    st = ensure_totals(w, tiles * 4);
+    if (st != SS_OK) return st;
+    cudaError_t e = ss::launch_reduce_then_scan(to_dtype(dtype), inclusive != 0, tile_scan, in, out, n,
+                                                w->totals, s);
+    return e == cudaSuccess ? SS_OK : cuda_fail(e, "reduce-then-scan launch");
+}
+
+ss_status ss_copy_u32(const uint32_t* in, uint32_t* out, size_t n, ss_stream_t stream) {
+    ss_status st = check_scan_args(in, out, n, ss::scan_config(g_config.load()).tile());
+    if (st != SS_OK) return st;
+    if (n == 0) return SS_OK;
+    cudaError_t e = ss::launch_copy_probe(g_config.load(), in, out, n, (cudaStream_t)stream);
+    return e == cudaSuccess ? SS_OK : cuda_fail(e, "copy launch");
+}
+
+ss_status ss_stream_status(ss_stream_t stream, int64_t* failing_tile) {
+    cudaStream_t s = (cudaStream_t)stream;
+    if (failing_tile) *failing_tile = -1;
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    Workspace* w = nullptr;
+    {
+        int dev = 0;
+        e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_ws.find(std::make_pair(dev, reinterpret_cast<uintptr_t>(s)));
+        if (it != g_ws.end()) w = it->second;
+    }
+    if (w == nullptr) return SS_OK;
+    uint32_t words[2] = {0, 0};
+    e = cudaMemcpyAsync(words, ws_status(w), sizeof(words), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ws_status(w), 0, sizeof(words), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "status read-back");
+    if (words[0] & ss::kErrCounter) {
+        // Start the workspace afresh: counter and every descriptor to zero.
+        cudaMemsetAsync(ws_counter(w), 0, 8, s);
+        if (w->desc) cudaMemsetAsync(w->desc, 0, w->desc_cap * 8, s);
+        cudaStreamSynchronize(s);
+        return fail(SS_ERR_CUDA, "tile counter out of step with the launch (concurrent use of one stream's workspace?)");
+    }
+    if (words[0] & ss::kErrLookbackTimeout) {
+        if (failing_tile) *failing_tile = words[1] ? (int64_t)words[1] - 1 : -1;
+        return fail(SS_ERR_LOOKBACK_TIMEOUT, "a look-back wait ran out");
+    }
+    return SS_OK;
+}
+
+static ss_status host_pipe_init(Workspace* w, size_t elems) {
+    HostPipe& p = w->pipe;
+    if (p.ready) return SS_OK;
+    cudaError_t e;
+    for (int b = 0; b < kHostBuffers; ++b) {
+        e = cudaMalloc(&p.buf[b], elems * 4);
+        if (e != cudaSuccess) return fail(SS_ERR_NO_MEMORY, "host pipeline buffers");
+        if ((e = cudaEventCreateWithFlags(&p.ev_in[b], cudaEventDisableTiming)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&p.ev_scan[b], cudaEventDisableTiming)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&p.ev_out[b], cudaEventDisableTiming)) != cudaSuccess)
+            return cuda_fail(e, "cudaEventCreate");
+    }
+    if ((e = cudaStreamCreateWithFlags(&p.h2d, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaStreamCreateWithFlags(&p.d2h, cudaStreamNonBlocking)) != cudaSuccess)
+        return cuda_fail(e, "cudaStreamCreate");
+    p.ready = true;
+    return SS_OK;
+}
+
+ss_status ss_scan_host(ss_dtype dtype, int inclusive, const void* h_in, void* h_out, size_t n,
+                       ss_stream_t stream) {
+    if (!valid_dtype(dtype)) return fail(SS_ERR_UNSUPPORTED, "unknown dtype");
+    if (n == 0) return SS_OK;
+    if (h_in == nullptr || h_out == nullptr) return fail(SS_ERR_INVALID_ARG, "null pointer with n > 0");
+    if (h_in != h_out && overlaps(h_in, n * 4, h_out, n * 4))
+        return fail(SS_ERR_INVALID_ARG, "h_in and h_out partially overlap");
+    cudaStream_t s = (cudaStream_t)stream;
+    Workspace* w = nullptr;
+    ss_status st = get_workspace(s, &w);
+    if (st != SS_OK) return st;
+    std::lock_guard<std::mutex> lk(w->pipe_mu);
+    st = host_pipe_init(w, kHostChunk);
+    if (st != SS_OK) return st;
+    HostPipe& p = w->pipe;
+    void* carry = ws_carry(w);
+    cudaError_t e = cudaMemsetAsync(carry, 0, 4, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    const size_t chunks = (n + kHostChunk - 1) / kHostChunk;
+    const char* src = static_cast<const char*>(h_in);
+    char* dst = static_cast<char*>(h_out);
+    // The d2h stream must not start before earlier work on `s`; the h2d stream
+    // must not overwrite a buffer before its previous results were copied out.
+    cudaEvent_t start_ev = p.ev_scan[0];
+    if ((e = cudaEventRecord(start_ev, s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    if ((e = cudaStreamWaitEvent(p.h2d, start_ev, 0)) != cudaSuccess) return cuda_fail(e, "wait");
+    if ((e = cudaStreamWaitEvent(p.d2h, start_ev, 0)) != cudaSuccess) return cuda_fail(e, "wait");
+    for (size_t c = 0; c < chunks; ++c) {
+        const int b = (int)(c % kHostBuffers);
+        const size_t off = c * kHostChunk;
+        const size_t cnt = (n - off) < kHostChunk ? (n - off) : kHostChunk;
+        if (c >= (size_t)kHostBuffers && (e = cudaStreamWaitEvent(p.h2d, p.ev_out[b], 0)) != cudaSuccess)
+            return cuda_fail(e, "wait");
+        if ((e = cudaMemcpyAsync(p.buf[b], src + off * 4, cnt * 4, cudaMemcpyHostToDevice, p.h2d)) != cudaSuccess)
+            return cuda_fail(e, "cudaMemcpyAsync H2D");
+        if ((e = cudaEventRecord(p.ev_in[b], p.h2d)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+        if ((e = cudaStreamWaitEvent(s, p.ev_in[b], 0)) != cudaSuccess) return cuda_fail(e, "wait");
+        st = scan_lookback(to_dtype(dtype), inclusive != 0, p.buf[b], p.buf[b], cnt, carry, carry, s);
+        if (st != SS_OK) return st;
+        if ((e = cudaEventRecord(p.ev_scan[b], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+        if ((e = cudaStreamWaitEvent(p.d2h, p.ev_scan[b], 0)) != cudaSuccess) return cuda_fail(e, "wait");
+        if ((e = cudaMemcpyAsync(dst + off * 4, p.buf[b], cnt * 4, cudaMemcpyDeviceToHost, p.d2h)) != cudaSuccess)
+            return cuda_fail(e, "cudaMemcpyAsync D2H");
+        if ((e = cudaEventRecord(p.ev_out[b], p.d2h)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    }
+    if ((e = cudaStreamSynchronize(p.d2h)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    return SS_OK;
+}
+
+const char* ss_status_string(ss_status status) {
+    switch (status) {
+        case SS_OK: return "ok";
+        case SS_ERR_INVALID_ARG: return "invalid argument";
+        case SS_ERR_CUDA: return "CUDA error";
+        case SS_ERR_LOOKBACK_TIMEOUT: return "look-back wait timed out";
+        case SS_ERR_NO_MEMORY: return "out of device memory";
+        case SS_ERR_UNSUPPORTED: return "unsupported";
+    }
+    return "unknown status";
+}
+
+const char* ss_last_error_detail(void) { return g_detail.c_str(); }
+
+size_t ss_scan_tile_elems(void) { return ss::scan_config(g_config.load()).tile(); }
+
+int ss_scan_config_count(void) { return ss::scan_config_count(); }
+
+ss_status ss_set_scan_config(int config) {
+    if (config < 0 || config >= ss::scan_config_count())
+        return fail(SS_ERR_INVALID_ARG, "no such configuration");
+    g_config.store(config);
+    return SS_OK;
+}
+
+void ss_shutdown(void) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    int cur = 0;
+    cudaGetDevice(&cur);
+    for (auto& kv : g_ws) {
+        Workspace* w = kv.second;
+        cudaSetDevice(w->device);
+        cudaDeviceSynchronize();
+        if (w->desc) cudaFree(w->desc);
+        if (w->totals) cudaFree(w->totals);
+        if (w->header) cudaFree(w->header);
+        HostPipe& p = w->pipe;
+        if (p.ready) {
+            for (int b = 0; b < kHostBuffers; ++b) {
+                cudaFree(p.buf[b]);
+                cudaEventDestroy(p.ev_in[b]);
+                cudaEventDestroy(p.ev_scan[b]);
+                cudaEventDestroy(p.ev_out[b]);
+            }
+            cudaStreamDestroy(p.h2d);
+            cudaStreamDestroy(p.d2h);
+        }
+        delete w;
+    }
+    g_ws.clear();
+    cudaSetDevice(cur);
+}
+
+ss_status ss_debug_set_lookback_fault(int64_t tile, uint64_t timeout_ns) {
+    if (tile < -1) return fail(SS_ERR_INVALID_ARG, "tile must be >= -1");
+    g_fault_tile.store(tile);
+    g_timeout_ns.store(timeout_ns);
+    return SS_OK;
+}
+
+}  // extern "C"

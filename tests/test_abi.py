@@ -1,0 +1,81 @@
+"""The C ABI without a GPU: the library loads, exports every function the
+header declares, and rejects bad arguments before touching CUDA."""
+
+import ctypes
+
+import pytest
+
+import stream_compaction_pass_gb300 as ss
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from stream_compaction_pass_gb300 import build
+    build.build()
+    return ss.lib()
+
+
+def test_every_declared_function_is_exported(lib):
+    names = ss.header_functions()
+    assert len(names) >= 19
+    raw = ctypes.CDLL(ss.LIB_PATH)
+    for name in names:
+        assert hasattr(raw, name), f"{name} declared in streamscan.h but not exported"
+    for name in ("scan_inclusive_i32", "scan_exclusive_i32", "scan_inclusive_u32",
+                 "scan_exclusive_u32", "scan_inclusive_f32", "scan_exclusive_f32", "compact_u32"):
+        assert name in names
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert ss.ss_status_string(code)
+    assert ss.ss_status_string(99) == "unknown status"
+
+
+def test_null_pointers_rejected_before_cuda(lib):
+    for name in ("scan_inclusive_i32", "scan_exclusive_f32", "scan_exclusive_u32"):
+        assert getattr(lib, name)(None, None, 5, None) == ss.SS_ERR_INVALID_ARG
+    assert lib.compact_u32(None, None, None, None, 5, None) == ss.SS_ERR_INVALID_ARG
+    assert "null" in ss.ss_last_error_detail()
+
+
+def test_zero_length_is_a_noop(lib):
+    assert lib.scan_inclusive_i32(None, None, 0, None) == ss.SS_OK
+    assert lib.ss_scan(ss.SS_F32, 1, ss.SS_ALGO_REDUCE_THEN_SCAN, None, None, 0, None) == ss.SS_OK
+    assert lib.ss_scan_host(ss.SS_I32, 0, None, None, 0, None) == ss.SS_OK
+
+
+def test_misaligned_and_overlapping_rejected(lib):
+    assert lib.scan_inclusive_i32(0x1002, 0x2000, 4, None) == ss.SS_ERR_INVALID_ARG
+    assert "aligned" in ss.ss_last_error_detail()
+    # out starts inside in's range: partial overlap
+    assert lib.scan_inclusive_u32(0x10000, 0x10010, 64, None) == ss.SS_ERR_INVALID_ARG
+    assert "overlap" in ss.ss_last_error_detail()
+    # compaction output overlapping the keys
+    assert lib.compact_u32(0x10000, 0x90000, 0x10040, 0xA0000, 64, None) == ss.SS_ERR_INVALID_ARG
+    assert lib.compact_u32(0x10000, 0x90000, 0x20000, 0xA0004, 64, None) == ss.SS_ERR_INVALID_ARG
+
+
+def test_bad_enums_and_sizes(lib):
+    assert lib.ss_scan(7, 1, 0, 0x1000, 0x2000, 4, None) == ss.SS_ERR_UNSUPPORTED
+    assert lib.ss_scan(0, 1, 9, 0x1000, 0x2000, 4, None) == ss.SS_ERR_UNSUPPORTED
+    assert lib.compact_u32(0x10000, 0x90000, 0x20000, 0xA0000, 1 << 33, None) == ss.SS_ERR_INVALID_ARG
+    assert lib.ss_set_scan_config(99) == ss.SS_ERR_INVALID_ARG
+    assert lib.ss_debug_set_lookback_fault(-5, 0) == ss.SS_ERR_INVALID_ARG
+
+
+def test_config_table(lib):
+    n = ss.ss_scan_config_count()
+    tiles = []
+    for c in range(n):
+        ss.ss_set_scan_config(c)
+        tiles.append(ss.ss_scan_tile_elems())
+    ss.ss_set_scan_config(0)
+    assert tiles[0] == 4096 and all(t % 128 == 0 for t in tiles)
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(ss, "_lib", None)
+    monkeypatch.setattr(ss, "LIB_PATH", str(tmp_path / "absent.so"))
+    with pytest.raises(ss.LibraryMissing):
+        ss.scan_inclusive_i32(0, 0, 0)

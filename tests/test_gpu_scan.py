@@ -1,0 +1,223 @@
+"""Single-pass look-back scans against the CPU oracle, through the C ABI.
+
+Integer results must match bit for bit (int32 wraps modulo 2^32); fp32
+results must satisfy max_i |y_i - ref_i| / max(1, sum_{j<=i} |x_j|) <= 1e-4
+against the float64 oracle, and be bit-exact on integer-valued inputs whose
+prefixes stay below 2^24.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+import seeded_inputs as si
+from gpu_helpers import (FP32_TOL, Guarded, assert_equal, assert_fp32_close, f32_input,
+                         f32_reference, oracle_scan, poisson_input, run_named_scan, sweep_input,
+                         sweep_reference)
+
+pytestmark = pytest.mark.gpu
+
+TILE = 4096
+SWEEP_MAX = (1 << 30) + 1
+
+
+@pytest.fixture(scope="module")
+def ss():
+    import stream_compaction_pass_gb300 as m
+    m.ss_set_scan_config(0)
+    return m
+
+
+# --- the single-tile case: int32 in [0, 100), seed 0 ----------------------
+
+@pytest.mark.parametrize("inclusive", [True, False])
+def test_single_tile_int32(ss, inclusive):
+    x = si.workload_int_0_100(4096, seed=0)
+    got = run_named_scan("i32", inclusive, x)
+    assert_equal(got, oracle.scan_i32(x, inclusive))
+
+
+# --- the pages' worked examples through the GPU ---------------------------
+
+@pytest.mark.parametrize("kind", ["i32", "u32", "f32"])
+def test_worked_example(ss, kind):
+    x = np.array([3, 1, 7, 0, 4, 1, 6, 3]).astype(np.dtype({"i32": np.int32, "u32": np.uint32, "f32": np.float32}[kind]))
+    assert run_named_scan(kind, True, x).tolist() == [3, 4, 11, 11, 15, 16, 22, 25]
+    assert run_named_scan(kind, False, x).tolist() == [0, 3, 4, 11, 11, 15, 16, 22]
+
+
+# --- int32 exclusive size sweep, seed 2, wraparound -----------------------
+
+def _sweep_sizes():
+    sizes = {1 << k for k in range(10, 31)}
+    for k in (10, 12, 13, 16, 20, 24, 27, 30):
+        sizes |= {(1 << k) - 1, (1 << k) + 1}
+    sizes |= {10 ** k for k in range(3, 10)}
+    return sorted(sizes)
+
+
+@pytest.mark.parametrize("n", _sweep_sizes())
+def test_int32_exclusive_size_sweep(ss, n):
+    x = sweep_input(SWEEP_MAX)[:n]
+    ref = sweep_reference(SWEEP_MAX)[:n]
+    got = run_named_scan("i32", False, x)
+    assert_equal(got, ref)
+
+
+def test_int32_wraparound_happens_and_matches(ss):
+    # 2^30 values of +-1000 drift far enough that partial sums leave the int32
+    # range only with large inputs; force wrapping with big constants too.
+    x = np.full(3 * TILE + 5, 1_900_000_000, dtype=np.int32)
+    got = run_named_scan("i32", True, x)
+    ref = oracle.scan_i32(x, True)
+    assert_equal(got, ref)
+    assert (ref < 0).any()  # it did wrap
+
+
+# --- fp32 at the pages' sizes, seed 1 --------------------------------------
+
+@pytest.mark.parametrize("n", [1_000_000, 10_000_000, 100_000_000])
+@pytest.mark.parametrize("inclusive", [True, False])
+def test_fp32_unit_uniform(ss, n, inclusive):
+    x = f32_input(n)
+    got = run_named_scan("f32", inclusive, x)
+    assert_fp32_close(got, f32_reference(n, inclusive), x)
+
+
+def test_fp32_structured_exact(ss):
+    # Every prefix is an exact integer < 2^24, so any add order is exact.
+    x = si.structured_period4(10_000_000)
+    got = run_named_scan("f32", True, x)
+    assert_equal(got, oracle.scan_f32(x, True).astype(np.float32))
+    assert got[-1] == 12_500_000.0
+    y = si.structured_i_mod_8(1_049_187)
+    for inclusive in (True, False):
+        got = run_named_scan("f32", inclusive, y)
+        assert_equal(got, oracle.scan_f32(y, inclusive).astype(np.float32))
+
+
+# --- uint32 Poisson(8) digit histograms, seed 4, in-place and not ----------
+
+@pytest.mark.parametrize("inplace", [False, True])
+def test_uint32_poisson_counts(ss, inplace):
+    n = 1 << 27
+    x = poisson_input(n)
+    got = run_named_scan("u32", False, x, inplace=inplace)
+    assert_equal(got, oracle.scan_u32(x, False))
+
+
+# --- edge cases --------------------------------------------------------------
+
+EDGE = [1, 2, 3, 4, 5, 31, 32, 33, 127, 128, 129, 511, 512, 513, TILE - 1, TILE, TILE + 1,
+        2 * TILE - 1, 2 * TILE, 2 * TILE + 1, 33 * TILE + 7]
+
+
+@pytest.mark.parametrize("n", EDGE)
+@pytest.mark.parametrize("kind", ["i32", "u32", "f32"])
+def test_edge_sizes(ss, n, kind):
+    if kind == "f32":
+        x = si.structured_i_mod_8(n)  # exact in any order
+    elif kind == "u32":
+        x = si.uniform_u32(n, seed=21)
+    else:
+        x = si.uniform_int32(n, -(1 << 31), (1 << 31) - 1, seed=22)
+    for inclusive in (True, False):
+        got = run_named_scan(kind, inclusive, x)
+        ref = oracle_scan(kind, inclusive, x)
+        assert_equal(got, ref.astype(got.dtype) if kind == "f32" else ref)
+
+
+def test_zero_length(ss):
+    import torch
+    t = torch.empty(0, dtype=torch.int32, device="cuda:0")
+    ss.scan_inclusive_i32(t, t)
+    st, _ = ss.ss_stream_status()
+    assert st == ss.SS_OK
+
+
+@pytest.mark.parametrize("offset", [1, 2, 3])
+def test_misaligned_pointers(ss, offset):
+    n = 5 * TILE + 77
+    x = sweep_input(SWEEP_MAX)[:n]
+    got = run_named_scan("i32", False, x, offset=offset)
+    assert_equal(got, sweep_reference(SWEEP_MAX)[:n])
+
+
+@pytest.mark.parametrize("kind", ["i32", "u32", "f32"])
+def test_in_place(ss, kind):
+    n = 40 * TILE + 3
+    x = {"i32": sweep_input(SWEEP_MAX)[:n], "u32": poisson_input(1 << 27)[:n],
+         "f32": si.structured_i_mod_8(n)}[kind]
+    for inclusive in (True, False):
+        got = run_named_scan(kind, inclusive, x, inplace=True)
+        ref = oracle_scan(kind, inclusive, x)
+        assert_equal(got, ref.astype(got.dtype) if kind == "f32" else ref)
+
+
+@pytest.mark.parametrize("config", range(5))
+def test_every_tile_configuration(ss, config):
+    ss.ss_set_scan_config(config)
+    try:
+        tile = ss.ss_scan_tile_elems()
+        for n in (tile - 1, tile, tile + 1, 17 * tile + 5, 1_000_003):
+            x = sweep_input(SWEEP_MAX)[:n]
+            for inclusive in (True, False):
+                assert_equal(run_named_scan("i32", inclusive, x), oracle.scan_i32(x, inclusive), tile)
+            f = f32_input(n)
+            assert_fp32_close(run_named_scan("f32", True, f), oracle.scan_f32(f, True), f)
+    finally:
+        ss.ss_set_scan_config(0)
+
+
+def test_repeated_launches_are_deterministic_and_epochs_advance(ss):
+    # Many launches of varying size on one workspace: descriptors from a
+    # previous launch must never be taken for this launch's.
+    import torch
+    rng = np.random.default_rng(5)
+    big = sweep_input(SWEEP_MAX)[: 300 * TILE]
+    d_in = torch.from_numpy(big.view(np.int32)).to("cuda:0")
+    d_out = torch.empty_like(d_in)
+    ref = oracle.scan_i32(big, True)
+    for it in range(60):
+        n = int(rng.integers(1, 300 * TILE))
+        ss.scan_inclusive_i32(d_in[:n], d_out[:n])
+        if it % 10 == 9 or n < 2 * TILE:
+            got = d_out[:n].cpu().numpy()
+            assert_equal(got, oracle.scan_i32(big[:n], True))
+    ss.scan_inclusive_i32(d_in, d_out)
+    first = d_out.cpu().numpy()
+    ss.scan_inclusive_i32(d_in, d_out)
+    assert np.array_equal(first, d_out.cpu().numpy())
+    assert_equal(first, ref)
+    assert ss.ss_stream_status()[0] == ss.SS_OK
+
+
+def test_seeded_chunks_compose(ss):
+    import torch
+    n = 10 * TILE + 999
+    x = sweep_input(SWEEP_MAX)[:n]
+    d_in = torch.from_numpy(x.view(np.int32)).to("cuda:0")
+    d_out = torch.empty_like(d_in)
+    carry = torch.zeros(1, dtype=torch.int32, device="cuda:0")
+    cuts = [0, 1, TILE + 3, 3 * TILE, 7 * TILE + 1, n]
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        ss.ss_scan_seeded(ss.SS_I32, False, d_in[a:b], d_out[a:b], carry, carry)
+    assert_equal(d_out.cpu().numpy(), oracle.scan_i32(x, False))
+    assert int(carry.item()) == int(oracle.scan_i32(x, True)[-1])
+
+
+def test_nondefault_stream(ss):
+    import torch
+    s = torch.cuda.Stream()
+    n = 100 * TILE + 1
+    x = sweep_input(SWEEP_MAX)[:n]
+    with torch.cuda.stream(s):
+        d_in = torch.from_numpy(x.view(np.int32)).to("cuda:0")
+        d_out = torch.empty_like(d_in)
+        ss.scan_exclusive_i32(d_in, d_out)
+        st, _ = ss.ss_stream_status(s)
+        assert st == ss.SS_OK
+        got = d_out.cpu().numpy()
+    assert_equal(got, sweep_reference(SWEEP_MAX)[:n])
