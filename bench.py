@@ -297,7 +297,10 @@ def row_rates(torch, ss, stream, dev, xs_d, xf_d, out_d):
         del flags
     del keys, kout
     # context only: torch.cumsum on the same int32 input, timed the same way
-    ms = time_region(torch, stream, lambda: torch.cumsum(xs_d, 0, out=out_d), 20)
+    def cumsum():
+        with torch.cuda.stream(stream):  # torch ops run on torch's current stream
+            torch.cumsum(xs_d, 0, dtype=torch.int32, out=out_d)
+    ms = time_region(torch, stream, cumsum, 20)
     rows["context_torch_cumsum_i32_1e8"] = {"ms": ms, "G-elem/s": N / ms / 1e6}
     return rows
 
