@@ -186,6 +186,31 @@ void ss_shutdown(void);
  */
 ss_status ss_debug_set_lookback_fault(int64_t tile, uint64_t timeout_ns);
 
+/*
+ * Single-pass scan that allocates nothing.  The pages have no counterpart:
+ * it exists for callers that cannot call cudaMalloc -- an application that
+ * serves all device memory from its own pool and forbids other allocations
+ * to keep its accounting exact, or a latency-critical loop that may never
+ * pay for an allocation.  The regular entry points allocate a per-stream
+ * workspace on first use; this one keeps its scratch (tile counter, status
+ * words, tile descriptors) in a fixed device array of 2 MiB + 256 bytes that
+ * every GPU loading the library holds until the process exits.
+ *   dtype, inclusive, in, out, stream: as for ss_scan (SS_ALGO_LOOKBACK);
+ *        out == in is allowed.  The caller passes inputs and outputs.
+ *   n    0 <= n <= 2^30; larger n returns SS_ERR_INVALID_ARG.
+ * The first call on a device sets up that device: it looks up the array's
+ * device address and zeroes it, which synchronises the device; make that
+ * first call before any stream capture.  Every call on a device shares the
+ * array and keeps the previous call's contents; no per-call clearing is
+ * needed (descriptors carry a launch epoch and the tile counter returns to
+ * zero at the end of each launch).  Calls that overlap on the GPU race on
+ * the shared array: serialise them (one stream, or events).  The returned
+ * status is the only error report: device-side look-back timeouts are not
+ * read back by this entry point, nor reported by ss_stream_status().
+ */
+ss_status ss_scan_noalloc(ss_dtype dtype, int inclusive, const void *in, void *out, size_t n,
+                          ss_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

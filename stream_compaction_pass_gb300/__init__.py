@@ -70,6 +70,7 @@ def _declare(lib):
         "ss_stream_status": [P, ctypes.POINTER(I64)],
         "ss_set_scan_config": [I],
         "ss_debug_set_lookback_fault": [I64, U64],
+        "ss_scan_noalloc": [I, I, P, P, SZ, P],
     }
     for name, args in sigs.items():
         f = getattr(lib, name)
@@ -246,3 +247,14 @@ def ss_shutdown() -> None:
 
 def ss_debug_set_lookback_fault(tile: int, timeout_ns: int = 0) -> None:
     _check(lib().ss_debug_set_lookback_fault(tile, timeout_ns), "ss_debug_set_lookback_fault")
+
+
+def ss_scan_noalloc(dtype: int, inclusive: bool, inp, out, n=None, stream=None):
+    """Single-pass scan whose scratch is a fixed device array: allocates
+    nothing (n <= 2^30; the first call on a device sets that device up)."""
+    if n is None:
+        n = _numel(inp)
+    st = lib().ss_scan_noalloc(dtype, int(bool(inclusive)), _addr(inp), _addr(out), n,
+                               _stream(stream, inp, out))
+    if st != SS_OK:
+        raise StreamScanError(st, "ss_scan_noalloc", ss_status_string(st))
