@@ -44,9 +44,10 @@ DATA = ("synthetic: seeded SplitMix64 counter streams; int32 uniform in [-1000, 
         "(seed 2) and fp32 uniform in [0, 1) (seed 1)")
 WORKLOAD = ("device-wide scan, n=1e8 per launch; one step = int32 exclusive + inclusive "
             "and fp32 exclusive + inclusive (4 launches)")
-KERNEL_SOURCES = ["stream_compaction_pass_gb300/csrc/scan.cu", "stream_compaction_pass_gb300/csrc/tile.cuh",
-                  "stream_compaction_pass_gb300/csrc/lookback.cuh"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "k_scan_lookback_n1e8.md")
+KERNEL_SOURCES = ["stream_compaction_pass_gb300/csrc/scan_pipe.cu", "stream_compaction_pass_gb300/csrc/scan.cu",
+                  "stream_compaction_pass_gb300/csrc/scan_body.cuh", "stream_compaction_pass_gb300/csrc/tile.cuh",
+                  "stream_compaction_pass_gb300/csrc/lookback.cuh", "stream_compaction_pass_gb300/csrc/bulk.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "k_scan_lookback_pipe_n1e8.md")
 
 
 def dist_env():
@@ -318,7 +319,8 @@ def run_ours(args) -> None:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     ss.lib()  # fail loudly if the library is missing
-    ss.ss_set_scan_config(args.config)
+    if args.config is not None:
+        ss.ss_set_scan_config(args.config)
 
     xs = si.workload_int_pm1000(N, seed=2)
     xf = si.workload_f32_unit(N, seed=1)
@@ -398,7 +400,7 @@ def run_ours(args) -> None:
     mean_launch_ms = statistics.fmean(launch_ms)
     achieved = BYTES_PER_ELEM * N / (mean_launch_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": recorded_traffic(), "kernel": "k_scan_lookback",
+                "frac": achieved / peak, "traffic": recorded_traffic(), "kernel": "k_scan_lookback_pipe",
                 "bytes_per_launch": BYTES_PER_ELEM * N, "mean_launch_ms": mean_launch_ms,
                 "median_launch_ms": statistics.median(launch_ms), "peak_source": peak_src,
                 "frac_of_nominal_8TBs": achieved / 8000.0}
@@ -434,7 +436,8 @@ def run_ours(args) -> None:
           "config": {"workload": WORKLOAD, "n": N, "elements_per_step": len(launches) * N,
                      "l2": "inputs larger than L2 (400 MB per array vs 129 MB), no flush",
                      "parallelism": "replicas" if world > 1 else "single GPU",
-                     "tile_elems": ss.ss_scan_tile_elems(), "scan_config": args.config},
+                     "tile_elems": ss.ss_scan_tile_elems(),
+                     "scan_config": "library default" if args.config is None else args.config},
           "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
           "gpu_launches": len(launches) * args.steps, "clocks": clocks,
           "GB/s": value * BYTES_PER_ELEM, "rows": rows})
@@ -448,7 +451,8 @@ def main() -> None:
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=0, help="single-pass tile configuration")
+    ap.add_argument("--config", type=int, default=None,
+                    help="single-pass tile configuration (default: the library's)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-rows", action="store_true")

@@ -149,6 +149,24 @@ ss_status ss_scan_host(ss_dtype dtype, int inclusive, const void *h_in, void *h_
 ss_status ss_copy_u32(const uint32_t *in, uint32_t *out, size_t n, ss_stream_t stream);
 
 /*
+ * Diagnostic: the exclusive uint32 (= int32 bits) single-pass scan under
+ * tile configuration `config`, recording a timing trace of every tile's
+ * look-back ("Prefix sum and other parallel patterns", A device-level scan:
+ * how long a tile waits on what earlier tiles published).  d_trace (device,
+ * 8-byte aligned) receives 8 uint64 per tile of that configuration
+ * (ss_scan_tile_elems() after ss_set_scan_config(config)):
+ *   [0] %globaltimer (ns) when the CTA began the tile  [1] aggregate known
+ *   [2] aggregate published   [3] look-back resolved   [4] outputs issued
+ *   [5] descriptor windows read   [6] polls that found an unpublished tile
+ *   [7] SM id (low 32 bits) | CTA index << 32
+ * Rows 0 and 1 and every persistent row have traced builds; others return
+ * SS_ERR_UNSUPPORTED.  A persistent row needs 16-byte aligned in/out and
+ * n above one tile.  The scan result is the same as scan_exclusive_u32's.
+ */
+ss_status ss_scan_trace(int config, const uint32_t *in, uint32_t *out, size_t n, uint64_t *d_trace,
+                        ss_stream_t stream);
+
+/*
  * Waits for `stream`, then returns and clears the device-side status of
  * that stream's workspace: SS_OK, SS_ERR_LOOKBACK_TIMEOUT, or SS_ERR_CUDA if
  * the stream itself failed.  *failing_tile (may be NULL) receives the first
@@ -168,7 +186,8 @@ size_t ss_scan_tile_elems(void);
 int ss_scan_config_count(void);
 
 /* Selects the single-pass scan's tile configuration for later calls in this
- * process (0 = default: 256 threads x 16 elements).  Results do not depend
+ * process (ss_scan_config_count() rows: one CTA per tile, or a persistent
+ * grid streaming tiles through a shared-memory ring).  Results do not depend
  * on it, except for the rounding of fp32 sums. */
 ss_status ss_set_scan_config(int config);
 

@@ -67,6 +67,7 @@ def _declare(lib):
         "ss_scan_seeded": [I, I, P, P, SZ, P, P, P],
         "ss_scan_host": [I, I, P, P, SZ, P],
         "ss_copy_u32": [P, P, SZ, P],
+        "ss_scan_trace": [I, P, P, SZ, P, P],
         "ss_stream_status": [P, ctypes.POINTER(I64)],
         "ss_set_scan_config": [I],
         "ss_debug_set_lookback_fault": [I64, U64],
@@ -209,6 +210,14 @@ def ss_copy_u32(inp, out, n=None, stream=None):
     if n is None:
         n = _numel(inp)
     _check(lib().ss_copy_u32(_addr(inp), _addr(out), n, _stream(stream, inp, out)), "ss_copy_u32")
+
+
+def ss_scan_trace(config: int, inp, out, trace, n=None, stream=None):
+    """Exclusive uint32 scan recording 8 uint64 per tile of look-back timing."""
+    if n is None:
+        n = _numel(inp)
+    _check(lib().ss_scan_trace(config, _addr(inp), _addr(out), n, _addr(trace),
+                               _stream(stream, inp, out)), "ss_scan_trace")
 
 
 def ss_stream_status(stream=None):

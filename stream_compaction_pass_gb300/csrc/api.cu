@@ -20,7 +20,7 @@ using ss::Dtype;
 
 thread_local std::string g_detail;
 
-std::atomic<int> g_config{0};
+std::atomic<int> g_config{ss::scan_default_config()};
 std::atomic<int64_t> g_fault_tile{-1};
 std::atomic<uint64_t> g_timeout_ns{0};
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
@@ -175,11 +175,10 @@ ss_status check_scan_args(const void* in, const void* out, size_t n, size_t tile
 ss_status scan_lookback(Dtype dt, bool inclusive, const void* in, void* out, size_t n,
                         const void* carry_in, void* carry_out, cudaStream_t s) {
     const int cfg = g_config.load();
-    const size_t tile = ss::scan_config(cfg).tile();
-    ss_status st = check_scan_args(in, out, n, tile);
+    ss_status st = check_scan_args(in, out, n, ss::kMinScanTile);
     if (st != SS_OK) return st;
     if (n == 0) return SS_OK;
-    const size_t tiles = (n + tile - 1) / tile;
+    const size_t tiles = (n + ss::kMinScanTile - 1) / ss::kMinScanTile;  // the most any kernel uses
     Workspace* w = nullptr;
     if (tiles > 1 || g_fault_tile.load() >= 0) {
         st = get_workspace(s, &w);
@@ -301,6 +300,30 @@ ss_status ss_scan(ss_dtype dtype, int inclusive, ss_algo algo, const void* in, v
     return e == cudaSuccess ? SS_OK : cuda_fail(e, "reduce-then-scan launch");
 }
 
+ss_status ss_scan_trace(int config, const uint32_t* in, uint32_t* out, size_t n, uint64_t* d_trace,
+                        ss_stream_t stream) {
+    cudaStream_t s = (cudaStream_t)stream;
+    if (config < 0 || config >= ss::scan_config_count())
+        return fail(SS_ERR_INVALID_ARG, "no such configuration");
+    ss_status st = check_scan_args(in, out, n, ss::kMinScanTile);
+    if (st != SS_OK) return st;
+    if (n == 0) return SS_OK;
+    if (d_trace == nullptr || (reinterpret_cast<uintptr_t>(d_trace) & 7u))
+        return fail(SS_ERR_INVALID_ARG, "trace must be a non-null, 8-byte aligned device pointer");
+    const ss::ScanConfig c = ss::scan_config(config);
+    if (!c.persistent && config > 1) return fail(SS_ERR_UNSUPPORTED, "no traced build of this configuration");
+    if (c.persistent && (n <= c.tile() || ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) & 15u)))
+        return fail(SS_ERR_INVALID_ARG, "a persistent trace needs 16-byte aligned in/out and more than one tile");
+    Workspace* w = nullptr;
+    st = get_workspace(s, &w);
+    if (st != SS_OK) return st;
+    st = ensure_desc(w, (n + ss::kMinScanTile - 1) / ss::kMinScanTile);
+    if (st != SS_OK) return st;
+    cudaError_t e = ss::launch_scan_trace(config, in, out, n, make_ws(w),
+                                          reinterpret_cast<unsigned long long*>(d_trace), s);
+    return e == cudaSuccess ? SS_OK : cuda_fail(e, "trace launch");
+}
+
 ss_status ss_copy_u32(const uint32_t* in, uint32_t* out, size_t n, ss_stream_t stream) {
     ss_status st = check_scan_args(in, out, n, ss::scan_config(g_config.load()).tile());
     if (st != SS_OK) return st;
@@ -336,6 +359,8 @@ ss_status ss_stream_status(ss_stream_t stream, int64_t* failing_tile) {
         cudaStreamSynchronize(s);
         return fail(SS_ERR_CUDA, "tile counter out of step with the launch (concurrent use of one stream's workspace?)");
     }
+    if (words[0] & ss::kErrBulkTimeout)
+        return fail(SS_ERR_CUDA, "a bulk copy into shared memory did not complete in time");
     if (words[0] & ss::kErrLookbackTimeout) {
         if (failing_tile) *failing_tile = words[1] ? (int64_t)words[1] - 1 : -1;
         return fail(SS_ERR_LOOKBACK_TIMEOUT, "a look-back wait ran out");

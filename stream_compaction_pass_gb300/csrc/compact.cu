@@ -146,7 +146,8 @@ k_compact_u32(const uint32_t* keys, const uint8_t* flags, uint32_t* out,
             failed = true;
         } else {
             if (lane == 0) st_relaxed_u64(ctx.desc + tile, pack_desc(epoch, kStateA, tile_count));
-            excl = lookback<uint32_t>(ctx, tile, epoch, lane, &failed);
+            compiler_fence();  // publish before looking back
+            excl = lookback<uint32_t, 4>(ctx, tile, epoch, lane, &failed);
             if (lane == 0) {
                 if (!failed) {
                     st_relaxed_u64(ctx.desc + tile, pack_desc(epoch, kStateP, excl + tile_count));

@@ -12,7 +12,8 @@ enum class Dtype : int { I32 = 0, U32 = 1, F32 = 2 };
 
 // Status word bits written by kernels and read back by ss_stream_status.
 constexpr uint32_t kErrLookbackTimeout = 1u;
-constexpr uint32_t kErrCounter = 2u;  // a CTA claimed a tile id past the grid
+constexpr uint32_t kErrCounter = 2u;      // a CTA claimed a tile id past the grid
+constexpr uint32_t kErrBulkTimeout = 4u;  // a bulk copy into shared memory never completed
 
 // Device pointers into a workspace for the single-pass kernels.
 struct LookbackWs {
@@ -24,16 +25,41 @@ struct LookbackWs {
     int64_t fault_tile = -1;                // test hook: tile that never publishes
 };
 
-// Tile geometry of a single-pass scan configuration.
+// A single-pass scan configuration: which kernel, its tile geometry and
+// its look-back window.
 struct ScanConfig {
+    int persistent;  // 0: one CTA per tile (scan.cu); 1: persistent, bulk-copy ring (scan_pipe.cu)
     int threads;
-    int items;  // per thread, a multiple of 4
+    int items;       // per thread, a multiple of 4
+    int stages;      // ring depth of the persistent kernel
+    int lookback_k;  // look-back window = 32 * lookback_k descriptors per poll
     size_t tile() const { return (size_t)threads * (size_t)items; }
 };
 
-// Selectable scan configurations (index 0 is the default).
+// Selectable scan configurations.  Index 0 (one CTA per 4096-element tile,
+// 32-descriptor window) is fixed; scan_default_config() is the one the
+// library starts with.
 int scan_config_count();
 ScanConfig scan_config(int idx);
+int scan_default_config();
+
+// Smallest tile of any configuration: workspaces are sized with it, so a
+// launch that falls back to a smaller tile still has a descriptor per tile.
+constexpr size_t kMinScanTile = 4096;
+
+// The persistent variant of launch_scan_lookback (scan_pipe.cu); `config`
+// must name a persistent configuration and in/out must be 16-byte aligned.
+cudaError_t launch_scan_lookback_pipe(Dtype dt, bool inclusive, int config, const void* in, void* out,
+                                      size_t n, const LookbackWs& ws, const void* carry_in,
+                                      void* carry_out, cudaStream_t s);
+
+// Exclusive uint32 scan with a per-tile timing trace (8 x uint64 per tile,
+// layout in scan_body.cuh).  Rows 0, 1 and the persistent rows have traced
+// builds; others return cudaErrorInvalidValue.
+cudaError_t launch_scan_trace(int config, const void* in, void* out, size_t n, const LookbackWs& ws,
+                              unsigned long long* trace, cudaStream_t s);
+cudaError_t launch_scan_trace_pipe(int config, const void* in, void* out, size_t n,
+                                   const LookbackWs& ws, unsigned long long* trace, cudaStream_t s);
 
 // Single-pass decoupled look-back scan.  `carry_in` (device, may be null)
 // seeds the prefix of element 0; `carry_out` (device, may be null) receives

@@ -51,6 +51,15 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
     return v;
 }
 
+// Compiler-only barrier: no instruction, but no memory access moves across
+// it.  Placed after a descriptor is published so that the publishing store is
+// emitted before the code that follows (a look-back loop in the same warp):
+// without it the compiler was free to sink the store of a tile's aggregate
+// below that tile's own look-back, which hides the aggregate from successors
+// until the look-back ends and turns the decoupled chain back into a serial
+// one (measured: 2.9x slower).
+__device__ __forceinline__ void compiler_fence() { asm volatile("" ::: "memory"); }
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -108,33 +117,65 @@ __device__ __forceinline__ void record_error(uint32_t* status, uint32_t bits, ui
 }
 
 // Look-back for tile `tile` > 0, run by all 32 lanes of one warp after the
-// tile's aggregate A was published.  Reads predecessors' descriptors 32 at a
-// time (lane i reads tile - 1 - i - 32k), waits while any descriptor up to
-// the nearest P is still X, and sums values back to and including that P.
-// Returns the tile's exclusive prefix in every lane; sets *failed (warp
-// uniform) if the wait ran out or a predecessor was poisoned.
-template <typename T>
+// tile's aggregate A was published.  Each poll reads a window of 32*K
+// predecessors' descriptors (lane l reads tiles pred - K*l - q, q = 0..K-1,
+// so lane order is distance order), waits while any descriptor up to the
+// nearest P is still X, and sums values back to and including that P; with
+// no P in the window it sums the whole window and moves 32*K tiles further
+// back.  Returns the tile's exclusive prefix in every lane; sets *failed
+// (warp uniform) if the wait ran out or the nearest stop was poisoned.
+// Counters one look-back fills in when a trace is taken.
+struct LookbackStats {
+    uint32_t windows;  // windows read
+    uint32_t waits;    // polls that found an unpublished predecessor
+};
+
+//
+// `floor` (optional) is a tile whose inclusive prefix `floor_value` the caller
+// already knows (a persistent CTA's own previous tile); the walk treats it as
+// a published P and never reads at or below it.  Without a floor, tile -1
+// plays that role with value 0.
+template <typename T, int K, bool TRACE = false>
 __device__ __forceinline__ T lookback(const LookbackCtx& c, uint32_t tile, uint32_t epoch, int lane,
-                                      bool* failed) {
+                                      bool* failed, LookbackStats* stats = nullptr,
+                                      int64_t floor = -1, T floor_value = T(0)) {
     const uint32_t tag = epoch << 2;
+    const unsigned long long floor_desc = pack_desc(epoch, kStateP, to_bits<T>(floor_value));
+    if (TRACE) *stats = LookbackStats{0u, 0u};
     T acc = T(0);
     int64_t pred = (int64_t)tile - 1;
     uint32_t polls = 0;
     uint64_t t0 = 0;
     *failed = false;
     while (true) {
-        const int64_t idx = pred - lane;
-        unsigned long long d = idx >= 0 ? ld_relaxed_u64(c.desc + idx)
-                                        : pack_desc(epoch, kStateP, 0u);
-        const uint32_t hi = (uint32_t)(d >> 32);
-        const uint32_t state = ((hi & ~3u) == tag) ? (hi & 3u) : kStateX;
-        const uint32_t stop_mask = __ballot_sync(kFullMask, state == kStateP || state == kStatePoison);
+        unsigned long long d[K];
+        uint32_t st[K];
+#pragma unroll
+        for (int q = 0; q < K; ++q) {
+            const int64_t idx = pred - (int64_t)lane * K - q;
+            d[q] = idx > floor ? ld_relaxed_u64(c.desc + idx) : floor_desc;
+        }
+#pragma unroll
+        for (int q = 0; q < K; ++q) {
+            const uint32_t hi = (uint32_t)(d[q] >> 32);
+            st[q] = ((hi & ~3u) == tag) ? (hi & 3u) : kStateX;
+        }
+        int qs = K;  // this lane's nearest stop (P or POISON), K if none
+#pragma unroll
+        for (int q = K - 1; q >= 0; --q)
+            if (st[q] == kStateP || st[q] == kStatePoison) qs = q;
+        bool lane_x = false;  // an unpublished descriptor before this lane's stop
+#pragma unroll
+        for (int q = 0; q < K; ++q)
+            if (q < qs && st[q] == kStateX) lane_x = true;
+        if (TRACE) stats->windows += 1;
+        const uint32_t stop_mask = __ballot_sync(kFullMask, qs < K);
         const int first = stop_mask ? __ffs(stop_mask) - 1 : 31;
         const uint32_t upto = (first == 31) ? kFullMask : ((2u << first) - 1u);
-        const uint32_t x_mask = __ballot_sync(kFullMask, state == kStateX) & upto;
-        if (x_mask) {
+        if (__ballot_sync(kFullMask, lane_x) & upto) {
             // A predecessor up to the nearest P has not published yet: wait.
             ++polls;
+            if (TRACE) stats->waits += 1;
             if (polls == 1) t0 = globaltimer_ns();
             if (polls > 4) __nanosleep(polls < 16 ? 32 : (polls < 64 ? 128 : 256));
             bool give_up = polls >= c.max_polls || (globaltimer_ns() - t0) > c.timeout_ns;
@@ -145,15 +186,25 @@ __device__ __forceinline__ T lookback(const LookbackCtx& c, uint32_t tile, uint3
             }
             continue;
         }
-        const uint32_t poison_mask = __ballot_sync(kFullMask, state == kStatePoison) & upto;
-        if (poison_mask) {
-            *failed = true;
-            return T(0);
+        if (stop_mask) {
+            bool poisoned = false;
+#pragma unroll
+            for (int q = 0; q < K; ++q)
+                if (q == qs && st[q] == kStatePoison) poisoned = true;
+            if ((__ballot_sync(kFullMask, poisoned) >> first) & 1u) {
+                *failed = true;
+                return T(0);
+            }
         }
-        T v = (lane <= first) ? from_bits<T>((uint32_t)d) : T(0);
+        T v = T(0);
+        const bool whole = (stop_mask == 0) || lane < first;
+        const bool part = (stop_mask != 0) && lane == first;
+#pragma unroll
+        for (int q = 0; q < K; ++q)
+            if (whole || (part && q <= qs)) v += from_bits<T>((uint32_t)d[q]);
         acc += warp_sum(v);
         if (stop_mask) return acc;
-        pred -= 32;
+        pred -= 32 * K;
         polls = 0;
     }
 }

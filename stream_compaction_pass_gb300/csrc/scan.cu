@@ -15,24 +15,23 @@
 // int32 and uint32 share the uint32 kernels: two's-complement addition and
 // unsigned addition produce the same bits.
 #include "internal.h"
-#include "tile.cuh"
+#include "scan_body.cuh"
 
 namespace ss {
 
-template <typename T, bool INCLUSIVE, int THREADS, int VPT>
+template <typename T, bool INCLUSIVE, int THREADS, int VPT, int K, bool TRACE>
 __global__ void __launch_bounds__(THREADS)
 k_scan_lookback(const T* in, T* out, size_t n, uint32_t num_tiles, LookbackCtx ctx, bool aligned,
-                const T* carry_in, T* carry_out) {
-    constexpr int WARPS = THREADS / 32;
+                const T* carry_in, T* carry_out, unsigned long long* trace) {
     constexpr size_t TILE = (size_t)THREADS * VPT * 4;
     constexpr size_t SEG = (size_t)32 * VPT * 4;  // elements per warp segment
 
-    __shared__ T s_warp[WARPS];
-    __shared__ T s_prefix;
-    __shared__ uint32_t s_tile, s_epoch, s_fail;
+    __shared__ ScanSmem<T, THREADS / 32> sm;
+    __shared__ uint32_t s_tile, s_epoch;
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
+    const unsigned long long t_begin = TRACE ? globaltimer_ns() : 0ull;
 
     if (threadIdx.x == 0) {
         uint32_t tile = 0, epoch = 0;
@@ -47,58 +46,15 @@ k_scan_lookback(const T* in, T* out, size_t n, uint32_t num_tiles, LookbackCtx c
         if (threadIdx.x == 0) record_error(ctx.status, kErrCounter, tile);
         return;
     }
+    unsigned long long* rec = TRACE ? trace + (size_t)tile * kTraceWords : nullptr;
+    if (TRACE && threadIdx.x == 0) rec[0] = t_begin;
 
-    const size_t tile_base = (size_t)tile * TILE;
-    const size_t seg = tile_base + (size_t)warp * SEG;
+    const size_t seg = (size_t)tile * TILE + (size_t)warp * SEG;
     const bool fast = aligned && (seg + SEG <= n);
-
     T v[VPT][4];
     load_rows<T, VPT>(in, n, seg, lane, fast, v);
-
-    T pre[VPT];
-    const T warp_total = warp_rows_scan<T, VPT>(v, lane, pre);
-    T warp_prefix, block_total;
-    block_combine<T, WARPS>(warp_total, warp, lane, s_warp, &warp_prefix, &block_total);
-
-    if (warp == 0) {
-        T excl = T(0);
-        bool failed = false;
-        const bool dead = (int64_t)tile == ctx.fault_tile;  // test hook only
-        if (tile == 0) {
-            excl = carry_in ? *carry_in : T(0);
-            if (num_tiles > 1 && lane == 0 && !dead)
-                st_relaxed_u64(ctx.desc, pack_desc(epoch, kStateP, to_bits<T>(excl + block_total)));
-            failed = dead;
-        } else if (dead) {
-            failed = true;  // publishes nothing, so successors must time out
-        } else {
-            if (lane == 0)
-                st_relaxed_u64(ctx.desc + tile, pack_desc(epoch, kStateA, to_bits<T>(block_total)));
-            excl = lookback<T>(ctx, tile, epoch, lane, &failed);
-            if (lane == 0) {
-                if (!failed) {
-                    st_relaxed_u64(ctx.desc + tile,
-                                   pack_desc(epoch, kStateP, to_bits<T>(excl + block_total)));
-                } else {
-                    st_relaxed_u64(ctx.desc + tile, pack_desc(epoch, kStatePoison, 0u));
-                    record_error(ctx.status, kErrLookbackTimeout, tile);
-                }
-            }
-        }
-        if (lane == 0) {
-            s_prefix = excl;
-            s_fail = failed ? 1u : 0u;
-        }
-    }
-    __syncthreads();
-    if (s_fail) return;
-
-    T y[VPT][4];
-    rows_output<T, VPT, INCLUSIVE>(v, pre, s_prefix + warp_prefix, y);
-    store_rows<T, VPT>(out, n, seg, lane, fast, y);
-
-    if (carry_out != nullptr && tile == num_tiles - 1 && threadIdx.x == 0)
-        *carry_out = s_prefix + block_total;
+    scan_tile_body<T, INCLUSIVE, THREADS, VPT, K, TRACE>(v, out, n, seg, fast, tile, num_tiles, epoch,
+                                                         ctx, carry_in, carry_out, sm, rec);
 }
 
 template <int THREADS, int VPT>
@@ -115,32 +71,41 @@ k_copy_probe(const uint32_t* in, uint32_t* out, size_t n, bool aligned) {
     store_rows<uint32_t, VPT>(out, n, seg, lane, fast, v);
 }
 
-// Configurations: {threads, items per thread}.  Index 0 is the default.
+// Configurations: {persistent, threads, items, stages, look-back K}.
 static const ScanConfig kConfigs[] = {
-    {256, 16},  // 4096-element tiles
-    {256, 32},  // 8192
-    {512, 16},  // 8192
-    {128, 32},  // 4096
-    {256, 24},  // 6144
+    {0, 256, 16, 0, 1},  // 0: one CTA per 4096-element tile, 32-descriptor window
+    {0, 256, 32, 0, 1},  // 1: one CTA per 8192-element tile
+    {0, 512, 16, 0, 1},  // 2: 8192, 512 threads
+    {0, 256, 32, 0, 2},  // 3: 8192, 64-descriptor window
+    {0, 512, 16, 0, 2},  // 4: 8192, 512 threads, 64
+    {1, 512, 32, 2, 1},  // 5: persistent, 16384-element tiles, 2-stage ring (128 KB), 32
+    {1, 512, 32, 3, 1},  // 6: persistent, 16384, 3 stages (192 KB), 32
+    {1, 512, 16, 3, 1},  // 7: persistent, 8192, 3 stages (96 KB, two CTAs per SM), 32
+    {1, 512, 32, 2, 2},  // 8: persistent, 16384, 2 stages, 64
+    {1, 512, 24, 3, 1},  // 9: persistent, 12288, 3 stages (144 KB), 32
+    {1, 1024, 16, 2, 1}, // 10: persistent, 16384, 1024 threads, 2 stages, 32
 };
 constexpr int kNumConfigs = sizeof(kConfigs) / sizeof(kConfigs[0]);
+constexpr int kDefaultConfig = 5;
 
 int scan_config_count() { return kNumConfigs; }
 ScanConfig scan_config(int idx) { return kConfigs[(idx >= 0 && idx < kNumConfigs) ? idx : 0]; }
+int scan_default_config() { return kDefaultConfig; }
 
 static bool aligned16(const void* a, const void* b) {
     return ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b)) & 15u) == 0;
 }
 
-template <typename T, bool INCL, int THREADS, int VPT>
+template <typename T, bool INCL, int THREADS, int VPT, int K, bool TRACE = false>
 static cudaError_t launch_one(const void* in, void* out, size_t n, const LookbackWs& ws,
-                             const void* carry_in, void* carry_out, cudaStream_t s) {
+                             const void* carry_in, void* carry_out, cudaStream_t s,
+                             unsigned long long* trace = nullptr) {
     const size_t tile = (size_t)THREADS * VPT * 4;
     const uint32_t tiles = (uint32_t)((n + tile - 1) / tile);
     LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};
-    k_scan_lookback<T, INCL, THREADS, VPT><<<tiles, THREADS, 0, s>>>(
+    k_scan_lookback<T, INCL, THREADS, VPT, K, TRACE><<<tiles, THREADS, 0, s>>>(
         static_cast<const T*>(in), static_cast<T*>(out), n, tiles, ctx, aligned16(in, out),
-        static_cast<const T*>(carry_in), static_cast<T*>(carry_out));
+        static_cast<const T*>(carry_in), static_cast<T*>(carry_out), trace);
     return cudaGetLastError();
 }
 
@@ -148,22 +113,50 @@ template <typename T, bool INCL>
 static cudaError_t dispatch_config(int config, const void* in, void* out, size_t n,
                                    const LookbackWs& ws, const void* ci, void* co, cudaStream_t s) {
     switch (config) {
-        case 1: return launch_one<T, INCL, 256, 8>(in, out, n, ws, ci, co, s);
-        case 2: return launch_one<T, INCL, 512, 4>(in, out, n, ws, ci, co, s);
-        case 3: return launch_one<T, INCL, 128, 8>(in, out, n, ws, ci, co, s);
-        case 4: return launch_one<T, INCL, 256, 6>(in, out, n, ws, ci, co, s);
-        default: return launch_one<T, INCL, 256, 4>(in, out, n, ws, ci, co, s);
+        case 1: return launch_one<T, INCL, 256, 8, 1>(in, out, n, ws, ci, co, s);
+        case 2: return launch_one<T, INCL, 512, 4, 1>(in, out, n, ws, ci, co, s);
+        case 3: return launch_one<T, INCL, 256, 8, 2>(in, out, n, ws, ci, co, s);
+        case 4: return launch_one<T, INCL, 512, 4, 2>(in, out, n, ws, ci, co, s);
+        default: return launch_one<T, INCL, 256, 4, 1>(in, out, n, ws, ci, co, s);
     }
+}
+
+// The persistent kernel needs 16-byte aligned in/out (bulk copies) and at
+// least two tiles; anything else runs on the one-CTA-per-tile kernel of the
+// same tile size, or on configuration 0.
+static int per_tile_fallback(int config) {
+    (void)config;
+    return 1;  // 8192-element tiles, the fastest one-CTA-per-tile row
 }
 
 cudaError_t launch_scan_lookback(Dtype dt, bool inclusive, int config, const void* in, void* out,
                                  size_t n, const LookbackWs& ws, const void* carry_in,
                                  void* carry_out, cudaStream_t s) {
+    const ScanConfig c = scan_config(config);
+    if (c.persistent) {
+        if (aligned16(in, out) && n > c.tile())
+            return launch_scan_lookback_pipe(dt, inclusive, config, in, out, n, ws, carry_in, carry_out, s);
+        config = per_tile_fallback(config);
+    }
     if (dt == Dtype::F32)
         return inclusive ? dispatch_config<float, true>(config, in, out, n, ws, carry_in, carry_out, s)
                          : dispatch_config<float, false>(config, in, out, n, ws, carry_in, carry_out, s);
     return inclusive ? dispatch_config<uint32_t, true>(config, in, out, n, ws, carry_in, carry_out, s)
                      : dispatch_config<uint32_t, false>(config, in, out, n, ws, carry_in, carry_out, s);
+}
+
+cudaError_t launch_scan_trace(int config, const void* in, void* out, size_t n, const LookbackWs& ws,
+                              unsigned long long* trace, cudaStream_t s) {
+    const ScanConfig c = scan_config(config);
+    if (c.persistent) {
+        if (!aligned16(in, out) || n <= c.tile()) return cudaErrorInvalidValue;
+        return launch_scan_trace_pipe(config, in, out, n, ws, trace, s);
+    }
+    switch (config) {
+        case 1: return launch_one<uint32_t, false, 256, 8, 1, true>(in, out, n, ws, nullptr, nullptr, s, trace);
+        case 0: return launch_one<uint32_t, false, 256, 4, 1, true>(in, out, n, ws, nullptr, nullptr, s, trace);
+        default: return cudaErrorInvalidValue;  // traced builds exist for rows 0, 1 and the persistent rows
+    }
 }
 
 template <int THREADS, int VPT>
@@ -177,13 +170,8 @@ static cudaError_t launch_copy(const void* in, void* out, size_t n, cudaStream_t
 }
 
 cudaError_t launch_copy_probe(int config, const void* in, void* out, size_t n, cudaStream_t s) {
-    switch (config) {
-        case 1: return launch_copy<256, 8>(in, out, n, s);
-        case 2: return launch_copy<512, 4>(in, out, n, s);
-        case 3: return launch_copy<128, 8>(in, out, n, s);
-        case 4: return launch_copy<256, 6>(in, out, n, s);
-        default: return launch_copy<256, 4>(in, out, n, s);
-    }
+    (void)config;  // one geometry: 256 threads x 16 elements, the scan's default loader shape
+    return launch_copy<256, 4>(in, out, n, s);
 }
 
 }  // namespace ss

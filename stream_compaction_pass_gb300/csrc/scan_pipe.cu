@@ -1,0 +1,298 @@
+// scan_pipe.cu -- the single-pass look-back scan as a persistent kernel fed
+// by the bulk-copy engine.
+//
+// The one-CTA-per-tile kernel (scan.cu) stops loading while a tile waits in
+// its look-back, and with thousands of small tiles in flight each look-back
+// walks far back to the last published inclusive prefix.  Here a grid of one
+// or two CTAs per SM streams large tiles through a shared-memory ring: the
+// bulk-copy engine (cp.async.bulk, one instruction per tile, completion
+// counted on an mbarrier) fills the next STAGES-1 tiles while the CTA scans,
+// looks back and stores the current one.
+//
+// Schedule: each CTA takes a rank r from the workspace counter when it
+// starts, then processes tiles r, r + G, r + 2G, ... (G = grid size).  Ranks
+// are handed out in start order, so the CTA owning the smallest unfinished
+// tile has always started and reaches that tile after finishing its own
+// smaller ones: every look-back wait ends without relying on all CTAs being
+// resident.  Consecutive tiles belong to different CTAs and are processed at
+// about the same time, and no atomic sits inside the loop.
+//
+// The per-tile arithmetic is the same as scan.cu's (scan_body.cuh).  Reading
+// the ring back is conflict-free: lane l of a warp reads the l-th 16-byte
+// vector of a 512-byte row.
+#include "bulk.cuh"
+#include "internal.h"
+#include "scan_body.cuh"
+
+namespace ss {
+
+template <typename T, bool INCLUSIVE, int THREADS, int VPT, int STAGES, int K, bool TRACE>
+__global__ void __launch_bounds__(THREADS, 1)
+k_scan_lookback_pipe(const T* in, T* out, size_t n, uint32_t num_tiles, LookbackCtx ctx,
+                     const T* carry_in, T* carry_out, unsigned long long* trace) {
+    static_assert(STAGES >= 2, "the ring needs two stages at least");
+    constexpr int WARPS = THREADS / 32;
+    constexpr uint32_t TILE = (uint32_t)THREADS * VPT * 4;
+    constexpr uint32_t TILE_BYTES = TILE * (uint32_t)sizeof(T);
+    constexpr uint32_t SEG = 32u * VPT * 4;
+
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    T* ring = reinterpret_cast<T*>(smem_raw);
+    __shared__ __align__(8) uint64_t bars[STAGES];
+    __shared__ ScanSmem<T, WARPS> sm;
+    __shared__ uint32_t s_rank, s_epoch;
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const uint32_t G = gridDim.x;
+    const uint64_t policy = policy_evict_first();
+
+    if (threadIdx.x == 0) {
+        uint32_t rank, epoch;
+        claim_tile(ctx.counter, G, &rank, &epoch);  // one claim per CTA; the last resets the counter
+        s_rank = rank;
+        s_epoch = epoch;
+        for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
+        fence_async_shared();
+    }
+    __syncthreads();
+    const uint32_t rank = s_rank;
+    const uint32_t epoch = s_epoch;
+    if (rank >= G) {  // counter out of step: never index past the descriptors
+        if (threadIdx.x == 0) record_error(ctx.status, kErrCounter, rank);
+        return;
+    }
+    // This CTA's tiles: rank + k*G for k = 0 .. count-1.
+    const uint32_t count = rank < num_tiles ? (num_tiles - rank + G - 1) / G : 0;
+    uint32_t issued = 0, fetched = 0;  // thread 0: copies started / tiles read from the ring
+
+    auto issue = [&](uint32_t k) {  // thread 0: start the copy of this CTA's k-th tile
+        const int s = (int)(k % STAGES);
+        const size_t base = (size_t)(rank + k * G) * TILE;
+        if (base + TILE <= n) {
+            fence_async_shared();  // earlier reads of this stage before the copy's writes
+            mbar_arrive_expect_tx(&bars[s], TILE_BYTES);
+            bulk_load(ring + (size_t)s * TILE, in + base, TILE_BYTES, &bars[s], policy);
+        } else {
+            mbar_arrive(&bars[s]);  // ragged last tile: read from global by the consumers
+        }
+        issued = k + 1;
+    };
+
+    // Reads the k-th tile into v, frees its stage and starts the copy of tile
+    // k + STAGES.  False (CTA-uniform) if the copy did not arrive in time.
+    auto fetch = [&](uint32_t k, T (&v)[VPT][4]) -> bool {
+        const uint32_t t = rank + k * G;
+        const int s = (int)(k % STAGES);
+        const size_t tile_base = (size_t)t * TILE;
+        if (TRACE && threadIdx.x == 0) trace[(size_t)t * kTraceWords] = globaltimer_ns();
+        const bool ok = mbar_wait_bounded(&bars[s], (k / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
+        if (__syncthreads_or(!ok)) {
+            if (threadIdx.x == 0) record_error(ctx.status, kErrBulkTimeout, t);
+            return false;
+        }
+        if (tile_base + TILE <= n) {
+            const T* src = ring + (size_t)s * TILE + (size_t)warp * SEG + (size_t)lane * 4;
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const uint4 r = lds_vec(src + 128 * j);
+                v[j][0] = from_bits<T>(r.x);
+                v[j][1] = from_bits<T>(r.y);
+                v[j][2] = from_bits<T>(r.z);
+                v[j][3] = from_bits<T>(r.w);
+            }
+        } else {
+            load_rows<T, VPT>(in, n, tile_base + (size_t)warp * SEG, lane, false, v);
+        }
+        __syncthreads();  // stage s has been read
+        if (threadIdx.x == 0) {
+            fetched = k + 1;
+            if (k + STAGES < count) issue(k + STAGES);
+        }
+        return true;
+    };
+
+    // Sums tile t (rows v) and publishes its aggregate at once: A, or P for
+    // tile 0 (whose prefix is the seed).
+    auto reduce_publish = [&](uint32_t t, const T (&v)[VPT][4], T* wp, T* agg) {
+        T x = T(0);
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) x += ((v[j][0] + v[j][1]) + v[j][2]) + v[j][3];
+        block_combine<T, WARPS>(warp_sum(x), warp, lane, sm.warp, wp, agg);
+        if (threadIdx.x == 0 && (int64_t)t != ctx.fault_tile) {
+            if (t == 0) {
+                if (num_tiles > 1)
+                    st_relaxed_u64(ctx.desc, pack_desc(epoch, kStateP,
+                                                       to_bits<T>((carry_in ? *carry_in : T(0)) + *agg)));
+            } else {
+                st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStateA, to_bits<T>(*agg)));
+            }
+            if (TRACE) {
+                unsigned long long* rec = trace + (size_t)t * kTraceWords;
+                rec[1] = rec[2] = globaltimer_ns();
+            }
+        }
+    };
+
+    T wp_cur = T(0), agg_cur = T(0);  // warp prefix and aggregate of the current tile
+    T prev_incl = T(0);               // warp 0: inclusive prefix through this CTA's previous tile
+    uint32_t fail_at = 0xffffffffu;
+
+    // One iteration: fetch + reduce + publish tile k+1, look back for tile
+    // k and scan it, store it.  vc holds tile k, vn receives tile k+1.
+    auto step = [&](uint32_t k, T (&vc)[VPT][4], T (&vn)[VPT][4]) -> bool {
+        const uint32_t t = rank + k * G;
+        T wp_next = T(0), agg_next = T(0);
+        if (k + 1 < count) {
+            if (!fetch(k + 1, vn)) {
+                fail_at = k;
+                return false;
+            }
+            reduce_publish(t + G, vn, &wp_next, &agg_next);
+        }
+        compiler_fence();  // the aggregate just published stays ahead of the look-back
+        if (warp == 0) {
+            LookbackStats stats{0u, 0u};
+            T excl = T(0);
+            bool failed = false;
+            const bool dead = (int64_t)t == ctx.fault_tile;  // test hook only
+            if (t == 0) {
+                excl = carry_in ? *carry_in : T(0);
+                failed = dead;
+            } else if (dead) {
+                failed = true;  // it published nothing, so its successors' waits run out
+            } else {
+                // The walk stops at this CTA's previous tile at the latest.
+                const int64_t floor = k > 0 ? (int64_t)t - (int64_t)G : -1;
+                excl = lookback<T, K, TRACE>(ctx, t, epoch, lane, &failed, &stats, floor, prev_incl);
+                if (lane == 0) {
+                    if (!failed) {
+                        st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStateP, to_bits<T>(excl + agg_cur)));
+                    } else {
+                        st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStatePoison, 0u));
+                        record_error(ctx.status, kErrLookbackTimeout, t);
+                    }
+                }
+            }
+            prev_incl = excl + agg_cur;
+            if (lane == 0) {
+                sm.prefix = excl;
+                sm.fail = failed ? 1u : 0u;
+                if (TRACE) {
+                    unsigned long long* rec = trace + (size_t)t * kTraceWords;
+                    rec[3] = globaltimer_ns();
+                    rec[5] = stats.windows;
+                    rec[6] = stats.waits;
+                    rec[7] = (unsigned long long)sm_id() | ((unsigned long long)blockIdx.x << 32);
+                }
+            }
+        }
+        T pre[VPT];
+        warp_rows_scan<T, VPT>(vc, lane, pre);
+        __syncthreads();
+        if (sm.fail) {
+            fail_at = k;
+            return false;
+        }
+        const size_t tile_base = (size_t)t * TILE;
+        rows_output_inplace<T, VPT, INCLUSIVE>(vc, pre, sm.prefix + wp_cur);
+        store_rows<T, VPT>(out, n, tile_base + (size_t)warp * SEG, lane, tile_base + TILE <= n, vc);
+        if (carry_out != nullptr && t == num_tiles - 1 && threadIdx.x == 0) *carry_out = sm.prefix + agg_cur;
+        if (TRACE && threadIdx.x == 0) trace[(size_t)t * kTraceWords + 4] = globaltimer_ns();
+        wp_cur = wp_next;
+        agg_cur = agg_next;
+        return true;
+    };
+
+    T va[VPT][4], vb[VPT][4];  // register double buffer: current and next tile
+    bool failed = false;
+    if (count > 0) {
+        if (threadIdx.x == 0)
+            for (uint32_t k = 0; k < count && k < (uint32_t)STAGES; ++k) issue(k);
+        if (!fetch(0, va)) {
+            failed = true;
+            fail_at = 0;
+        } else {
+            reduce_publish(rank, va, &wp_cur, &agg_cur);
+        }
+        compiler_fence();
+    }
+    for (uint32_t k = 0; !failed && k < count; k += 2) {
+        if (!step(k, va, vb)) {
+            failed = true;
+        } else if (k + 1 < count && !step(k + 1, vb, va)) {
+            failed = true;
+        }
+    }
+
+    if (failed && threadIdx.x == 0) {
+        // Leaving early: poison this CTA's later tiles so that their
+        // successors fail fast, and let its copies in flight land before the
+        // shared memory goes away (bounded waits).
+        for (uint32_t k = fail_at + 1; k < count; ++k) {
+            const uint32_t t = rank + k * G;
+            if ((int64_t)t != ctx.fault_tile) st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStatePoison, 0u));
+        }
+        for (uint32_t k = fetched; k < issued; ++k)
+            mbar_wait_bounded(&bars[k % STAGES], (k / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
+    }
+}
+
+template <typename T, bool INCL, int THREADS, int VPT, int STAGES, int K, bool TRACE>
+static cudaError_t launch_pipe(const void* in, void* out, size_t n, const LookbackWs& ws,
+                               const void* carry_in, void* carry_out, unsigned long long* trace,
+                               cudaStream_t s) {
+    constexpr size_t TILE = (size_t)THREADS * VPT * 4;
+    constexpr size_t SMEM = (size_t)STAGES * TILE * sizeof(T);
+    auto kern = k_scan_lookback_pipe<T, INCL, THREADS, VPT, STAGES, K, TRACE>;
+    static int blocks_per_sm = -1;  // per instantiation; one device model in a process
+    static int sms = 0;
+    if (blocks_per_sm < 0) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
+        if (e != cudaSuccess) return e;
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        int b = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, THREADS, SMEM);
+        if (e != cudaSuccess) return e;
+        blocks_per_sm = b > 0 ? b : 1;
+    }
+    const uint32_t tiles = (uint32_t)((n + TILE - 1) / TILE);
+    const size_t resident = (size_t)sms * (size_t)blocks_per_sm;
+    const uint32_t grid = (uint32_t)(tiles < resident ? tiles : resident);
+    LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};
+    kern<<<grid, THREADS, SMEM, s>>>(static_cast<const T*>(in), static_cast<T*>(out), n, tiles, ctx,
+                                      static_cast<const T*>(carry_in), static_cast<T*>(carry_out), trace);
+    return cudaGetLastError();
+}
+
+template <typename T, bool INCL, bool TRACE>
+static cudaError_t dispatch_pipe(int config, const void* in, void* out, size_t n, const LookbackWs& ws,
+                                 const void* ci, void* co, unsigned long long* tr, cudaStream_t s) {
+    switch (config) {  // the persistent rows of the configuration table (scan.cu)
+        case 6: return launch_pipe<T, INCL, 512, 8, 3, 1, TRACE>(in, out, n, ws, ci, co, tr, s);
+        case 7: return launch_pipe<T, INCL, 512, 4, 3, 1, TRACE>(in, out, n, ws, ci, co, tr, s);
+        case 8: return launch_pipe<T, INCL, 512, 8, 2, 2, TRACE>(in, out, n, ws, ci, co, tr, s);
+        case 9: return launch_pipe<T, INCL, 512, 6, 3, 1, TRACE>(in, out, n, ws, ci, co, tr, s);
+        case 10: return launch_pipe<T, INCL, 1024, 4, 2, 1, TRACE>(in, out, n, ws, ci, co, tr, s);
+        default: return launch_pipe<T, INCL, 512, 8, 2, 1, TRACE>(in, out, n, ws, ci, co, tr, s);  // 5
+    }
+}
+
+cudaError_t launch_scan_lookback_pipe(Dtype dt, bool inclusive, int config, const void* in, void* out,
+                                      size_t n, const LookbackWs& ws, const void* carry_in,
+                                      void* carry_out, cudaStream_t s) {
+    if (dt == Dtype::F32)
+        return inclusive ? dispatch_pipe<float, true, false>(config, in, out, n, ws, carry_in, carry_out, nullptr, s)
+                         : dispatch_pipe<float, false, false>(config, in, out, n, ws, carry_in, carry_out, nullptr, s);
+    return inclusive ? dispatch_pipe<uint32_t, true, false>(config, in, out, n, ws, carry_in, carry_out, nullptr, s)
+                     : dispatch_pipe<uint32_t, false, false>(config, in, out, n, ws, carry_in, carry_out, nullptr, s);
+}
+
+cudaError_t launch_scan_trace_pipe(int config, const void* in, void* out, size_t n, const LookbackWs& ws,
+                                   unsigned long long* trace, cudaStream_t s) {
+    return dispatch_pipe<uint32_t, false, true>(config, in, out, n, ws, nullptr, nullptr, trace, s);
+}
+
+}  // namespace ss

@@ -155,4 +155,24 @@ __device__ __forceinline__ void rows_output(const T (&v)[VPT][4], const T (&pre)
     }
 }
 
+// rows_output written over the rows themselves (saves a register copy).
+template <typename T, int VPT, bool INCLUSIVE>
+__device__ __forceinline__ void rows_output_inplace(T (&v)[VPT][4], const T (&pre)[VPT], T base) {
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        T r = base + pre[j];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const T x = v[j][k];
+            if (INCLUSIVE) {
+                r += x;
+                v[j][k] = r;
+            } else {
+                v[j][k] = r;
+                r += x;
+            }
+        }
+    }
+}
+
 }  // namespace ss

@@ -17,12 +17,13 @@ pytestmark = pytest.mark.gpu
 TILE = 4096
 
 
-@pytest.fixture(scope="module")
-def ss():
+@pytest.fixture(scope="module", params=[0, 5], ids=["one-cta-per-tile", "persistent"])
+def ss(request):
     import stream_compaction_pass_gb300 as m
-    m.ss_set_scan_config(0)
+    m.ss_set_scan_config(request.param)
     yield m
     m.ss_debug_set_lookback_fault(-1, 0)
+    m.ss_set_scan_config(5)
 
 
 def _scan(ss, x):
@@ -35,7 +36,7 @@ def _scan(ss, x):
 
 @pytest.mark.parametrize("dead_tile", [0, 5, 63])
 def test_scan_timeout_is_reported_and_recovered(ss, dead_tile):
-    x = si.workload_int_pm1000(64 * TILE + 9, seed=2)
+    x = si.workload_int_pm1000(64 * ss.ss_scan_tile_elems() + 9, seed=2)
     ss.ss_debug_set_lookback_fault(dead_tile, 2_000_000)
     try:
         _scan(ss, x)

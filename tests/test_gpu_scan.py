@@ -23,10 +23,13 @@ TILE = 4096
 SWEEP_MAX = (1 << 30) + 1
 
 
+DEFAULT_CONFIG = 5
+
+
 @pytest.fixture(scope="module")
 def ss():
     import stream_compaction_pass_gb300 as m
-    m.ss_set_scan_config(0)
+    m.ss_set_scan_config(DEFAULT_CONFIG)
     return m
 
 
@@ -110,13 +113,17 @@ def test_uint32_poisson_counts(ss, inplace):
 
 # --- edge cases --------------------------------------------------------------
 
-EDGE = [1, 2, 3, 4, 5, 31, 32, 33, 127, 128, 129, 511, 512, 513, TILE - 1, TILE, TILE + 1,
-        2 * TILE - 1, 2 * TILE, 2 * TILE + 1, 33 * TILE + 7]
+# (whole tiles of the configured size, extra elements): sizes around tile
+# boundaries of whatever tile the library runs with, plus small absolutes.
+EDGE = [(0, 1), (0, 2), (0, 3), (0, 4), (0, 5), (0, 31), (0, 32), (0, 33), (0, 127), (0, 128),
+        (0, 129), (0, 511), (0, 512), (0, 513), (0, 4095), (0, 4096), (0, 4097), (1, -1), (1, 0),
+        (1, 1), (2, -1), (2, 0), (2, 1), (33, 7)]
 
 
-@pytest.mark.parametrize("n", EDGE)
+@pytest.mark.parametrize("edge", EDGE, ids=[f"{t}T{d:+d}" for t, d in EDGE])
 @pytest.mark.parametrize("kind", ["i32", "u32", "f32"])
-def test_edge_sizes(ss, n, kind):
+def test_edge_sizes(ss, edge, kind):
+    n = edge[0] * ss.ss_scan_tile_elems() + edge[1]
     if kind == "f32":
         x = si.structured_i_mod_8(n)  # exact in any order
     elif kind == "u32":
@@ -156,8 +163,10 @@ def test_in_place(ss, kind):
         assert_equal(got, ref.astype(got.dtype) if kind == "f32" else ref)
 
 
-@pytest.mark.parametrize("config", range(5))
+@pytest.mark.parametrize("config", range(11))
 def test_every_tile_configuration(ss, config):
+    assert ss.ss_scan_config_count() == 11
+    default = ss.ss_scan_tile_elems()
     ss.ss_set_scan_config(config)
     try:
         tile = ss.ss_scan_tile_elems()
@@ -168,7 +177,8 @@ def test_every_tile_configuration(ss, config):
             f = f32_input(n)
             assert_fp32_close(run_named_scan("f32", True, f), oracle.scan_f32(f, True), f)
     finally:
-        ss.ss_set_scan_config(0)
+        ss.ss_set_scan_config(DEFAULT_CONFIG)
+    assert ss.ss_scan_tile_elems() == default
 
 
 def test_repeated_launches_are_deterministic_and_epochs_advance(ss):
@@ -221,3 +231,28 @@ def test_nondefault_stream(ss):
         assert st == ss.SS_OK
         got = d_out.cpu().numpy()
     assert_equal(got, sweep_reference(SWEEP_MAX)[:n])
+
+
+@pytest.mark.parametrize("config", [0, 1, 5, 6, 7, 8, 9, 10])
+def test_trace_build_scans_and_records(ss, config):
+    import torch
+    n = 10_000_000 + 123
+    x = sweep_input(SWEEP_MAX)[:n]
+    ss.ss_set_scan_config(config)
+    try:
+        tile = ss.ss_scan_tile_elems()
+    finally:
+        ss.ss_set_scan_config(DEFAULT_CONFIG)
+    tiles = (n + tile - 1) // tile
+    d_in = torch.from_numpy(x).to("cuda:0")
+    d_out = torch.empty_like(d_in)
+    tr = torch.zeros(tiles * 8, dtype=torch.int64, device="cuda:0")
+    ss.ss_scan_trace(config, d_in, d_out, tr)
+    assert ss.ss_stream_status()[0] == ss.SS_OK
+    assert_equal(d_out.cpu().numpy(), sweep_reference(SWEEP_MAX)[:n], tile)
+    rec = tr.cpu().numpy().reshape(tiles, 8)
+    t = rec[:, :5]
+    assert (t > 0).all()
+    assert (np.diff(t, axis=1) >= 0).all()        # begin <= aggregate <= published <= resolved <= end
+    assert (rec[1:, 5] >= 1).all()                # every tile after the first read a window
+    assert (rec[0, 5] == 0)
