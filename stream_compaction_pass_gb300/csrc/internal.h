@@ -28,7 +28,8 @@ struct LookbackWs {
 // A single-pass scan configuration: which kernel, its tile geometry and
 // its look-back window.
 struct ScanConfig {
-    int persistent;  // 0: one CTA per tile (scan.cu); 1: persistent, bulk-copy ring (scan_pipe.cu)
+    int persistent;  // 0: one CTA per tile (scan.cu); 1: persistent, bulk-copy ring (scan_pipe.cu);
+                     // 2: persistent and warp-specialised (scan_ws.cu; threads = data threads)
     int threads;
     int items;       // per thread, a multiple of 4
     int stages;      // ring depth of the persistent kernel
@@ -60,6 +61,11 @@ cudaError_t launch_scan_trace(int config, const void* in, void* out, size_t n, c
                               unsigned long long* trace, cudaStream_t s);
 cudaError_t launch_scan_trace_pipe(int config, const void* in, void* out, size_t n,
                                    const LookbackWs& ws, unsigned long long* trace, cudaStream_t s);
+cudaError_t launch_scan_lookback_ws(Dtype dt, bool inclusive, int config, const void* in, void* out,
+                                    size_t n, const LookbackWs& ws, const void* carry_in, void* carry_out,
+                                    cudaStream_t s);
+cudaError_t launch_scan_trace_ws(int config, const void* in, void* out, size_t n, const LookbackWs& ws,
+                                 unsigned long long* trace, cudaStream_t s);
 
 // Single-pass decoupled look-back scan.  `carry_in` (device, may be null)
 // seeds the prefix of element 0; `carry_out` (device, may be null) receives

@@ -78,12 +78,16 @@ static const ScanConfig kConfigs[] = {
     {0, 512, 16, 0, 1},  // 2: 8192, 512 threads
     {0, 256, 32, 0, 2},  // 3: 8192, 64-descriptor window
     {0, 512, 16, 0, 2},  // 4: 8192, 512 threads, 64
-    {1, 512, 32, 2, 1},  // 5: persistent, 16384-element tiles, 2-stage ring (128 KB), 32
-    {1, 512, 32, 3, 1},  // 6: persistent, 16384, 3 stages (192 KB), 32
+    {1, 512, 32, 2, 1},  // 5: persistent, 16384-element tiles, 2-stage ring (128 KB), 32 (the default)
+    {1, 512, 32, 3, 1},  // 6: persistent, 16384, 3 stages (192 KB), 32, single register buffer
     {1, 512, 16, 3, 1},  // 7: persistent, 8192, 3 stages (96 KB, two CTAs per SM), 32
     {1, 512, 32, 2, 2},  // 8: persistent, 16384, 2 stages, 64
     {1, 512, 24, 3, 1},  // 9: persistent, 12288, 3 stages (144 KB), 32
     {1, 1024, 16, 2, 1}, // 10: persistent, 16384, 1024 threads, 2 stages, 32
+    {2, 512, 32, 3, 5},  // 11: warp-specialised, 16384-element tiles, 3-stage ring (192 KB), 160, lagged
+    {2, 512, 32, 3, 1},  // 12: warp-specialised, 16384, 3 stages, 32, lagged
+    {2, 512, 32, 3, 5},  // 13: warp-specialised, 16384, 3 stages, 160, not lagged
+    {2, 256, 32, 3, 5},  // 14: warp-specialised, 8192, 3 stages (96 KB, two CTAs per SM), 160, lagged
 };
 constexpr int kNumConfigs = sizeof(kConfigs) / sizeof(kConfigs[0]);
 constexpr int kDefaultConfig = 5;
@@ -135,7 +139,9 @@ cudaError_t launch_scan_lookback(Dtype dt, bool inclusive, int config, const voi
     const ScanConfig c = scan_config(config);
     if (c.persistent) {
         if (aligned16(in, out) && n > c.tile())
-            return launch_scan_lookback_pipe(dt, inclusive, config, in, out, n, ws, carry_in, carry_out, s);
+            return c.persistent == 2
+                       ? launch_scan_lookback_ws(dt, inclusive, config, in, out, n, ws, carry_in, carry_out, s)
+                       : launch_scan_lookback_pipe(dt, inclusive, config, in, out, n, ws, carry_in, carry_out, s);
         config = per_tile_fallback(config);
     }
     if (dt == Dtype::F32)
@@ -150,7 +156,8 @@ cudaError_t launch_scan_trace(int config, const void* in, void* out, size_t n, c
     const ScanConfig c = scan_config(config);
     if (c.persistent) {
         if (!aligned16(in, out) || n <= c.tile()) return cudaErrorInvalidValue;
-        return launch_scan_trace_pipe(config, in, out, n, ws, trace, s);
+        return c.persistent == 2 ? launch_scan_trace_ws(config, in, out, n, ws, trace, s)
+                                 : launch_scan_trace_pipe(config, in, out, n, ws, trace, s);
     }
     switch (config) {
         case 1: return launch_one<uint32_t, false, 256, 8, 1, true>(in, out, n, ws, nullptr, nullptr, s, trace);

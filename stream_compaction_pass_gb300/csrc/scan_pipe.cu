@@ -20,6 +20,8 @@
 // The per-tile arithmetic is the same as scan.cu's (scan_body.cuh).  Reading
 // the ring back is conflict-free: lane l of a warp reads the l-th 16-byte
 // vector of a 512-byte row.
+#include <type_traits>
+
 #include "bulk.cuh"
 #include "internal.h"
 #include "scan_body.cuh"
@@ -238,13 +240,201 @@ k_scan_lookback_pipe(const T* in, T* out, size_t n, uint32_t num_tiles, Lookback
     }
 }
 
-template <typename T, bool INCL, int THREADS, int VPT, int STAGES, int K, bool TRACE>
+// Single-register-buffer form of the same schedule: the next tile is summed
+// straight out of the ring (no registers held for it) and the current tile
+// is read again for its scan, so a tile stays in the ring until its scan and
+// the ring needs three stages.  Same arithmetic and look-back as above; it
+// exists because the double register buffer does not fit 128 registers for
+// every element type without spilling.
+template <typename T, bool INCLUSIVE, int THREADS, int VPT, int STAGES, int K, bool TRACE>
+__global__ void __launch_bounds__(THREADS, 1)
+k_scan_lookback_pipe_sb(const T* in, T* out, size_t n, uint32_t num_tiles, LookbackCtx ctx,
+                        const T* carry_in, T* carry_out, unsigned long long* trace) {
+    static_assert(STAGES >= 3, "tile k stays in the ring while tile k+1 is summed");
+    constexpr int WARPS = THREADS / 32;
+    constexpr uint32_t TILE = (uint32_t)THREADS * VPT * 4;
+    constexpr uint32_t TILE_BYTES = TILE * (uint32_t)sizeof(T);
+    constexpr uint32_t SEG = 32u * VPT * 4;
+
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    T* ring = reinterpret_cast<T*>(smem_raw);
+    __shared__ __align__(8) uint64_t bars[STAGES];
+    __shared__ ScanSmem<T, WARPS> sm;
+    __shared__ uint32_t s_rank, s_epoch;
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const uint32_t G = gridDim.x;
+    const uint64_t policy = policy_evict_first();
+
+    if (threadIdx.x == 0) {
+        uint32_t rank, epoch;
+        claim_tile(ctx.counter, G, &rank, &epoch);
+        s_rank = rank;
+        s_epoch = epoch;
+        for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
+        fence_async_shared();
+    }
+    __syncthreads();
+    const uint32_t rank = s_rank;
+    const uint32_t epoch = s_epoch;
+    if (rank >= G) {
+        if (threadIdx.x == 0) record_error(ctx.status, kErrCounter, rank);
+        return;
+    }
+    const uint32_t count = rank < num_tiles ? (num_tiles - rank + G - 1) / G : 0;
+    uint32_t issued = 0, consumed = 0;  // thread 0
+
+    auto issue = [&](uint32_t k) {
+        const int s = (int)(k % STAGES);
+        const size_t base = (size_t)(rank + k * G) * TILE;
+        if (base + TILE <= n) {
+            fence_async_shared();
+            mbar_arrive_expect_tx(&bars[s], TILE_BYTES);
+            bulk_load(ring + (size_t)s * TILE, in + base, TILE_BYTES, &bars[s], policy);
+        } else {
+            mbar_arrive(&bars[s]);
+        }
+        issued = k + 1;
+    };
+    auto read_rows = [&](uint32_t k, T (&v)[VPT][4]) {
+        const size_t tile_base = (size_t)(rank + k * G) * TILE;
+        if (tile_base + TILE <= n) {
+            const T* src = ring + (size_t)(k % STAGES) * TILE + (size_t)warp * SEG + (size_t)lane * 4;
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const uint4 r = lds_vec(src + 128 * j);
+                v[j][0] = from_bits<T>(r.x);
+                v[j][1] = from_bits<T>(r.y);
+                v[j][2] = from_bits<T>(r.z);
+                v[j][3] = from_bits<T>(r.w);
+            }
+        } else {
+            load_rows<T, VPT>(in, n, tile_base + (size_t)warp * SEG, lane, false, v);
+        }
+    };
+    // Waits for tile k, sums it, publishes its aggregate; false if the copy did not arrive.
+    auto reduce_publish = [&](uint32_t k, T* wp, T* agg) -> bool {
+        const uint32_t t = rank + k * G;
+        if (TRACE && threadIdx.x == 0) trace[(size_t)t * kTraceWords] = globaltimer_ns();
+        const bool ok = mbar_wait_bounded(&bars[k % STAGES], (k / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
+        if (__syncthreads_or(!ok)) {
+            if (threadIdx.x == 0) record_error(ctx.status, kErrBulkTimeout, t);
+            return false;
+        }
+        T v[VPT][4];
+        read_rows(k, v);
+        T x = T(0);
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) x += ((v[j][0] + v[j][1]) + v[j][2]) + v[j][3];
+        block_combine<T, WARPS>(warp_sum(x), warp, lane, sm.warp, wp, agg);
+        if (threadIdx.x == 0 && (int64_t)t != ctx.fault_tile) {
+            if (t == 0) {
+                if (num_tiles > 1)
+                    st_relaxed_u64(ctx.desc, pack_desc(epoch, kStateP,
+                                                       to_bits<T>((carry_in ? *carry_in : T(0)) + *agg)));
+            } else {
+                st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStateA, to_bits<T>(*agg)));
+            }
+            if (TRACE) trace[(size_t)t * kTraceWords + 1] = trace[(size_t)t * kTraceWords + 2] = globaltimer_ns();
+        }
+        compiler_fence();  // the aggregate just published stays ahead of the look-back
+        return true;
+    };
+
+    T wp_cur = T(0), agg_cur = T(0), prev_incl = T(0);
+    bool failed = false;
+    uint32_t fail_at = 0;
+    if (threadIdx.x == 0)
+        for (uint32_t k = 0; k < count && k < (uint32_t)STAGES; ++k) issue(k);
+    if (count > 0 && !reduce_publish(0, &wp_cur, &agg_cur)) failed = true;
+
+    for (uint32_t k = 0; !failed && k < count; ++k) {
+        const uint32_t t = rank + k * G;
+        T wp_next = T(0), agg_next = T(0);
+        if (k + 1 < count && !reduce_publish(k + 1, &wp_next, &agg_next)) {
+            failed = true;
+            fail_at = k;
+            break;
+        }
+        if (warp == 0) {
+            LookbackStats stats{0u, 0u};
+            T excl = T(0);
+            bool lb_failed = false;
+            const bool dead = (int64_t)t == ctx.fault_tile;  // test hook only
+            if (t == 0) {
+                excl = carry_in ? *carry_in : T(0);
+                lb_failed = dead;
+            } else if (dead) {
+                lb_failed = true;
+            } else {
+                const int64_t floor = k > 0 ? (int64_t)t - (int64_t)G : -1;
+                excl = lookback<T, K, TRACE>(ctx, t, epoch, lane, &lb_failed, &stats, floor, prev_incl);
+                if (lane == 0) {
+                    if (!lb_failed) {
+                        st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStateP, to_bits<T>(excl + agg_cur)));
+                    } else {
+                        st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStatePoison, 0u));
+                        record_error(ctx.status, kErrLookbackTimeout, t);
+                    }
+                }
+            }
+            prev_incl = excl + agg_cur;
+            if (lane == 0) {
+                sm.prefix = excl;
+                sm.fail = lb_failed ? 1u : 0u;
+                if (TRACE) {
+                    unsigned long long* rec = trace + (size_t)t * kTraceWords;
+                    rec[3] = globaltimer_ns();
+                    rec[5] = stats.windows;
+                    rec[6] = stats.waits;
+                    rec[7] = (unsigned long long)sm_id() | ((unsigned long long)blockIdx.x << 32);
+                }
+            }
+        }
+        T v[VPT][4];
+        read_rows(k, v);
+        T pre[VPT];
+        warp_rows_scan<T, VPT>(v, lane, pre);
+        __syncthreads();  // tile k read by everyone; the prefix is in shared memory
+        if (threadIdx.x == 0) {
+            consumed = k + 1;
+            if (k + STAGES < count) issue(k + STAGES);
+        }
+        if (sm.fail) {
+            failed = true;
+            fail_at = k;
+            break;
+        }
+        const size_t tile_base = (size_t)t * TILE;
+        rows_output_inplace<T, VPT, INCLUSIVE>(v, pre, sm.prefix + wp_cur);
+        store_rows<T, VPT>(out, n, tile_base + (size_t)warp * SEG, lane, tile_base + TILE <= n, v);
+        if (carry_out != nullptr && t == num_tiles - 1 && threadIdx.x == 0) *carry_out = sm.prefix + agg_cur;
+        if (TRACE && threadIdx.x == 0) trace[(size_t)t * kTraceWords + 4] = globaltimer_ns();
+        wp_cur = wp_next;
+        agg_cur = agg_next;
+    }
+
+    if (failed && threadIdx.x == 0) {
+        for (uint32_t k = fail_at + 1; k < count; ++k) {
+            const uint32_t t = rank + k * G;
+            if ((int64_t)t != ctx.fault_tile) st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStatePoison, 0u));
+        }
+        for (uint32_t k = consumed; k < issued; ++k)
+            mbar_wait_bounded(&bars[k % STAGES], (k / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
+    }
+}
+
+template <typename T, bool INCL, int THREADS, int VPT, int STAGES, int K, bool TRACE, bool SB = false>
 static cudaError_t launch_pipe(const void* in, void* out, size_t n, const LookbackWs& ws,
                                const void* carry_in, void* carry_out, unsigned long long* trace,
                                cudaStream_t s) {
     constexpr size_t TILE = (size_t)THREADS * VPT * 4;
     constexpr size_t SMEM = (size_t)STAGES * TILE * sizeof(T);
-    auto kern = k_scan_lookback_pipe<T, INCL, THREADS, VPT, STAGES, K, TRACE>;
+    auto kern = [] {
+        if constexpr (SB) return k_scan_lookback_pipe_sb<T, INCL, THREADS, VPT, STAGES, K, TRACE>;
+        else return k_scan_lookback_pipe<T, INCL, THREADS, VPT, STAGES, K, TRACE>;
+    }();
     static int blocks_per_sm = -1;  // per instantiation; one device model in a process
     static int sms = 0;
     if (blocks_per_sm < 0) {
@@ -271,12 +461,17 @@ template <typename T, bool INCL, bool TRACE>
 static cudaError_t dispatch_pipe(int config, const void* in, void* out, size_t n, const LookbackWs& ws,
                                  const void* ci, void* co, unsigned long long* tr, cudaStream_t s) {
     switch (config) {  // the persistent rows of the configuration table (scan.cu)
-        case 6: return launch_pipe<T, INCL, 512, 8, 3, 1, TRACE>(in, out, n, ws, ci, co, tr, s);
+        case 6: return launch_pipe<T, INCL, 512, 8, 3, 1, TRACE, true>(in, out, n, ws, ci, co, tr, s);
         case 7: return launch_pipe<T, INCL, 512, 4, 3, 1, TRACE>(in, out, n, ws, ci, co, tr, s);
         case 8: return launch_pipe<T, INCL, 512, 8, 2, 2, TRACE>(in, out, n, ws, ci, co, tr, s);
         case 9: return launch_pipe<T, INCL, 512, 6, 3, 1, TRACE>(in, out, n, ws, ci, co, tr, s);
         case 10: return launch_pipe<T, INCL, 1024, 4, 2, 1, TRACE>(in, out, n, ws, ci, co, tr, s);
-        default: return launch_pipe<T, INCL, 512, 8, 2, 1, TRACE>(in, out, n, ws, ci, co, tr, s);  // 5
+        default:  // 5: the double register buffer spills for fp32 exclusive; that case takes the
+                  // single-buffer kernel with the same 16384-element tiles (and a third stage)
+            if constexpr (std::is_same<T, float>::value && !INCL)
+                return launch_pipe<T, INCL, 512, 8, 3, 1, TRACE, true>(in, out, n, ws, ci, co, tr, s);
+            else
+                return launch_pipe<T, INCL, 512, 8, 2, 1, TRACE>(in, out, n, ws, ci, co, tr, s);
     }
 }
 

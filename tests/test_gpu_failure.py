@@ -17,7 +17,7 @@ pytestmark = pytest.mark.gpu
 TILE = 4096
 
 
-@pytest.fixture(scope="module", params=[0, 5], ids=["one-cta-per-tile", "persistent"])
+@pytest.fixture(scope="module", params=[0, 5, 11], ids=["one-cta-per-tile", "persistent", "warp-specialised"])
 def ss(request):
     import stream_compaction_pass_gb300 as m
     m.ss_set_scan_config(request.param)
