@@ -147,7 +147,7 @@ k_compact_u32(const uint32_t* keys, const uint8_t* flags, uint32_t* out,
         } else {
             if (lane == 0) st_relaxed_u64(ctx.desc + tile, pack_desc(epoch, kStateA, tile_count));
             compiler_fence();  // publish before looking back
-            excl = lookback<uint32_t, 4>(ctx, tile, epoch, lane, &failed);
+            excl = lookback<uint32_t, 1>(ctx, tile, epoch, lane, &failed);
             if (lane == 0) {
                 if (!failed) {
                     st_relaxed_u64(ctx.desc + tile, pack_desc(epoch, kStateP, excl + tile_count));
@@ -175,6 +175,11 @@ k_compact_u32(const uint32_t* keys, const uint8_t* flags, uint32_t* out,
 cudaError_t launch_compact_u32(const uint32_t* keys, const uint8_t* flags, uint32_t* out,
                                unsigned long long* d_count, size_t n, const LookbackWs& ws,
                                cudaStream_t s) {
+    // Large aligned inputs take the persistent kernel (bulk copies need
+    // 16-byte aligned sources); the rest stay on one CTA per 4096-element tile.
+    if (((reinterpret_cast<uintptr_t>(keys) | reinterpret_cast<uintptr_t>(flags)) & 15u) == 0 &&
+        n > (size_t)16384)
+        return launch_compact_pipe(keys, flags, out, d_count, n, ws, s);
     const uint32_t tiles = (uint32_t)((n + kCompactTile - 1) / kCompactTile);
     LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};
     const bool aligned = ((reinterpret_cast<uintptr_t>(keys) & 15u) == 0) &&

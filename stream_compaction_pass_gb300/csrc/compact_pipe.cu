@@ -1,0 +1,286 @@
+// compact_pipe.cu -- the fused order-preserving compaction as a persistent
+// kernel fed by the bulk-copy engine.
+//
+// Same result as compact.cu (keep keys[i] where flags[i] != 0, in order;
+// "Prefix sum and other parallel patterns", Stream compaction and Exercise
+// 1), on the schedule of the persistent scan (scan_pipe.cu): each CTA takes
+// a rank from the workspace counter and handles tiles rank, rank + G, ...;
+// a two-stage shared-memory ring receives each tile's keys and flags with two
+// bulk copies.  Iteration k:
+//   1. count the kept elements of tile k+1 from its flags alone and publish
+//      that count one iteration early (the count is the tile's aggregate);
+//   2. warp 0 looks back for tile k, no further than this CTA's previous
+//      tile, while the other warps rank tile k's kept keys in registers
+//      (per-row keep masks; the rows' counts packed one byte per row and
+//      scanned across the warp; popc of the mask below an element inside a
+//      vector);
+//   3. the stage is released and the next copy started;
+//   4. the kept keys go straight from registers to their output slots: a
+//      warp row's kept keys form one contiguous run of the output, so no
+//      shared-memory staging is needed.
+#include <type_traits>
+
+#include "bulk.cuh"
+#include "internal.h"
+#include "tile.cuh"
+
+namespace ss {
+
+namespace {
+
+__device__ __forceinline__ uint32_t byte_keep_mask(uint32_t w) {
+    return ((w & 0x000000ffu) ? 1u : 0u) | ((w & 0x0000ff00u) ? 2u : 0u) |
+           ((w & 0x00ff0000u) ? 4u : 0u) | ((w & 0xff000000u) ? 8u : 0u);
+}
+
+__device__ __forceinline__ uint32_t lds_u32(const void* p) {
+    uint32_t r;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(smem_u32(p)) : "memory");
+    return r;
+}
+
+}  // namespace
+
+template <int THREADS, int VPT, int STAGES>
+__global__ void __launch_bounds__(THREADS, 1)
+k_compact_pipe(const uint32_t* keys, const uint8_t* flags, uint32_t* out, unsigned long long* d_count,
+               size_t n, uint32_t num_tiles, LookbackCtx ctx) {
+    static_assert(VPT % 4 == 0, "rows are packed four to a word");
+    constexpr int WARPS = THREADS / 32;
+    constexpr int NW = VPT / 4;  // packed count words per lane
+    constexpr uint32_t TILE = (uint32_t)THREADS * VPT * 4;
+    constexpr uint32_t KEY_BYTES = TILE * 4;
+    constexpr uint32_t STAGE_BYTES = KEY_BYTES + TILE;  // keys, then flags
+    constexpr uint32_t SEG = 32u * VPT * 4;
+
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t bars[STAGES];
+    __shared__ uint32_t s_warp[WARPS];
+    __shared__ uint32_t s_prefix, s_fail, s_rank, s_epoch;
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const uint32_t G = gridDim.x;
+    const uint64_t policy = policy_evict_first();
+
+    if (threadIdx.x == 0) {
+        uint32_t rank, epoch;
+        claim_tile(ctx.counter, G, &rank, &epoch);  // one claim per CTA; the last resets the counter
+        s_rank = rank;
+        s_epoch = epoch;
+        for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
+        fence_async_shared();
+    }
+    __syncthreads();
+    const uint32_t rank = s_rank;
+    const uint32_t epoch = s_epoch;
+    if (rank >= G) {
+        if (threadIdx.x == 0) record_error(ctx.status, kErrCounter, rank);
+        return;
+    }
+    const uint32_t count = rank < num_tiles ? (num_tiles - rank + G - 1) / G : 0;
+    uint32_t issued = 0, consumed = 0;  // thread 0
+
+    auto stage_keys = [&](uint32_t k) -> unsigned char* { return smem_raw + (size_t)(k % STAGES) * STAGE_BYTES; };
+    auto issue = [&](uint32_t k) {  // thread 0
+        const int s = (int)(k % STAGES);
+        const size_t base = (size_t)(rank + k * G) * TILE;
+        if (base + TILE <= n) {
+            fence_async_shared();
+            mbar_arrive_expect_tx(&bars[s], STAGE_BYTES);
+            bulk_load(stage_keys(k), keys + base, KEY_BYTES, &bars[s], policy);
+            bulk_load(stage_keys(k) + KEY_BYTES, flags + base, TILE, &bars[s], policy);
+        } else {
+            mbar_arrive(&bars[s]);  // ragged last tile: read from global
+        }
+        issued = k + 1;
+    };
+    // Keep masks of this lane's rows of tile k (bit e of m[j]: element e of row j is kept).
+    auto read_masks = [&](uint32_t k, uint32_t (&m)[VPT]) {
+        const size_t tile_base = (size_t)(rank + k * G) * TILE;
+        const size_t seg = tile_base + (size_t)warp * SEG;
+        if (tile_base + TILE <= n) {
+            const unsigned char* f = stage_keys(k) + KEY_BYTES + (size_t)warp * SEG + (size_t)lane * 4;
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) m[j] = byte_keep_mask(lds_u32(f + 128 * j));
+        } else {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                m[j] = 0;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const size_t i = seg + (size_t)(32 * j + lane) * 4 + e;
+                    if (i < n && flags[i] != 0) m[j] |= 1u << e;
+                }
+            }
+        }
+    };
+    // Waits for tile k, counts its kept elements and publishes the count.
+    auto count_publish = [&](uint32_t k, uint32_t* wp, uint32_t* agg) -> bool {
+        const uint32_t t = rank + k * G;
+        const bool ok = mbar_wait_bounded(&bars[k % STAGES], (k / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
+        if (__syncthreads_or(!ok)) {
+            if (threadIdx.x == 0) record_error(ctx.status, kErrBulkTimeout, t);
+            return false;
+        }
+        uint32_t m[VPT];
+        read_masks(k, m);
+        uint32_t c = 0;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) c += (uint32_t)__popc(m[j]);
+        block_combine<uint32_t, WARPS>(warp_sum(c), warp, lane, s_warp, wp, agg);
+        if (threadIdx.x == 0 && (int64_t)t != ctx.fault_tile) {
+            if (t == 0) {
+                if (num_tiles > 1) st_relaxed_u64(ctx.desc, pack_desc(epoch, kStateP, *agg));
+            } else {
+                st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStateA, *agg));
+            }
+        }
+        compiler_fence();  // the count just published stays ahead of the look-back
+        return true;
+    };
+
+    uint32_t wp_cur = 0, agg_cur = 0, prev_incl = 0;
+    bool failed = false;
+    uint32_t fail_at = 0;
+    if (threadIdx.x == 0)
+        for (uint32_t k = 0; k < count && k < (uint32_t)STAGES; ++k) issue(k);
+    if (count > 0 && !count_publish(0, &wp_cur, &agg_cur)) failed = true;
+
+    for (uint32_t k = 0; !failed && k < count; ++k) {
+        const uint32_t t = rank + k * G;
+        uint32_t wp_next = 0, agg_next = 0;
+        if (k + 1 < count && !count_publish(k + 1, &wp_next, &agg_next)) {
+            failed = true;
+            fail_at = k;
+            break;
+        }
+        if (warp == 0) {
+            uint32_t excl = 0;
+            bool lb_failed = false;
+            const bool dead = (int64_t)t == ctx.fault_tile;  // test hook only
+            if (t == 0) {
+                lb_failed = dead;
+            } else if (dead) {
+                lb_failed = true;
+            } else {
+                const int64_t floor = k > 0 ? (int64_t)t - (int64_t)G : -1;
+                excl = lookback<uint32_t, 1>(ctx, t, epoch, lane, &lb_failed, nullptr, floor, prev_incl);
+                if (lane == 0) {
+                    if (!lb_failed) {
+                        st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStateP, excl + agg_cur));
+                    } else {
+                        st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStatePoison, 0u));
+                        record_error(ctx.status, kErrLookbackTimeout, t);
+                    }
+                }
+            }
+            prev_incl = excl + agg_cur;
+            if (lane == 0) {
+                s_prefix = excl;
+                s_fail = lb_failed ? 1u : 0u;
+            }
+        }
+        // Rank tile k's kept keys.
+        const size_t tile_base = (size_t)t * TILE;
+        const size_t seg = tile_base + (size_t)warp * SEG;
+        uint32_t m[VPT];
+        uint32_t key[VPT][4];
+        read_masks(k, m);
+        if (tile_base + TILE <= n) {
+            const unsigned char* kb = stage_keys(k) + ((size_t)warp * SEG + (size_t)lane * 4) * 4;
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const uint4 r = lds_vec(kb + 512 * j);
+                key[j][0] = r.x;
+                key[j][1] = r.y;
+                key[j][2] = r.z;
+                key[j][3] = r.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const size_t i = seg + (size_t)(32 * j + lane) * 4 + e;
+                    key[j][e] = ((m[j] >> e) & 1u) ? keys[i] : 0u;
+                }
+        }
+        uint32_t row_base[VPT];
+        uint32_t run = 0;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            uint32_t packed = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) packed |= (uint32_t)__popc(m[4 * w + q]) << (8 * q);
+            const uint32_t inc = warp_inclusive_scan<uint32_t>(packed, lane);
+            const uint32_t exc = inc - packed;  // bytewise, no borrows (each byte <= 128)
+            const uint32_t rows = __shfl_sync(kFullMask, inc, 31);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                row_base[4 * w + q] = run + ((exc >> (8 * q)) & 0xffu);
+                run += (rows >> (8 * q)) & 0xffu;
+            }
+        }
+        __syncthreads();  // tile k read by everyone; the prefix is in shared memory
+        if (threadIdx.x == 0) {
+            consumed = k + 1;
+            if (k + STAGES < count) issue(k + STAGES);
+        }
+        if (s_fail) {
+            failed = true;
+            fail_at = k;
+            break;
+        }
+        uint32_t* dst = out + (size_t)s_prefix + wp_cur;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            uint32_t pos = row_base[j];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if ((m[j] >> e) & 1u) dst[pos++] = key[j][e];
+            }
+        }
+        if (t == num_tiles - 1 && threadIdx.x == 0) *d_count = (unsigned long long)s_prefix + agg_cur;
+        wp_cur = wp_next;
+        agg_cur = agg_next;
+    }
+
+    if (failed && threadIdx.x == 0) {
+        for (uint32_t k = fail_at + 1; k < count; ++k) {
+            const uint32_t t = rank + k * G;
+            if ((int64_t)t != ctx.fault_tile) st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStatePoison, 0u));
+        }
+        for (uint32_t k = consumed; k < issued; ++k)
+            mbar_wait_bounded(&bars[k % STAGES], (k / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
+    }
+}
+
+cudaError_t launch_compact_pipe(const uint32_t* keys, const uint8_t* flags, uint32_t* out,
+                                unsigned long long* d_count, size_t n, const LookbackWs& ws, cudaStream_t s) {
+    constexpr int THREADS = 512, VPT = 8, STAGES = 2;
+    constexpr size_t TILE = (size_t)THREADS * VPT * 4;
+    constexpr size_t SMEM = (size_t)STAGES * TILE * 5;
+    auto kern = k_compact_pipe<THREADS, VPT, STAGES>;
+    static int blocks_per_sm = -1;
+    static int sms = 0;
+    if (blocks_per_sm < 0) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
+        if (e != cudaSuccess) return e;
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        int b = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, THREADS, SMEM);
+        if (e != cudaSuccess) return e;
+        blocks_per_sm = b > 0 ? b : 1;
+    }
+    const uint32_t tiles = (uint32_t)((n + TILE - 1) / TILE);
+    const size_t resident = (size_t)sms * (size_t)blocks_per_sm;
+    const uint32_t grid = (uint32_t)(tiles < resident ? tiles : resident);
+    LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};
+    kern<<<grid, THREADS, SMEM, s>>>(keys, flags, out, d_count, n, tiles, ctx);
+    return cudaGetLastError();
+}
+
+}  // namespace ss
