@@ -445,6 +445,27 @@ def run_ours(args) -> None:
         torch.distributed.destroy_process_group()
 
 
+def profile_ablations(n: int) -> None:
+    """One warm-up and one measured launch of each reduce-then-scan ablation
+    (int32 exclusive, seeded [-1000, 1000] input), for a profiler to capture;
+    checks the result of each against the oracle."""
+    import torch
+    import seeded_inputs as si
+    import stream_compaction_pass_gb300 as ss
+    import oracle as orc
+    x = si.workload_int_pm1000(n, seed=2)
+    ref = orc.scan_i32(x, False)
+    d = torch.from_numpy(x).cuda()
+    o = torch.empty_like(d)
+    for algo in (ss.SS_ALGO_REDUCE_THEN_SCAN, ss.SS_ALGO_RTS_BLELLOCH, ss.SS_ALGO_RTS_BLELLOCH_PAD32,
+                 ss.SS_ALGO_RTS_BLELLOCH_PAD2):
+        for _ in range(2):
+            ss.ss_scan(ss.SS_I32, False, algo, d, o)
+        torch.cuda.synchronize()
+        assert np.array_equal(o.cpu().numpy(), ref), f"ablation {algo} mismatch"
+    print(f"ablations ok at n={n}")
+
+
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -458,7 +479,12 @@ def main() -> None:
     ap.add_argument("--no-rows", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--skip-check", action="store_true")
+    ap.add_argument("--profile-ablations", type=int, default=0, metavar="N",
+                    help="only run each ablation twice at n=N (for a profiler) and exit")
     args = ap.parse_args()
+    if args.profile_ablations:
+        profile_ablations(args.profile_ablations)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

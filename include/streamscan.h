@@ -191,6 +191,14 @@ int ss_scan_config_count(void);
  * on it, except for the rounding of fp32 sums. */
 ss_status ss_set_scan_config(int config);
 
+/* Selects the persistent compaction kernel used for 16-byte aligned inputs
+ * above 16384 elements, for later calls in this process: 0 streams keys and
+ * flags through shared memory with bulk copies; 1 (the default) bulk-copies
+ * only the flags and loads a 16-byte key vector only where one of its four
+ * flags is set, which reads far fewer key bytes when few elements are kept.
+ * Results are identical. */
+ss_status ss_set_compact_config(int config);
+
 /* Frees every workspace the library allocated (all devices and streams).
  * No call may be in flight. */
 void ss_shutdown(void);

@@ -70,6 +70,7 @@ def _declare(lib):
         "ss_scan_trace": [I, P, P, SZ, P, P],
         "ss_stream_status": [P, ctypes.POINTER(I64)],
         "ss_set_scan_config": [I],
+        "ss_set_compact_config": [I],
         "ss_debug_set_lookback_fault": [I64, U64],
         "ss_scan_noalloc": [I, I, P, P, SZ, P],
     }
@@ -248,6 +249,10 @@ def ss_scan_config_count() -> int:
 
 def ss_set_scan_config(config: int) -> None:
     _check(lib().ss_set_scan_config(config), "ss_set_scan_config")
+
+
+def ss_set_compact_config(config: int) -> None:
+    _check(lib().ss_set_compact_config(config), "ss_set_compact_config")
 
 
 def ss_shutdown() -> None:

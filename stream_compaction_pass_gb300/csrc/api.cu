@@ -462,6 +462,13 @@ ss_status ss_set_scan_config(int config) {
     return SS_OK;
 }
 
+ss_status ss_set_compact_config(int config) {
+    if (config < 0 || config >= ss::compact_kernel_count())
+        return fail(SS_ERR_INVALID_ARG, "no such compaction configuration");
+    ss::set_compact_kernel(config);
+    return SS_OK;
+}
+
 void ss_shutdown(void) {
     std::lock_guard<std::mutex> lk(g_mu);
     int cur = 0;

@@ -256,12 +256,229 @@ k_compact_pipe(const uint32_t* keys, const uint8_t* flags, uint32_t* out, unsign
     }
 }
 
-cudaError_t launch_compact_pipe(const uint32_t* keys, const uint8_t* flags, uint32_t* out,
-                                unsigned long long* d_count, size_t n, const LookbackWs& ws, cudaStream_t s) {
-    constexpr int THREADS = 512, VPT = 8, STAGES = 2;
+// Selective-load form: only the flags go through the bulk-copy ring (one
+// byte per element); each thread loads a 16-byte key vector only when one of
+// its four flags is set, one tile ahead, into a second register buffer.  With
+// sparse flags most key sectors are never read (at p = 0.01 about 8 % of the
+// 32-byte sectors hold a kept key); with dense flags it moves the same bytes
+// as the bulk-copy form.
+template <int THREADS, int VPT, int STAGES>
+__global__ void __launch_bounds__(THREADS, 1)
+k_compact_sel(const uint32_t* keys, const uint8_t* flags, uint32_t* out, unsigned long long* d_count,
+              size_t n, uint32_t num_tiles, LookbackCtx ctx) {
+    static_assert(VPT % 4 == 0, "rows are packed four to a word");
+    static_assert(STAGES >= 2, "the ring needs two stages at least");
+    constexpr int WARPS = THREADS / 32;
+    constexpr int NW = VPT / 4;
+    constexpr uint32_t TILE = (uint32_t)THREADS * VPT * 4;
+    constexpr uint32_t SEG = 32u * VPT * 4;
+
+    extern __shared__ __align__(128) unsigned char smem_raw[];  // STAGES x TILE flag bytes
+    __shared__ __align__(8) uint64_t bars[STAGES];
+    __shared__ uint32_t s_warp[WARPS];
+    __shared__ uint32_t s_prefix, s_fail, s_rank, s_epoch;
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const uint32_t G = gridDim.x;
+    const uint64_t policy = policy_evict_first();
+
+    if (threadIdx.x == 0) {
+        uint32_t rank, epoch;
+        claim_tile(ctx.counter, G, &rank, &epoch);  // one claim per CTA; the last resets the counter
+        s_rank = rank;
+        s_epoch = epoch;
+        for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
+        fence_async_shared();
+    }
+    __syncthreads();
+    const uint32_t rank = s_rank;
+    const uint32_t epoch = s_epoch;
+    if (rank >= G) {
+        if (threadIdx.x == 0) record_error(ctx.status, kErrCounter, rank);
+        return;
+    }
+    const uint32_t count = rank < num_tiles ? (num_tiles - rank + G - 1) / G : 0;
+    uint32_t issued = 0, consumed = 0;  // thread 0
+
+    auto issue = [&](uint32_t k) {  // thread 0: flags of this CTA's k-th tile
+        const int s = (int)(k % STAGES);
+        const size_t base = (size_t)(rank + k * G) * TILE;
+        if (base + TILE <= n) {
+            fence_async_shared();
+            mbar_arrive_expect_tx(&bars[s], TILE);
+            bulk_load(smem_raw + (size_t)s * TILE, flags + base, TILE, &bars[s], policy);
+        } else {
+            mbar_arrive(&bars[s]);  // ragged last tile: flags read from global
+        }
+        issued = k + 1;
+    };
+    // Waits for tile k's flags; this lane's keep masks, the tile's count and
+    // this warp's prefix; publishes the count; starts the loads of the key
+    // vectors that hold a kept element.  False if the copy did not arrive.
+    auto prepare = [&](uint32_t k, uint32_t (&m)[VPT], uint32_t (&key)[VPT][4], uint32_t* wp,
+                       uint32_t* agg) -> bool {
+        const uint32_t t = rank + k * G;
+        const size_t tile_base = (size_t)t * TILE;
+        const size_t seg = tile_base + (size_t)warp * SEG;
+        const bool ok = mbar_wait_bounded(&bars[k % STAGES], (k / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
+        if (__syncthreads_or(!ok)) {
+            if (threadIdx.x == 0) record_error(ctx.status, kErrBulkTimeout, t);
+            return false;
+        }
+        const bool full = tile_base + TILE <= n;
+        if (full) {
+            const unsigned char* f = smem_raw + (size_t)(k % STAGES) * TILE + (size_t)warp * SEG + (size_t)lane * 4;
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) m[j] = byte_keep_mask(lds_u32(f + 128 * j));
+            const uint4* kp = reinterpret_cast<const uint4*>(keys + seg) + lane;
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                uint4 r = make_uint4(0u, 0u, 0u, 0u);
+                if (m[j]) r = ld_vec(kp + 32 * j);
+                key[j][0] = r.x;
+                key[j][1] = r.y;
+                key[j][2] = r.z;
+                key[j][3] = r.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                m[j] = 0;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const size_t i = seg + (size_t)(32 * j + lane) * 4 + e;
+                    const bool keep = i < n && flags[i] != 0;
+                    key[j][e] = keep ? keys[i] : 0u;
+                    m[j] |= keep ? (1u << e) : 0u;
+                }
+            }
+        }
+        uint32_t c = 0;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) c += (uint32_t)__popc(m[j]);
+        block_combine<uint32_t, WARPS>(warp_sum(c), warp, lane, s_warp, wp, agg);  // also frees the stage
+        if (threadIdx.x == 0) {
+            if ((int64_t)t != ctx.fault_tile) {
+                if (t == 0) {
+                    if (num_tiles > 1) st_relaxed_u64(ctx.desc, pack_desc(epoch, kStateP, *agg));
+                } else {
+                    st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStateA, *agg));
+                }
+            }
+            consumed = k + 1;
+            if (k + STAGES < count) issue(k + STAGES);
+        }
+        compiler_fence();  // the count just published stays ahead of the look-back
+        return true;
+    };
+
+    uint32_t wp_cur = 0, agg_cur = 0, prev_incl = 0;
+    uint32_t fail_at = 0;
+
+    // One iteration: prepare tile k+1 into (mn, kn), look back for tile k
+    // and write tile k from (mc, kc).
+    auto step = [&](uint32_t k, uint32_t (&mc)[VPT], uint32_t (&kc)[VPT][4], uint32_t (&mn)[VPT],
+                    uint32_t (&kn)[VPT][4]) -> bool {
+        const uint32_t t = rank + k * G;
+        uint32_t wp_next = 0, agg_next = 0;
+        if (k + 1 < count && !prepare(k + 1, mn, kn, &wp_next, &agg_next)) {
+            fail_at = k;
+            return false;
+        }
+        if (warp == 0) {
+            uint32_t excl = 0;
+            bool lb_failed = false;
+            const bool dead = (int64_t)t == ctx.fault_tile;  // test hook only
+            if (t == 0) {
+                lb_failed = dead;
+            } else if (dead) {
+                lb_failed = true;
+            } else {
+                const int64_t floor = k > 0 ? (int64_t)t - (int64_t)G : -1;
+                excl = lookback<uint32_t, 1>(ctx, t, epoch, lane, &lb_failed, nullptr, floor, prev_incl);
+                if (lane == 0) {
+                    if (!lb_failed) {
+                        st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStateP, excl + agg_cur));
+                    } else {
+                        st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStatePoison, 0u));
+                        record_error(ctx.status, kErrLookbackTimeout, t);
+                    }
+                }
+            }
+            prev_incl = excl + agg_cur;
+            if (lane == 0) {
+                s_prefix = excl;
+                s_fail = lb_failed ? 1u : 0u;
+            }
+        }
+        uint32_t row_base[VPT];
+        uint32_t run = 0;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            uint32_t packed = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) packed |= (uint32_t)__popc(mc[4 * w + q]) << (8 * q);
+            const uint32_t inc = warp_inclusive_scan<uint32_t>(packed, lane);
+            const uint32_t exc = inc - packed;  // bytewise, no borrows (each byte <= 128)
+            const uint32_t rows = __shfl_sync(kFullMask, inc, 31);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                row_base[4 * w + q] = run + ((exc >> (8 * q)) & 0xffu);
+                run += (rows >> (8 * q)) & 0xffu;
+            }
+        }
+        __syncthreads();  // the prefix is in shared memory
+        if (s_fail) {
+            fail_at = k;
+            return false;
+        }
+        uint32_t* dst = out + (size_t)s_prefix + wp_cur;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            uint32_t pos = row_base[j];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if ((mc[j] >> e) & 1u) dst[pos++] = kc[j][e];
+            }
+        }
+        if (t == num_tiles - 1 && threadIdx.x == 0) *d_count = (unsigned long long)s_prefix + agg_cur;
+        wp_cur = wp_next;
+        agg_cur = agg_next;
+        return true;
+    };
+
+    uint32_t ma[VPT], mb[VPT];
+    uint32_t ka[VPT][4], kb[VPT][4];
+    bool failed = false;
+    if (threadIdx.x == 0)
+        for (uint32_t k = 0; k < count && k < (uint32_t)STAGES; ++k) issue(k);
+    if (count > 0 && !prepare(0, ma, ka, &wp_cur, &agg_cur)) failed = true;
+    for (uint32_t k = 0; !failed && k < count; k += 2) {
+        if (!step(k, ma, ka, mb, kb)) failed = true;
+        else if (k + 1 < count && !step(k + 1, mb, kb, ma, ka)) failed = true;
+    }
+
+    if (failed && threadIdx.x == 0) {
+        for (uint32_t k = fail_at + 1; k < count; ++k) {
+            const uint32_t t = rank + k * G;
+            if ((int64_t)t != ctx.fault_tile) st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStatePoison, 0u));
+        }
+        for (uint32_t k = consumed; k < issued; ++k)
+            mbar_wait_bounded(&bars[k % STAGES], (k / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
+    }
+}
+
+template <int THREADS, int VPT, int STAGES, bool SELECTIVE>
+static cudaError_t launch_compact_persistent(const uint32_t* keys, const uint8_t* flags, uint32_t* out,
+                                             unsigned long long* d_count, size_t n, const LookbackWs& ws,
+                                             cudaStream_t s) {
     constexpr size_t TILE = (size_t)THREADS * VPT * 4;
-    constexpr size_t SMEM = (size_t)STAGES * TILE * 5;
-    auto kern = k_compact_pipe<THREADS, VPT, STAGES>;
+    constexpr size_t SMEM = (size_t)STAGES * TILE * (SELECTIVE ? 1 : 5);
+    auto kern = [] {
+        if constexpr (SELECTIVE) return k_compact_sel<THREADS, VPT, STAGES>;
+        else return k_compact_pipe<THREADS, VPT, STAGES>;
+    }();
     static int blocks_per_sm = -1;
     static int sms = 0;
     if (blocks_per_sm < 0) {
@@ -281,6 +498,19 @@ cudaError_t launch_compact_pipe(const uint32_t* keys, const uint8_t* flags, uint
     LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};
     kern<<<grid, THREADS, SMEM, s>>>(keys, flags, out, d_count, n, tiles, ctx);
     return cudaGetLastError();
+}
+
+// 0: bulk-copied keys and flags; 1: bulk-copied flags, selective key loads.
+static int g_compact_kernel = 1;
+
+int compact_kernel_count() { return 2; }
+void set_compact_kernel(int k) { g_compact_kernel = k; }
+
+cudaError_t launch_compact_pipe(const uint32_t* keys, const uint8_t* flags, uint32_t* out,
+                                unsigned long long* d_count, size_t n, const LookbackWs& ws, cudaStream_t s) {
+    if (g_compact_kernel == 0)
+        return launch_compact_persistent<512, 8, 2, false>(keys, flags, out, d_count, n, ws, s);
+    return launch_compact_persistent<512, 8, 3, true>(keys, flags, out, d_count, n, ws, s);
 }
 
 }  // namespace ss

@@ -87,6 +87,8 @@ cudaError_t launch_compact_u32(const uint32_t* keys, const uint8_t* flags, uint3
 // and flags, n above one 16384-element tile.
 cudaError_t launch_compact_pipe(const uint32_t* keys, const uint8_t* flags, uint32_t* out,
                                 unsigned long long* d_count, size_t n, const LookbackWs& ws, cudaStream_t s);
+int compact_kernel_count();
+void set_compact_kernel(int k);
 
 // Ablations (reduce-then-scan, three kernels).  `totals` holds one value
 // per 4096-element tile.  tile_scan: 0 = register/shuffle tile scan,

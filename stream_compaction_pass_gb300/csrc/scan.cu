@@ -73,24 +73,15 @@ k_copy_probe(const uint32_t* in, uint32_t* out, size_t n, bool aligned) {
 
 // Configurations: {persistent, threads, items, stages, look-back K}.
 static const ScanConfig kConfigs[] = {
-    {0, 256, 16, 0, 1},  // 0: one CTA per 4096-element tile, 32-descriptor window
-    {0, 256, 32, 0, 1},  // 1: one CTA per 8192-element tile
-    {0, 512, 16, 0, 1},  // 2: 8192, 512 threads
-    {0, 256, 32, 0, 2},  // 3: 8192, 64-descriptor window
-    {0, 512, 16, 0, 2},  // 4: 8192, 512 threads, 64
-    {1, 512, 32, 2, 1},  // 5: persistent, 16384-element tiles, 2-stage ring (128 KB), 32 (the default)
-    {1, 512, 32, 3, 1},  // 6: persistent, 16384, 3 stages (192 KB), 32, single register buffer
-    {1, 512, 16, 3, 1},  // 7: persistent, 8192, 3 stages (96 KB, two CTAs per SM), 32
-    {1, 512, 32, 2, 2},  // 8: persistent, 16384, 2 stages, 64
-    {1, 512, 24, 3, 1},  // 9: persistent, 12288, 3 stages (144 KB), 32
-    {1, 1024, 16, 2, 1}, // 10: persistent, 16384, 1024 threads, 2 stages, 32
-    {2, 512, 32, 3, 5},  // 11: warp-specialised, 16384-element tiles, 3-stage ring (192 KB), 160, lagged
-    {2, 512, 32, 3, 1},  // 12: warp-specialised, 16384, 3 stages, 32, lagged
-    {2, 512, 32, 3, 5},  // 13: warp-specialised, 16384, 3 stages, 160, not lagged
-    {2, 256, 32, 3, 5},  // 14: warp-specialised, 8192, 3 stages (96 KB, two CTAs per SM), 160, lagged
+    {0, 256, 16, 0, 1},  // 0: one CTA per 4096-element tile (the allocation-free entry point's kernel)
+    {0, 256, 32, 0, 1},  // 1: one CTA per 8192-element tile (the fallback for unaligned or small inputs)
+    {1, 512, 32, 2, 1},  // 2: persistent, 16384-element tiles, 2-stage ring (128 KB) -- the default
+    {1, 512, 32, 3, 1},  // 3: persistent, 16384, 3 stages (192 KB), single register buffer
+    {1, 512, 16, 3, 1},  // 4: persistent, 8192, 3 stages (96 KB, two CTAs per SM)
+    {2, 512, 32, 3, 1},  // 5: persistent and warp-specialised, 16384, 3 stages, look-back one tile late
 };
 constexpr int kNumConfigs = sizeof(kConfigs) / sizeof(kConfigs[0]);
-constexpr int kDefaultConfig = 5;
+constexpr int kDefaultConfig = 2;
 
 int scan_config_count() { return kNumConfigs; }
 ScanConfig scan_config(int idx) { return kConfigs[(idx >= 0 && idx < kNumConfigs) ? idx : 0]; }
@@ -116,13 +107,8 @@ static cudaError_t launch_one(const void* in, void* out, size_t n, const Lookbac
 template <typename T, bool INCL>
 static cudaError_t dispatch_config(int config, const void* in, void* out, size_t n,
                                    const LookbackWs& ws, const void* ci, void* co, cudaStream_t s) {
-    switch (config) {
-        case 1: return launch_one<T, INCL, 256, 8, 1>(in, out, n, ws, ci, co, s);
-        case 2: return launch_one<T, INCL, 512, 4, 1>(in, out, n, ws, ci, co, s);
-        case 3: return launch_one<T, INCL, 256, 8, 2>(in, out, n, ws, ci, co, s);
-        case 4: return launch_one<T, INCL, 512, 4, 2>(in, out, n, ws, ci, co, s);
-        default: return launch_one<T, INCL, 256, 4, 1>(in, out, n, ws, ci, co, s);
-    }
+    if (config == 1) return launch_one<T, INCL, 256, 8, 1>(in, out, n, ws, ci, co, s);
+    return launch_one<T, INCL, 256, 4, 1>(in, out, n, ws, ci, co, s);
 }
 
 // The persistent kernel needs 16-byte aligned in/out (bulk copies) and at

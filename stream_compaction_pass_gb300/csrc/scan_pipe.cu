@@ -461,12 +461,9 @@ template <typename T, bool INCL, bool TRACE>
 static cudaError_t dispatch_pipe(int config, const void* in, void* out, size_t n, const LookbackWs& ws,
                                  const void* ci, void* co, unsigned long long* tr, cudaStream_t s) {
     switch (config) {  // the persistent rows of the configuration table (scan.cu)
-        case 6: return launch_pipe<T, INCL, 512, 8, 3, 1, TRACE, true>(in, out, n, ws, ci, co, tr, s);
-        case 7: return launch_pipe<T, INCL, 512, 4, 3, 1, TRACE>(in, out, n, ws, ci, co, tr, s);
-        case 8: return launch_pipe<T, INCL, 512, 8, 2, 2, TRACE>(in, out, n, ws, ci, co, tr, s);
-        case 9: return launch_pipe<T, INCL, 512, 6, 3, 1, TRACE>(in, out, n, ws, ci, co, tr, s);
-        case 10: return launch_pipe<T, INCL, 1024, 4, 2, 1, TRACE>(in, out, n, ws, ci, co, tr, s);
-        default:  // 5: the double register buffer spills for fp32 exclusive; that case takes the
+        case 3: return launch_pipe<T, INCL, 512, 8, 3, 1, TRACE, true>(in, out, n, ws, ci, co, tr, s);
+        case 4: return launch_pipe<T, INCL, 512, 4, 3, 1, TRACE>(in, out, n, ws, ci, co, tr, s);
+        default:  // 2: the double register buffer spills for fp32 exclusive; that case takes the
                   // single-buffer kernel with the same 16384-element tiles (and a third stage)
             if constexpr (std::is_same<T, float>::value && !INCL)
                 return launch_pipe<T, INCL, 512, 8, 3, 1, TRACE, true>(in, out, n, ws, ci, co, tr, s);

@@ -341,12 +341,8 @@ static cudaError_t launch_ws(const void* in, void* out, size_t n, const Lookback
 template <typename T, bool INCL, bool TRACE>
 static cudaError_t dispatch_ws(int config, const void* in, void* out, size_t n, const LookbackWs& ws,
                                const void* ci, void* co, unsigned long long* tr, cudaStream_t s) {
-    switch (config) {  // the warp-specialised rows of the configuration table (scan.cu)
-        case 12: return launch_ws<T, INCL, 16, 8, 3, 1, true, TRACE>(in, out, n, ws, ci, co, tr, s);
-        case 13: return launch_ws<T, INCL, 16, 8, 3, 5, false, TRACE>(in, out, n, ws, ci, co, tr, s);
-        case 14: return launch_ws<T, INCL, 8, 8, 3, 5, true, TRACE>(in, out, n, ws, ci, co, tr, s);
-        default: return launch_ws<T, INCL, 16, 8, 3, 5, true, TRACE>(in, out, n, ws, ci, co, tr, s);  // 11
-    }
+    (void)config;  // row 5, the only warp-specialised row
+    return launch_ws<T, INCL, 16, 8, 3, 1, true, TRACE>(in, out, n, ws, ci, co, tr, s);
 }
 
 cudaError_t launch_scan_lookback_ws(Dtype dt, bool inclusive, int config, const void* in, void* out,

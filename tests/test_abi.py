@@ -70,7 +70,7 @@ def test_config_table(lib):
     for c in range(n):
         ss.ss_set_scan_config(c)
         tiles.append(ss.ss_scan_tile_elems())
-    ss.ss_set_scan_config(5)  # the library's default row
+    ss.ss_set_scan_config(2)  # the library's default row
     assert tiles[0] == 4096 and all(t % 128 == 0 for t in tiles)
 
 

@@ -13,10 +13,12 @@ from gpu_helpers import SENTINEL, Guarded, assert_equal, compaction_input
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module")
-def ss():
+@pytest.fixture(scope="module", params=[1, 0], ids=["selective-keys", "bulk-keys"])
+def ss(request):
     import stream_compaction_pass_gb300 as m
-    return m
+    m.ss_set_compact_config(request.param)
+    yield m
+    m.ss_set_compact_config(1)
 
 
 def run_compact(ss, keys: np.ndarray, flags: np.ndarray, key_offset: int = 0, flag_offset: int = 0):

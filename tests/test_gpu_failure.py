@@ -17,13 +17,13 @@ pytestmark = pytest.mark.gpu
 TILE = 4096
 
 
-@pytest.fixture(scope="module", params=[0, 5, 11], ids=["one-cta-per-tile", "persistent", "warp-specialised"])
+@pytest.fixture(scope="module", params=[0, 2, 5], ids=["one-cta-per-tile", "persistent", "warp-specialised"])
 def ss(request):
     import stream_compaction_pass_gb300 as m
     m.ss_set_scan_config(request.param)
     yield m
     m.ss_debug_set_lookback_fault(-1, 0)
-    m.ss_set_scan_config(5)
+    m.ss_set_scan_config(2)
 
 
 def _scan(ss, x):
