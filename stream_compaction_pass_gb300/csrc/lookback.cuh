@@ -130,15 +130,40 @@ struct LookbackStats {
     uint32_t waits;    // polls that found an unpublished predecessor
 };
 
-//
+// The first window of a look-back, loaded ahead of time: the loads are
+// issued here and their values consumed by lookback(), so that their round
+// trip overlaps whatever the warp does in between.
+template <int K>
+struct LookbackWindow {
+    unsigned long long d[K];
+};
+
+template <typename T, int K>
+__device__ __forceinline__ LookbackWindow<K> lookback_prefetch(const LookbackCtx& c, uint32_t tile, uint32_t epoch,
+                                                               int lane, int64_t floor = -1,
+                                                               T floor_value = T(0)) {
+    LookbackWindow<K> w;
+    const unsigned long long floor_desc = pack_desc(epoch, kStateP, to_bits<T>(floor_value));
+    const int64_t pred = (int64_t)tile - 1;
+#pragma unroll
+    for (int q = 0; q < K; ++q) {
+        const int64_t idx = pred - (int64_t)lane * K - q;
+        w.d[q] = idx > floor ? ld_relaxed_u64(c.desc + idx) : floor_desc;
+    }
+    return w;
+}
+
+// Look-back for tile `tile` > 0 (see the description above LookbackStats).
 // `floor` (optional) is a tile whose inclusive prefix `floor_value` the caller
 // already knows (a persistent CTA's own previous tile); the walk treats it as
 // a published P and never reads at or below it.  Without a floor, tile -1
-// plays that role with value 0.
+// plays that role with value 0.  `window` (optional) is the first window,
+// already loaded by lookback_prefetch() with the same tile and floor.
 template <typename T, int K, bool TRACE = false>
 __device__ __forceinline__ T lookback(const LookbackCtx& c, uint32_t tile, uint32_t epoch, int lane,
                                       bool* failed, LookbackStats* stats = nullptr,
-                                      int64_t floor = -1, T floor_value = T(0)) {
+                                      int64_t floor = -1, T floor_value = T(0),
+                                      const LookbackWindow<K>* window = nullptr) {
     const uint32_t tag = epoch << 2;
     const unsigned long long floor_desc = pack_desc(epoch, kStateP, to_bits<T>(floor_value));
     if (TRACE) *stats = LookbackStats{0u, 0u};
@@ -146,14 +171,21 @@ __device__ __forceinline__ T lookback(const LookbackCtx& c, uint32_t tile, uint3
     int64_t pred = (int64_t)tile - 1;
     uint32_t polls = 0;
     uint64_t t0 = 0;
+    bool use_window = window != nullptr;
     *failed = false;
     while (true) {
         unsigned long long d[K];
         uint32_t st[K];
+        if (use_window) {
 #pragma unroll
-        for (int q = 0; q < K; ++q) {
-            const int64_t idx = pred - (int64_t)lane * K - q;
-            d[q] = idx > floor ? ld_relaxed_u64(c.desc + idx) : floor_desc;
+            for (int q = 0; q < K; ++q) d[q] = window->d[q];
+            use_window = false;
+        } else {
+#pragma unroll
+            for (int q = 0; q < K; ++q) {
+                const int64_t idx = pred - (int64_t)lane * K - q;
+                d[q] = idx > floor ? ld_relaxed_u64(c.desc + idx) : floor_desc;
+            }
         }
 #pragma unroll
         for (int q = 0; q < K; ++q) {

@@ -79,6 +79,7 @@ static const ScanConfig kConfigs[] = {
     {1, 512, 32, 3, 1},  // 3: persistent, 16384, 3 stages (192 KB), single register buffer
     {1, 512, 16, 3, 1},  // 4: persistent, 8192, 3 stages (96 KB, two CTAs per SM)
     {2, 512, 32, 3, 1},  // 5: persistent and warp-specialised, 16384, 3 stages, look-back one tile late
+    {1, 512, 32, 3, 1},  // 6: persistent, lean iteration (one barrier), 16384, 3 stages
 };
 constexpr int kNumConfigs = sizeof(kConfigs) / sizeof(kConfigs[0]);
 constexpr int kDefaultConfig = 2;

@@ -425,14 +425,226 @@ k_scan_lookback_pipe_sb(const T* in, T* out, size_t n, uint32_t num_tiles, Lookb
     }
 }
 
-template <typename T, bool INCL, int THREADS, int VPT, int STAGES, int K, bool TRACE, bool SB = false>
+// Lean form: one CTA-wide barrier per iteration.
+//  - Tile k+1's aggregate is formed without a barrier: each warp writes its
+//    total to shared memory and bumps an arrival counter; the warp that
+//    arrives last adds the totals up and publishes the aggregate.
+//  - Warp 0 issues the first window of tile k's look-back before its own row
+//    scan and consumes it afterwards, so that round trip overlaps the scan.
+//  - The iteration's one barrier both hands warp 0's prefix to everyone and
+//    tells the producer that tile k's stage has been read.
+// Warp totals rotate through three slots and prefixes through two, so no
+// slot is rewritten while a slower warp may still read it.
+template <typename T, bool INCLUSIVE, int THREADS, int VPT, int STAGES, int K, bool TRACE>
+__global__ void __launch_bounds__(THREADS, 1)
+k_scan_lookback_lean(const T* in, T* out, size_t n, uint32_t num_tiles, LookbackCtx ctx,
+                     const T* carry_in, T* carry_out, unsigned long long* trace) {
+    static_assert(STAGES >= 3, "tile k stays in the ring while tile k+1 is summed");
+    constexpr int WARPS = THREADS / 32;
+    constexpr uint32_t TILE = (uint32_t)THREADS * VPT * 4;
+    constexpr uint32_t TILE_BYTES = TILE * (uint32_t)sizeof(T);
+    constexpr uint32_t SEG = 32u * VPT * 4;
+
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    T* ring = reinterpret_cast<T*>(smem_raw);
+    __shared__ __align__(8) uint64_t bars[STAGES];
+    __shared__ T s_warp[3][WARPS];
+    __shared__ T s_agg[3];
+    __shared__ uint32_t s_arrive[3];
+    __shared__ T s_prefix[2];
+    __shared__ uint32_t s_fail[2];
+    __shared__ uint32_t s_abort, s_rank, s_epoch;
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const uint32_t G = gridDim.x;
+    const uint64_t policy = policy_evict_first();
+
+    if (threadIdx.x == 0) {
+        uint32_t rank, epoch;
+        claim_tile(ctx.counter, G, &rank, &epoch);
+        s_rank = rank;
+        s_epoch = epoch;
+        s_abort = 0;
+        for (int i = 0; i < 3; ++i) s_arrive[i] = 0;
+        for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
+        fence_async_shared();
+    }
+    __syncthreads();
+    const uint32_t rank = s_rank;
+    const uint32_t epoch = s_epoch;
+    if (rank >= G) {
+        if (threadIdx.x == 0) record_error(ctx.status, kErrCounter, rank);
+        return;
+    }
+    const uint32_t count = rank < num_tiles ? (num_tiles - rank + G - 1) / G : 0;
+    uint32_t issued = 0, consumed = 0;  // thread 0
+
+    auto issue = [&](uint32_t k) {
+        const int s = (int)(k % STAGES);
+        const size_t base = (size_t)(rank + k * G) * TILE;
+        if (base + TILE <= n) {
+            fence_async_shared();
+            mbar_arrive_expect_tx(&bars[s], TILE_BYTES);
+            bulk_load(ring + (size_t)s * TILE, in + base, TILE_BYTES, &bars[s], policy);
+        } else {
+            mbar_arrive(&bars[s]);
+        }
+        issued = k + 1;
+    };
+    auto read_rows = [&](uint32_t k, T (&v)[VPT][4]) {
+        const size_t tile_base = (size_t)(rank + k * G) * TILE;
+        if (tile_base + TILE <= n) {
+            const T* src = ring + (size_t)(k % STAGES) * TILE + (size_t)warp * SEG + (size_t)lane * 4;
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const uint4 r = lds_vec(src + 128 * j);
+                v[j][0] = from_bits<T>(r.x);
+                v[j][1] = from_bits<T>(r.y);
+                v[j][2] = from_bits<T>(r.z);
+                v[j][3] = from_bits<T>(r.w);
+            }
+        } else {
+            load_rows<T, VPT>(in, n, tile_base + (size_t)warp * SEG, lane, false, v);
+        }
+    };
+    // Waits for tile k and sums it; the last warp to finish publishes the
+    // aggregate.  A wait that runs out raises s_abort (seen after the barrier).
+    auto reduce_publish = [&](uint32_t k) {
+        const uint32_t t = rank + k * G;
+        const int slot = (int)(k % 3);
+        if (TRACE && threadIdx.x == 0) trace[(size_t)t * kTraceWords] = globaltimer_ns();
+        if (!mbar_wait_bounded(&bars[k % STAGES], (k / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns)) {
+            s_abort = 1u;
+            record_error(ctx.status, kErrBulkTimeout, t);
+        }
+        T v[VPT][4];
+        read_rows(k, v);
+        T x = T(0);
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) x += ((v[j][0] + v[j][1]) + v[j][2]) + v[j][3];
+        x = warp_sum(x);
+        if (lane == 0) {
+            s_warp[slot][warp] = x;
+            __threadfence_block();
+            if (atomicAdd(&s_arrive[slot], 1u) == (uint32_t)WARPS - 1u) {
+                __threadfence_block();
+                T agg = T(0);
+#pragma unroll
+                for (int w = 0; w < WARPS; ++w) agg += *reinterpret_cast<volatile T*>(&s_warp[slot][w]);
+                s_agg[slot] = agg;
+                s_arrive[slot] = 0u;
+                if ((int64_t)t != ctx.fault_tile) {
+                    if (t == 0) {
+                        if (num_tiles > 1)
+                            st_relaxed_u64(ctx.desc, pack_desc(epoch, kStateP,
+                                                               to_bits<T>((carry_in ? *carry_in : T(0)) + agg)));
+                    } else {
+                        st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStateA, to_bits<T>(agg)));
+                    }
+                }
+                if (TRACE) trace[(size_t)t * kTraceWords + 1] = trace[(size_t)t * kTraceWords + 2] = globaltimer_ns();
+            }
+        }
+        compiler_fence();  // a publish by this warp stays ahead of its look-back
+    };
+
+    if (threadIdx.x == 0)
+        for (uint32_t k = 0; k < count && k < (uint32_t)STAGES; ++k) issue(k);
+    if (count > 0) reduce_publish(0);
+    __syncthreads();  // tile 0's aggregate and warp totals are visible
+
+    T prev_incl = T(0);  // warp 0
+    uint32_t k = 0;
+    bool failed = s_abort != 0u;
+    for (; !failed && k < count; ++k) {
+        const uint32_t t = rank + k * G;
+        if (k + 1 < count) reduce_publish(k + 1);
+
+        LookbackWindow<K> win;
+        const T agg = s_agg[k % 3];  // formed in the previous iteration, visible since its barrier
+        const bool dead = (int64_t)t == ctx.fault_tile;  // test hook only
+        const int64_t floor = k > 0 ? (int64_t)t - (int64_t)G : -1;
+        if (warp == 0 && t != 0 && !dead) win = lookback_prefetch<T, K>(ctx, t, epoch, lane, floor, prev_incl);
+
+        T v[VPT][4];
+        read_rows(k, v);
+        T pre[VPT];
+        warp_rows_scan<T, VPT>(v, lane, pre);
+
+        if (warp == 0) {
+            LookbackStats stats{0u, 0u};
+            T excl = T(0);
+            bool lb_failed = false;
+            if (t == 0) {
+                excl = carry_in ? *carry_in : T(0);
+                lb_failed = dead;
+            } else if (dead) {
+                lb_failed = true;
+            } else {
+                excl = lookback<T, K, TRACE>(ctx, t, epoch, lane, &lb_failed, &stats, floor, prev_incl, &win);
+                if (lane == 0) {
+                    if (!lb_failed) {
+                        st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStateP, to_bits<T>(excl + agg)));
+                    } else {
+                        st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStatePoison, 0u));
+                        record_error(ctx.status, kErrLookbackTimeout, t);
+                    }
+                }
+            }
+            prev_incl = excl + agg;
+            if (lane == 0) {
+                s_prefix[k & 1] = excl;
+                s_fail[k & 1] = lb_failed ? 1u : 0u;
+                if (TRACE) {
+                    unsigned long long* rec = trace + (size_t)t * kTraceWords;
+                    rec[3] = globaltimer_ns();
+                    rec[5] = stats.windows;
+                    rec[6] = stats.waits;
+                    rec[7] = (unsigned long long)sm_id() | ((unsigned long long)blockIdx.x << 32);
+                }
+            }
+        }
+        __syncthreads();  // the prefix is out; tile k's stage has been read by everyone
+        if (threadIdx.x == 0) {
+            consumed = k + 1;
+            if (k + STAGES < count) issue(k + STAGES);
+        }
+        if (s_abort != 0u || s_fail[k & 1] != 0u) {
+            failed = true;
+            break;
+        }
+        T wp = T(0);
+#pragma unroll
+        for (int w = 0; w < WARPS; ++w)
+            if (w < warp) wp += s_warp[k % 3][w];
+        const size_t tile_base = (size_t)t * TILE;
+        rows_output_inplace<T, VPT, INCLUSIVE>(v, pre, s_prefix[k & 1] + wp);
+        store_rows<T, VPT>(out, n, tile_base + (size_t)warp * SEG, lane, tile_base + TILE <= n, v);
+        if (carry_out != nullptr && t == num_tiles - 1 && threadIdx.x == 0) *carry_out = s_prefix[k & 1] + agg;
+        if (TRACE && threadIdx.x == 0) trace[(size_t)t * kTraceWords + 4] = globaltimer_ns();
+    }
+
+    if (failed && threadIdx.x == 0) {
+        for (uint32_t j = k + 1; j < count; ++j) {
+            const uint32_t tt = rank + j * G;
+            if ((int64_t)tt != ctx.fault_tile) st_relaxed_u64(ctx.desc + tt, pack_desc(epoch, kStatePoison, 0u));
+        }
+        for (uint32_t j = consumed; j < issued; ++j)
+            mbar_wait_bounded(&bars[j % STAGES], (j / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
+    }
+}
+
+template <typename T, bool INCL, int THREADS, int VPT, int STAGES, int K, bool TRACE, bool SB = false,
+          bool LEAN = false>
 static cudaError_t launch_pipe(const void* in, void* out, size_t n, const LookbackWs& ws,
                                const void* carry_in, void* carry_out, unsigned long long* trace,
                                cudaStream_t s) {
     constexpr size_t TILE = (size_t)THREADS * VPT * 4;
     constexpr size_t SMEM = (size_t)STAGES * TILE * sizeof(T);
     auto kern = [] {
-        if constexpr (SB) return k_scan_lookback_pipe_sb<T, INCL, THREADS, VPT, STAGES, K, TRACE>;
+        if constexpr (LEAN) return k_scan_lookback_lean<T, INCL, THREADS, VPT, STAGES, K, TRACE>;
+        else if constexpr (SB) return k_scan_lookback_pipe_sb<T, INCL, THREADS, VPT, STAGES, K, TRACE>;
         else return k_scan_lookback_pipe<T, INCL, THREADS, VPT, STAGES, K, TRACE>;
     }();
     static int blocks_per_sm = -1;  // per instantiation; one device model in a process
@@ -463,6 +675,7 @@ static cudaError_t dispatch_pipe(int config, const void* in, void* out, size_t n
     switch (config) {  // the persistent rows of the configuration table (scan.cu)
         case 3: return launch_pipe<T, INCL, 512, 8, 3, 1, TRACE, true>(in, out, n, ws, ci, co, tr, s);
         case 4: return launch_pipe<T, INCL, 512, 4, 3, 1, TRACE>(in, out, n, ws, ci, co, tr, s);
+        case 6: return launch_pipe<T, INCL, 512, 8, 3, 1, TRACE, false, true>(in, out, n, ws, ci, co, tr, s);
         default:  // 2: the double register buffer spills for fp32 exclusive; that case takes the
                   // single-buffer kernel with the same 16384-element tiles (and a third stage)
             if constexpr (std::is_same<T, float>::value && !INCL)

@@ -17,7 +17,7 @@ pytestmark = pytest.mark.gpu
 TILE = 4096
 
 
-@pytest.fixture(scope="module", params=[0, 2, 5], ids=["one-cta-per-tile", "persistent", "warp-specialised"])
+@pytest.fixture(scope="module", params=[0, 2, 5, 6], ids=["one-cta-per-tile", "persistent", "warp-specialised", "lean"])
 def ss(request):
     import stream_compaction_pass_gb300 as m
     m.ss_set_scan_config(request.param)
