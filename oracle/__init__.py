@@ -44,8 +44,12 @@ def _declare(lib):
     lib.oracle_abs_prefix_f32.restype = None
     lib.oracle_compact_u32.argtypes = [p, p, p, sz]
     lib.oracle_compact_u32.restype = u64
-    lib.oracle_compact_positive_f32.argtypes = [p, p, sz]
-    lib.oracle_compact_positive_f32.restype = u64
+    for name in ("oracle_compact_positive_f32", "oracle_compact_positive_i32", "oracle_compact_positive_u32"):
+        f = getattr(lib, name)
+        f.argtypes = [p, p, sz]
+        f.restype = u64
+    lib.oracle_moe_counts_offsets.argtypes = [p, sz, ctypes.c_int32, ctypes.c_uint32, p, p]
+    lib.oracle_moe_counts_offsets.restype = None
     lib.oracle_blelloch_adds.argtypes = [u64]
     lib.oracle_blelloch_adds.restype = u64
     lib.oracle_hillis_steele_adds.argtypes = [u64]
@@ -107,10 +111,37 @@ def compact_u32(keys: np.ndarray, flags: np.ndarray, lib=None) -> np.ndarray:
 
 
 def compact_positive_f32(x: np.ndarray, lib=None) -> np.ndarray:
-    x = np.ascontiguousarray(x, dtype=np.float32)
-    out = np.empty(x.size, dtype=np.float32)
-    cnt = (lib or load()).oracle_compact_positive_f32(_ptr(x), _ptr(out), x.size)
+    """Elements with x > 0 (fp32 compare), in index order."""
+    return _compact_positive(x, np.float32, "oracle_compact_positive_f32", lib)
+
+
+def compact_positive_i32(x: np.ndarray, lib=None) -> np.ndarray:
+    """Elements with x > 0 (signed), in index order."""
+    return _compact_positive(x, np.int32, "oracle_compact_positive_i32", lib)
+
+
+def compact_positive_u32(x: np.ndarray, lib=None) -> np.ndarray:
+    """Nonzero elements, in index order."""
+    return _compact_positive(x, np.uint32, "oracle_compact_positive_u32", lib)
+
+
+def _compact_positive(x, dtype, fn, lib):
+    x = np.ascontiguousarray(x, dtype=dtype)
+    out = np.empty(x.size, dtype=dtype)
+    cnt = getattr(lib or load(), fn)(_ptr(x), _ptr(out), x.size)
     return out[:cnt].copy()
+
+
+def moe_counts_offsets(ids: np.ndarray, num_experts: int, align: int, lib=None):
+    """(counts[E] uint32, offsets[E+1] uint64): the histogram of expert ids
+    and each expert's start, segments rounded up to a multiple of `align`."""
+    ids = np.ascontiguousarray(ids, dtype=np.int32).reshape(-1)
+    assert num_experts >= 1 and align >= 1
+    counts = np.empty(num_experts, dtype=np.uint32)
+    offsets = np.empty(num_experts + 1, dtype=np.uint64)
+    (lib or load()).oracle_moe_counts_offsets(_ptr(ids), ids.size, num_experts, align, _ptr(counts),
+                                              _ptr(offsets))
+    return counts, offsets
 
 
 def blelloch_adds(tile: int, lib=None) -> int:

@@ -27,7 +27,10 @@
  *   - compaction keeps element i when flags[i] != 0, in index order; the
  *     number kept is the count ("Prefix sum and other parallel patterns",
  *     Stream compaction and Exercise 1: out[pos[i]] = in[i] where pos is the
- *     exclusive scan of the flags, total = pos[n-1] + flags[n-1]).
+ *     exclusive scan of the flags, total = pos[n-1] + flags[n-1]); the
+ *     predicate form keeps element i when x[i] > 0 in the element's type.
+ *   - MoE offsets: each expert's segment is rounded up to a whole number of
+ *     `align`-element GEMM tiles, and ids outside [0, E) are not counted.
  *
  * Parity pins: every function here is checked in tests/ against the pages'
  * worked examples (tests/golden/), closed forms, invariants and brute force;
@@ -125,4 +128,58 @@ uint64_t oracle_compact_positive_f32(const float *x, float *out, size_t n)
         }
     }
     return count;
+}
+
+/* The same predicate in the other element types: signed for int32, and
+ * "nonzero" for uint32 (an unsigned value is > 0 exactly when it is not 0). */
+uint64_t oracle_compact_positive_i32(const int32_t *x, int32_t *out, size_t n)
+{
+    uint64_t count = 0;
+    for (size_t i = 0; i < n; ++i) {
+        if (x[i] > 0) {
+            out[count] = x[i];
+            count += 1;
+        }
+    }
+    return count;
+}
+
+uint64_t oracle_compact_positive_u32(const uint32_t *x, uint32_t *out, size_t n)
+{
+    uint64_t count = 0;
+    for (size_t i = 0; i < n; ++i) {
+        if (x[i] > 0u) {
+            out[count] = x[i];
+            count += 1;
+        }
+    }
+    return count;
+}
+
+/*
+ * MoE token counts and aligned offsets ("Prefix sum and other parallel
+ * patterns", In LLMs: MoE token dispatch, steps 1-2, and Exercise 2):
+ *   counts[e]    = number of i < m with ids[i] == e        (the histogram)
+ *   offsets[0]   = 0
+ *   offsets[e+1] = offsets[e] + align * ceil(counts[e] / align)
+ * i.e. the exclusive prefix sum of the counts, each expert's segment rounded
+ * up to a multiple of the GEMM tile size `align`, so that offsets[e] is where
+ * expert e's tokens start and offsets[E] the padded total.  An id outside
+ * [0, E) belongs to no expert here and is not counted.  `offsets` holds E+1
+ * entries.
+ */
+void oracle_moe_counts_offsets(const int32_t *ids, size_t m, int32_t num_experts, uint32_t align,
+                               uint32_t *counts, uint64_t *offsets)
+{
+    for (int32_t e = 0; e < num_experts; ++e)
+        counts[e] = 0;
+    for (size_t i = 0; i < m; ++i) {
+        if (ids[i] >= 0 && ids[i] < num_experts)
+            counts[ids[i]] += 1;
+    }
+    offsets[0] = 0;
+    for (int32_t e = 0; e < num_experts; ++e) {
+        uint64_t blocks = ((uint64_t)counts[e] + align - 1) / align;
+        offsets[e + 1] = offsets[e] + blocks * align;
+    }
 }

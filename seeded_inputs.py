@@ -180,6 +180,38 @@ def workload_compaction(n: int, p: float, seed: int = 3):
     return keys, flags
 
 
+def workload_positive_f32(n: int, p: float, seed: int = 5) -> np.ndarray:
+    """fp32 uniform in [-(1 - p), p) for the predicate compaction (keep v > 0):
+    a fraction of about p is positive.  The [0, 1) draw is shifted by the
+    fp32 value nearest 1 - p, in fp32."""
+    return (uniform_f32(n, seed) - np.float32(1.0 - p)).astype(np.float32)
+
+
+def topk_ids(num_tokens: int, top_k: int, num_experts: int, seed: int = 6) -> np.ndarray:
+    """Router choices for an MoE layer: int32 [num_tokens, top_k], each row
+    top_k distinct experts drawn uniformly from [0, num_experts).
+
+    Column j of every row is drawn as ``((x >> 32) * E) >> 32`` from counter
+    range ``[(r * top_k + j) * num_tokens, ...)`` of the stream, redrawing
+    (r = 1, 2, ...) the rows where it repeats an earlier column of the row.
+    """
+    assert 1 <= top_k <= num_experts
+    E = np.uint64(num_experts)
+    out = np.empty((num_tokens, top_k), dtype=np.int32)
+    for j in range(top_k):
+        todo = np.arange(num_tokens)
+        r = 0
+        while todo.size:
+            x = raw_u64(seed, (r * top_k + j) * num_tokens, num_tokens)[todo]
+            out[todo, j] = (((x >> np.uint64(32)) * E) >> np.uint64(32)).astype(np.int32)
+            dup = np.zeros(todo.size, dtype=bool)
+            for q in range(j):
+                dup |= out[todo, q] == out[todo, j]
+            todo = todo[dup]
+            r += 1
+    return out
+
+
 def workload_poisson_counts(n: int, lam: float = 8.0, seed: int = 4) -> np.ndarray:
     """Radix-digit-histogram style counts: Poisson(8) as uint32."""
     return poisson_u32(n, lam, seed)

@@ -37,6 +37,13 @@ MUTANTS = [
     ("scan_ref.c", "            out[count] = keys[i];\n            count += 1;",
      "            count += 1;\n            out[count - 1] = keys[i - (i > 0)];", "compaction copies the wrong index"),
     ("scan_ref.c", "if (x[i] > 0.0f) {", "if (x[i] >= 0.0f) {", "predicate keeps zeros"),
+    ("scan_ref.c", "if (x[i] > 0) {", "if (x[i] >= 0) {", "int32 predicate keeps zeros"),
+    ("scan_ref.c", "if (x[i] > 0u) {", "if ((int32_t)x[i] > 0) {", "uint32 predicate compares signed"),
+    ("scan_ref.c", "uint64_t blocks = ((uint64_t)counts[e] + align - 1) / align;",
+     "uint64_t blocks = (uint64_t)counts[e] / align;", "MoE segments rounded down"),
+    ("scan_ref.c", "offsets[e + 1] = offsets[e] + blocks * align;",
+     "offsets[e + 1] = blocks * align;", "MoE offsets not accumulated"),
+    ("scan_ref.c", "counts[ids[i]] += 1;", "counts[ids[i]] += (i + 1 < m);", "MoE histogram drops the last id"),
     ("tile_model.c", "return i + i / 32 + i / 1024;", "return i + i / 32 + i / 512;", "two-term padding uses /512"),
     ("tile_model.c", "return i + i / 32;\n", "return i + i / 16;\n", "one-term padding uses /16"),
     ("tile_model.c", "total += 2 * level;", "total += level;", "model counts one sweep"),
@@ -100,6 +107,17 @@ def _checks(lib):
         == [int(k) for k, f in zip(keys, flags) if f != 0])
     xp = np.array([0.5, -1.0, 0.0, 2.0, -0.0, 3.5], dtype=np.float32)
     pin("compact_positive", lambda: oracle.compact_positive_f32(xp, lib=lib).tolist() == [0.5, 2.0, 3.5])
+    xi = np.array([5, 0, -3, 2147483647, -2147483648, 1], dtype=np.int32)
+    pin("compact_positive_i32", lambda: oracle.compact_positive_i32(xi, lib=lib).tolist() == [5, 2147483647, 1])
+    xu = np.array([0, 7, 0x80000000, 0, 0xFFFFFFFF], dtype=np.uint32)
+    pin("compact_positive_u32",
+        lambda: oracle.compact_positive_u32(xu, lib=lib).tolist() == [7, 0x80000000, 0xFFFFFFFF])
+
+    def moe_pin():
+        c, o = oracle.moe_counts_offsets(np.array([0, 2, 2, 3, 0, 2, 2]), 4, 4, lib=lib)
+        return c.tolist() == [2, 0, 4, 1] and o.tolist() == [0, 4, 4, 8, 12]
+
+    pin("moe_worked", moe_pin)
 
     pin("model_plain", lambda: oracle.blelloch_requests(4096, oracle.LAYOUT_PLAIN, lib=lib) == 1534)
     pin("model_pad32", lambda: oracle.blelloch_requests(4096, oracle.LAYOUT_PAD32, lib=lib) == 294)

@@ -10,8 +10,13 @@ Which pin covers which oracle function:
   O(n^2) brute force with Python big integers / exact fractions, and
   wraparound through an independent uint32 running sum.
 * abs_prefix_f32: brute force with exact fractions.
-* compact_u32 / compact_positive_f32: brute-force list filter, the count
-  identity pos[n-1] + flags[n-1], subsequence check, all-zero / all-one flags.
+* compact_u32 / compact_positive_*: brute-force list filter, the count
+  identity pos[n-1] + flags[n-1], subsequence check, all-zero / all-one
+  flags, IEEE special values written out by hand, agreement of the
+  predicate form with the flag form.
+* moe_counts_offsets: a worked example by hand, the histogram against
+  numpy's bincount, tile size 1 against the (pinned) exclusive scan, the
+  rounding invariants, one-expert and out-of-range cases.
 * the tile model: the pages' printed tables (tests/golden/).
 """
 
@@ -235,6 +240,98 @@ def test_compact_degenerate():
 def test_compact_positive_predicate():
     x = np.array([0.5, -1.0, 0.0, 2.0, -0.0, 3.5, float("nan")], dtype=np.float32)
     assert oracle.compact_positive_f32(x).tolist() == [0.5, 2.0, 3.5]
+
+
+def test_compact_positive_ieee_special_values():
+    # IEEE 754 ordering: NaN compares false, -0 == +0 is not > 0, infinities
+    # and the smallest subnormal order as numbers.  Expected output written
+    # out by hand, as bit patterns.
+    bits = np.array([0x7F800000,   # +inf   kept
+                     0xFF800000,   # -inf
+                     0x7FC00000,   # NaN
+                     0xFFC00000,   # -NaN
+                     0x00000000,   # +0
+                     0x80000000,   # -0
+                     0x00000001,   # smallest subnormal  kept
+                     0x80000001,   # its negative
+                     0x3F800000,   # 1.0    kept
+                     0x7F7FFFFF],  # FLT_MAX  kept
+                    dtype=np.uint32)
+    got = oracle.compact_positive_f32(bits.view(np.float32)).view(np.uint32)
+    assert got.tolist() == [0x7F800000, 0x00000001, 0x3F800000, 0x7F7FFFFF]
+
+
+def test_compact_positive_int_special_values():
+    xi = np.array([-2147483648, -1, 0, 1, 2147483647, 0, 42], dtype=np.int32)
+    assert oracle.compact_positive_i32(xi).tolist() == [1, 2147483647, 42]
+    xu = np.array([0, 1, 0x80000000, 0xFFFFFFFF, 0], dtype=np.uint32)
+    assert oracle.compact_positive_u32(xu).tolist() == [1, 0x80000000, 0xFFFFFFFF]
+
+
+@pytest.mark.parametrize("n", [0, 1, 7, 64])
+def test_compact_positive_brute_force(n):
+    x = si.workload_positive_f32(n, 0.5, seed=11)
+    got = oracle.compact_positive_f32(x)
+    assert [float(v) for v in got] == [float(v) for v in x if float(v) > 0.0]
+
+
+def test_compact_positive_agrees_with_flag_form():
+    # The predicate form equals the flag form with flags = (x > 0), through
+    # the separately pinned compact_u32 and the exclusive flag scan.
+    n = 1 << 15
+    for p in (0.01, 0.5, 0.99):
+        x = si.workload_positive_f32(n, p, seed=12)
+        f01 = (x > 0).astype(np.uint8)
+        got = oracle.compact_positive_f32(x)
+        assert np.array_equal(got.view(np.uint32), oracle.compact_u32(x.view(np.uint32), f01))
+        pos = oracle.scan_u32(f01.astype(np.uint32), False)
+        assert got.size == int(pos[-1]) + int(f01[-1])
+    xi = si.uniform_int32(n, -50, 50, seed=13)
+    assert np.array_equal(oracle.compact_positive_i32(xi).view(np.uint32),
+                          oracle.compact_u32(xi.view(np.uint32), (xi > 0).astype(np.uint8)))
+
+
+def test_moe_worked_example():
+    # E = 4 experts, GEMM tile 4: counts [2, 0, 4, 1] round up to segments
+    # [4, 0, 4, 4], so the starts are [0, 4, 4, 8] and the padded total 12.
+    counts, offsets = oracle.moe_counts_offsets(np.array([0, 2, 2, 3, 0, 2, 2]), 4, 4)
+    assert counts.tolist() == [2, 0, 4, 1]
+    assert offsets.tolist() == [0, 4, 4, 8, 12]
+
+
+def test_moe_histogram_is_bincount_and_align1_is_the_scan():
+    ids = si.topk_ids(4096, 8, 256, seed=6)
+    counts, offsets = oracle.moe_counts_offsets(ids, 256, 1)
+    assert np.array_equal(counts, np.bincount(ids.ravel(), minlength=256).astype(np.uint32))
+    assert counts.sum() == ids.size
+    # with a tile of one element the starts are the exclusive scan of the counts
+    assert np.array_equal(offsets[:-1].astype(np.uint32), oracle.scan_u32(counts, False))
+    assert int(offsets[-1]) == ids.size
+
+
+@pytest.mark.parametrize("align", [1, 16, 64, 128])
+def test_moe_alignment_invariants(align):
+    ids = si.topk_ids(1000, 6, 160, seed=7)
+    counts, offsets = oracle.moe_counts_offsets(ids, 160, align)
+    seg = np.diff(offsets.astype(np.int64))
+    assert (seg % align == 0).all()
+    assert (seg >= counts).all() and (seg < counts.astype(np.int64) + align).all()
+    assert ((counts == 0) == (seg == 0)).all()
+    assert offsets[0] == 0
+
+
+def test_moe_degenerate():
+    m = 1000
+    # every token on one expert: a single segment of ceil(m / 64) tiles
+    counts, offsets = oracle.moe_counts_offsets(np.full(m, 3), 5, 64)
+    assert counts.tolist() == [0, 0, 0, m, 0]
+    assert offsets.tolist() == [0, 0, 0, 0, 1024, 1024]
+    # ids outside [0, E) belong to no expert
+    counts, offsets = oracle.moe_counts_offsets(np.array([-1, 5, 7, 0, 4]), 5, 8)
+    assert counts.tolist() == [1, 0, 0, 0, 1]
+    assert offsets.tolist() == [0, 8, 8, 8, 8, 16]
+    counts, offsets = oracle.moe_counts_offsets(np.zeros(0, np.int32), 3, 64)
+    assert counts.tolist() == [0, 0, 0] and offsets.tolist() == [0, 0, 0, 0]
 
 
 def test_tile_model_against_page_tables(golden_dir):
