@@ -30,7 +30,7 @@
  *     wait that ran out) are recorded in the stream's status word and
  *     returned by the next ss_stream_status() call on that stream; the
  *     outputs of the failing call are then undefined.
- *   - n == 0 is a valid no-op (compact_u32 still writes *d_count = 0).
+ *   - n == 0 is a valid no-op (the compactions still write *d_count = 0).
  *   - The library owns a small per-(device, stream) workspace (tile
  *     descriptors, a tile counter, the status word), about 8 bytes per 4096
  *     elements, grown on demand with stream-ordered allocation and freed
@@ -105,6 +105,43 @@ ss_status scan_exclusive_f32(const float *in, float *out, size_t n, ss_stream_t 
  */
 ss_status compact_u32(const uint32_t *keys, const uint8_t *flags, uint32_t *out,
                       uint64_t *d_count, size_t n, ss_stream_t stream);
+
+/*
+ * Order-preserving compaction with a built-in predicate instead of a flag
+ * array: out receives, in index order, every in[i] with in[i] > 0, and
+ * *d_count the number kept ("Prefix sum and other parallel patterns",
+ * Stream compaction, compact.cu's predicate v > 0, and Exercise 1's flags
+ * in[i] > 0 fused into the scan's passes).  The predicate is evaluated in
+ * the element type: for fp32, NaN, +0.0 and -0.0 are dropped and +inf is
+ * kept; for int32 it is signed; for uint32 it means nonzero.  Kept elements
+ * are copied bit for bit.
+ *   in       device, n elements of `dtype`, read once.
+ *   out      device, room for n elements (only the first *d_count written);
+ *            must not overlap in.
+ *   d_count  device, one uint64, written by the call.
+ *   n        0 <= n < 2^32.
+ * Errors as compact_u32.
+ */
+ss_status compact_positive_f32(const float *in, float *out, uint64_t *d_count, size_t n, ss_stream_t stream);
+ss_status ss_compact_positive(ss_dtype dtype, const void *in, void *out, uint64_t *d_count, size_t n,
+                              ss_stream_t stream);
+
+/*
+ * Unordered compaction (the measured ablation): the same kept elements and
+ * count as compact_u32 / ss_compact_positive, but in no fixed order.  Each
+ * warp claims room for its kept elements with one atomic add on *d_count
+ * and writes them at the claimed offset plus their rank inside the warp
+ * ("Prefix sum and other parallel patterns", Stream compaction: the
+ * warp-aggregated atomic, ballot and popc).  Within each 512-element batch
+ * of a warp the order is kept; the order of the batches depends on the
+ * timing of the atomics.  Needs no workspace and no look-back.  *d_count is
+ * zeroed on the stream first, then counted up by the kernel.  Arguments and
+ * errors as the ordered calls.
+ */
+ss_status ss_compact_u32_unordered(const uint32_t *keys, const uint8_t *flags, uint32_t *out,
+                                   uint64_t *d_count, size_t n, ss_stream_t stream);
+ss_status ss_compact_positive_unordered(ss_dtype dtype, const void *in, void *out, uint64_t *d_count,
+                                        size_t n, ss_stream_t stream);
 
 /*
  * Generic scan entry: dtype, inclusive (0/1) and algorithm chosen at run

@@ -63,6 +63,10 @@ def _declare(lib):
         "scan_inclusive_f32": [P, P, SZ, P],
         "scan_exclusive_f32": [P, P, SZ, P],
         "compact_u32": [P, P, P, P, SZ, P],
+        "compact_positive_f32": [P, P, P, SZ, P],
+        "ss_compact_positive": [I, P, P, P, SZ, P],
+        "ss_compact_u32_unordered": [P, P, P, P, SZ, P],
+        "ss_compact_positive_unordered": [I, P, P, P, SZ, P],
         "ss_scan": [I, I, I, P, P, SZ, P],
         "ss_scan_seeded": [I, I, P, P, SZ, P, P, P],
         "ss_scan_host": [I, I, P, P, SZ, P],
@@ -182,6 +186,34 @@ def compact_u32(keys, flags, out, d_count, n=None, stream=None):
         n = _numel(keys)
     _check(lib().compact_u32(_addr(keys), _addr(flags), _addr(out), _addr(d_count), n,
                              _stream(stream, keys, flags, out)), "compact_u32")
+
+
+def compact_positive_f32(inp, out, d_count, n=None, stream=None):
+    if n is None:
+        n = _numel(inp)
+    _check(lib().compact_positive_f32(_addr(inp), _addr(out), _addr(d_count), n, _stream(stream, inp, out)),
+           "compact_positive_f32")
+
+
+def ss_compact_positive(dtype: int, inp, out, d_count, n=None, stream=None):
+    if n is None:
+        n = _numel(inp)
+    _check(lib().ss_compact_positive(dtype, _addr(inp), _addr(out), _addr(d_count), n, _stream(stream, inp, out)),
+           "ss_compact_positive")
+
+
+def ss_compact_u32_unordered(keys, flags, out, d_count, n=None, stream=None):
+    if n is None:
+        n = _numel(keys)
+    _check(lib().ss_compact_u32_unordered(_addr(keys), _addr(flags), _addr(out), _addr(d_count), n,
+                                          _stream(stream, keys, flags, out)), "ss_compact_u32_unordered")
+
+
+def ss_compact_positive_unordered(dtype: int, inp, out, d_count, n=None, stream=None):
+    if n is None:
+        n = _numel(inp)
+    _check(lib().ss_compact_positive_unordered(dtype, _addr(inp), _addr(out), _addr(d_count), n,
+                                               _stream(stream, inp, out)), "ss_compact_positive_unordered")
 
 
 def ss_scan(dtype: int, inclusive: bool, algo: int, inp, out, n=None, stream=None):

@@ -198,6 +198,58 @@ Dtype to_dtype(ss_dtype d) {
 
 bool valid_dtype(ss_dtype d) { return d == SS_I32 || d == SS_U32 || d == SS_F32; }
 
+ss::KeepRule positive_rule(ss_dtype dtype) {
+    switch (dtype) {
+        case SS_F32: return ss::KeepRule::PositiveF32;
+        case SS_I32: return ss::KeepRule::PositiveI32;
+        default: return ss::KeepRule::PositiveU32;
+    }
+}
+
+// Every compaction entry point: argument checks, then the ordered
+// (look-back) or the unordered (warp-aggregated atomic) kernel.  `flags` is
+// used, and required, only under KeepRule::Flags.
+ss_status compact_any(ss::KeepRule rule, const void* keys_v, const uint8_t* flags, void* out_v, uint64_t* d_count,
+                      size_t n, bool unordered, cudaStream_t s) {
+    const uint32_t* keys = static_cast<const uint32_t*>(keys_v);
+    uint32_t* out = static_cast<uint32_t*>(out_v);
+    const bool with_flags = rule == ss::KeepRule::Flags;
+    if (d_count == nullptr) return fail(SS_ERR_INVALID_ARG, "d_count is null");
+    if (reinterpret_cast<uintptr_t>(d_count) & 7u)
+        return fail(SS_ERR_INVALID_ARG, "d_count must be 8-byte aligned");
+    if (n > 0) {
+        if (!keys || !out || (with_flags && !flags)) return fail(SS_ERR_INVALID_ARG, "null pointer with n > 0");
+        if ((reinterpret_cast<uintptr_t>(keys) | reinterpret_cast<uintptr_t>(out)) & 3u)
+            return fail(SS_ERR_INVALID_ARG, "keys/out must be 4-byte aligned");
+        if (n > 0xffffffffull) return fail(SS_ERR_INVALID_ARG, "n must be < 2^32");
+        if (overlaps(out, n * 4, keys, n * 4) || (with_flags && overlaps(out, n * 4, flags, n)))
+            return fail(SS_ERR_INVALID_ARG, "out overlaps keys or flags");
+        if (overlaps(d_count, 8, out, n * 4) || overlaps(d_count, 8, keys, n * 4) ||
+            (with_flags && overlaps(d_count, 8, flags, n)))
+            return fail(SS_ERR_INVALID_ARG, "d_count overlaps an array");
+    }
+    if (n == 0) {
+        cudaError_t e = cudaMemsetAsync(d_count, 0, 8, s);
+        return e == cudaSuccess ? SS_OK : cuda_fail(e, "cudaMemsetAsync");
+    }
+    if (unordered) {
+        cudaError_t e = ss::launch_compact_unordered(rule, keys, flags, out,
+                                                     reinterpret_cast<unsigned long long*>(d_count), n, s);
+        return e == cudaSuccess ? SS_OK : cuda_fail(e, "unordered compaction launch");
+    }
+    const size_t tiles = (n + ss::kCompactTile - 1) / ss::kCompactTile;
+    Workspace* w = nullptr;
+    if (tiles > 1 || g_fault_tile.load() >= 0) {
+        ss_status st = get_workspace(s, &w);
+        if (st != SS_OK) return st;
+        st = ensure_desc(w, tiles);
+        if (st != SS_OK) return st;
+    }
+    cudaError_t e = ss::launch_compact(rule, keys, flags, out, reinterpret_cast<unsigned long long*>(d_count), n,
+                                       make_ws(w), s);
+    return e == cudaSuccess ? SS_OK : cuda_fail(e, "compaction launch");
+}
+
 }  // namespace
 
 extern "C" {
@@ -241,35 +293,28 @@ ss_status ss_scan_seeded(ss_dtype dtype, int inclusive, const void* in, void* ou
 
 ss_status compact_u32(const uint32_t* keys, const uint8_t* flags, uint32_t* out, uint64_t* d_count,
                       size_t n, ss_stream_t stream) {
-    cudaStream_t s = (cudaStream_t)stream;
-    if (d_count == nullptr) return fail(SS_ERR_INVALID_ARG, "d_count is null");
-    if (reinterpret_cast<uintptr_t>(d_count) & 7u)
-        return fail(SS_ERR_INVALID_ARG, "d_count must be 8-byte aligned");
-    if (n > 0) {
-        if (!keys || !flags || !out) return fail(SS_ERR_INVALID_ARG, "null pointer with n > 0");
-        if ((reinterpret_cast<uintptr_t>(keys) | reinterpret_cast<uintptr_t>(out)) & 3u)
-            return fail(SS_ERR_INVALID_ARG, "keys/out must be 4-byte aligned");
-        if (n > 0xffffffffull) return fail(SS_ERR_INVALID_ARG, "n must be < 2^32");
-        if (overlaps(out, n * 4, keys, n * 4) || overlaps(out, n * 4, flags, n))
-            return fail(SS_ERR_INVALID_ARG, "out overlaps keys or flags");
-        if (overlaps(d_count, 8, out, n * 4))
-            return fail(SS_ERR_INVALID_ARG, "d_count overlaps out");
-    }
-    if (n == 0) {
-        cudaError_t e = cudaMemsetAsync(d_count, 0, 8, s);
-        return e == cudaSuccess ? SS_OK : cuda_fail(e, "cudaMemsetAsync");
-    }
-    const size_t tiles = (n + ss::kCompactTile - 1) / ss::kCompactTile;
-    Workspace* w = nullptr;
-    if (tiles > 1 || g_fault_tile.load() >= 0) {
-        ss_status st = get_workspace(s, &w);
-        if (st != SS_OK) return st;
-        st = ensure_desc(w, tiles);
-        if (st != SS_OK) return st;
-    }
-    cudaError_t e = ss::launch_compact_u32(keys, flags, out, reinterpret_cast<unsigned long long*>(d_count),
-                                           n, make_ws(w), s);
-    return e == cudaSuccess ? SS_OK : cuda_fail(e, "compaction launch");
+    return compact_any(ss::KeepRule::Flags, keys, flags, out, d_count, n, false, (cudaStream_t)stream);
+}
+
+ss_status compact_positive_f32(const float* in, float* out, uint64_t* d_count, size_t n, ss_stream_t stream) {
+    return compact_any(ss::KeepRule::PositiveF32, in, nullptr, out, d_count, n, false, (cudaStream_t)stream);
+}
+
+ss_status ss_compact_positive(ss_dtype dtype, const void* in, void* out, uint64_t* d_count, size_t n,
+                              ss_stream_t stream) {
+    if (!valid_dtype(dtype)) return fail(SS_ERR_UNSUPPORTED, "unknown dtype");
+    return compact_any(positive_rule(dtype), in, nullptr, out, d_count, n, false, (cudaStream_t)stream);
+}
+
+ss_status ss_compact_u32_unordered(const uint32_t* keys, const uint8_t* flags, uint32_t* out, uint64_t* d_count,
+                                   size_t n, ss_stream_t stream) {
+    return compact_any(ss::KeepRule::Flags, keys, flags, out, d_count, n, true, (cudaStream_t)stream);
+}
+
+ss_status ss_compact_positive_unordered(ss_dtype dtype, const void* in, void* out, uint64_t* d_count, size_t n,
+                                        ss_stream_t stream) {
+    if (!valid_dtype(dtype)) return fail(SS_ERR_UNSUPPORTED, "unknown dtype");
+    return compact_any(positive_rule(dtype), in, nullptr, out, d_count, n, true, (cudaStream_t)stream);
 }
 
 ss_status ss_scan(ss_dtype dtype, int inclusive, ss_algo algo, const void* in, void* out, size_t n,

@@ -1,6 +1,7 @@
 // compact.cu -- single-pass, order-preserving stream compaction.
 //
-// keep[i] = (flags[i] != 0); out[pos[i]] = keys[i] for kept i, where pos is
+// keep[i] = (flags[i] != 0), or a built-in predicate of keys[i] (keep.cuh);
+// out[pos[i]] = keys[i] for kept i, where pos is
 // the exclusive scan of keep; count = pos[n-1] + keep[n-1] ("Prefix sum and
 // other parallel patterns", Stream compaction and Exercise 1).  The flag
 // scan, the look-back and the scatter are fused into one pass, so neither
@@ -10,7 +11,8 @@
 // Per tile of 4096 elements (256 threads, warp-striped rows of 4-element
 // vectors as in tile.cuh):
 //   1. load the flag bytes (one 32-bit word per 4 keys) and the key vectors;
-//      a key vector whose four flags are all zero is not loaded;
+//      a key vector whose four flags are all zero is not loaded (under a
+//      predicate every key vector is loaded and tested instead);
 //   2. per-row keep masks; the four rows' counts are packed into the bytes
 //      of one 32-bit word and scanned across the warp in one shuffle scan
 //      (each byte stays <= 128, so bytes never carry into each other); inside
@@ -21,6 +23,7 @@
 //   4. kept keys are staged in shared memory at their tile-local rank and
 //      written out as one contiguous, coalesced run.
 #include "internal.h"
+#include "keep.cuh"
 #include "tile.cuh"
 
 namespace ss {
@@ -47,6 +50,7 @@ __device__ __forceinline__ uint32_t nonzero_byte_mask(uint32_t w) {
 
 }  // namespace
 
+template <KeepRule RULE>
 __global__ void __launch_bounds__(kThreads)
 k_compact_u32(const uint32_t* keys, const uint8_t* flags, uint32_t* out,
               unsigned long long* d_count, size_t n, uint32_t num_tiles, LookbackCtx ctx,
@@ -77,7 +81,7 @@ k_compact_u32(const uint32_t* keys, const uint8_t* flags, uint32_t* out,
 
     uint32_t m[kVpt];
     uint32_t key[kVpt][4];
-    if (fast) {
+    if (fast && RULE == KeepRule::Flags) {
         uint32_t fw[kVpt];
 #pragma unroll
         for (int j = 0; j < kVpt; ++j) fw[j] = ld_u32(flags + seg + (size_t)(32 * j + lane) * 4);
@@ -92,6 +96,17 @@ k_compact_u32(const uint32_t* keys, const uint8_t* flags, uint32_t* out,
             key[j][2] = r.z;
             key[j][3] = r.w;
         }
+    } else if (fast) {  // predicate: every key vector is loaded and tested
+        const uint4* kp = reinterpret_cast<const uint4*>(keys + seg) + lane;
+#pragma unroll
+        for (int j = 0; j < kVpt; ++j) {
+            const uint4 r = ld_vec(kp + 32 * j);
+            key[j][0] = r.x;
+            key[j][1] = r.y;
+            key[j][2] = r.z;
+            key[j][3] = r.w;
+            m[j] = keep_mask4<RULE>(key[j]);
+        }
     } else {
 #pragma unroll
         for (int j = 0; j < kVpt; ++j) {
@@ -99,8 +114,17 @@ k_compact_u32(const uint32_t* keys, const uint8_t* flags, uint32_t* out,
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const size_t i = seg + (size_t)(32 * j + lane) * 4 + k;
-                const bool keep = i < n && flags[i] != 0;
-                key[j][k] = keep ? keys[i] : 0u;
+                bool keep = false;
+                key[j][k] = 0u;
+                if (i < n) {
+                    if constexpr (RULE == KeepRule::Flags) {
+                        keep = flags[i] != 0;
+                        if (keep) key[j][k] = keys[i];
+                    } else {
+                        key[j][k] = keys[i];
+                        keep = keep_bits<RULE>(key[j][k]);
+                    }
+                }
                 m[j] |= keep ? (1u << k) : 0u;
             }
         }
@@ -172,20 +196,30 @@ k_compact_u32(const uint32_t* keys, const uint8_t* flags, uint32_t* out,
         *d_count = (unsigned long long)s_prefix + tile_count;
 }
 
-cudaError_t launch_compact_u32(const uint32_t* keys, const uint8_t* flags, uint32_t* out,
-                               unsigned long long* d_count, size_t n, const LookbackWs& ws,
-                               cudaStream_t s) {
-    // Large aligned inputs take the persistent kernel (bulk copies need
-    // 16-byte aligned sources); the rest stay on one CTA per 4096-element tile.
-    if (((reinterpret_cast<uintptr_t>(keys) | reinterpret_cast<uintptr_t>(flags)) & 15u) == 0 &&
-        n > (size_t)16384)
-        return launch_compact_pipe(keys, flags, out, d_count, n, ws, s);
+template <KeepRule RULE>
+static cudaError_t launch_per_tile(const uint32_t* keys, const uint8_t* flags, uint32_t* out,
+                                   unsigned long long* d_count, size_t n, const LookbackWs& ws, cudaStream_t s) {
     const uint32_t tiles = (uint32_t)((n + kCompactTile - 1) / kCompactTile);
     LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};
     const bool aligned = ((reinterpret_cast<uintptr_t>(keys) & 15u) == 0) &&
-                         ((reinterpret_cast<uintptr_t>(flags) & 3u) == 0);
-    k_compact_u32<<<tiles, kThreads, 0, s>>>(keys, flags, out, d_count, n, tiles, ctx, aligned);
+                         (RULE != KeepRule::Flags || (reinterpret_cast<uintptr_t>(flags) & 3u) == 0);
+    k_compact_u32<RULE><<<tiles, kThreads, 0, s>>>(keys, flags, out, d_count, n, tiles, ctx, aligned);
     return cudaGetLastError();
+}
+
+cudaError_t launch_compact(KeepRule rule, const uint32_t* keys, const uint8_t* flags, uint32_t* out,
+                           unsigned long long* d_count, size_t n, const LookbackWs& ws, cudaStream_t s) {
+    // Large aligned inputs take the persistent kernel (bulk copies need
+    // 16-byte aligned sources); the rest stay on one CTA per 4096-element tile.
+    uintptr_t align = reinterpret_cast<uintptr_t>(keys);
+    if (rule == KeepRule::Flags) align |= reinterpret_cast<uintptr_t>(flags);
+    if ((align & 15u) == 0 && n > (size_t)16384) return launch_compact_pipe(rule, keys, flags, out, d_count, n, ws, s);
+    switch (rule) {
+        case KeepRule::Flags: return launch_per_tile<KeepRule::Flags>(keys, flags, out, d_count, n, ws, s);
+        case KeepRule::PositiveF32: return launch_per_tile<KeepRule::PositiveF32>(keys, flags, out, d_count, n, ws, s);
+        case KeepRule::PositiveI32: return launch_per_tile<KeepRule::PositiveI32>(keys, flags, out, d_count, n, ws, s);
+        default: return launch_per_tile<KeepRule::PositiveU32>(keys, flags, out, d_count, n, ws, s);
+    }
 }
 
 }  // namespace ss

@@ -1,14 +1,15 @@
 // compact_pipe.cu -- the fused order-preserving compaction as a persistent
 // kernel fed by the bulk-copy engine.
 //
-// Same result as compact.cu (keep keys[i] where flags[i] != 0, in order;
-// "Prefix sum and other parallel patterns", Stream compaction and Exercise
-// 1), on the schedule of the persistent scan (scan_pipe.cu): each CTA takes
-// a rank from the workspace counter and handles tiles rank, rank + G, ...;
-// a two-stage shared-memory ring receives each tile's keys and flags with two
-// bulk copies.  Iteration k:
-//   1. count the kept elements of tile k+1 from its flags alone and publish
-//      that count one iteration early (the count is the tile's aggregate);
+// Same result as compact.cu (keep keys[i] where flags[i] != 0, or where a
+// built-in predicate of keys[i] holds, in order; "Prefix sum and other
+// parallel patterns", Stream compaction and Exercise 1), on the schedule of
+// the persistent scan (scan_pipe.cu): each CTA takes a rank from the
+// workspace counter and handles tiles rank, rank + G, ...; a shared-memory
+// ring receives each tile's keys and flags with two bulk copies (the keys
+// alone under a predicate).  Iteration k:
+//   1. count the kept elements of tile k+1 from its flags (or keys) and
+//      publish that count one iteration early (the tile's aggregate);
 //   2. warp 0 looks back for tile k, no further than this CTA's previous
 //      tile, while the other warps rank tile k's kept keys in registers
 //      (per-row keep masks; the rows' counts packed one byte per row and
@@ -22,6 +23,7 @@
 
 #include "bulk.cuh"
 #include "internal.h"
+#include "keep.cuh"
 #include "tile.cuh"
 
 namespace ss {
@@ -41,7 +43,7 @@ __device__ __forceinline__ uint32_t lds_u32(const void* p) {
 
 }  // namespace
 
-template <int THREADS, int VPT, int STAGES>
+template <int THREADS, int VPT, int STAGES, KeepRule RULE>
 __global__ void __launch_bounds__(THREADS, 1)
 k_compact_pipe(const uint32_t* keys, const uint8_t* flags, uint32_t* out, unsigned long long* d_count,
                size_t n, uint32_t num_tiles, LookbackCtx ctx) {
@@ -50,7 +52,8 @@ k_compact_pipe(const uint32_t* keys, const uint8_t* flags, uint32_t* out, unsign
     constexpr int NW = VPT / 4;  // packed count words per lane
     constexpr uint32_t TILE = (uint32_t)THREADS * VPT * 4;
     constexpr uint32_t KEY_BYTES = TILE * 4;
-    constexpr uint32_t STAGE_BYTES = KEY_BYTES + TILE;  // keys, then flags
+    constexpr bool FLAGS = RULE == KeepRule::Flags;
+    constexpr uint32_t STAGE_BYTES = KEY_BYTES + (FLAGS ? TILE : 0u);  // keys, then flags
     constexpr uint32_t SEG = 32u * VPT * 4;
 
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -89,17 +92,44 @@ k_compact_pipe(const uint32_t* keys, const uint8_t* flags, uint32_t* out, unsign
             fence_async_shared();
             mbar_arrive_expect_tx(&bars[s], STAGE_BYTES);
             bulk_load(stage_keys(k), keys + base, KEY_BYTES, &bars[s], policy);
-            bulk_load(stage_keys(k) + KEY_BYTES, flags + base, TILE, &bars[s], policy);
+            if constexpr (FLAGS) bulk_load(stage_keys(k) + KEY_BYTES, flags + base, TILE, &bars[s], policy);
         } else {
             mbar_arrive(&bars[s]);  // ragged last tile: read from global
         }
         issued = k + 1;
     };
+    // This lane's key vectors of tile k (full tiles only).
+    auto read_keys = [&](uint32_t k, uint32_t (&key)[VPT][4]) {
+        const unsigned char* kb = stage_keys(k) + ((size_t)warp * SEG + (size_t)lane * 4) * 4;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const uint4 r = lds_vec(kb + 512 * j);
+            key[j][0] = r.x;
+            key[j][1] = r.y;
+            key[j][2] = r.z;
+            key[j][3] = r.w;
+        }
+    };
     // Keep masks of this lane's rows of tile k (bit e of m[j]: element e of row j is kept).
     auto read_masks = [&](uint32_t k, uint32_t (&m)[VPT]) {
         const size_t tile_base = (size_t)(rank + k * G) * TILE;
         const size_t seg = tile_base + (size_t)warp * SEG;
-        if (tile_base + TILE <= n) {
+        if (!FLAGS && tile_base + TILE <= n) {
+            uint32_t key[VPT][4];
+            read_keys(k, key);
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) m[j] = keep_mask4<RULE>(key[j]);
+        } else if (!FLAGS) {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                m[j] = 0;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const size_t i = seg + (size_t)(32 * j + lane) * 4 + e;
+                    if (i < n && keep_bits<RULE>(keys[i])) m[j] |= 1u << e;
+                }
+            }
+        } else if (tile_base + TILE <= n) {
             const unsigned char* f = stage_keys(k) + KEY_BYTES + (size_t)warp * SEG + (size_t)lane * 4;
 #pragma unroll
             for (int j = 0; j < VPT; ++j) m[j] = byte_keep_mask(lds_u32(f + 128 * j));
@@ -186,18 +216,15 @@ k_compact_pipe(const uint32_t* keys, const uint8_t* flags, uint32_t* out, unsign
         const size_t seg = tile_base + (size_t)warp * SEG;
         uint32_t m[VPT];
         uint32_t key[VPT][4];
-        read_masks(k, m);
-        if (tile_base + TILE <= n) {
-            const unsigned char* kb = stage_keys(k) + ((size_t)warp * SEG + (size_t)lane * 4) * 4;
+        if (!FLAGS && tile_base + TILE <= n) {
+            read_keys(k, key);
 #pragma unroll
-            for (int j = 0; j < VPT; ++j) {
-                const uint4 r = lds_vec(kb + 512 * j);
-                key[j][0] = r.x;
-                key[j][1] = r.y;
-                key[j][2] = r.z;
-                key[j][3] = r.w;
-            }
+            for (int j = 0; j < VPT; ++j) m[j] = keep_mask4<RULE>(key[j]);
+        } else if (tile_base + TILE <= n) {
+            read_masks(k, m);
+            read_keys(k, key);
         } else {
+            read_masks(k, m);
 #pragma unroll
             for (int j = 0; j < VPT; ++j)
 #pragma unroll
@@ -469,15 +496,16 @@ k_compact_sel(const uint32_t* keys, const uint8_t* flags, uint32_t* out, unsigne
     }
 }
 
-template <int THREADS, int VPT, int STAGES, bool SELECTIVE>
+template <int THREADS, int VPT, int STAGES, bool SELECTIVE, KeepRule RULE = KeepRule::Flags>
 static cudaError_t launch_compact_persistent(const uint32_t* keys, const uint8_t* flags, uint32_t* out,
                                              unsigned long long* d_count, size_t n, const LookbackWs& ws,
                                              cudaStream_t s) {
+    static_assert(!SELECTIVE || RULE == KeepRule::Flags, "selective key loads need a flag array");
     constexpr size_t TILE = (size_t)THREADS * VPT * 4;
-    constexpr size_t SMEM = (size_t)STAGES * TILE * (SELECTIVE ? 1 : 5);
+    constexpr size_t SMEM = (size_t)STAGES * TILE * (SELECTIVE ? 1 : (RULE == KeepRule::Flags ? 5 : 4));
     auto kern = [] {
         if constexpr (SELECTIVE) return k_compact_sel<THREADS, VPT, STAGES>;
-        else return k_compact_pipe<THREADS, VPT, STAGES>;
+        else return k_compact_pipe<THREADS, VPT, STAGES, RULE>;
     }();
     static int blocks_per_sm = -1;
     static int sms = 0;
@@ -506,8 +534,20 @@ static int g_compact_kernel = 1;
 int compact_kernel_count() { return 2; }
 void set_compact_kernel(int k) { g_compact_kernel = k; }
 
-cudaError_t launch_compact_pipe(const uint32_t* keys, const uint8_t* flags, uint32_t* out,
+cudaError_t launch_compact_pipe(KeepRule rule, const uint32_t* keys, const uint8_t* flags, uint32_t* out,
                                 unsigned long long* d_count, size_t n, const LookbackWs& ws, cudaStream_t s) {
+    switch (rule) {  // a predicate needs every key, so its keys come through the ring
+        case KeepRule::PositiveF32:
+            return launch_compact_persistent<512, 8, 3, false, KeepRule::PositiveF32>(keys, flags, out, d_count, n,
+                                                                                       ws, s);
+        case KeepRule::PositiveI32:
+            return launch_compact_persistent<512, 8, 3, false, KeepRule::PositiveI32>(keys, flags, out, d_count, n,
+                                                                                       ws, s);
+        case KeepRule::PositiveU32:
+            return launch_compact_persistent<512, 8, 3, false, KeepRule::PositiveU32>(keys, flags, out, d_count, n,
+                                                                                       ws, s);
+        default: break;
+    }
     if (g_compact_kernel == 0)
         return launch_compact_persistent<512, 8, 2, false>(keys, flags, out, d_count, n, ws, s);
     return launch_compact_persistent<512, 8, 3, true>(keys, flags, out, d_count, n, ws, s);

@@ -77,18 +77,27 @@ cudaError_t launch_scan_lookback(Dtype dt, bool inclusive, int config, const voi
 // Streaming copy with the scan's loader and storer (the bandwidth probe).
 cudaError_t launch_copy_probe(int config, const void* in, void* out, size_t n, cudaStream_t s);
 
-// Fused order-preserving compaction.
+// What a compaction keeps: keys whose flag byte is nonzero, or keys that
+// satisfy "v > 0" in their own type (keep.cuh).
+enum class KeepRule : int { Flags = 0, PositiveF32 = 1, PositiveI32 = 2, PositiveU32 = 3 };
+
+// Fused order-preserving compaction.  `flags` is read only under
+// KeepRule::Flags (null otherwise).
 constexpr size_t kCompactTile = 4096;
-cudaError_t launch_compact_u32(const uint32_t* keys, const uint8_t* flags, uint32_t* out,
-                               unsigned long long* d_count, size_t n, const LookbackWs& ws,
-                               cudaStream_t s);
+cudaError_t launch_compact(KeepRule rule, const uint32_t* keys, const uint8_t* flags, uint32_t* out,
+                           unsigned long long* d_count, size_t n, const LookbackWs& ws, cudaStream_t s);
 
 // Persistent form of the compaction (compact_pipe.cu): 16-byte aligned keys
-// and flags, n above one 16384-element tile.
-cudaError_t launch_compact_pipe(const uint32_t* keys, const uint8_t* flags, uint32_t* out,
+// (and flags), n above one 16384-element tile.
+cudaError_t launch_compact_pipe(KeepRule rule, const uint32_t* keys, const uint8_t* flags, uint32_t* out,
                                 unsigned long long* d_count, size_t n, const LookbackWs& ws, cudaStream_t s);
 int compact_kernel_count();
 void set_compact_kernel(int k);
+
+// Unordered compaction by warp-aggregated atomics (compact_unordered.cu):
+// the kept keys in no fixed order, *d_count reset and counted on `s`.
+cudaError_t launch_compact_unordered(KeepRule rule, const uint32_t* keys, const uint8_t* flags, uint32_t* out,
+                                     unsigned long long* d_count, size_t n, cudaStream_t s);
 
 // Ablations (reduce-then-scan, three kernels).  `totals` holds one value
 // per 4096-element tile.  tile_scan: 0 = register/shuffle tile scan,

@@ -56,6 +56,22 @@ def test_misaligned_and_overlapping_rejected(lib):
     assert lib.compact_u32(0x10000, 0x90000, 0x20000, 0xA0004, 64, None) == ss.SS_ERR_INVALID_ARG
 
 
+def test_predicate_and_unordered_compaction_arguments(lib):
+    inv = ss.SS_ERR_INVALID_ARG
+    assert lib.compact_positive_f32(None, None, None, 5, None) == inv
+    assert lib.compact_positive_f32(0x10000, 0x20000, None, 5, None) == inv          # no count
+    assert lib.compact_positive_f32(0x10000, 0x20000, 0xA0004, 5, None) == inv       # count misaligned
+    assert lib.compact_positive_f32(0x10000, 0x10040, 0xA0000, 64, None) == inv      # out overlaps in
+    assert lib.compact_positive_f32(0x10002, 0x20000, 0xA0000, 64, None) == inv      # in misaligned
+    assert lib.ss_compact_positive(9, 0x10000, 0x20000, 0xA0000, 4, None) == ss.SS_ERR_UNSUPPORTED
+    assert lib.ss_compact_positive(ss.SS_I32, 0x10000, 0x20000, 0xA0000, 1 << 33, None) == inv
+    assert lib.ss_compact_positive(ss.SS_U32, 0x10000, 0x20000, 0x10008, 64, None) == inv  # count in input
+    assert lib.ss_compact_u32_unordered(0x10000, None, 0x20000, 0xA0000, 5, None) == inv  # flags required
+    assert lib.ss_compact_u32_unordered(0x10000, 0x90000, 0x90010, 0xA0000, 64, None) == inv
+    assert lib.ss_compact_positive_unordered(7, 0x10000, 0x20000, 0xA0000, 4, None) == ss.SS_ERR_UNSUPPORTED
+    assert lib.ss_compact_positive_unordered(ss.SS_F32, 0x10000, 0x10000, 0xA0000, 4, None) == inv
+
+
 def test_bad_enums_and_sizes(lib):
     assert lib.ss_scan(7, 1, 0, 0x1000, 0x2000, 4, None) == ss.SS_ERR_UNSUPPORTED
     assert lib.ss_scan(0, 1, 9, 0x1000, 0x2000, 4, None) == ss.SS_ERR_UNSUPPORTED

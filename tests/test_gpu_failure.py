@@ -70,3 +70,23 @@ def test_compaction_timeout_is_reported_and_recovered(ss):
     assert ss.ss_stream_status()[0] == ss.SS_OK
     c = int(cnt.item())
     assert_equal(d_o[:c].cpu().numpy().view(np.uint32), oracle.compact_u32(keys, flags))
+
+
+def test_predicate_compaction_timeout_is_reported_and_recovered(ss):
+    import torch
+    n = 50 * 16384 + 5
+    x = si.workload_positive_f32(n, 0.5, seed=5)
+    d_x = torch.from_numpy(x).to("cuda:0")
+    d_o = torch.empty_like(d_x)
+    cnt = torch.zeros(1, dtype=torch.int64, device="cuda:0")
+    ss.ss_debug_set_lookback_fault(7, 2_000_000)
+    try:
+        ss.compact_positive_f32(d_x, d_o, cnt)
+        st, tile = ss.ss_stream_status()
+    finally:
+        ss.ss_debug_set_lookback_fault(-1, 0)
+    assert st == ss.SS_ERR_LOOKBACK_TIMEOUT and tile > 7
+    ss.compact_positive_f32(d_x, d_o, cnt)
+    assert ss.ss_stream_status()[0] == ss.SS_OK
+    c = int(cnt.item())
+    assert_equal(d_o[:c].cpu().numpy().view(np.uint32), oracle.compact_positive_f32(x).view(np.uint32))
