@@ -144,6 +144,28 @@ ss_status ss_compact_positive_unordered(ss_dtype dtype, const void *in, void *ou
                                         size_t n, ss_stream_t stream);
 
 /*
+ * MoE token counts and expert offsets aligned to GEMM tiles ("Prefix sum and
+ * other parallel patterns", In LLMs: MoE token dispatch, steps 1-2, and
+ * Exercise 2: a histogram of the router's expert ids, then an exclusive
+ * prefix sum for each expert's start, each expert's segment rounded up to a
+ * multiple of the tile size):
+ *   counts[e]    = number of i < m with topk_ids[i] == e
+ *   offsets[0]   = 0,  offsets[e+1] = offsets[e] + align * ceil(counts[e] / align)
+ * An id outside [0, num_experts) is counted nowhere.
+ *   topk_ids     device, m int32 (a row-major num_tokens x top_k array, flat).
+ *   m            number of ids, 0 <= m < 2^31.
+ *   num_experts  E, 1 <= E <= 16384.
+ *   align        tile size, 1 <= align <= 2^20 (1 gives the plain exclusive
+ *                scan of the counts); m + E * (align - 1) must fit 32 bits.
+ *   d_counts     device, E uint32, written.
+ *   d_offsets    device, E + 1 uint32, written (offsets[E] = padded total).
+ * One kernel launch; no allocation after the stream's first call with this
+ * E and grid size.  Arrays must not overlap.
+ */
+ss_status ss_moe_counts_offsets(const int32_t *topk_ids, size_t m, int32_t num_experts, uint32_t align,
+                                uint32_t *d_counts, uint32_t *d_offsets, ss_stream_t stream);
+
+/*
  * Generic scan entry: dtype, inclusive (0/1) and algorithm chosen at run
  * time.  Same argument rules as the named scans.  The reduce-then-scan
  * algorithms ("Prefix sum and other parallel patterns", three passes with

@@ -67,6 +67,7 @@ def _declare(lib):
         "ss_compact_positive": [I, P, P, P, SZ, P],
         "ss_compact_u32_unordered": [P, P, P, P, SZ, P],
         "ss_compact_positive_unordered": [I, P, P, P, SZ, P],
+        "ss_moe_counts_offsets": [P, SZ, ctypes.c_int32, ctypes.c_uint32, P, P, P],
         "ss_scan": [I, I, I, P, P, SZ, P],
         "ss_scan_seeded": [I, I, P, P, SZ, P, P, P],
         "ss_scan_host": [I, I, P, P, SZ, P],
@@ -214,6 +215,13 @@ def ss_compact_positive_unordered(dtype: int, inp, out, d_count, n=None, stream=
         n = _numel(inp)
     _check(lib().ss_compact_positive_unordered(dtype, _addr(inp), _addr(out), _addr(d_count), n,
                                                _stream(stream, inp, out)), "ss_compact_positive_unordered")
+
+
+def ss_moe_counts_offsets(topk_ids, num_experts: int, align: int, counts, offsets, m=None, stream=None):
+    if m is None:
+        m = _numel(topk_ids)
+    _check(lib().ss_moe_counts_offsets(_addr(topk_ids), m, num_experts, align, _addr(counts), _addr(offsets),
+                                       _stream(stream, topk_ids, counts, offsets)), "ss_moe_counts_offsets")
 
 
 def ss_scan(dtype: int, inclusive: bool, algo: int, inp, out, n=None, stream=None):

@@ -52,12 +52,15 @@ struct HostPipe {
 struct Workspace {
     int device = 0;
     cudaStream_t stream = nullptr;
-    // Header: [0] tile counter (u64), [8] status words (2 x u32), [16] carry (8 B).
+    // Header: [0] tile counter (u64), [8] status words (2 x u32), [16] carry (8 B),
+    // [24] MoE ticket (u32).
     unsigned char* header = nullptr;
     unsigned long long* desc = nullptr;
     size_t desc_cap = 0;  // descriptors
     void* totals = nullptr;
     size_t totals_cap = 0;  // bytes
+    uint32_t* moe_acc = nullptr;  // MoE bin accumulator, kept all-zero between launches
+    size_t moe_acc_cap = 0;       // words
     uint64_t launches_since_clear = 0;
     HostPipe pipe;
     std::mutex pipe_mu;  // one host pipeline at a time per workspace
@@ -69,6 +72,7 @@ std::map<std::pair<int, uintptr_t>, Workspace*> g_ws;
 unsigned long long* ws_counter(Workspace* w) { return reinterpret_cast<unsigned long long*>(w->header); }
 uint32_t* ws_status(Workspace* w) { return reinterpret_cast<uint32_t*>(w->header + 8); }
 void* ws_carry(Workspace* w) { return w->header + 16; }
+uint32_t* ws_ticket(Workspace* w) { return reinterpret_cast<uint32_t*>(w->header + 24); }
 
 ss_status get_workspace(cudaStream_t s, Workspace** out) {
     int dev = 0;
@@ -140,6 +144,36 @@ ss_status ensure_totals(Workspace* w, size_t bytes) {
                                               : cuda_fail(e, "cudaMallocAsync");
     w->totals_cap = cap;
     return SS_OK;
+}
+
+ss_status ensure_moe_acc(Workspace* w, size_t words) {
+    if (words <= w->moe_acc_cap) return SS_OK;
+    if (w->moe_acc) {
+        cudaError_t e = cudaFreeAsync(w->moe_acc, w->stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync");
+        w->moe_acc = nullptr;
+        w->moe_acc_cap = 0;
+    }
+    const size_t cap = (size_t)ss::kMoeMaxExperts;
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&w->moe_acc), cap * 4, w->stream);
+    if (e != cudaSuccess)
+        return e == cudaErrorMemoryAllocation ? fail(SS_ERR_NO_MEMORY, "MoE accumulator")
+                                              : cuda_fail(e, "cudaMallocAsync");
+    e = cudaMemsetAsync(w->moe_acc, 0, cap * 4, w->stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    w->moe_acc_cap = cap;
+    return SS_OK;
+}
+
+int device_sms(int dev) {
+    static std::atomic<int> cached[64];
+    if (dev < 0 || dev >= 64) return 1;
+    int v = cached[dev].load();
+    if (v <= 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 1;
+        cached[dev].store(v);
+    }
+    return v;
 }
 
 ss::LookbackWs make_ws(Workspace* w) {
@@ -315,6 +349,34 @@ ss_status ss_compact_positive_unordered(ss_dtype dtype, const void* in, void* ou
                                         ss_stream_t stream) {
     if (!valid_dtype(dtype)) return fail(SS_ERR_UNSUPPORTED, "unknown dtype");
     return compact_any(positive_rule(dtype), in, nullptr, out, d_count, n, true, (cudaStream_t)stream);
+}
+
+ss_status ss_moe_counts_offsets(const int32_t* topk_ids, size_t m, int32_t num_experts, uint32_t align,
+                                uint32_t* d_counts, uint32_t* d_offsets, ss_stream_t stream) {
+    cudaStream_t s = (cudaStream_t)stream;
+    if (num_experts < 1 || num_experts > ss::kMoeMaxExperts)
+        return fail(SS_ERR_INVALID_ARG, "num_experts must be in [1, 16384]");
+    if (align < 1 || align > (1u << 20)) return fail(SS_ERR_INVALID_ARG, "align must be in [1, 2^20]");
+    if (m > 0x7fffffffull) return fail(SS_ERR_INVALID_ARG, "m must be < 2^31");
+    if ((uint64_t)m + (uint64_t)num_experts * (align - 1u) > 0xffffffffull)
+        return fail(SS_ERR_INVALID_ARG, "the padded total does not fit in 32 bits");
+    if (!d_counts || !d_offsets || (m > 0 && !topk_ids)) return fail(SS_ERR_INVALID_ARG, "null pointer");
+    if ((reinterpret_cast<uintptr_t>(d_counts) | reinterpret_cast<uintptr_t>(d_offsets) |
+         reinterpret_cast<uintptr_t>(topk_ids)) & 3u)
+        return fail(SS_ERR_INVALID_ARG, "pointers must be 4-byte aligned");
+    const size_t cb = (size_t)num_experts * 4, ob = cb + 4;
+    if (overlaps(d_counts, cb, d_offsets, ob) || (m > 0 && (overlaps(d_counts, cb, topk_ids, m * 4) ||
+                                                            overlaps(d_offsets, ob, topk_ids, m * 4))))
+        return fail(SS_ERR_INVALID_ARG, "counts, offsets and ids must not overlap");
+    Workspace* w = nullptr;
+    ss_status st = get_workspace(s, &w);
+    if (st != SS_OK) return st;
+    st = ensure_moe_acc(w, (size_t)num_experts);
+    if (st != SS_OK) return st;
+    const uint32_t grid = ss::moe_grid(m, device_sms(w->device));
+    cudaError_t e = ss::launch_moe_counts_offsets(topk_ids, m, num_experts, align, d_counts, d_offsets, w->moe_acc,
+                                                  ws_ticket(w), grid, s);
+    return e == cudaSuccess ? SS_OK : cuda_fail(e, "MoE counts launch");
 }
 
 ss_status ss_scan(ss_dtype dtype, int inclusive, ss_algo algo, const void* in, void* out, size_t n,
@@ -524,6 +586,7 @@ void ss_shutdown(void) {
         cudaDeviceSynchronize();
         if (w->desc) cudaFree(w->desc);
         if (w->totals) cudaFree(w->totals);
+        if (w->moe_acc) cudaFree(w->moe_acc);
         if (w->header) cudaFree(w->header);
         HostPipe& p = w->pipe;
         if (p.ready) {

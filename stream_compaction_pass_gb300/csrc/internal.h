@@ -99,6 +99,15 @@ void set_compact_kernel(int k);
 cudaError_t launch_compact_unordered(KeepRule rule, const uint32_t* keys, const uint8_t* flags, uint32_t* out,
                                      unsigned long long* d_count, size_t n, cudaStream_t s);
 
+// MoE token counts and tile-aligned offsets (moe.cu).  `acc` holds
+// num_experts uint32 and `ticket` one; both are zero on entry and the launch
+// leaves them zero.
+constexpr int32_t kMoeMaxExperts = 16384;
+cudaError_t launch_moe_counts_offsets(const int32_t* ids, size_t m, int32_t num_experts, uint32_t align,
+                                      uint32_t* counts, uint32_t* offsets, uint32_t* acc, uint32_t* ticket,
+                                      uint32_t grid, cudaStream_t s);
+uint32_t moe_grid(size_t m, int sms);
+
 // Ablations (reduce-then-scan, three kernels).  `totals` holds one value
 // per 4096-element tile.  tile_scan: 0 = register/shuffle tile scan,
 // 1 = Blelloch tree unpadded, 2 = Blelloch padded i + i/32,

@@ -72,6 +72,22 @@ def test_predicate_and_unordered_compaction_arguments(lib):
     assert lib.ss_compact_positive_unordered(ss.SS_F32, 0x10000, 0x10000, 0xA0000, 4, None) == inv
 
 
+def test_moe_arguments(lib):
+    inv = ss.SS_ERR_INVALID_ARG
+    f = lib.ss_moe_counts_offsets
+    assert f(0x10000, 64, 0, 64, 0x20000, 0x30000, None) == inv           # no experts
+    assert f(0x10000, 64, 16385, 64, 0x20000, 0x30000, None) == inv       # too many experts
+    assert f(0x10000, 64, 8, 0, 0x20000, 0x30000, None) == inv            # align 0
+    assert f(0x10000, 1 << 31, 8, 1, 0x20000, 0x30000, None) == inv       # m too large
+    assert f(0x10000, (1 << 31) - 1, 16384, 1 << 20, 0x20000, 0x30000, None) == inv  # total overflows
+    assert f(None, 64, 8, 64, 0x20000, 0x30000, None) == inv              # null ids
+    assert f(0x10000, 64, 8, 64, None, 0x30000, None) == inv              # null counts
+    assert f(0x10002, 64, 8, 64, 0x20000, 0x30000, None) == inv           # misaligned ids
+    assert f(0x10000, 64, 8, 64, 0x20000, 0x20010, None) == inv           # counts overlap offsets
+    assert f(0x10000, 64, 8, 64, 0x10010, 0x30000, None) == inv           # counts overlap ids
+    assert "overlap" in ss.ss_last_error_detail()
+
+
 def test_bad_enums_and_sizes(lib):
     assert lib.ss_scan(7, 1, 0, 0x1000, 0x2000, 4, None) == ss.SS_ERR_UNSUPPORTED
     assert lib.ss_scan(0, 1, 9, 0x1000, 0x2000, 4, None) == ss.SS_ERR_UNSUPPORTED
