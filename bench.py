@@ -295,8 +295,38 @@ def row_rates(torch, ss, stream, dev, xs_d, xf_d, out_d):
                                       "GB/s_on_5n+4k": gbs(alg, ms), "frac_on_5n+4k": gbs(alg, ms) / peak,
                                       "GB/s_on_sector_minimum": gbs(minimal, ms),
                                       "frac_on_sector_minimum": gbs(minimal, ms) / peak}
+        ms_u = time_region(torch, stream, lambda: ss.ss_compact_u32_unordered(
+            keys, flags, kout, dcount, stream=stream.cuda_stream), 20)
+        rows[f"compact_unordered_2p28_p{p}"] = {"ms": ms_u, "frac_on_5n+4k": gbs(alg, ms_u) / peak}
         del flags
-    del keys, kout
+    del keys
+    # predicate compaction (keep v > 0, fp32, no flag array), n = 2^28, ordered and unordered
+    for p in (0.01, 0.5, 0.99):
+        xp = torch.from_numpy(si.workload_positive_f32(nk, p, seed=5)).to(dev)
+        pout = kout.view(torch.float32)
+        ss.compact_positive_f32(xp, pout, dcount, stream=stream.cuda_stream)
+        stream.synchronize()
+        kept = int(dcount.item())
+        alg = nk * 4 + 4 * kept + 8
+        ms = time_region(torch, stream, lambda: ss.compact_positive_f32(xp, pout, dcount, stream=stream.cuda_stream),
+                         20)
+        ms_u = time_region(torch, stream, lambda: ss.ss_compact_positive_unordered(
+            ss.SS_F32, xp, pout, dcount, stream=stream.cuda_stream), 20)
+        rows[f"compact_positive_f32_2p28_p{p}"] = {"ms": ms, "kept": kept, "GB/s_on_4n+4k": gbs(alg, ms),
+                                                   "frac_on_4n+4k": gbs(alg, ms) / peak,
+                                                   "unordered_ms": ms_u,
+                                                   "unordered_frac_on_4n+4k": gbs(alg, ms_u) / peak}
+        del xp
+    del kout
+    # MoE counts and 64-aligned offsets: 256 experts, top-8, decode and prefill batch sizes
+    for tokens in (4096, 65536, 1 << 20):
+        ids = torch.from_numpy(si.topk_ids(tokens, 8, 256, seed=6)).to(dev)
+        cnt_e = torch.empty(256, dtype=torch.int32, device=dev)
+        off_e = torch.empty(257, dtype=torch.int32, device=dev)
+        ms = time_region(torch, stream, lambda: ss.ss_moe_counts_offsets(
+            ids, 256, 64, cnt_e, off_e, stream=stream.cuda_stream), 100)
+        rows[f"moe_counts_offsets_t{tokens}_k8_e256"] = {"us": ms * 1e3, "GB/s_on_ids": gbs(4 * tokens * 8, ms)}
+        del ids
     # context only: torch.cumsum on the same int32 input, timed the same way
     def cumsum():
         with torch.cuda.stream(stream):  # torch ops run on torch's current stream
