@@ -42,6 +42,12 @@ def _declare(lib):
         f.restype = None
     lib.oracle_abs_prefix_f32.argtypes = [p, p, sz]
     lib.oracle_abs_prefix_f32.restype = None
+    for name in ("oracle_scan_u32_u64", "oracle_scan_i32_i64", "oracle_scan_i64", "oracle_scan_f64"):
+        f = getattr(lib, name)
+        f.argtypes = [p, p, sz, i]
+        f.restype = None
+    lib.oracle_abs_prefix_f64.argtypes = [p, p, sz]
+    lib.oracle_abs_prefix_f64.restype = None
     lib.oracle_compact_u32.argtypes = [p, p, p, sz]
     lib.oracle_compact_u32.restype = u64
     for name in ("oracle_compact_positive_f32", "oracle_compact_positive_i32", "oracle_compact_positive_u32"):
@@ -97,6 +103,40 @@ def abs_prefix_f32(x: np.ndarray, lib=None) -> np.ndarray:
     x = np.ascontiguousarray(x, dtype=np.float32)
     y = np.empty(x.size, dtype=np.float64)
     (lib or load()).oracle_abs_prefix_f32(_ptr(x), _ptr(y), x.size)
+    return y
+
+
+def _scan_typed(x, in_dtype, out_dtype, fn, inclusive, lib):
+    x = np.ascontiguousarray(x, dtype=in_dtype)
+    y = np.empty(x.size, dtype=out_dtype)
+    getattr(lib or load(), fn)(_ptr(x), _ptr(y), x.size, int(bool(inclusive)))
+    return y
+
+
+def scan_u32_u64(x: np.ndarray, inclusive: bool, lib=None) -> np.ndarray:
+    """uint32 in, exact uint64 prefix sums out."""
+    return _scan_typed(x, np.uint32, np.uint64, "oracle_scan_u32_u64", inclusive, lib)
+
+
+def scan_i32_i64(x: np.ndarray, inclusive: bool, lib=None) -> np.ndarray:
+    """int32 in, exact int64 prefix sums out."""
+    return _scan_typed(x, np.int32, np.int64, "oracle_scan_i32_i64", inclusive, lib)
+
+
+def scan_i64(x: np.ndarray, inclusive: bool, lib=None) -> np.ndarray:
+    """int64 prefix sums modulo 2^64."""
+    return _scan_typed(x, np.int64, np.int64, "oracle_scan_i64", inclusive, lib)
+
+
+def scan_f64(x: np.ndarray, inclusive: bool, lib=None) -> np.ndarray:
+    """fp64 prefix sums, compensated, within about one rounding of exact."""
+    return _scan_typed(x, np.float64, np.float64, "oracle_scan_f64", inclusive, lib)
+
+
+def abs_prefix_f64(x: np.ndarray, lib=None) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.empty(x.size, dtype=np.float64)
+    (lib or load()).oracle_abs_prefix_f64(_ptr(x), _ptr(y), x.size)
     return y
 
 

@@ -85,6 +85,101 @@ void oracle_scan_f32(const float *x, double *y, size_t n, int inclusive)
     }
 }
 
+/*
+ * Widened and 64-bit scans ("Parallel Prefix Sum (Scan) for NVIDIA T4
+ * (sm_75)", Key Features: 64-bit indexing for large arrays; a 32-bit sum of
+ * many 32-bit counts wraps, so the sum is carried in 64 bits).
+ *   u32 -> u64: the exact sum (it cannot exceed 2^64 for n < 2^32).
+ *   i32 -> i64: the exact signed sum.
+ *   i64 (and u64, the same bits): two's-complement wraparound modulo 2^64,
+ *       carried in uint64 arithmetic.
+ */
+void oracle_scan_u32_u64(const uint32_t *x, uint64_t *y, size_t n, int inclusive)
+{
+    uint64_t acc = 0;
+    for (size_t i = 0; i < n; ++i) {
+        if (inclusive) {
+            acc += x[i];
+            y[i] = acc;
+        } else {
+            y[i] = acc;
+            acc += x[i];
+        }
+    }
+}
+
+void oracle_scan_i32_i64(const int32_t *x, int64_t *y, size_t n, int inclusive)
+{
+    int64_t acc = 0;
+    for (size_t i = 0; i < n; ++i) {
+        if (inclusive) {
+            acc += x[i];
+            y[i] = acc;
+        } else {
+            y[i] = acc;
+            acc += x[i];
+        }
+    }
+}
+
+void oracle_scan_i64(const int64_t *x, int64_t *y, size_t n, int inclusive)
+{
+    uint64_t acc = 0;
+    for (size_t i = 0; i < n; ++i) {
+        if (inclusive) {
+            acc += (uint64_t)x[i];
+            y[i] = (int64_t)acc;
+        } else {
+            y[i] = (int64_t)acc;
+            acc += (uint64_t)x[i];
+        }
+    }
+}
+
+/*
+ * fp64 scan.  A float64 running sum would carry the same order of rounding
+ * error as the GPU result it is meant to judge, so the running sum is kept
+ * compensated: Neumaier's variant of Kahan summation (A. Neumaier,
+ * "Rundungsfehleranalyse einiger Verfahren zur Summation endlicher Summen",
+ * ZAMM 54, 1974) carries the rounding error of every add in `comp` and adds
+ * it back when an output is taken.  Each output is then within about one
+ * rounding of the exact prefix, whatever n is.
+ */
+void oracle_scan_f64(const double *x, double *y, size_t n, int inclusive)
+{
+    double sum = 0.0, comp = 0.0;
+    for (size_t i = 0; i < n; ++i) {
+        if (!inclusive)
+            y[i] = sum + comp;
+        double v = x[i];
+        double t = sum + v;
+        double av = v < 0.0 ? -v : v, as = sum < 0.0 ? -sum : sum;
+        if (as >= av)
+            comp += (sum - t) + v;
+        else
+            comp += (v - t) + sum;
+        sum = t;
+        if (inclusive)
+            y[i] = sum + comp;
+    }
+}
+
+/* Error normaliser for fp64 parity: a_i = sum_{j <= i} |x_j|, compensated. */
+void oracle_abs_prefix_f64(const double *x, double *y, size_t n)
+{
+    double sum = 0.0, comp = 0.0;
+    for (size_t i = 0; i < n; ++i) {
+        double v = x[i] < 0.0 ? -x[i] : x[i];
+        double t = sum + v;
+        if (sum >= v)
+            comp += (sum - t) + v;
+        else
+            comp += (v - t) + sum;
+        sum = t;
+        y[i] = sum + comp;
+    }
+}
+
 /* Error normaliser for fp32 parity: a_i = sum_{j <= i} |x_j| in float64. */
 void oracle_abs_prefix_f32(const float *x, double *y, size_t n)
 {

@@ -17,6 +17,7 @@ import oracle
 import seeded_inputs as si
 
 HERE = os.path.dirname(os.path.abspath(__file__))
+M64 = 1 << 64
 ORACLE_DIR = os.path.join(os.path.dirname(HERE), "oracle")
 
 # (file, text to find, replacement, what the mistake is)
@@ -44,6 +45,15 @@ MUTANTS = [
     ("scan_ref.c", "offsets[e + 1] = offsets[e] + blocks * align;",
      "offsets[e + 1] = blocks * align;", "MoE offsets not accumulated"),
     ("scan_ref.c", "counts[ids[i]] += 1;", "counts[ids[i]] += (i + 1 < m);", "MoE histogram drops the last id"),
+    ("scan_ref.c", "uint64_t *y, size_t n, int inclusive)\n{\n    uint64_t acc = 0;",
+     "uint64_t *y, size_t n, int inclusive)\n{\n    uint32_t acc = 0;", "widened scan keeps a 32-bit sum"),
+    ("scan_ref.c", "int64_t *y, size_t n, int inclusive)\n{\n    int64_t acc = 0;",
+     "int64_t *y, size_t n, int inclusive)\n{\n    uint32_t acc = 0;", "int32 -> int64 loses the sign"),
+    ("scan_ref.c", "            acc += (uint64_t)x[i];\n            y[i] = (int64_t)acc;",
+     "            y[i] = (int64_t)acc;\n            acc += (uint64_t)x[i];", "int64 inclusive becomes exclusive"),
+    ("scan_ref.c", "if (inclusive)\n            y[i] = sum + comp;", "if (inclusive)\n            y[i] = sum;",
+     "fp64 inclusive drops the compensation"),
+    ("scan_ref.c", "if (as >= av)", "if (as <= av)", "fp64 compensation takes the wrong branch"),
     ("tile_model.c", "return i + i / 32 + i / 1024;", "return i + i / 32 + i / 512;", "two-term padding uses /512"),
     ("tile_model.c", "return i + i / 32;\n", "return i + i / 16;\n", "one-term padding uses /16"),
     ("tile_model.c", "total += 2 * level;", "total += level;", "model counts one sweep"),
@@ -118,6 +128,18 @@ def _checks(lib):
         return c.tolist() == [2, 0, 4, 1] and o.tolist() == [0, 4, 4, 8, 12]
 
     pin("moe_worked", moe_pin)
+
+    xw = np.array([0xFFFFFFFF, 0xFFFFFFFF, 5, 0xFFFFFFFF], dtype=np.uint32)
+    pin("widened_u64", lambda: oracle.scan_u32_u64(xw, True, lib=lib).tolist()
+        == [4294967295, 8589934590, 8589934595, 12884901890])
+    xs = np.array([-5, 3, -(2**31), 7], dtype=np.int32)
+    pin("widened_i64", lambda: oracle.scan_i32_i64(xs, False, lib=lib).tolist() == [0, -5, -2, -2147483650])
+    x64 = np.array([2**62, 2**62, 2**62, 5], dtype=np.int64)
+    pin("i64_wrap", lambda: oracle.scan_i64(x64, True, lib=lib).tolist()
+        == [2**62, 2**63 - M64, 3 * 2**62 - M64, 3 * 2**62 + 5 - M64])
+    xn = np.array([1.0, 1e100, 1.0, -1e100], dtype=np.float64)
+    pin("f64_neumaier", lambda: oracle.scan_f64(xn, True, lib=lib).tolist() == [1.0, 1e100, 1e100, 2.0]
+        and oracle.scan_f64(xn[::-1].copy(), True, lib=lib).tolist() == [-1e100, -1e100, 1.0, 2.0])
 
     pin("model_plain", lambda: oracle.blelloch_requests(4096, oracle.LAYOUT_PLAIN, lib=lib) == 1534)
     pin("model_pad32", lambda: oracle.blelloch_requests(4096, oracle.LAYOUT_PAD32, lib=lib) == 294)

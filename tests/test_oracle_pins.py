@@ -14,6 +14,12 @@ Which pin covers which oracle function:
   identity pos[n-1] + flags[n-1], subsequence check, all-zero / all-one
   flags, IEEE special values written out by hand, agreement of the
   predicate form with the flag form.
+* scan_u32_u64 / scan_i32_i64 / scan_i64: the worked examples, brute force
+  with Python integers (mod 2^64 for int64), the low 32 bits against the
+  pinned 32-bit scans.
+* scan_f64 / abs_prefix_f64: exact rational brute force within the
+  compensated-sum bound, Neumaier's classic cancellation case,
+  integer-valued inputs exactly.
 * moe_counts_offsets: a worked example by hand, the histogram against
   numpy's bincount, tile size 1 against the (pinned) exclusive scan, the
   rounding invariants, one-expert and out-of-range cases.
@@ -372,3 +378,114 @@ def test_work_closed_forms(golden_dir):
         n = 1 << k
         assert oracle.hillis_steele_adds(n) == n * k - (n - 1)  # n log2 n - (n - 1)
         assert oracle.blelloch_adds(n) == 2 * (n - 1)
+
+
+# ---- widened and 64-bit scans ----
+
+M64 = 1 << 64
+
+
+def _py_scan(vals, inclusive, mod=None):
+    out, acc = [], 0
+    for v in vals:
+        if inclusive:
+            acc += v
+            out.append(acc if mod is None else acc % mod)
+        else:
+            out.append(acc if mod is None else acc % mod)
+            acc += v
+    return out
+
+
+def test_worked_examples_wide(golden_dir):
+    for name, x, inc, exc, src in _worked_examples(golden_dir):
+        if x is None or any(v < 0 for v in x):
+            continue
+        a = np.array(x)
+        for inclusive, want in ((True, inc), (False, exc)):
+            if want is None:
+                continue
+            assert oracle.scan_u32_u64(a, inclusive).tolist() == want, name
+            assert oracle.scan_i32_i64(a, inclusive).tolist() == want, name
+            assert oracle.scan_i64(a, inclusive).tolist() == want, name
+            assert oracle.scan_f64(a.astype(np.float64), inclusive).tolist() == want, name
+
+
+@pytest.mark.parametrize("n", [1, 2, 17, 64])
+@pytest.mark.parametrize("inclusive", [True, False])
+def test_brute_force_widened(n, inclusive):
+    xu = si.uniform_u32(n, seed=40)
+    xu[::3] = 0xFFFFFFFF  # sums pass 2^32 quickly
+    assert oracle.scan_u32_u64(xu, inclusive).tolist() == _py_scan([int(v) for v in xu], inclusive)
+    xi = si.uniform_int32(n, -(2**31), 2**31 - 1, seed=41)
+    assert oracle.scan_i32_i64(xi, inclusive).tolist() == _py_scan([int(v) for v in xi], inclusive)
+
+
+@pytest.mark.parametrize("inclusive", [True, False])
+def test_brute_force_i64_wraps_mod_2_64(inclusive):
+    n = 64
+    hi = si.uniform_u32(n, seed=42).astype(np.uint64)
+    lo = si.uniform_u32(n, seed=43).astype(np.uint64)
+    x = ((hi << np.uint64(32)) | lo).view(np.int64)
+    want = [(v - M64 if v >= 1 << 63 else v) for v in _py_scan([int(v) for v in x], inclusive, mod=M64)]
+    assert oracle.scan_i64(x, inclusive).tolist() == want
+
+
+def test_widened_low_bits_are_the_32_bit_scan():
+    n = 1 << 16
+    x = si.uniform_u32(n, seed=44)
+    for inclusive in (True, False):
+        wide = oracle.scan_u32_u64(x, inclusive)
+        assert np.array_equal((wide & np.uint64(0xFFFFFFFF)).astype(np.uint32), oracle.scan_u32(x, inclusive))
+        xi = x.view(np.int32)
+        wi = oracle.scan_i32_i64(xi, inclusive)
+        assert np.array_equal(wi.astype(np.uint64).astype(np.uint32).view(np.int32), oracle.scan_i32(xi, inclusive))
+
+
+def test_f64_compensation_classic_case():
+    # 1 + 1e100 + 1 - 1e100 = 2 exactly; an uncompensated float64 running
+    # sum returns 0 for the last prefix.
+    x = np.array([1.0, 1e100, 1.0, -1e100], dtype=np.float64)
+    assert oracle.scan_f64(x, True).tolist() == [1.0, 1e100, 1e100, 2.0]
+    assert oracle.scan_f64(x, False).tolist() == [0.0, 1.0, 1e100, 1e100]
+
+
+@pytest.mark.parametrize("n", [1, 5, 64])
+def test_f64_within_one_rounding_of_exact(n):
+    # random doubles over 40 binades, both signs: exact rational prefixes
+    u = si.uniform_f32(n, seed=45).astype(np.float64)
+    e = si.uniform_int32(n, -20, 20, seed=46).astype(np.float64)
+    sgn = np.where(si.bernoulli_flags(n, 0.5, seed=47) != 0, 1.0, -1.0)
+    x = sgn * (u + 0.5) * np.exp2(e)
+    u64 = 2.0 ** -53
+    for inclusive in (True, False):
+        got = oracle.scan_f64(x, inclusive)
+        acc = Fraction(0)
+        abs_acc = Fraction(0)
+        for i in range(n):
+            if inclusive:
+                acc += Fraction(float(x[i]))
+                abs_acc += abs(Fraction(float(x[i])))
+            err = abs(Fraction(float(got[i])) - acc)
+            bound = 2 * u64 * abs(acc) + 8 * n * u64 * u64 * abs_acc
+            assert err <= bound, (i, float(err), float(bound))
+            if not inclusive:
+                acc += Fraction(float(x[i]))
+                abs_acc += abs(Fraction(float(x[i])))
+
+
+def test_f64_integer_valued_is_exact():
+    n = 100_000
+    x = si.uniform_int32(n, -(2**20), 2**20, seed=48).astype(np.float64)
+    want = np.cumsum(x.astype(np.int64))  # |prefix| < 2^37, exact in float64
+    assert np.array_equal(oracle.scan_f64(x, True), want.astype(np.float64))
+
+
+def test_abs_prefix_f64_exact():
+    n = 64
+    x = (si.uniform_f32(n, seed=49).astype(np.float64) - 0.5) * np.exp2(si.uniform_int32(n, -30, 30, seed=50))
+    got = oracle.abs_prefix_f64(x)
+    acc = Fraction(0)
+    for i in range(n):
+        acc += abs(Fraction(float(x[i])))
+        assert abs(Fraction(float(got[i])) - acc) <= 2 * (2.0 ** -53) * acc
