@@ -90,6 +90,38 @@ ss_status scan_inclusive_f32(const float *in, float *out, size_t n, ss_stream_t 
 ss_status scan_exclusive_f32(const float *in, float *out, size_t n, ss_stream_t stream);
 
 /*
+ * Scans with 64-bit sums ("Parallel Prefix Sum (Scan) for NVIDIA T4
+ * (sm_75)", Key Features: 64-bit indexing for large arrays; the sum of many
+ * 32-bit counts needs 64 bits).  Same definitions and method as the 32-bit
+ * scans, with 16-byte tile descriptors.
+ *   u32_u64  uint32 in, uint64 out: the exact sums (no wrap below 2^64).
+ *   i32_i64  (ss_scan_wide only) int32 in, int64 out: the exact sums.
+ *   i64      int64 in and out, wrapping modulo 2^64 (uint64 data gives the
+ *            same bits).
+ *   f64      fp64 in and out, IEEE round-to-nearest adds in an order the
+ *            caller does not control (as for fp32).
+ *   in   device, n elements, aligned to the element size (16-byte aligned
+ *        in and out take the bulk-copy path).
+ *   out  device, n 8-byte elements.  out == in is allowed for i64 and f64;
+ *        any other overlap is SS_ERR_INVALID_ARG.
+ *   n    0 <= n < 2^31 * 8192.
+ */
+typedef enum ss_wide_type {
+    SS_WIDE_U32_U64 = 0,
+    SS_WIDE_I32_I64 = 1,
+    SS_WIDE_I64 = 2,
+    SS_WIDE_F64 = 3
+} ss_wide_type;
+ss_status scan_inclusive_u32_u64(const uint32_t *in, uint64_t *out, size_t n, ss_stream_t stream);
+ss_status scan_exclusive_u32_u64(const uint32_t *in, uint64_t *out, size_t n, ss_stream_t stream);
+ss_status scan_inclusive_i64(const int64_t *in, int64_t *out, size_t n, ss_stream_t stream);
+ss_status scan_exclusive_i64(const int64_t *in, int64_t *out, size_t n, ss_stream_t stream);
+ss_status scan_inclusive_f64(const double *in, double *out, size_t n, ss_stream_t stream);
+ss_status scan_exclusive_f64(const double *in, double *out, size_t n, ss_stream_t stream);
+ss_status ss_scan_wide(ss_wide_type type, int inclusive, const void *in, void *out, size_t n,
+                       ss_stream_t stream);
+
+/*
  * Order-preserving stream compaction in one pass: out receives, in index
  * order, every keys[i] whose flags[i] != 0, and *d_count the number kept
  * ("Prefix sum and other parallel patterns", Stream compaction and

@@ -38,6 +38,8 @@ SS_ALGO_RTS_BLELLOCH = 2
 SS_ALGO_RTS_BLELLOCH_PAD32 = 3
 SS_ALGO_RTS_BLELLOCH_PAD2 = 4
 
+SS_WIDE_U32_U64, SS_WIDE_I32_I64, SS_WIDE_I64, SS_WIDE_F64 = 0, 1, 2, 3
+
 
 class LibraryMissing(ImportError):
     pass
@@ -68,6 +70,13 @@ def _declare(lib):
         "ss_compact_u32_unordered": [P, P, P, P, SZ, P],
         "ss_compact_positive_unordered": [I, P, P, P, SZ, P],
         "ss_moe_counts_offsets": [P, SZ, ctypes.c_int32, ctypes.c_uint32, P, P, P],
+        "scan_inclusive_u32_u64": [P, P, SZ, P],
+        "scan_exclusive_u32_u64": [P, P, SZ, P],
+        "scan_inclusive_i64": [P, P, SZ, P],
+        "scan_exclusive_i64": [P, P, SZ, P],
+        "scan_inclusive_f64": [P, P, SZ, P],
+        "scan_exclusive_f64": [P, P, SZ, P],
+        "ss_scan_wide": [I, I, P, P, SZ, P],
         "ss_scan": [I, I, I, P, P, SZ, P],
         "ss_scan_seeded": [I, I, P, P, SZ, P, P, P],
         "ss_scan_host": [I, I, P, P, SZ, P],
@@ -215,6 +224,37 @@ def ss_compact_positive_unordered(dtype: int, inp, out, d_count, n=None, stream=
         n = _numel(inp)
     _check(lib().ss_compact_positive_unordered(dtype, _addr(inp), _addr(out), _addr(d_count), n,
                                                _stream(stream, inp, out)), "ss_compact_positive_unordered")
+
+
+def scan_inclusive_u32_u64(inp, out, n=None, stream=None):
+    _scan_named("scan_inclusive_u32_u64", inp, out, n, stream)
+
+
+def scan_exclusive_u32_u64(inp, out, n=None, stream=None):
+    _scan_named("scan_exclusive_u32_u64", inp, out, n, stream)
+
+
+def scan_inclusive_i64(inp, out, n=None, stream=None):
+    _scan_named("scan_inclusive_i64", inp, out, n, stream)
+
+
+def scan_exclusive_i64(inp, out, n=None, stream=None):
+    _scan_named("scan_exclusive_i64", inp, out, n, stream)
+
+
+def scan_inclusive_f64(inp, out, n=None, stream=None):
+    _scan_named("scan_inclusive_f64", inp, out, n, stream)
+
+
+def scan_exclusive_f64(inp, out, n=None, stream=None):
+    _scan_named("scan_exclusive_f64", inp, out, n, stream)
+
+
+def ss_scan_wide(wide_type: int, inclusive: bool, inp, out, n=None, stream=None):
+    if n is None:
+        n = _numel(inp)
+    _check(lib().ss_scan_wide(wide_type, int(bool(inclusive)), _addr(inp), _addr(out), n,
+                              _stream(stream, inp, out)), "ss_scan_wide")
 
 
 def ss_moe_counts_offsets(topk_ids, num_experts: int, align: int, counts, offsets, m=None, stream=None):

@@ -226,6 +226,28 @@ ss_status scan_lookback(Dtype dt, bool inclusive, const void* in, void* out, siz
     return SS_OK;
 }
 
+// Scans with 64-bit sums: input element size 4 (widened) or 8 bytes, output
+// 8 bytes.  in == out is allowed when both are 8 bytes wide.
+ss_status scan_wide(ss::WideType type, bool inclusive, const void* in, void* out, size_t n, cudaStream_t s) {
+    const size_t in_size = (type == ss::WideType::U32toU64 || type == ss::WideType::I32toI64) ? 4 : 8;
+    if (n == 0) return SS_OK;
+    if (in == nullptr || out == nullptr) return fail(SS_ERR_INVALID_ARG, "null pointer with n > 0");
+    if ((reinterpret_cast<uintptr_t>(in) & (in_size - 1)) || (reinterpret_cast<uintptr_t>(out) & 7u))
+        return fail(SS_ERR_INVALID_ARG, "in/out must be aligned to their element size");
+    if (n / ss::kWideTile >= ((size_t)1 << 31) - 1 || n > SIZE_MAX / 16) return fail(SS_ERR_INVALID_ARG, "n too large");
+    if (!(in_size == 8 && in == out) && overlaps(in, n * in_size, out, n * 8))
+        return fail(SS_ERR_INVALID_ARG, in_size == 8 ? "in and out partially overlap"
+                                                     : "a widened scan cannot overlap its input");
+    const size_t tiles = (n + ss::kWideTile - 1) / ss::kWideTile;
+    Workspace* w = nullptr;
+    ss_status st = get_workspace(s, &w);
+    if (st != SS_OK) return st;
+    st = ensure_desc(w, 2 * tiles);  // two words per tile
+    if (st != SS_OK) return st;
+    cudaError_t e = ss::launch_scan_wide(type, inclusive, in, out, n, make_ws(w), s);
+    return e == cudaSuccess ? SS_OK : cuda_fail(e, "64-bit scan launch");
+}
+
 Dtype to_dtype(ss_dtype d) {
     return d == SS_F32 ? Dtype::F32 : (d == SS_U32 ? Dtype::U32 : Dtype::I32);
 }
@@ -349,6 +371,37 @@ ss_status ss_compact_positive_unordered(ss_dtype dtype, const void* in, void* ou
                                         ss_stream_t stream) {
     if (!valid_dtype(dtype)) return fail(SS_ERR_UNSUPPORTED, "unknown dtype");
     return compact_any(positive_rule(dtype), in, nullptr, out, d_count, n, true, (cudaStream_t)stream);
+}
+
+ss_status scan_inclusive_u32_u64(const uint32_t* in, uint64_t* out, size_t n, ss_stream_t stream) {
+    return scan_wide(ss::WideType::U32toU64, true, in, out, n, (cudaStream_t)stream);
+}
+ss_status scan_exclusive_u32_u64(const uint32_t* in, uint64_t* out, size_t n, ss_stream_t stream) {
+    return scan_wide(ss::WideType::U32toU64, false, in, out, n, (cudaStream_t)stream);
+}
+ss_status scan_inclusive_i64(const int64_t* in, int64_t* out, size_t n, ss_stream_t stream) {
+    return scan_wide(ss::WideType::I64, true, in, out, n, (cudaStream_t)stream);
+}
+ss_status scan_exclusive_i64(const int64_t* in, int64_t* out, size_t n, ss_stream_t stream) {
+    return scan_wide(ss::WideType::I64, false, in, out, n, (cudaStream_t)stream);
+}
+ss_status scan_inclusive_f64(const double* in, double* out, size_t n, ss_stream_t stream) {
+    return scan_wide(ss::WideType::F64, true, in, out, n, (cudaStream_t)stream);
+}
+ss_status scan_exclusive_f64(const double* in, double* out, size_t n, ss_stream_t stream) {
+    return scan_wide(ss::WideType::F64, false, in, out, n, (cudaStream_t)stream);
+}
+
+ss_status ss_scan_wide(ss_wide_type type, int inclusive, const void* in, void* out, size_t n, ss_stream_t stream) {
+    ss::WideType t;
+    switch (type) {
+        case SS_WIDE_U32_U64: t = ss::WideType::U32toU64; break;
+        case SS_WIDE_I32_I64: t = ss::WideType::I32toI64; break;
+        case SS_WIDE_I64: t = ss::WideType::I64; break;
+        case SS_WIDE_F64: t = ss::WideType::F64; break;
+        default: return fail(SS_ERR_UNSUPPORTED, "unknown 64-bit scan type");
+    }
+    return scan_wide(t, inclusive != 0, in, out, n, (cudaStream_t)stream);
 }
 
 ss_status ss_moe_counts_offsets(const int32_t* topk_ids, size_t m, int32_t num_experts, uint32_t align,

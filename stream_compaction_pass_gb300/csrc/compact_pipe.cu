@@ -59,7 +59,7 @@ k_compact_pipe(const uint32_t* keys, const uint8_t* flags, uint32_t* out, unsign
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bars[STAGES];
     __shared__ uint32_t s_warp[WARPS];
-    __shared__ uint32_t s_prefix, s_fail, s_rank, s_epoch;
+    __shared__ uint32_t s_prefix[2], s_fail[2], s_rank, s_epoch;  // prefix/fail alternate by tile parity
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -207,8 +207,8 @@ k_compact_pipe(const uint32_t* keys, const uint8_t* flags, uint32_t* out, unsign
             }
             prev_incl = excl + agg_cur;
             if (lane == 0) {
-                s_prefix = excl;
-                s_fail = lb_failed ? 1u : 0u;
+                s_prefix[k & 1] = excl;
+                s_fail[k & 1] = lb_failed ? 1u : 0u;
             }
         }
         // Rank tile k's kept keys.
@@ -254,12 +254,12 @@ k_compact_pipe(const uint32_t* keys, const uint8_t* flags, uint32_t* out, unsign
             consumed = k + 1;
             if (k + STAGES < count) issue(k + STAGES);
         }
-        if (s_fail) {
+        if (s_fail[k & 1]) {
             failed = true;
             fail_at = k;
             break;
         }
-        uint32_t* dst = out + (size_t)s_prefix + wp_cur;
+        uint32_t* dst = out + (size_t)s_prefix[k & 1] + wp_cur;
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
             uint32_t pos = row_base[j];
@@ -268,7 +268,7 @@ k_compact_pipe(const uint32_t* keys, const uint8_t* flags, uint32_t* out, unsign
                 if ((m[j] >> e) & 1u) dst[pos++] = key[j][e];
             }
         }
-        if (t == num_tiles - 1 && threadIdx.x == 0) *d_count = (unsigned long long)s_prefix + agg_cur;
+        if (t == num_tiles - 1 && threadIdx.x == 0) *d_count = (unsigned long long)s_prefix[k & 1] + agg_cur;
         wp_cur = wp_next;
         agg_cur = agg_next;
     }
@@ -303,7 +303,7 @@ k_compact_sel(const uint32_t* keys, const uint8_t* flags, uint32_t* out, unsigne
     extern __shared__ __align__(128) unsigned char smem_raw[];  // STAGES x TILE flag bytes
     __shared__ __align__(8) uint64_t bars[STAGES];
     __shared__ uint32_t s_warp[WARPS];
-    __shared__ uint32_t s_prefix, s_fail, s_rank, s_epoch;
+    __shared__ uint32_t s_prefix[2], s_fail[2], s_rank, s_epoch;  // prefix/fail alternate by tile parity
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -435,8 +435,8 @@ k_compact_sel(const uint32_t* keys, const uint8_t* flags, uint32_t* out, unsigne
             }
             prev_incl = excl + agg_cur;
             if (lane == 0) {
-                s_prefix = excl;
-                s_fail = lb_failed ? 1u : 0u;
+                s_prefix[k & 1] = excl;
+                s_fail[k & 1] = lb_failed ? 1u : 0u;
             }
         }
         uint32_t row_base[VPT];
@@ -456,11 +456,11 @@ k_compact_sel(const uint32_t* keys, const uint8_t* flags, uint32_t* out, unsigne
             }
         }
         __syncthreads();  // the prefix is in shared memory
-        if (s_fail) {
+        if (s_fail[k & 1]) {
             fail_at = k;
             return false;
         }
-        uint32_t* dst = out + (size_t)s_prefix + wp_cur;
+        uint32_t* dst = out + (size_t)s_prefix[k & 1] + wp_cur;
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
             uint32_t pos = row_base[j];
@@ -469,7 +469,7 @@ k_compact_sel(const uint32_t* keys, const uint8_t* flags, uint32_t* out, unsigne
                 if ((mc[j] >> e) & 1u) dst[pos++] = kc[j][e];
             }
         }
-        if (t == num_tiles - 1 && threadIdx.x == 0) *d_count = (unsigned long long)s_prefix + agg_cur;
+        if (t == num_tiles - 1 && threadIdx.x == 0) *d_count = (unsigned long long)s_prefix[k & 1] + agg_cur;
         wp_cur = wp_next;
         agg_cur = agg_next;
         return true;

@@ -99,6 +99,14 @@ void set_compact_kernel(int k);
 cudaError_t launch_compact_unordered(KeepRule rule, const uint32_t* keys, const uint8_t* flags, uint32_t* out,
                                      unsigned long long* d_count, size_t n, cudaStream_t s);
 
+// Scans with 64-bit sums (scan_wide.cu): uint32 -> uint64, int32 -> int64,
+// int64 (modulo 2^64; uint64 is the same bits) and fp64.  Descriptors are 16
+// bytes, two 64-bit words per tile of kWideTile elements.
+enum class WideType : int { U32toU64 = 0, I32toI64 = 1, I64 = 2, F64 = 3 };
+constexpr size_t kWideTile = 8192;
+cudaError_t launch_scan_wide(WideType type, bool inclusive, const void* in, void* out, size_t n,
+                             const LookbackWs& ws, cudaStream_t s);
+
 // MoE token counts and tile-aligned offsets (moe.cu).  `acc` holds
 // num_experts uint32 and `ticket` one; both are zero on entry and the launch
 // leaves them zero.

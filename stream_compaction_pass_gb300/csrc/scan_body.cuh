@@ -16,11 +16,15 @@
 
 namespace ss {
 
+// The prefix and the failure flag of a tile are handed from warp 0 to the
+// other warps through shared memory.  A persistent kernel alternates two
+// slots by tile parity: warp 0 may publish tile k+1's prefix (its last tile
+// has no barrier before that) while a slower warp still reads tile k's.
 template <typename T, int WARPS>
 struct ScanSmem {
     T warp[WARPS];
-    T prefix;
-    uint32_t fail;
+    T prefix[2];
+    uint32_t fail[2];
 };
 
 // Per-tile trace record (8 x uint64), written when a trace is taken:
@@ -87,8 +91,8 @@ __device__ __forceinline__ bool scan_tile_body(const T (&v)[VPT][4], T* out, siz
             }
         }
         if (lane == 0) {
-            sm.prefix = excl;
-            sm.fail = failed ? 1u : 0u;
+            sm.prefix[0] = excl;
+            sm.fail[0] = failed ? 1u : 0u;
             if (TRACE) {
                 const unsigned long long now = globaltimer_ns();
                 if (tile == 0) rec[2] = now;
@@ -103,13 +107,13 @@ __device__ __forceinline__ bool scan_tile_body(const T (&v)[VPT][4], T* out, siz
     T pre[VPT];
     warp_rows_scan<T, VPT>(v, lane, pre);
     __syncthreads();
-    if (sm.fail) return false;
+    if (sm.fail[0]) return false;
 
     T y[VPT][4];
-    rows_output<T, VPT, INCLUSIVE>(v, pre, sm.prefix + warp_prefix, y);
+    rows_output<T, VPT, INCLUSIVE>(v, pre, sm.prefix[0] + warp_prefix, y);
     store_rows<T, VPT>(out, n, seg, lane, full, y);
     if (carry_out != nullptr && tile == num_tiles - 1 && threadIdx.x == 0)
-        *carry_out = sm.prefix + block_total;
+        *carry_out = sm.prefix[0] + block_total;
     if (TRACE && threadIdx.x == 0) rec[4] = globaltimer_ns();
     return true;
 }

@@ -178,8 +178,8 @@ k_scan_lookback_pipe(const T* in, T* out, size_t n, uint32_t num_tiles, Lookback
             }
             prev_incl = excl + agg_cur;
             if (lane == 0) {
-                sm.prefix = excl;
-                sm.fail = failed ? 1u : 0u;
+                sm.prefix[k & 1] = excl;
+                sm.fail[k & 1] = failed ? 1u : 0u;
                 if (TRACE) {
                     unsigned long long* rec = trace + (size_t)t * kTraceWords;
                     rec[3] = globaltimer_ns();
@@ -192,14 +192,14 @@ k_scan_lookback_pipe(const T* in, T* out, size_t n, uint32_t num_tiles, Lookback
         T pre[VPT];
         warp_rows_scan<T, VPT>(vc, lane, pre);
         __syncthreads();
-        if (sm.fail) {
+        if (sm.fail[k & 1]) {
             fail_at = k;
             return false;
         }
         const size_t tile_base = (size_t)t * TILE;
-        rows_output_inplace<T, VPT, INCLUSIVE>(vc, pre, sm.prefix + wp_cur);
+        rows_output_inplace<T, VPT, INCLUSIVE>(vc, pre, sm.prefix[k & 1] + wp_cur);
         store_rows<T, VPT>(out, n, tile_base + (size_t)warp * SEG, lane, tile_base + TILE <= n, vc);
-        if (carry_out != nullptr && t == num_tiles - 1 && threadIdx.x == 0) *carry_out = sm.prefix + agg_cur;
+        if (carry_out != nullptr && t == num_tiles - 1 && threadIdx.x == 0) *carry_out = sm.prefix[k & 1] + agg_cur;
         if (TRACE && threadIdx.x == 0) trace[(size_t)t * kTraceWords + 4] = globaltimer_ns();
         wp_cur = wp_next;
         agg_cur = agg_next;
@@ -381,8 +381,8 @@ k_scan_lookback_pipe_sb(const T* in, T* out, size_t n, uint32_t num_tiles, Lookb
             }
             prev_incl = excl + agg_cur;
             if (lane == 0) {
-                sm.prefix = excl;
-                sm.fail = lb_failed ? 1u : 0u;
+                sm.prefix[k & 1] = excl;
+                sm.fail[k & 1] = lb_failed ? 1u : 0u;
                 if (TRACE) {
                     unsigned long long* rec = trace + (size_t)t * kTraceWords;
                     rec[3] = globaltimer_ns();
@@ -401,15 +401,15 @@ k_scan_lookback_pipe_sb(const T* in, T* out, size_t n, uint32_t num_tiles, Lookb
             consumed = k + 1;
             if (k + STAGES < count) issue(k + STAGES);
         }
-        if (sm.fail) {
+        if (sm.fail[k & 1]) {
             failed = true;
             fail_at = k;
             break;
         }
         const size_t tile_base = (size_t)t * TILE;
-        rows_output_inplace<T, VPT, INCLUSIVE>(v, pre, sm.prefix + wp_cur);
+        rows_output_inplace<T, VPT, INCLUSIVE>(v, pre, sm.prefix[k & 1] + wp_cur);
         store_rows<T, VPT>(out, n, tile_base + (size_t)warp * SEG, lane, tile_base + TILE <= n, v);
-        if (carry_out != nullptr && t == num_tiles - 1 && threadIdx.x == 0) *carry_out = sm.prefix + agg_cur;
+        if (carry_out != nullptr && t == num_tiles - 1 && threadIdx.x == 0) *carry_out = sm.prefix[k & 1] + agg_cur;
         if (TRACE && threadIdx.x == 0) trace[(size_t)t * kTraceWords + 4] = globaltimer_ns();
         wp_cur = wp_next;
         agg_cur = agg_next;

@@ -1,0 +1,345 @@
+// scan_wide.cu -- single-pass scans with 64-bit sums: uint32 -> uint64 and
+// int32 -> int64 (widened accumulation), int64 (wrapping modulo 2^64) and
+// fp64.
+//
+// "Parallel Prefix Sum (Scan) for NVIDIA T4 (sm_75)", Key Features (64-bit
+// indexing for large arrays): the sum of many 32-bit counts overflows 32
+// bits, so it is carried and stored in 64 bits.  The method is the one of
+// the 32-bit kernels ("Prefix sum and other parallel patterns", A
+// device-level scan: scan then propagate, with decoupled look-back), on the
+// schedule of the single-register-buffer persistent kernel (scan_pipe.cu):
+//   - each CTA takes a rank and owns tiles rank, rank + G, ...;
+//   - a three-stage ring receives each tile's input with one bulk copy;
+//   - tile k+1 is summed and its aggregate published while tile k waits for
+//     its look-back, which stops at this CTA's own previous tile;
+//   - tile k is read again from the ring, scanned in registers and stored.
+// The descriptors are 16 bytes (lookback_wide.cuh).
+//
+// A tile is 8192 elements: 512 threads, each holding 8 rows of 2 elements.
+// Warp w owns a contiguous segment; row j of it is 64 consecutive elements
+// and lane l holds elements 2l and 2l+1, so the scan order inside a warp is
+// (row, lane, element), every output store of a warp is 512 contiguous bytes
+// (one 16-byte pair per lane), and every shared-memory read of a row is
+// conflict-free (8 or 16 bytes per lane, consecutive).
+//
+// Inputs that are not 16-byte aligned, and the ragged last tile, are read
+// and written element by element with bounds checks.
+#include <type_traits>
+
+#include "bulk.cuh"
+#include "internal.h"
+#include "lookback_wide.cuh"
+
+namespace ss {
+
+namespace {
+
+constexpr int kWThreads = 512;
+constexpr int kWWarps = kWThreads / 32;
+constexpr uint32_t kWTile = 8192;
+static_assert(kWTile == kWideTile, "tile size shared with the host side");
+
+template <typename TI, typename TA> __device__ __forceinline__ TA widen(TI x);
+template <> __device__ __forceinline__ unsigned long long widen<uint32_t, unsigned long long>(uint32_t x) {
+    return (unsigned long long)x;
+}
+template <> __device__ __forceinline__ unsigned long long widen<int32_t, unsigned long long>(int32_t x) {
+    return (unsigned long long)(long long)x;  // sign-extended; the adds are the same bits as int64's
+}
+template <> __device__ __forceinline__ unsigned long long widen<unsigned long long, unsigned long long>(
+    unsigned long long x) {
+    return x;
+}
+template <> __device__ __forceinline__ double widen<double, double>(double x) { return x; }
+
+// A lane's two consecutive input elements from shared memory.
+template <typename TI>
+__device__ __forceinline__ void lds_pair(const void* p, TI (&x)[2]) {
+    if constexpr (sizeof(TI) == 4) {
+        uint32_t a, b;
+        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(smem_u32(p)));
+        x[0] = (TI)a;
+        x[1] = (TI)b;
+    } else {
+        unsigned long long a, b;
+        asm volatile("ld.shared.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "r"(smem_u32(p)));
+        if constexpr (std::is_same<TI, double>::value) {
+            x[0] = __longlong_as_double((long long)a);
+            x[1] = __longlong_as_double((long long)b);
+        } else {
+            x[0] = a;
+            x[1] = b;
+        }
+    }
+}
+
+__device__ __forceinline__ void st_v2_u64(void* p, unsigned long long a, unsigned long long b) {
+    asm volatile("st.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
+}
+
+}  // namespace
+
+template <typename TI, typename TA, bool INCLUSIVE>
+__global__ void __launch_bounds__(kWThreads, 1)
+k_scan_wide(const TI* in, TA* out, size_t n, uint32_t num_tiles, bool fast, LookbackCtx ctx) {
+    constexpr int STAGES = 3;
+    constexpr int EPV = 2;                                // elements per lane per row
+    constexpr int VPT = (int)kWTile / (kWThreads * EPV);  // rows per lane
+    constexpr uint32_t SEG = 32u * VPT * EPV;     // elements per warp segment
+    constexpr uint32_t IN_BYTES = kWTile * (uint32_t)sizeof(TI);
+    static_assert(SEG * kWWarps == kWTile, "tile geometry");
+
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t bars[STAGES];
+    // Warp totals, prefix and failure flag alternate between two slots by
+    // tile parity, so a slot is never rewritten while a slower warp may still
+    // read it.
+    __shared__ TA s_warp[2][kWWarps];
+    __shared__ TA s_prefix[2];
+    __shared__ uint32_t s_fail[2], s_rank, s_epoch;
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const uint32_t G = gridDim.x;
+    const uint64_t policy = policy_evict_first();
+
+    if (threadIdx.x == 0) {
+        uint32_t rank, epoch;
+        claim_tile(ctx.counter, G, &rank, &epoch);
+        s_rank = rank;
+        s_epoch = epoch;
+        for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
+        fence_async_shared();
+    }
+    __syncthreads();
+    const uint32_t rank = s_rank;
+    const uint32_t epoch = s_epoch;
+    if (rank >= G) {
+        if (threadIdx.x == 0) record_error(ctx.status, kErrCounter, rank);
+        return;
+    }
+    const uint32_t count = rank < num_tiles ? (num_tiles - rank + G - 1) / G : 0;
+    uint32_t issued = 0, consumed = 0;  // thread 0
+
+    auto full_tile = [&](uint32_t k) { return fast && (size_t)(rank + k * G) * kWTile + kWTile <= n; };
+    auto issue = [&](uint32_t k) {
+        const int s = (int)(k % STAGES);
+        if (full_tile(k)) {
+            fence_async_shared();
+            mbar_arrive_expect_tx(&bars[s], IN_BYTES);
+            bulk_load(smem_raw + (size_t)s * IN_BYTES, in + (size_t)(rank + k * G) * kWTile, IN_BYTES, &bars[s],
+                      policy);
+        } else {
+            mbar_arrive(&bars[s]);  // read from global with bounds checks instead
+        }
+        issued = k + 1;
+    };
+    // This lane's rows of tile k, widened.
+    auto read_rows = [&](uint32_t k, TA (&v)[VPT][EPV]) {
+        const size_t seg = (size_t)(rank + k * G) * kWTile + (size_t)warp * SEG;
+        if (full_tile(k)) {
+            const unsigned char* src =
+                smem_raw + (size_t)(k % STAGES) * IN_BYTES + ((size_t)warp * SEG + (size_t)lane * EPV) * sizeof(TI);
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                TI x[EPV];
+                lds_pair<TI>(src + (size_t)j * 32 * EPV * sizeof(TI), x);
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) v[j][e] = widen<TI, TA>(x[e]);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j)
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) {
+                    const size_t i = seg + (size_t)(32 * j + lane) * EPV + e;
+                    v[j][e] = i < n ? widen<TI, TA>(in[i]) : TA(0);
+                }
+        }
+    };
+    // Waits for tile k, sums it, publishes its aggregate; false if the copy did not arrive.
+    auto reduce_publish = [&](uint32_t k, TA* wp, TA* agg) -> bool {
+        const uint32_t t = rank + k * G;
+        const bool ok = mbar_wait_bounded(&bars[k % STAGES], (k / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
+        if (__syncthreads_or(!ok)) {
+            if (threadIdx.x == 0) record_error(ctx.status, kErrBulkTimeout, t);
+            return false;
+        }
+        TA v[VPT][EPV];
+        read_rows(k, v);
+        TA x = TA(0);
+#pragma unroll
+        for (int j = 0; j < VPT; ++j)
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) x += v[j][e];
+        x = warp_sum(x);
+        if (lane == 0) s_warp[k & 1][warp] = x;
+        __syncthreads();
+        // The warp totals scanned across the lanes of every warp (5 adds, not 16).
+        const TA inc = warp_inclusive_scan<TA>(lane < kWWarps ? s_warp[k & 1][lane] : TA(0), lane);
+        const TA w = __shfl_sync(kFullMask, inc, warp > 0 ? warp - 1 : 0);
+        *wp = warp > 0 ? w : TA(0);
+        *agg = __shfl_sync(kFullMask, inc, kWWarps - 1);
+        const TA b = *agg;
+        if (threadIdx.x == 0 && (int64_t)t != ctx.fault_tile) {
+            if (t == 0) {
+                if (num_tiles > 1) st_relaxed_desc16(ctx.desc, pack_desc16(epoch, kStateP, acc_bits<TA>(b)));
+            } else {
+                st_relaxed_desc16(ctx.desc + 2 * (size_t)t, pack_desc16(epoch, kStateA, acc_bits<TA>(b)));
+            }
+        }
+        compiler_fence();  // the aggregate just published stays ahead of the look-back
+        return true;
+    };
+
+    TA wp_cur = TA(0), agg_cur = TA(0), prev_incl = TA(0);
+    bool failed = false;
+    uint32_t fail_at = 0;
+    if (threadIdx.x == 0)
+        for (uint32_t k = 0; k < count && k < (uint32_t)STAGES; ++k) issue(k);
+    if (count > 0 && !reduce_publish(0, &wp_cur, &agg_cur)) failed = true;
+
+    for (uint32_t k = 0; !failed && k < count; ++k) {
+        const uint32_t t = rank + k * G;
+        TA wp_next = TA(0), agg_next = TA(0);
+        if (k + 1 < count && !reduce_publish(k + 1, &wp_next, &agg_next)) {
+            failed = true;
+            fail_at = k;
+            break;
+        }
+        if (warp == 0) {
+            TA excl = TA(0);
+            bool lb_failed = false;
+            const bool dead = (int64_t)t == ctx.fault_tile;  // test hook only
+            if (t == 0) {
+                lb_failed = dead;
+            } else if (dead) {
+                lb_failed = true;
+            } else {
+                const int64_t floor = k > 0 ? (int64_t)t - (int64_t)G : -1;
+                excl = lookback_wide<TA>(ctx.desc, ctx, t, epoch, lane, &lb_failed, floor, prev_incl);
+                if (lane == 0) {
+                    if (!lb_failed) {
+                        st_relaxed_desc16(ctx.desc + 2 * (size_t)t,
+                                          pack_desc16(epoch, kStateP, acc_bits<TA>(excl + agg_cur)));
+                    } else {
+                        st_relaxed_desc16(ctx.desc + 2 * (size_t)t, pack_desc16(epoch, kStatePoison, 0ull));
+                        record_error(ctx.status, kErrLookbackTimeout, t);
+                    }
+                }
+            }
+            prev_incl = excl + agg_cur;
+            if (lane == 0) {
+                s_prefix[k & 1] = excl;
+                s_fail[k & 1] = lb_failed ? 1u : 0u;
+            }
+        }
+        // Scan tile k in registers: per row, the lane's vector sum, a warp
+        // scan across lanes, and the rows chained in order.
+        TA v[VPT][EPV];
+        read_rows(k, v);
+        TA row_excl[VPT], row_tot[VPT];
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            TA s = TA(0);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) s += v[j][e];
+            const TA inc = warp_inclusive_scan<TA>(s, lane);
+            const TA before = __shfl_up_sync(kFullMask, inc, 1);
+            row_excl[j] = lane > 0 ? before : TA(0);
+            row_tot[j] = __shfl_sync(kFullMask, inc, 31);
+        }
+        __syncthreads();  // tile k read by everyone; the prefix is in shared memory
+        if (threadIdx.x == 0) {
+            consumed = k + 1;
+            if (k + STAGES < count) issue(k + STAGES);
+        }
+        if (s_fail[k & 1]) {
+            failed = true;
+            fail_at = k;
+            break;
+        }
+        TA base = s_prefix[k & 1] + wp_cur;
+        const size_t seg = (size_t)t * kWTile + (size_t)warp * SEG;
+        const bool full = full_tile(k);
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            TA r = base + row_excl[j];
+            TA y[EPV];
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) {
+                if (INCLUSIVE) {
+                    r += v[j][e];
+                    y[e] = r;
+                } else {
+                    y[e] = r;
+                    r += v[j][e];
+                }
+            }
+            base += row_tot[j];
+            const size_t i0 = seg + (size_t)(32 * j + lane) * EPV;
+            if (full) {
+                st_v2_u64(out + i0, acc_bits<TA>(y[0]), acc_bits<TA>(y[1]));
+            } else {
+#pragma unroll
+                for (int e = 0; e < EPV; ++e)
+                    if (i0 + e < n) out[i0 + e] = y[e];
+            }
+        }
+        wp_cur = wp_next;
+        agg_cur = agg_next;
+    }
+
+    if (failed && threadIdx.x == 0) {
+        for (uint32_t k = fail_at + 1; k < count; ++k) {
+            const uint32_t t = rank + k * G;
+            if ((int64_t)t != ctx.fault_tile)
+                st_relaxed_desc16(ctx.desc + 2 * (size_t)t, pack_desc16(epoch, kStatePoison, 0ull));
+        }
+        for (uint32_t k = consumed; k < issued; ++k)
+            mbar_wait_bounded(&bars[k % STAGES], (k / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
+    }
+}
+
+template <typename TI, typename TA, bool INCL>
+static cudaError_t launch_wide(const void* in, void* out, size_t n, const LookbackWs& ws, cudaStream_t s) {
+    constexpr size_t SMEM = 3 * (size_t)kWTile * sizeof(TI);
+    auto kern = k_scan_wide<TI, TA, INCL>;
+    static int sms = 0;
+    if (sms == 0) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
+        if (e != cudaSuccess) return e;
+        int dev = 0;
+        cudaGetDevice(&dev);
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        sms = v > 0 ? v : 1;
+    }
+    const uint32_t tiles = (uint32_t)((n + kWTile - 1) / kWTile);
+    const uint32_t grid = tiles < (uint32_t)sms ? tiles : (uint32_t)sms;
+    const bool fast = ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) & 15u) == 0;
+    LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};
+    kern<<<grid, kWThreads, SMEM, s>>>(static_cast<const TI*>(in), static_cast<TA*>(out), n, tiles, fast, ctx);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scan_wide(WideType type, bool inclusive, const void* in, void* out, size_t n,
+                             const LookbackWs& ws, cudaStream_t s) {
+    using u64 = unsigned long long;
+    switch (type) {
+        case WideType::U32toU64:
+            return inclusive ? launch_wide<uint32_t, u64, true>(in, out, n, ws, s)
+                             : launch_wide<uint32_t, u64, false>(in, out, n, ws, s);
+        case WideType::I32toI64:
+            return inclusive ? launch_wide<int32_t, u64, true>(in, out, n, ws, s)
+                             : launch_wide<int32_t, u64, false>(in, out, n, ws, s);
+        case WideType::I64:
+            return inclusive ? launch_wide<u64, u64, true>(in, out, n, ws, s)
+                             : launch_wide<u64, u64, false>(in, out, n, ws, s);
+        default:
+            return inclusive ? launch_wide<double, double, true>(in, out, n, ws, s)
+                             : launch_wide<double, double, false>(in, out, n, ws, s);
+    }
+}
+
+}  // namespace ss

@@ -72,6 +72,18 @@ def test_predicate_and_unordered_compaction_arguments(lib):
     assert lib.ss_compact_positive_unordered(ss.SS_F32, 0x10000, 0x10000, 0xA0000, 4, None) == inv
 
 
+def test_wide_scan_arguments(lib):
+    inv = ss.SS_ERR_INVALID_ARG
+    assert lib.scan_inclusive_f64(None, None, 5, None) == inv
+    assert lib.scan_inclusive_f64(0x10004, 0x20000, 5, None) == inv          # fp64 input 4-byte aligned
+    assert lib.scan_exclusive_u32_u64(0x10004, 0x20004, 5, None) == inv      # output not 8-byte aligned
+    assert lib.scan_exclusive_u32_u64(0x10000, 0x10000, 5, None) == inv      # widened in place
+    assert "widened" in ss.ss_last_error_detail()
+    assert lib.scan_inclusive_i64(0x10000, 0x10008, 64, None) == inv         # partial overlap
+    assert lib.ss_scan_wide(9, 1, 0x10000, 0x20000, 4, None) == ss.SS_ERR_UNSUPPORTED
+    assert lib.scan_inclusive_i64(None, None, 0, None) == ss.SS_OK           # empty
+
+
 def test_moe_arguments(lib):
     inv = ss.SS_ERR_INVALID_ARG
     f = lib.ss_moe_counts_offsets

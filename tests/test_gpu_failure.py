@@ -90,3 +90,21 @@ def test_predicate_compaction_timeout_is_reported_and_recovered(ss):
     assert ss.ss_stream_status()[0] == ss.SS_OK
     c = int(cnt.item())
     assert_equal(d_o[:c].cpu().numpy().view(np.uint32), oracle.compact_positive_f32(x).view(np.uint32))
+
+
+def test_wide_scan_timeout_is_reported_and_recovered(ss):
+    import torch
+    n = 40 * 8192 + 3
+    x = si.uniform_int32(n, -1000, 1000, seed=2).astype(np.int64)
+    d = torch.from_numpy(x).to("cuda:0")
+    o = torch.empty_like(d)
+    ss.ss_debug_set_lookback_fault(9, 2_000_000)
+    try:
+        ss.scan_inclusive_i64(d, o)
+        st, tile = ss.ss_stream_status()
+    finally:
+        ss.ss_debug_set_lookback_fault(-1, 0)
+    assert st == ss.SS_ERR_LOOKBACK_TIMEOUT and tile > 9
+    ss.scan_inclusive_i64(d, o)
+    assert ss.ss_stream_status() == (ss.SS_OK, -1)
+    assert_equal(o.cpu().numpy(), oracle.scan_i64(x, True))
