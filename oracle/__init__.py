@@ -48,6 +48,12 @@ def _declare(lib):
         f.restype = None
     lib.oracle_abs_prefix_f64.argtypes = [p, p, sz]
     lib.oracle_abs_prefix_f64.restype = None
+    for name in ("oracle_scan_rows_i32", "oracle_scan_rows_u32", "oracle_scan_rows_f32"):
+        f = getattr(lib, name)
+        f.argtypes = [p, p, sz, sz, i]
+        f.restype = None
+    lib.oracle_abs_prefix_rows_f32.argtypes = [p, p, sz, sz]
+    lib.oracle_abs_prefix_rows_f32.restype = None
     lib.oracle_compact_u32.argtypes = [p, p, p, sz]
     lib.oracle_compact_u32.restype = u64
     for name in ("oracle_compact_positive_f32", "oracle_compact_positive_i32", "oracle_compact_positive_u32"):
@@ -137,6 +143,29 @@ def abs_prefix_f64(x: np.ndarray, lib=None) -> np.ndarray:
     x = np.ascontiguousarray(x, dtype=np.float64)
     y = np.empty(x.size, dtype=np.float64)
     (lib or load()).oracle_abs_prefix_f64(_ptr(x), _ptr(y), x.size)
+    return y
+
+
+def scan_rows(x: np.ndarray, inclusive: bool, lib=None) -> np.ndarray:
+    """Every row of a 2-D int32 / uint32 / fp32 array scanned on its own
+    (fp32 rows in float64)."""
+    x = np.ascontiguousarray(x)
+    assert x.ndim == 2
+    rows, cols = x.shape
+    kinds = {np.dtype(np.int32): ("oracle_scan_rows_i32", np.int32),
+             np.dtype(np.uint32): ("oracle_scan_rows_u32", np.uint32),
+             np.dtype(np.float32): ("oracle_scan_rows_f32", np.float64)}
+    fn, out_dt = kinds[x.dtype]
+    y = np.empty((rows, cols), dtype=out_dt)
+    getattr(lib or load(), fn)(_ptr(x), _ptr(y), rows, cols, int(bool(inclusive)))
+    return y
+
+
+def abs_prefix_rows_f32(x: np.ndarray, lib=None) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    rows, cols = x.shape
+    y = np.empty((rows, cols), dtype=np.float64)
+    (lib or load()).oracle_abs_prefix_rows_f32(_ptr(x), _ptr(y), rows, cols)
     return y
 
 

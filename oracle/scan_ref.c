@@ -192,6 +192,43 @@ void oracle_abs_prefix_f32(const float *x, double *y, size_t n)
 }
 
 /*
+ * Batched scans: a row-major rows x cols matrix, every row scanned on its
+ * own, the running sum starting again from zero at each row (the per-row
+ * cumulative sum of top-p sampling, "Prefix sum and other parallel
+ * patterns", In LLMs: MoE token dispatch, last paragraph).  Each row is the
+ * one-dimensional scan above, applied to that row's elements.
+ */
+void oracle_scan_i32(const int32_t *x, int32_t *y, size_t n, int inclusive);
+void oracle_scan_u32(const uint32_t *x, uint32_t *y, size_t n, int inclusive);
+void oracle_scan_f32(const float *x, double *y, size_t n, int inclusive);
+void oracle_abs_prefix_f32(const float *x, double *y, size_t n);
+
+void oracle_scan_rows_i32(const int32_t *x, int32_t *y, size_t rows, size_t cols, int inclusive)
+{
+    for (size_t r = 0; r < rows; ++r)
+        oracle_scan_i32(x + r * cols, y + r * cols, cols, inclusive);
+}
+
+void oracle_scan_rows_u32(const uint32_t *x, uint32_t *y, size_t rows, size_t cols, int inclusive)
+{
+    for (size_t r = 0; r < rows; ++r)
+        oracle_scan_u32(x + r * cols, y + r * cols, cols, inclusive);
+}
+
+void oracle_scan_rows_f32(const float *x, double *y, size_t rows, size_t cols, int inclusive)
+{
+    for (size_t r = 0; r < rows; ++r)
+        oracle_scan_f32(x + r * cols, y + r * cols, cols, inclusive);
+}
+
+void oracle_abs_prefix_rows_f32(const float *x, double *y, size_t rows, size_t cols)
+{
+    for (size_t r = 0; r < rows; ++r)
+        oracle_abs_prefix_f32(x + r * cols, y + r * cols, cols);
+}
+
+
+/*
  * Order-preserving compaction: copy keys[i] for every i with flags[i] != 0,
  * in index order.  Returns the number kept.  `out` must hold n elements.
  */

@@ -54,6 +54,11 @@ MUTANTS = [
     ("scan_ref.c", "if (inclusive)\n            y[i] = sum + comp;", "if (inclusive)\n            y[i] = sum;",
      "fp64 inclusive drops the compensation"),
     ("scan_ref.c", "if (as >= av)", "if (as <= av)", "fp64 compensation takes the wrong branch"),
+    ("scan_ref.c", "        oracle_scan_u32(x + r * cols, y + r * cols, cols, inclusive);",
+     "        oracle_scan_u32(x + r * cols, y + r * cols, cols - (r > 0), inclusive);", "batched scan skips a column"),
+    ("scan_ref.c", "        oracle_scan_i32(x + r * cols, y + r * cols, cols, inclusive);",
+     "        oracle_scan_i32(x + r * cols, y + r * cols, cols, !inclusive);",
+     "batched int32 scan flips inclusive"),
     ("tile_model.c", "return i + i / 32 + i / 1024;", "return i + i / 32 + i / 512;", "two-term padding uses /512"),
     ("tile_model.c", "return i + i / 32;\n", "return i + i / 16;\n", "one-term padding uses /16"),
     ("tile_model.c", "total += 2 * level;", "total += level;", "model counts one sweep"),
@@ -140,6 +145,11 @@ def _checks(lib):
     xn = np.array([1.0, 1e100, 1.0, -1e100], dtype=np.float64)
     pin("f64_neumaier", lambda: oracle.scan_f64(xn, True, lib=lib).tolist() == [1.0, 1e100, 1e100, 2.0]
         and oracle.scan_f64(xn[::-1].copy(), True, lib=lib).tolist() == [-1e100, -1e100, 1.0, 2.0])
+
+    xr = np.array([[3, 1, 7, 0], [4, 1, 6, 3]], dtype=np.int32)
+    pin("rows_i32", lambda: oracle.scan_rows(xr, True, lib=lib).tolist() == [[3, 4, 11, 11], [4, 5, 11, 14]])
+    pin("rows_u32", lambda: oracle.scan_rows(xr.astype(np.uint32), False, lib=lib).tolist()
+        == [[0, 3, 4, 11], [0, 4, 5, 11]])
 
     pin("model_plain", lambda: oracle.blelloch_requests(4096, oracle.LAYOUT_PLAIN, lib=lib) == 1534)
     pin("model_pad32", lambda: oracle.blelloch_requests(4096, oracle.LAYOUT_PAD32, lib=lib) == 294)

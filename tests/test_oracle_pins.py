@@ -20,6 +20,9 @@ Which pin covers which oracle function:
 * scan_f64 / abs_prefix_f64: exact rational brute force within the
   compensated-sum bound, Neumaier's classic cancellation case,
   integer-valued inputs exactly.
+* scan_rows / abs_prefix_rows_f32: a worked example by hand, all-ones rows
+  restart at every row, brute force with Python integers, each row equal to
+  the pinned one-dimensional scan.
 * moe_counts_offsets: a worked example by hand, the histogram against
   numpy's bincount, tile size 1 against the (pinned) exclusive scan, the
   rounding invariants, one-expert and out-of-range cases.
@@ -489,3 +492,35 @@ def test_abs_prefix_f64_exact():
     for i in range(n):
         acc += abs(Fraction(float(x[i])))
         assert abs(Fraction(float(got[i])) - acc) <= 2 * (2.0 ** -53) * acc
+
+
+# ---- batched (per-row) scans ----
+
+def test_rows_worked_example():
+    x = np.array([[3, 1, 7, 0], [4, 1, 6, 3]], dtype=np.int32)
+    assert oracle.scan_rows(x, True).tolist() == [[3, 4, 11, 11], [4, 5, 11, 14]]
+    assert oracle.scan_rows(x, False).tolist() == [[0, 3, 4, 11], [0, 4, 5, 11]]
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 1), (3, 1), (1, 7), (5, 64), (64, 3)])
+def test_rows_all_ones_restart_at_every_row(rows, cols):
+    x = np.ones((rows, cols), dtype=np.uint32)
+    inc = np.tile(np.arange(1, cols + 1, dtype=np.uint32), (rows, 1))
+    assert np.array_equal(oracle.scan_rows(x, True), inc)
+    assert np.array_equal(oracle.scan_rows(x, False), inc - 1)
+
+
+def test_rows_brute_force_and_one_row_is_the_flat_scan():
+    x = si.uniform_int32(7 * 33, -(2**31), 2**31 - 1, seed=70).reshape(7, 33)
+    got = oracle.scan_rows(x, True)
+    for r in range(7):
+        acc = 0
+        for c in range(33):
+            acc += int(x[r, c])
+            assert int(got[r, c]) == (acc + 2**31) % 2**32 - 2**31
+    flat = si.workload_int_pm1000(1000, seed=2)
+    assert np.array_equal(oracle.scan_rows(flat.reshape(1, -1), False)[0], oracle.scan_i32(flat, False))
+    xf = si.uniform_f32(4 * 50, seed=71).reshape(4, 50)
+    for r in range(4):
+        assert np.array_equal(oracle.scan_rows(xf, True)[r], oracle.scan_f32(xf[r], True))
+        assert np.array_equal(oracle.abs_prefix_rows_f32(xf)[r], oracle.abs_prefix_f32(xf[r]))
