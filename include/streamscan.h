@@ -176,6 +176,25 @@ ss_status ss_compact_positive_unordered(ss_dtype dtype, const void *in, void *ou
                                         size_t n, ss_stream_t stream);
 
 /*
+ * Batched scans: every row of a row-major rows x cols matrix scanned on its
+ * own, the sum starting from zero at each row (for example the cumulative
+ * sum over each row's sorted probabilities in top-p sampling, "Prefix sum
+ * and other parallel patterns", In LLMs: MoE token dispatch, last
+ * paragraph).  Same element types, wraparound and fp32 rules as the flat
+ * scans.
+ *   in    device, rows * cols elements, row r at in + r * cols.
+ *   out   device, same shape; out == in is allowed, any other overlap is
+ *         SS_ERR_INVALID_ARG.
+ *   rows, cols  either may be 0 (a no-op); rows * cols < 2^31 * 4096, and
+ *         for rows longer than 2048 elements rows * ceil(cols / 4096) < 2^31.
+ * Rows longer than 2048 elements use row-aligned tiles with the decoupled
+ * look-back (the per-stream workspace); shorter rows take one warp each;
+ * rows of 2^21 elements or more run as one flat scan each.
+ */
+ss_status ss_scan_rows(ss_dtype dtype, int inclusive, const void *in, void *out, size_t rows, size_t cols,
+                       ss_stream_t stream);
+
+/*
  * MoE token counts and expert offsets aligned to GEMM tiles ("Prefix sum and
  * other parallel patterns", In LLMs: MoE token dispatch, steps 1-2, and
  * Exercise 2: a histogram of the router's expert ids, then an exclusive

@@ -77,6 +77,7 @@ def _declare(lib):
         "scan_inclusive_f64": [P, P, SZ, P],
         "scan_exclusive_f64": [P, P, SZ, P],
         "ss_scan_wide": [I, I, P, P, SZ, P],
+        "ss_scan_rows": [I, I, P, P, SZ, SZ, P],
         "ss_scan": [I, I, I, P, P, SZ, P],
         "ss_scan_seeded": [I, I, P, P, SZ, P, P, P],
         "ss_scan_host": [I, I, P, P, SZ, P],
@@ -255,6 +256,11 @@ def ss_scan_wide(wide_type: int, inclusive: bool, inp, out, n=None, stream=None)
         n = _numel(inp)
     _check(lib().ss_scan_wide(wide_type, int(bool(inclusive)), _addr(inp), _addr(out), n,
                               _stream(stream, inp, out)), "ss_scan_wide")
+
+
+def ss_scan_rows(dtype: int, inclusive: bool, inp, out, rows: int, cols: int, stream=None):
+    _check(lib().ss_scan_rows(dtype, int(bool(inclusive)), _addr(inp), _addr(out), rows, cols,
+                              _stream(stream, inp, out)), "ss_scan_rows")
 
 
 def ss_moe_counts_offsets(topk_ids, num_experts: int, align: int, counts, offsets, m=None, stream=None):

@@ -30,6 +30,7 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 constexpr uint64_t kClearEvery = 1ull << 29;
 
 constexpr size_t kHostChunk = (size_t)16 << 20;  // elements per host-pipeline chunk
+constexpr size_t kRowsFlat = (size_t)1 << 21;    // batched rows at least this long run as flat scans
 constexpr int kHostBuffers = 3;
 
 ss_status fail(ss_status st, const std::string& why) {
@@ -402,6 +403,38 @@ ss_status ss_scan_wide(ss_wide_type type, int inclusive, const void* in, void* o
         default: return fail(SS_ERR_UNSUPPORTED, "unknown 64-bit scan type");
     }
     return scan_wide(t, inclusive != 0, in, out, n, (cudaStream_t)stream);
+}
+
+ss_status ss_scan_rows(ss_dtype dtype, int inclusive, const void* in, void* out, size_t rows, size_t cols,
+                       ss_stream_t stream) {
+    if (!valid_dtype(dtype)) return fail(SS_ERR_UNSUPPORTED, "unknown dtype");
+    cudaStream_t s = (cudaStream_t)stream;
+    if (rows == 0 || cols == 0) return SS_OK;
+    if (rows > SIZE_MAX / 8 / cols) return fail(SS_ERR_INVALID_ARG, "rows * cols too large");
+    const size_t n = rows * cols;
+    ss_status st = check_scan_args(in, out, n, ss::kMinScanTile);
+    if (st != SS_OK) return st;
+    if (cols >= kRowsFlat) {
+        // Rows this long fill the GPU on their own: one flat single-pass scan
+        // per row (the persistent kernel) beats tiles of every row in one launch.
+        for (size_t r = 0; r < rows; ++r) {
+            st = scan_lookback(to_dtype(dtype), inclusive != 0, static_cast<const uint32_t*>(in) + r * cols,
+                               static_cast<uint32_t*>(out) + r * cols, cols, nullptr, nullptr, s);
+            if (st != SS_OK) return st;
+        }
+        return SS_OK;
+    }
+    Workspace* w = nullptr;
+    if (cols > ss::kRowsWarpMax) {
+        const size_t tiles = rows * ((cols + ss::kRowsTile - 1) / ss::kRowsTile);
+        if (tiles >= ((size_t)1 << 31)) return fail(SS_ERR_INVALID_ARG, "too many tiles");
+        st = get_workspace(s, &w);
+        if (st != SS_OK) return st;
+        st = ensure_desc(w, tiles);
+        if (st != SS_OK) return st;
+    }
+    cudaError_t e = ss::launch_scan_rows(to_dtype(dtype), inclusive != 0, in, out, rows, cols, make_ws(w), s);
+    return e == cudaSuccess ? SS_OK : cuda_fail(e, "batched scan launch");
 }
 
 ss_status ss_moe_counts_offsets(const int32_t* topk_ids, size_t m, int32_t num_experts, uint32_t align,

@@ -107,6 +107,15 @@ constexpr size_t kWideTile = 8192;
 cudaError_t launch_scan_wide(WideType type, bool inclusive, const void* in, void* out, size_t n,
                              const LookbackWs& ws, cudaStream_t s);
 
+// Batched scans (scan_rows.cu): every row of a row-major rows x cols matrix
+// scanned on its own.  Rows longer than kRowsWarpMax go through row-aligned
+// kRowsTile-element tiles with the look-back (one descriptor per tile);
+// shorter rows take one warp each and need no workspace.
+constexpr size_t kRowsTile = 4096;
+constexpr size_t kRowsWarpMax = 2048;
+cudaError_t launch_scan_rows(Dtype dt, bool inclusive, const void* in, void* out, size_t rows, size_t cols,
+                             const LookbackWs& ws, cudaStream_t s);
+
 // MoE token counts and tile-aligned offsets (moe.cu).  `acc` holds
 // num_experts uint32 and `ticket` one; both are zero on entry and the launch
 // leaves them zero.

@@ -84,6 +84,16 @@ def test_wide_scan_arguments(lib):
     assert lib.scan_inclusive_i64(None, None, 0, None) == ss.SS_OK           # empty
 
 
+def test_rows_scan_arguments(lib):
+    inv = ss.SS_ERR_INVALID_ARG
+    assert lib.ss_scan_rows(ss.SS_F32, 1, None, None, 0, 100, None) == ss.SS_OK     # no rows
+    assert lib.ss_scan_rows(ss.SS_F32, 1, None, None, 4, 0, None) == ss.SS_OK       # empty rows
+    assert lib.ss_scan_rows(ss.SS_F32, 1, None, None, 4, 5, None) == inv
+    assert lib.ss_scan_rows(ss.SS_I32, 0, 0x10000, 0x10004, 4, 100, None) == inv    # partial overlap
+    assert lib.ss_scan_rows(ss.SS_U32, 0, 0x10000, 0x20000, 1 << 40, 1 << 30, None) == inv  # too large
+    assert lib.ss_scan_rows(7, 0, 0x10000, 0x20000, 4, 4, None) == ss.SS_ERR_UNSUPPORTED
+
+
 def test_moe_arguments(lib):
     inv = ss.SS_ERR_INVALID_ARG
     f = lib.ss_moe_counts_offsets
