@@ -327,6 +327,29 @@ def row_rates(torch, ss, stream, dev, xs_d, xf_d, out_d):
             ids, 256, 64, cnt_e, off_e, stream=stream.cuda_stream), 100)
         rows[f"moe_counts_offsets_t{tokens}_k8_e256"] = {"us": ms * 1e3, "GB/s_on_ids": gbs(4 * tokens * 8, ms)}
         del ids
+    # scans with 64-bit sums at n = 1e8: uint32 -> uint64 (4 + 8 B per element) and int64 / fp64 (8 + 8)
+    w_in = torch.from_numpy(si.uniform_u32(N, seed=60).view(np.int32)).to(dev)
+    w_64 = torch.from_numpy(si.uniform_f32(N, seed=64).astype(np.float64)).to(dev)
+    w_out = torch.empty(N, dtype=torch.float64, device=dev)
+    for name, fn, per in (
+            ("u32_u64_incl", lambda: ss.ss_scan_wide(ss.SS_WIDE_U32_U64, True, w_in, w_out,
+                                                     stream=stream.cuda_stream), 12),
+            ("i64_incl", lambda: ss.ss_scan_wide(ss.SS_WIDE_I64, True, w_64.view(torch.int64), w_out,
+                                                 stream=stream.cuda_stream), 16),
+            ("f64_incl", lambda: ss.ss_scan_wide(ss.SS_WIDE_F64, True, w_64, w_out, stream=stream.cuda_stream), 16)):
+        ms = time_region(torch, stream, fn, 20)
+        rows[f"scan_{name}_1e8"] = {"ms": ms, "G-elem/s": N / ms / 1e6, "GB/s": gbs(per * N, ms),
+                                    "frac": gbs(per * N, ms) / peak}
+    del w_in, w_64, w_out
+    # batched per-row scans, fp32 inclusive: top-p over a 128,256-entry vocabulary, and short rows
+    for r_, c_ in ((512, 128256), (262144, 256), (16384, 4096)):
+        xr = torch.from_numpy(si.uniform_f32(r_ * c_, seed=82)).to(dev)
+        orr = torch.empty_like(xr)
+        ms = time_region(torch, stream, lambda: ss.ss_scan_rows(ss.SS_F32, True, xr, orr, r_, c_,
+                                                                stream=stream.cuda_stream), 20)
+        rows[f"scan_rows_f32_{r_}x{c_}"] = {"ms": ms, "GB/s": gbs(8 * r_ * c_, ms),
+                                            "frac": gbs(8 * r_ * c_, ms) / peak}
+        del xr, orr
     # context only: torch.cumsum on the same int32 input, timed the same way
     def cumsum():
         with torch.cuda.stream(stream):  # torch ops run on torch's current stream
