@@ -241,15 +241,25 @@ ss_status ss_scan_seeded(ss_dtype dtype, int inclusive, const void *in, void *ou
                          const void *d_carry_in, void *d_carry_out, ss_stream_t stream);
 
 /*
- * Host-memory scan: h_in and h_out are HOST pointers (pinned memory gives
- * full copy bandwidth; pageable memory works, slower).  The library copies
- * the input to the device in chunks, scans each chunk seeded with the
- * running carry, and copies results back, overlapping the copies of one
- * chunk with the scan of another.  Returns when h_out holds the result
- * (device errors are reported directly).  h_out == h_in is allowed.
+ * Host-memory scan: h_in and h_out are HOST pointers.  Returns when h_out
+ * holds the result (device errors are reported directly).  h_out == h_in is
+ * allowed.  Two paths:
+ *   - both buffers pinned and mapped into the device address space (for
+ *     example from cudaHostAlloc): the scan kernel reads h_in and writes
+ *     h_out directly, over NVLink-C2C on a Grace host, with no staging
+ *     copies.  It uses the one-CTA-per-tile kernel, whose accesses are plain
+ *     16-byte loads and stores;
+ *   - otherwise (pageable memory, or ss_set_host_mode(1)): the input is
+ *     copied to the device in chunks, each chunk is scanned seeded with the
+ *     running carry, and the results are copied back, the copies of one chunk
+ *     overlapping the scan of another.
  */
 ss_status ss_scan_host(ss_dtype dtype, int inclusive, const void *h_in, void *h_out, size_t n,
                        ss_stream_t stream);
+
+/* Path of ss_scan_host: 0 (default) = direct access when both buffers are
+ * mapped pinned memory, else staged; 1 = always staged.  Process-wide. */
+ss_status ss_set_host_mode(int mode);
 
 /*
  * Bandwidth probe: copies n uint32 from in to out with the scan's loader and

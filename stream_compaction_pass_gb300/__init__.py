@@ -78,6 +78,7 @@ def _declare(lib):
         "scan_exclusive_f64": [P, P, SZ, P],
         "ss_scan_wide": [I, I, P, P, SZ, P],
         "ss_scan_rows": [I, I, P, P, SZ, SZ, P],
+        "ss_set_host_mode": [I],
         "ss_scan": [I, I, I, P, P, SZ, P],
         "ss_scan_seeded": [I, I, P, P, SZ, P, P, P],
         "ss_scan_host": [I, I, P, P, SZ, P],
@@ -335,6 +336,10 @@ def ss_scan_config_count() -> int:
 
 def ss_set_scan_config(config: int) -> None:
     _check(lib().ss_set_scan_config(config), "ss_set_scan_config")
+
+
+def ss_set_host_mode(mode: int) -> None:
+    _check(lib().ss_set_host_mode(mode), "ss_set_host_mode")
 
 
 def ss_set_compact_config(config: int) -> None:

@@ -23,6 +23,7 @@ thread_local std::string g_detail;
 std::atomic<int> g_config{ss::scan_default_config()};
 std::atomic<int64_t> g_fault_tile{-1};
 std::atomic<uint64_t> g_timeout_ns{0};
+std::atomic<int> g_host_mode{0};  // 0: direct access to mapped host buffers when possible; 1: always stage
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 
 // Descriptor epochs are 30 bits; clear the descriptors well before a tag can
@@ -247,6 +248,34 @@ ss_status scan_wide(ss::WideType type, bool inclusive, const void* in, void* out
     if (st != SS_OK) return st;
     cudaError_t e = ss::launch_scan_wide(type, inclusive, in, out, n, make_ws(w), s);
     return e == cudaSuccess ? SS_OK : cuda_fail(e, "64-bit scan launch");
+}
+
+// The device address of a host buffer that the GPU can access directly
+// (pinned and mapped, e.g. from cudaHostAlloc), or nullptr.
+const void* mapped_device_ptr(const void* h) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, h) != cudaSuccess) {
+        cudaGetLastError();  // not a pointer CUDA knows: clear the error and stage instead
+        return nullptr;
+    }
+    if (a.type != cudaMemoryTypeHost || a.devicePointer == nullptr) return nullptr;
+    return a.devicePointer;
+}
+
+// The look-back scan on buffers that may live in host memory.  It runs the
+// one-CTA-per-tile row of the configuration table, whose loads and stores
+// are plain 16-byte accesses; the persistent rows stage tiles with bulk
+// copies, which are kept to device memory.
+ss_status scan_direct(Dtype dt, bool inclusive, const void* in, void* out, size_t n, cudaStream_t s) {
+    constexpr int kDirectConfig = 1;
+    const size_t tiles = (n + ss::kMinScanTile - 1) / ss::kMinScanTile;
+    Workspace* w = nullptr;
+    ss_status st = get_workspace(s, &w);
+    if (st != SS_OK) return st;
+    st = ensure_desc(w, tiles);
+    if (st != SS_OK) return st;
+    cudaError_t e = ss::launch_scan_lookback(dt, inclusive, kDirectConfig, in, out, n, make_ws(w), nullptr, nullptr, s);
+    return e == cudaSuccess ? SS_OK : cuda_fail(e, "scan launch");
 }
 
 Dtype to_dtype(ss_dtype d) {
@@ -580,6 +609,12 @@ static ss_status host_pipe_init(Workspace* w, size_t elems) {
     return SS_OK;
 }
 
+ss_status ss_set_host_mode(int mode) {
+    if (mode < 0 || mode > 1) return fail(SS_ERR_INVALID_ARG, "host mode must be 0 or 1");
+    g_host_mode.store(mode);
+    return SS_OK;
+}
+
 ss_status ss_scan_host(ss_dtype dtype, int inclusive, const void* h_in, void* h_out, size_t n,
                        ss_stream_t stream) {
     if (!valid_dtype(dtype)) return fail(SS_ERR_UNSUPPORTED, "unknown dtype");
@@ -588,6 +623,18 @@ ss_status ss_scan_host(ss_dtype dtype, int inclusive, const void* h_in, void* h_
     if (h_in != h_out && overlaps(h_in, n * 4, h_out, n * 4))
         return fail(SS_ERR_INVALID_ARG, "h_in and h_out partially overlap");
     cudaStream_t s = (cudaStream_t)stream;
+    if (g_host_mode.load() == 0) {
+        // Both buffers pinned and mapped: the kernel reads and writes host
+        // memory directly (over NVLink-C2C on Grace), with no staging copies.
+        const void* d_in = mapped_device_ptr(h_in);
+        void* d_out = const_cast<void*>(mapped_device_ptr(h_out));
+        if (d_in != nullptr && d_out != nullptr) {
+            ss_status st = scan_direct(to_dtype(dtype), inclusive != 0, d_in, d_out, n, s);
+            if (st != SS_OK) return st;
+            cudaError_t e = cudaStreamSynchronize(s);
+            return e == cudaSuccess ? SS_OK : cuda_fail(e, "cudaStreamSynchronize");
+        }
+    }
     Workspace* w = nullptr;
     ss_status st = get_workspace(s, &w);
     if (st != SS_OK) return st;
