@@ -312,10 +312,14 @@ int ss_scan_config_count(void);
 ss_status ss_set_scan_config(int config);
 
 /* Selects the persistent compaction kernel used for 16-byte aligned inputs
- * above 16384 elements, for later calls in this process: 0 streams keys and
- * flags through shared memory with bulk copies; 1 (the default) bulk-copies
- * only the flags and loads a 16-byte key vector only where one of its four
- * flags is set, which reads far fewer key bytes when few elements are kept.
+ * above 16384 elements (flag form), for later calls in this process:
+ *   0  streams keys and flags through shared memory with bulk copies;
+ *   1  bulk-copies only the flags and loads a 16-byte key vector only where
+ *      one of its four flags is set, which reads far fewer key bytes when
+ *      few elements are kept; one look-back per 16384 elements;
+ *   2  (the default) as 1, with one look-back per 65536-element tile worked
+ *      in four chunks, which pays a tile's fixed costs once per 65536
+ *      elements (inputs of 65536 elements or fewer take 1).
  * Results are identical. */
 ss_status ss_set_compact_config(int config);
 

@@ -496,6 +496,270 @@ k_compact_sel(const uint32_t* keys, const uint8_t* flags, uint32_t* out, unsigne
     }
 }
 
+// Chunked form: one look-back per 65536-element tile, processed as four
+// 16384-element chunks.  With sparse flags the work per element is small and
+// a tile's fixed costs dominate: the wait for its flags, two barriers, and
+// the look-back round trips.  A tile four times larger pays them once for
+// four times the elements.
+//  - Only the flags go through the ring: three stages of 64 KB.
+//  - Counting tile k+1: every warp counts its 1024-element share of each
+//    chunk.  After a barrier, warp 0 scans the 64 (chunk, warp) counts into
+//    offsets inside the tile and publishes the tile's total.
+//  - Warp 0 then looks back for tile k.  After a barrier, every warp writes
+//    its share of each chunk of tile k at
+//    prefix + offset(chunk, warp) + rank inside the warp.  Key vectors with
+//    a kept element are loaded from global memory one chunk ahead.
+//  - Counts and offsets alternate between two slots by tile parity.
+template <int THREADS, int STAGES>
+__global__ void __launch_bounds__(THREADS, 1)
+k_compact_chunked(const uint32_t* keys, const uint8_t* flags, uint32_t* out, unsigned long long* d_count,
+                  size_t n, uint32_t num_tiles, LookbackCtx ctx) {
+    constexpr int WARPS = THREADS / 32;
+    constexpr int VPT = 8;                                // rows (16-byte key vectors) per lane per chunk
+    constexpr int NW = VPT / 4;                           // packed count words per lane
+    constexpr uint32_t SEG = 32u * VPT * 4;               // 1024 elements per warp per chunk
+    constexpr uint32_t CHUNK = SEG * WARPS;               // 16384
+    constexpr int CHUNKS = 4;
+    constexpr uint32_t TILE = CHUNK * CHUNKS;             // 65536
+    static_assert(CHUNKS * WARPS == 64, "two (chunk, warp) counts per lane of warp 0");
+
+    extern __shared__ __align__(128) unsigned char smem_raw[];  // STAGES x TILE flag bytes
+    __shared__ __align__(8) uint64_t bars[STAGES];
+    __shared__ uint32_t s_cnt[2][CHUNKS * WARPS];   // count, then exclusive offset, of (chunk, warp)
+    __shared__ uint32_t s_total[2];
+    __shared__ uint32_t s_prefix[2], s_fail[2], s_rank, s_epoch;
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const uint32_t G = gridDim.x;
+    const uint64_t policy = policy_evict_first();
+
+    if (threadIdx.x == 0) {
+        uint32_t rank, epoch;
+        claim_tile(ctx.counter, G, &rank, &epoch);
+        s_rank = rank;
+        s_epoch = epoch;
+        for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
+        fence_async_shared();
+    }
+    __syncthreads();
+    const uint32_t rank = s_rank;
+    const uint32_t epoch = s_epoch;
+    if (rank >= G) {
+        if (threadIdx.x == 0) record_error(ctx.status, kErrCounter, rank);
+        return;
+    }
+    const uint32_t count = rank < num_tiles ? (num_tiles - rank + G - 1) / G : 0;
+    uint32_t issued = 0, consumed = 0;  // thread 0
+
+    auto issue = [&](uint32_t k) {  // thread 0: flags of this CTA's k-th tile
+        const int s = (int)(k % STAGES);
+        const size_t base = (size_t)(rank + k * G) * TILE;
+        if (base + TILE <= n) {
+            fence_async_shared();
+            mbar_arrive_expect_tx(&bars[s], TILE);
+            bulk_load(smem_raw + (size_t)s * TILE, flags + base, TILE, &bars[s], policy);
+        } else {
+            mbar_arrive(&bars[s]);  // ragged last tile: flags read from global
+        }
+        issued = k + 1;
+    };
+    // Keep masks of this lane's rows of chunk c of tile k.
+    auto masks = [&](uint32_t k, int c, uint32_t (&m)[VPT]) {
+        const size_t seg = (size_t)(rank + k * G) * TILE + (size_t)c * CHUNK + (size_t)warp * SEG;
+        if ((size_t)(rank + k * G) * TILE + TILE <= n) {
+            const unsigned char* f =
+                smem_raw + (size_t)(k % STAGES) * TILE + (size_t)c * CHUNK + (size_t)warp * SEG + (size_t)lane * 4;
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) m[j] = byte_keep_mask(lds_u32(f + 128 * j));
+        } else {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                m[j] = 0;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const size_t i = seg + (size_t)(32 * j + lane) * 4 + e;
+                    if (i < n && flags[i] != 0) m[j] |= 1u << e;
+                }
+            }
+        }
+    };
+    // Key vectors of chunk c of tile k that hold a kept element.
+    auto load_keys = [&](uint32_t k, int c, const uint32_t (&m)[VPT], uint32_t (&key)[VPT][4]) {
+        const size_t seg = (size_t)(rank + k * G) * TILE + (size_t)c * CHUNK + (size_t)warp * SEG;
+        if (seg + SEG <= n) {
+            const uint4* kp = reinterpret_cast<const uint4*>(keys + seg) + lane;
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                uint4 r = make_uint4(0u, 0u, 0u, 0u);
+                if (m[j]) r = ld_vec(kp + 32 * j);
+                key[j][0] = r.x;
+                key[j][1] = r.y;
+                key[j][2] = r.z;
+                key[j][3] = r.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const size_t i = seg + (size_t)(32 * j + lane) * 4 + e;
+                    key[j][e] = ((m[j] >> e) & 1u) ? keys[i] : 0u;
+                }
+        }
+    };
+    // Waits for tile k's flags, counts them per (chunk, warp), turns the
+    // counts into offsets and publishes the total.  False if the copy did
+    // not arrive.
+    auto count_publish = [&](uint32_t k) -> bool {
+        const uint32_t t = rank + k * G;
+        const bool ok = mbar_wait_bounded(&bars[k % STAGES], (k / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
+        if (__syncthreads_or(!ok)) {
+            if (threadIdx.x == 0) record_error(ctx.status, kErrBulkTimeout, t);
+            return false;
+        }
+#pragma unroll
+        for (int c = 0; c < CHUNKS; ++c) {
+            uint32_t m[VPT];
+            masks(k, c, m);
+            uint32_t x = 0;
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) x += (uint32_t)__popc(m[j]);
+            x = warp_sum(x);
+            if (lane == 0) s_cnt[k & 1][c * WARPS + warp] = x;
+        }
+        __syncthreads();
+        if (warp == 0) {  // (chunk, warp) order is the elements' order
+            const uint32_t a = s_cnt[k & 1][2 * lane], b = s_cnt[k & 1][2 * lane + 1];
+            const uint32_t inc = warp_inclusive_scan<uint32_t>(a + b, lane);
+            s_cnt[k & 1][2 * lane] = inc - a - b;
+            s_cnt[k & 1][2 * lane + 1] = inc - b;
+            const uint32_t total = __shfl_sync(kFullMask, inc, 31);
+            if (lane == 0) {
+                s_total[k & 1] = total;
+                if ((int64_t)t != ctx.fault_tile) {
+                    if (t == 0) {
+                        if (num_tiles > 1) st_relaxed_u64(ctx.desc, pack_desc(epoch, kStateP, total));
+                    } else {
+                        st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStateA, total));
+                    }
+                }
+            }
+            compiler_fence();  // the count just published stays ahead of the look-back
+        }
+        return true;
+    };
+
+    uint32_t prev_incl = 0;  // warp 0
+    uint32_t fail_at = 0;
+    bool failed = false;
+    if (threadIdx.x == 0)
+        for (uint32_t k = 0; k < count && k < (uint32_t)STAGES; ++k) issue(k);
+    if (count > 0 && !count_publish(0)) failed = true;
+
+    for (uint32_t k = 0; !failed && k < count; ++k) {
+        const uint32_t t = rank + k * G;
+        if (k == 0) __syncthreads();  // tile 0's offsets and total are visible; later tiles' are by the
+                                      // previous iteration's last barrier
+        const uint32_t agg = s_total[k & 1];
+        if (k + 1 < count && !count_publish(k + 1)) {
+            failed = true;
+            fail_at = k;
+            break;
+        }
+        if (warp == 0) {
+            uint32_t excl = 0;
+            bool lb_failed = false;
+            const bool dead = (int64_t)t == ctx.fault_tile;  // test hook only
+            if (t == 0) {
+                lb_failed = dead;
+            } else if (dead) {
+                lb_failed = true;
+            } else {
+                const int64_t floor = k > 0 ? (int64_t)t - (int64_t)G : -1;
+                excl = lookback<uint32_t, 1>(ctx, t, epoch, lane, &lb_failed, nullptr, floor, prev_incl);
+                if (lane == 0) {
+                    if (!lb_failed) {
+                        st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStateP, excl + agg));
+                    } else {
+                        st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStatePoison, 0u));
+                        record_error(ctx.status, kErrLookbackTimeout, t);
+                    }
+                }
+            }
+            prev_incl = excl + agg;
+            if (lane == 0) {
+                s_prefix[k & 1] = excl;
+                s_fail[k & 1] = lb_failed ? 1u : 0u;
+            }
+        }
+        // Masks and keys of chunk 0 load while warp 0 looks back.
+        uint32_t ma[VPT], mb[VPT];
+        uint32_t ka[VPT][4], kb[VPT][4];
+        masks(k, 0, ma);
+        load_keys(k, 0, ma, ka);
+        __syncthreads();  // the prefix is in shared memory
+        if (s_fail[k & 1]) {
+            failed = true;
+            fail_at = k;
+            break;
+        }
+        const uint32_t base = s_prefix[k & 1];
+        auto scatter = [&](int c, const uint32_t (&m)[VPT], const uint32_t (&key)[VPT][4]) {
+            uint32_t row_base[VPT];
+            uint32_t run = 0;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                uint32_t packed = 0;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) packed |= (uint32_t)__popc(m[4 * w + q]) << (8 * q);
+                const uint32_t inc = warp_inclusive_scan<uint32_t>(packed, lane);
+                const uint32_t exc = inc - packed;  // bytewise, no borrows (each byte <= 128)
+                const uint32_t rows = __shfl_sync(kFullMask, inc, 31);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    row_base[4 * w + q] = run + ((exc >> (8 * q)) & 0xffu);
+                    run += (rows >> (8 * q)) & 0xffu;
+                }
+            }
+            uint32_t* dst = out + (size_t)base + s_cnt[k & 1][c * WARPS + warp];
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                uint32_t pos = row_base[j];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if ((m[j] >> e) & 1u) dst[pos++] = key[j][e];
+            }
+        };
+#pragma unroll
+        for (int c = 0; c < CHUNKS; c += 2) {
+            masks(k, c + 1, mb);
+            load_keys(k, c + 1, mb, kb);
+            scatter(c, ma, ka);
+            if (c + 2 < CHUNKS) {
+                masks(k, c + 2, ma);
+                load_keys(k, c + 2, ma, ka);
+            }
+            scatter(c + 1, mb, kb);
+        }
+        if (t == num_tiles - 1 && threadIdx.x == 0) *d_count = (unsigned long long)base + agg;
+        __syncthreads();  // tile k's flags read by everyone
+        if (threadIdx.x == 0) {
+            consumed = k + 1;
+            if (k + STAGES < count) issue(k + STAGES);
+        }
+    }
+
+    if (failed && threadIdx.x == 0) {
+        for (uint32_t j = fail_at + 1; j < count; ++j) {
+            const uint32_t tt = rank + j * G;
+            if ((int64_t)tt != ctx.fault_tile) st_relaxed_u64(ctx.desc + tt, pack_desc(epoch, kStatePoison, 0u));
+        }
+        for (uint32_t j = consumed; j < issued; ++j)
+            mbar_wait_bounded(&bars[j % STAGES], (j / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
+    }
+}
+
 template <int THREADS, int VPT, int STAGES, bool SELECTIVE, KeepRule RULE = KeepRule::Flags>
 static cudaError_t launch_compact_persistent(const uint32_t* keys, const uint8_t* flags, uint32_t* out,
                                              unsigned long long* d_count, size_t n, const LookbackWs& ws,
@@ -528,10 +792,34 @@ static cudaError_t launch_compact_persistent(const uint32_t* keys, const uint8_t
     return cudaGetLastError();
 }
 
-// 0: bulk-copied keys and flags; 1: bulk-copied flags, selective key loads.
-static int g_compact_kernel = 1;
+// 0: bulk-copied keys and flags; 1: bulk-copied flags, selective key loads;
+// 2: the same with one look-back per 65536-element tile (the default).
+static int g_compact_kernel = 2;
 
-int compact_kernel_count() { return 2; }
+int compact_kernel_count() { return 3; }
+
+static cudaError_t launch_compact_chunked(const uint32_t* keys, const uint8_t* flags, uint32_t* out,
+                                         unsigned long long* d_count, size_t n, const LookbackWs& ws,
+                                         cudaStream_t s) {
+    constexpr int THREADS = 512, STAGES = 3;
+    constexpr size_t TILE = 65536;
+    constexpr size_t SMEM = STAGES * TILE;
+    auto kern = k_compact_chunked<THREADS, STAGES>;
+    static int sms = 0;
+    if (sms == 0) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
+        if (e != cudaSuccess) return e;
+        int dev = 0, v = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        sms = v > 0 ? v : 1;
+    }
+    const uint32_t tiles = (uint32_t)((n + TILE - 1) / TILE);
+    const uint32_t grid = tiles < (uint32_t)sms ? tiles : (uint32_t)sms;
+    LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};
+    kern<<<grid, THREADS, SMEM, s>>>(keys, flags, out, d_count, n, tiles, ctx);
+    return cudaGetLastError();
+}
 void set_compact_kernel(int k) { g_compact_kernel = k; }
 
 cudaError_t launch_compact_pipe(KeepRule rule, const uint32_t* keys, const uint8_t* flags, uint32_t* out,
@@ -550,6 +838,8 @@ cudaError_t launch_compact_pipe(KeepRule rule, const uint32_t* keys, const uint8
     }
     if (g_compact_kernel == 0)
         return launch_compact_persistent<512, 8, 2, false>(keys, flags, out, d_count, n, ws, s);
+    if (g_compact_kernel == 2 && n > (size_t)65536)
+        return launch_compact_chunked(keys, flags, out, d_count, n, ws, s);
     return launch_compact_persistent<512, 8, 3, true>(keys, flags, out, d_count, n, ws, s);
 }
 

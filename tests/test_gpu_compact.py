@@ -13,12 +13,12 @@ from gpu_helpers import SENTINEL, Guarded, assert_equal, compaction_input
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module", params=[1, 0], ids=["selective-keys", "bulk-keys"])
+@pytest.fixture(scope="module", params=[2, 1, 0], ids=["chunked", "selective-keys", "bulk-keys"])
 def ss(request):
     import stream_compaction_pass_gb300 as m
     m.ss_set_compact_config(request.param)
     yield m
-    m.ss_set_compact_config(1)
+    m.ss_set_compact_config(2)  # the library's default
 
 
 def run_compact(ss, keys: np.ndarray, flags: np.ndarray, key_offset: int = 0, flag_offset: int = 0):
@@ -52,7 +52,7 @@ def test_compaction_full_size(ss, p):
 
 
 @pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 31, 33, 511, 512, 513, 4095, 4096, 4097, 8191, 8193,
-                               100_003, 1 << 20])
+                               65535, 65536, 65537, 65536 * 3 + 1000, 100_003, 1 << 20, 152 * 65536 + 17])
 @pytest.mark.parametrize("p", [0.0, 0.3, 1.0])
 def test_compaction_edges(ss, n, p):
     keys = si.uniform_u32(n, seed=31)
