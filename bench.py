@@ -519,6 +519,28 @@ def profile_ablations(n: int) -> None:
     print(f"ablations ok at n={n}")
 
 
+def profile_compaction(n: int, p: float) -> None:
+    """Two launches of the default (flag) compaction at n keys, keep
+    probability p (the compaction workload's generators), for a profiler to
+    capture; checks the result against the oracle."""
+    import torch
+    import seeded_inputs as si
+    import stream_compaction_pass_gb300 as ss
+    import oracle as orc
+    keys, flags = si.workload_compaction(n, p, seed=3)
+    ref = orc.compact_u32(keys, flags)
+    dk = torch.from_numpy(keys.view(np.int32)).cuda()
+    df = torch.from_numpy(flags).cuda()
+    do = torch.empty_like(dk)
+    cnt = torch.zeros(1, dtype=torch.int64, device="cuda")
+    for _ in range(2):
+        ss.compact_u32(dk, df, do, cnt)
+    torch.cuda.synchronize()
+    c = int(cnt.item())
+    assert c == ref.size and np.array_equal(do[:c].cpu().numpy().view(np.uint32), ref), "compaction mismatch"
+    print(f"compaction ok at n={n}, p={p}, kept {c}")
+
+
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -534,7 +556,13 @@ def main() -> None:
     ap.add_argument("--skip-check", action="store_true")
     ap.add_argument("--profile-ablations", type=int, default=0, metavar="N",
                     help="only run each ablation twice at n=N (for a profiler) and exit")
+    ap.add_argument("--profile-compaction", type=int, default=0, metavar="N",
+                    help="only run the default compaction twice at n=N (for a profiler) and exit")
+    ap.add_argument("--keep-p", type=float, default=0.5, help="keep probability for --profile-compaction")
     args = ap.parse_args()
+    if args.profile_compaction:
+        profile_compaction(args.profile_compaction, args.keep_p)
+        return
     if args.profile_ablations:
         profile_ablations(args.profile_ablations)
         return
