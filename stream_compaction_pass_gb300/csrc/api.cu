@@ -455,7 +455,7 @@ ss_status ss_scan_rows(ss_dtype dtype, int inclusive, const void* in, void* out,
     }
     Workspace* w = nullptr;
     if (cols > ss::kRowsWarpMax) {
-        const size_t tiles = rows * ((cols + ss::kRowsTile - 1) / ss::kRowsTile);
+        const size_t tiles = rows * ((cols + ss::kRowsTile - 1) / ss::kRowsTile);  // the most either kernel uses
         if (tiles >= ((size_t)1 << 31)) return fail(SS_ERR_INVALID_ARG, "too many tiles");
         st = get_workspace(s, &w);
         if (st != SS_OK) return st;

@@ -113,6 +113,8 @@ cudaError_t launch_scan_wide(WideType type, bool inclusive, const void* in, void
 // shorter rows take one warp each and need no workspace.
 constexpr size_t kRowsTile = 4096;
 constexpr size_t kRowsWarpMax = 2048;
+constexpr size_t kRowsPipeTile = 16384;  // persistent kernel for rows of at least kRowsPipeMin
+constexpr size_t kRowsPipeMin = 16384;
 cudaError_t launch_scan_rows(Dtype dt, bool inclusive, const void* in, void* out, size_t rows, size_t cols,
                              const LookbackWs& ws, cudaStream_t s);
 

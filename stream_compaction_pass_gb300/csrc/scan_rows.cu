@@ -3,8 +3,11 @@
 // in top-p sampling, "Prefix sum and other parallel patterns", In LLMs: MoE
 // token dispatch, last paragraph).
 //
-// Two kernels, by row length:
-//   - Rows longer than kRowsWarpMax elements are cut into 4096-element tiles
+// Three kernels, by row length:
+//   - Rows of at least kRowsPipeMin elements (row starts 16-byte aligned)
+//     run on a persistent grid with a bulk-copy ring, as the flat scan does
+//     (k_scan_rows_pipe below).
+//   - Other rows longer than kRowsWarpMax elements are cut into 4096-element tiles
 //     that never cross a row boundary.  Tiles are claimed in order from the
 //     workspace counter, and each runs the single-pass look-back of the flat
 //     scan ("A device-level scan: scan then propagate").  The row's first
@@ -18,6 +21,7 @@
 //     and no look-back.
 // Rows whose start is not 16-byte aligned (cols not a multiple of 4, or an
 // unaligned base) are read and written element by element with bounds checks.
+#include "bulk.cuh"
 #include "internal.h"
 #include "scan_body.cuh"
 #include "tile.cuh"
@@ -32,6 +36,29 @@ constexpr int kRVpt = 4;
 constexpr size_t kRSeg = (size_t)32 * kRVpt * 4;   // 512 elements per warp
 static_assert(kRSeg * kRWarps == kRowsTile, "tile geometry");
 constexpr int kRSteps = 4;                          // chunks per warp step in the short-row kernel
+constexpr int kRPThreads = 512;                     // persistent long-row kernel
+
+// store_rows for a segment that may run past n, when out + seg is 16-byte
+// aligned: whole vectors inside n are stored as 16-byte vectors, only the
+// one vector that straddles n element by element.  (Element-wise stores
+// from a whole warp leave every 32-byte sector partly written per
+// instruction, which measured several times slower than vector stores.)
+template <typename T, int VPT>
+__device__ __forceinline__ void store_rows_aligned_tail(T* out, size_t n, size_t seg, int lane,
+                                                        const T (&y)[VPT][4]) {
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const size_t i0 = seg + (size_t)(32 * j + lane) * 4;
+        if (i0 + 4 <= n) {
+            st_vec(reinterpret_cast<uint4*>(out + i0), make_uint4(to_bits<T>(y[j][0]), to_bits<T>(y[j][1]),
+                                                                  to_bits<T>(y[j][2]), to_bits<T>(y[j][3])));
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (i0 + k < n) out[i0 + k] = y[j][k];
+        }
+    }
+}
 
 }  // namespace
 
@@ -106,7 +133,10 @@ k_scan_rows_tiles(const T* in, T* out, size_t cols, uint32_t tiles_per_row, uint
     if (sm.fail[0]) return;
     T y[kRVpt][4];
     rows_output<T, kRVpt, INCLUSIVE>(v, pre, sm.prefix[0] + warp_prefix, y);
-    store_rows<T, kRVpt>(rout, cols, seg, lane, full && (reinterpret_cast<uintptr_t>(rout) & 15u) == 0, y);
+    if ((reinterpret_cast<uintptr_t>(rout) & 15u) == 0)
+        store_rows_aligned_tail<T, kRVpt>(rout, cols, seg, lane, y);
+    else
+        store_rows<T, kRVpt>(rout, cols, seg, lane, false, y);
 }
 
 template <typename T, bool INCLUSIVE>
@@ -166,6 +196,221 @@ k_scan_rows_warp(const T* in, T* out, size_t rows, size_t cols, bool vec) {
     }
 }
 
+// Persistent form for long rows (at least one 16384-element tile, row
+// starts 16-byte aligned).  It uses the single-register-buffer schedule of
+// the flat scan (scan_pipe.cu): a rank per CTA, tiles rank + k*G, a
+// three-stage bulk-copy ring, and the aggregate one iteration early.
+// Tiles are numbered row by row, and none crosses a row boundary:
+//  - a row's last tile is shorter, and is fetched by a shorter bulk copy
+//    (its byte count is a multiple of 16 because the row length is a
+//    multiple of 4);
+//  - lanes past the row's end read zeros and store nothing;
+//  - a row's first tile publishes its inclusive prefix at once;
+//  - every other tile looks back no further than the row's first tile, or
+//    than this CTA's previous tile when that lies in the same row (its
+//    inclusive prefix is then in hand).
+template <typename T, bool INCLUSIVE>
+__global__ void __launch_bounds__(kRPThreads, 1)
+k_scan_rows_pipe(const T* in, T* out, size_t cols, uint32_t tiles_per_row, uint32_t num_tiles, LookbackCtx ctx) {
+    constexpr int STAGES = 3;
+    constexpr int VPT = 8;
+    constexpr int WARPS = kRPThreads / 32;
+    constexpr uint32_t TILE = (uint32_t)kRPThreads * VPT * 4;
+    static_assert(TILE == kRowsPipeTile, "tile geometry");
+    constexpr uint32_t SEG = 32u * VPT * 4;
+
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    T* ring = reinterpret_cast<T*>(smem_raw);
+    __shared__ __align__(8) uint64_t bars[STAGES];
+    __shared__ ScanSmem<T, WARPS> sm;
+    __shared__ uint32_t s_rank, s_epoch;
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const uint32_t G = gridDim.x;
+    const uint64_t policy = policy_evict_first();
+
+    if (threadIdx.x == 0) {
+        uint32_t rank, epoch;
+        claim_tile(ctx.counter, G, &rank, &epoch);
+        s_rank = rank;
+        s_epoch = epoch;
+        for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
+        fence_async_shared();
+    }
+    __syncthreads();
+    const uint32_t rank = s_rank;
+    const uint32_t epoch = s_epoch;
+    if (rank >= G) {
+        if (threadIdx.x == 0) record_error(ctx.status, kErrCounter, rank);
+        return;
+    }
+    const uint32_t count = rank < num_tiles ? (num_tiles - rank + G - 1) / G : 0;
+    uint32_t issued = 0, consumed = 0;  // thread 0
+
+    // Tile geometry: element offset of tile t in the matrix, and its length.
+    auto tile_base = [&](uint32_t t) {
+        return (size_t)(t / tiles_per_row) * cols + (size_t)(t % tiles_per_row) * TILE;
+    };
+    auto tile_len = [&](uint32_t t) {
+        const size_t start = (size_t)(t % tiles_per_row) * TILE;
+        return (uint32_t)(cols - start < TILE ? cols - start : TILE);
+    };
+    auto issue = [&](uint32_t k) {
+        const int s = (int)(k % STAGES);
+        const uint32_t t = rank + k * G;
+        const uint32_t bytes = tile_len(t) * (uint32_t)sizeof(T);  // a multiple of 16
+        fence_async_shared();
+        mbar_arrive_expect_tx(&bars[s], bytes);
+        bulk_load(ring + (size_t)s * TILE, in + tile_base(t), bytes, &bars[s], policy);
+        issued = k + 1;
+    };
+    auto read_rows = [&](uint32_t k, T (&v)[VPT][4]) {
+        const uint32_t len = tile_len(rank + k * G);
+        const T* src = ring + (size_t)(k % STAGES) * TILE + (size_t)warp * SEG + (size_t)lane * 4;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const uint32_t e0 = warp * SEG + (32u * j + lane) * 4;  // element index in the tile
+            if (e0 < len) {  // len is a multiple of 4: a vector is all in or all out
+                const uint4 r = lds_vec(src + 128 * j);
+                v[j][0] = from_bits<T>(r.x);
+                v[j][1] = from_bits<T>(r.y);
+                v[j][2] = from_bits<T>(r.z);
+                v[j][3] = from_bits<T>(r.w);
+            } else {
+                v[j][0] = v[j][1] = v[j][2] = v[j][3] = T(0);
+            }
+        }
+    };
+    auto reduce_publish = [&](uint32_t k, T* wp, T* agg) -> bool {
+        const uint32_t t = rank + k * G;
+        const bool ok = mbar_wait_bounded(&bars[k % STAGES], (k / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
+        if (__syncthreads_or(!ok)) {
+            if (threadIdx.x == 0) record_error(ctx.status, kErrBulkTimeout, t);
+            return false;
+        }
+        T v[VPT][4];
+        read_rows(k, v);
+        T x = T(0);
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) x += ((v[j][0] + v[j][1]) + v[j][2]) + v[j][3];
+        block_combine<T, WARPS>(warp_sum(x), warp, lane, sm.warp, wp, agg);
+        if (threadIdx.x == 0 && (int64_t)t != ctx.fault_tile) {
+            const bool first = t % tiles_per_row == 0;
+            if (first) {
+                if (tiles_per_row > 1) st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStateP, to_bits<T>(*agg)));
+            } else {
+                st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStateA, to_bits<T>(*agg)));
+            }
+        }
+        compiler_fence();  // the aggregate just published stays ahead of the look-back
+        return true;
+    };
+
+    T wp_cur = T(0), agg_cur = T(0), prev_incl = T(0);
+    bool failed = false;
+    uint32_t fail_at = 0;
+    if (threadIdx.x == 0)
+        for (uint32_t k = 0; k < count && k < (uint32_t)STAGES; ++k) issue(k);
+    if (count > 0 && !reduce_publish(0, &wp_cur, &agg_cur)) failed = true;
+
+    for (uint32_t k = 0; !failed && k < count; ++k) {
+        const uint32_t t = rank + k * G;
+        T wp_next = T(0), agg_next = T(0);
+        if (k + 1 < count && !reduce_publish(k + 1, &wp_next, &agg_next)) {
+            failed = true;
+            fail_at = k;
+            break;
+        }
+        if (warp == 0) {
+            T excl = T(0);
+            bool lb_failed = false;
+            const bool dead = (int64_t)t == ctx.fault_tile;  // test hook only
+            const uint32_t j = t % tiles_per_row;
+            if (j == 0) {
+                lb_failed = dead;
+            } else if (dead) {
+                lb_failed = true;
+            } else {
+                // The row's first tile, or this CTA's previous tile if it is in the same row.
+                const uint32_t row_first = t - j;
+                const bool prev_same_row = k > 0 && t - G >= row_first;
+                const int64_t floor = prev_same_row ? (int64_t)t - (int64_t)G : (int64_t)row_first - 1;
+                excl = lookback<T, 1>(ctx, t, epoch, lane, &lb_failed, nullptr, floor,
+                                      prev_same_row ? prev_incl : T(0));
+                if (lane == 0) {
+                    if (!lb_failed) {
+                        st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStateP, to_bits<T>(excl + agg_cur)));
+                    } else {
+                        st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStatePoison, 0u));
+                        record_error(ctx.status, kErrLookbackTimeout, t);
+                    }
+                }
+            }
+            prev_incl = excl + agg_cur;
+            if (lane == 0) {
+                sm.prefix[k & 1] = excl;
+                sm.fail[k & 1] = lb_failed ? 1u : 0u;
+            }
+        }
+        T v[VPT][4];
+        read_rows(k, v);
+        T pre[VPT];
+        warp_rows_scan<T, VPT>(v, lane, pre);
+        __syncthreads();  // tile k read by everyone; the prefix is in shared memory
+        if (threadIdx.x == 0) {
+            consumed = k + 1;
+            if (k + STAGES < count) issue(k + STAGES);
+        }
+        if (sm.fail[k & 1]) {
+            failed = true;
+            fail_at = k;
+            break;
+        }
+        rows_output_inplace<T, VPT, INCLUSIVE>(v, pre, sm.prefix[k & 1] + wp_cur);
+        const uint32_t len = tile_len(t);
+        uint4* dst = reinterpret_cast<uint4*>(out + tile_base(t) + (size_t)warp * SEG) + lane;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j)  // 16-byte stores; a short tile's vectors are all in or all out
+            if (warp * SEG + (32u * j + lane) * 4 < len)
+                st_vec(dst + 32 * j, make_uint4(to_bits<T>(v[j][0]), to_bits<T>(v[j][1]), to_bits<T>(v[j][2]),
+                                                to_bits<T>(v[j][3])));
+        wp_cur = wp_next;
+        agg_cur = agg_next;
+    }
+
+    if (failed && threadIdx.x == 0) {
+        for (uint32_t j = fail_at + 1; j < count; ++j) {
+            const uint32_t tt = rank + j * G;
+            if ((int64_t)tt != ctx.fault_tile) st_relaxed_u64(ctx.desc + tt, pack_desc(epoch, kStatePoison, 0u));
+        }
+        for (uint32_t j = consumed; j < issued; ++j)
+            mbar_wait_bounded(&bars[j % STAGES], (j / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
+    }
+}
+
+template <typename T, bool INCL>
+static cudaError_t launch_rows_pipe(const T* in, T* out, size_t rows, size_t cols, const LookbackWs& ws,
+                                   cudaStream_t s) {
+    constexpr size_t SMEM = 3 * (size_t)kRowsPipeTile * sizeof(T);
+    auto kern = k_scan_rows_pipe<T, INCL>;
+    static int sms = 0;
+    if (sms == 0) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
+        if (e != cudaSuccess) return e;
+        int dev = 0, v = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        sms = v > 0 ? v : 1;
+    }
+    const uint32_t tpr = (uint32_t)((cols + kRowsPipeTile - 1) / kRowsPipeTile);
+    const uint32_t tiles = (uint32_t)(rows * tpr);
+    const uint32_t grid = tiles < (uint32_t)sms ? tiles : (uint32_t)sms;
+    LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};
+    kern<<<grid, kRPThreads, SMEM, s>>>(in, out, cols, tpr, tiles, ctx);
+    return cudaGetLastError();
+}
+
 template <typename T, bool INCL>
 static cudaError_t launch_rows(const void* in, void* out, size_t rows, size_t cols, const LookbackWs& ws,
                                cudaStream_t s) {
@@ -186,6 +431,9 @@ static cudaError_t launch_rows(const void* in, void* out, size_t rows, size_t co
         k_scan_rows_warp<T, INCL><<<grid, kRThreads, 0, s>>>(pin, pout, rows, cols, vec);
         return cudaGetLastError();
     }
+    if (cols >= kRowsPipeMin && cols % 4 == 0 &&
+        ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) & 15u) == 0)
+        return launch_rows_pipe<T, INCL>(pin, pout, rows, cols, ws, s);
     const uint32_t tpr = (uint32_t)((cols + kRowsTile - 1) / kRowsTile);
     const uint32_t tiles = (uint32_t)(rows * tpr);
     LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};

@@ -56,7 +56,9 @@ def check(ss, kind, inclusive, x, **kw):
 
 
 SHAPES = [(1, 1), (1, 5), (3, 7), (1000, 1), (17, 128), (5, 2047), (5, 2048), (5, 2049), (3, 4096),
-          (3, 4097), (100, 4095), (64, 32000), (4, 128256), (2, 1_000_003), (1000, 100), (4096, 256)]
+          (3, 4097), (100, 4095), (64, 32000), (4, 128256), (2, 1_000_003), (1000, 100), (4096, 256),
+          # persistent long-row kernel: one tile per row, a short last tile, many rows per CTA
+          (3, 16384), (5, 16388), (7, 32772), (1, 1 << 20), (300, 20000), (153, 16384 * 3)]
 
 
 @pytest.mark.parametrize("kind", ["i32", "u32", "f32"])
@@ -73,13 +75,13 @@ def test_bench_shapes(ss, shape):
     check(ss, "i32", False, rows_input("i32", *shape))
 
 
-@pytest.mark.parametrize("shape", [(9, 5000), (33, 300), (7, 2051)])
+@pytest.mark.parametrize("shape", [(9, 5000), (33, 300), (7, 2051), (5, 40000)])
 @pytest.mark.parametrize("offset", [1, 3])
 def test_unaligned(ss, shape, offset):
     check(ss, "i32", True, rows_input("i32", *shape), offset=offset)
 
 
-@pytest.mark.parametrize("shape", [(6, 9000), (300, 64)])
+@pytest.mark.parametrize("shape", [(6, 9000), (300, 64), (9, 50000)])
 def test_in_place(ss, shape):
     check(ss, "i32", False, rows_input("i32", *shape), inplace=True)
 
@@ -117,3 +119,22 @@ def test_row_tile_timeout_is_reported_and_recovered(ss):
     ss.ss_scan_rows(ss.SS_I32, True, d, o, rows, cols)
     assert ss.ss_stream_status() == (ss.SS_OK, -1)
     assert_equal(o.cpu().numpy(), oracle.scan_rows(x, True).reshape(-1), tile=cols)
+
+
+def test_long_row_pipe_timeout_is_reported_and_recovered(ss):
+    # 3 tiles of 16384 per row: tile 4 is row 1's second tile, and tile 5 waits on it
+    import torch
+    rows, cols = 3, 40000
+    x = rows_input("i32", rows, cols)
+    d = torch.from_numpy(x.reshape(-1)).cuda()
+    o = torch.empty_like(d)
+    ss.ss_debug_set_lookback_fault(4, 2_000_000)
+    try:
+        ss.ss_scan_rows(ss.SS_I32, False, d, o, rows, cols)
+        st, tile = ss.ss_stream_status()
+    finally:
+        ss.ss_debug_set_lookback_fault(-1, 0)
+    assert st == ss.SS_ERR_LOOKBACK_TIMEOUT and tile == 5
+    ss.ss_scan_rows(ss.SS_I32, False, d, o, rows, cols)
+    assert ss.ss_stream_status() == (ss.SS_OK, -1)
+    assert_equal(o.cpu().numpy(), oracle.scan_rows(x, False).reshape(-1), tile=cols)
