@@ -15,12 +15,16 @@
 //   - tile k is read again from the ring, scanned in registers and stored.
 // The descriptors are 16 bytes (lookback_wide.cuh).
 //
-// A tile is 8192 elements: 512 threads, each holding 8 rows of 2 elements.
-// Warp w owns a contiguous segment; row j of it is 64 consecutive elements
-// and lane l holds elements 2l and 2l+1, so the scan order inside a warp is
-// (row, lane, element), every output store of a warp is 512 contiguous bytes
-// (one 16-byte pair per lane), and every shared-memory read of a row is
-// conflict-free (8 or 16 bytes per lane, consecutive).
+// A tile is 64 KB of input: 16384 elements of a 32-bit input, 8192 of a
+// 64-bit one.  Each of the 512 threads takes rows of 2 elements (16 rows or
+// 8).  Warp w owns a contiguous segment; row j of it is 64 consecutive
+// elements and lane l holds elements 2l and 2l+1.  So the scan order inside a
+// warp is (row, lane, element), every output store of a warp is 512
+// contiguous bytes (one 16-byte pair per lane), and every shared-memory read
+// of a row is conflict-free (8 or 16 bytes per lane, consecutive).  The scan
+// pass streams a 32-bit input's rows out of the ring four at a time, so its
+// tile is never held whole in registers (a 64-bit input's eight rows are);
+// the first group is scanned while warp 0 looks back.
 //
 // Inputs that are not 16-byte aligned, and the ragged last tile, are read
 // and written element by element with bounds checks.
@@ -36,8 +40,13 @@ namespace {
 
 constexpr int kWThreads = 512;
 constexpr int kWWarps = kWThreads / 32;
-constexpr uint32_t kWTile = 8192;
-static_assert(kWTile == kWideTile, "tile size shared with the host side");
+// 64 KB of input per tile: 16384 elements of a 32-bit input, 8192 of a
+// 64-bit one.  The host sizes the descriptors for the smaller tile.
+template <typename TI>
+constexpr uint32_t wide_tile() {
+    return 65536u / (uint32_t)sizeof(TI);
+}
+static_assert(wide_tile<double>() == kWideTile, "tile size shared with the host side");
 
 template <typename TI, typename TA> __device__ __forceinline__ TA widen(TI x);
 template <> __device__ __forceinline__ unsigned long long widen<uint32_t, unsigned long long>(uint32_t x) {
@@ -83,11 +92,14 @@ template <typename TI, typename TA, bool INCLUSIVE>
 __global__ void __launch_bounds__(kWThreads, 1)
 k_scan_wide(const TI* in, TA* out, size_t n, uint32_t num_tiles, bool fast, LookbackCtx ctx) {
     constexpr int STAGES = 3;
-    constexpr int EPV = 2;                                // elements per lane per row
-    constexpr int VPT = (int)kWTile / (kWThreads * EPV);  // rows per lane
-    constexpr uint32_t SEG = 32u * VPT * EPV;     // elements per warp segment
-    constexpr uint32_t IN_BYTES = kWTile * (uint32_t)sizeof(TI);
-    static_assert(SEG * kWWarps == kWTile, "tile geometry");
+    constexpr uint32_t TILE = wide_tile<TI>();
+    constexpr int EPV = 2;                                 // elements per lane per row
+    constexpr int VPT = (int)TILE / (kWThreads * EPV);     // rows per lane
+    constexpr int GRP = sizeof(TI) == 8 ? VPT : 4;         // rows handled together
+    static_assert(VPT % GRP == 0, "rows come in groups");
+    constexpr uint32_t SEG = 32u * VPT * EPV;              // elements per warp segment
+    constexpr uint32_t IN_BYTES = TILE * (uint32_t)sizeof(TI);
+    static_assert(SEG * kWWarps == TILE, "tile geometry");
 
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bars[STAGES];
@@ -121,39 +133,39 @@ k_scan_wide(const TI* in, TA* out, size_t n, uint32_t num_tiles, bool fast, Look
     const uint32_t count = rank < num_tiles ? (num_tiles - rank + G - 1) / G : 0;
     uint32_t issued = 0, consumed = 0;  // thread 0
 
-    auto full_tile = [&](uint32_t k) { return fast && (size_t)(rank + k * G) * kWTile + kWTile <= n; };
+    auto full_tile = [&](uint32_t k) { return fast && (size_t)(rank + k * G) * TILE + TILE <= n; };
     auto issue = [&](uint32_t k) {
         const int s = (int)(k % STAGES);
         if (full_tile(k)) {
             fence_async_shared();
             mbar_arrive_expect_tx(&bars[s], IN_BYTES);
-            bulk_load(smem_raw + (size_t)s * IN_BYTES, in + (size_t)(rank + k * G) * kWTile, IN_BYTES, &bars[s],
+            bulk_load(smem_raw + (size_t)s * IN_BYTES, in + (size_t)(rank + k * G) * TILE, IN_BYTES, &bars[s],
                       policy);
         } else {
             mbar_arrive(&bars[s]);  // read from global with bounds checks instead
         }
         issued = k + 1;
     };
-    // This lane's rows of tile k, widened.
-    auto read_rows = [&](uint32_t k, TA (&v)[VPT][EPV]) {
-        const size_t seg = (size_t)(rank + k * G) * kWTile + (size_t)warp * SEG;
+    // This lane's rows g*GRP .. g*GRP+GRP-1 of tile k, widened.
+    auto read_group = [&](uint32_t k, int g, TA (&v)[GRP][EPV]) {
+        const size_t seg = (size_t)(rank + k * G) * TILE + (size_t)warp * SEG;
         if (full_tile(k)) {
             const unsigned char* src =
                 smem_raw + (size_t)(k % STAGES) * IN_BYTES + ((size_t)warp * SEG + (size_t)lane * EPV) * sizeof(TI);
 #pragma unroll
-            for (int j = 0; j < VPT; ++j) {
+            for (int q = 0; q < GRP; ++q) {
                 TI x[EPV];
-                lds_pair<TI>(src + (size_t)j * 32 * EPV * sizeof(TI), x);
+                lds_pair<TI>(src + (size_t)(g * GRP + q) * 32 * EPV * sizeof(TI), x);
 #pragma unroll
-                for (int e = 0; e < EPV; ++e) v[j][e] = widen<TI, TA>(x[e]);
+                for (int e = 0; e < EPV; ++e) v[q][e] = widen<TI, TA>(x[e]);
             }
         } else {
 #pragma unroll
-            for (int j = 0; j < VPT; ++j)
+            for (int q = 0; q < GRP; ++q)
 #pragma unroll
                 for (int e = 0; e < EPV; ++e) {
-                    const size_t i = seg + (size_t)(32 * j + lane) * EPV + e;
-                    v[j][e] = i < n ? widen<TI, TA>(in[i]) : TA(0);
+                    const size_t i = seg + (size_t)(32 * (g * GRP + q) + lane) * EPV + e;
+                    v[q][e] = i < n ? widen<TI, TA>(in[i]) : TA(0);
                 }
         }
     };
@@ -165,13 +177,16 @@ k_scan_wide(const TI* in, TA* out, size_t n, uint32_t num_tiles, bool fast, Look
             if (threadIdx.x == 0) record_error(ctx.status, kErrBulkTimeout, t);
             return false;
         }
-        TA v[VPT][EPV];
-        read_rows(k, v);
         TA x = TA(0);
 #pragma unroll
-        for (int j = 0; j < VPT; ++j)
+        for (int g = 0; g < VPT / GRP; ++g) {
+            TA v[GRP][EPV];
+            read_group(k, g, v);
 #pragma unroll
-            for (int e = 0; e < EPV; ++e) x += v[j][e];
+            for (int q = 0; q < GRP; ++q)
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) x += v[q][e];
+        }
         x = warp_sum(x);
         if (lane == 0) s_warp[k & 1][warp] = x;
         __syncthreads();
@@ -234,57 +249,61 @@ k_scan_wide(const TI* in, TA* out, size_t n, uint32_t num_tiles, bool fast, Look
                 s_fail[k & 1] = lb_failed ? 1u : 0u;
             }
         }
-        // Scan tile k in registers: per row, the lane's vector sum, a warp
-        // scan across lanes, and the rows chained in order.
-        TA v[VPT][EPV];
-        read_rows(k, v);
-        TA row_excl[VPT], row_tot[VPT];
+        // Scan tile k group by group straight out of the ring: per row, the
+        // lane's pair sum, a warp scan across lanes, the rows chained in
+        // order.  The first group is scanned before the barrier, while warp 0
+        // looks back.
+        TA v[GRP][EPV];
+        TA row_excl[GRP], row_tot[GRP];
+        auto scan_group = [&](int g) {
+            read_group(k, g, v);
 #pragma unroll
-        for (int j = 0; j < VPT; ++j) {
-            TA s = TA(0);
-#pragma unroll
-            for (int e = 0; e < EPV; ++e) s += v[j][e];
-            const TA inc = warp_inclusive_scan<TA>(s, lane);
-            const TA before = __shfl_up_sync(kFullMask, inc, 1);
-            row_excl[j] = lane > 0 ? before : TA(0);
-            row_tot[j] = __shfl_sync(kFullMask, inc, 31);
-        }
-        __syncthreads();  // tile k read by everyone; the prefix is in shared memory
-        if (threadIdx.x == 0) {
-            consumed = k + 1;
-            if (k + STAGES < count) issue(k + STAGES);
-        }
+            for (int q = 0; q < GRP; ++q) {
+                const TA s = v[q][0] + v[q][1];
+                const TA inc = warp_inclusive_scan<TA>(s, lane);
+                const TA before = __shfl_up_sync(kFullMask, inc, 1);
+                row_excl[q] = lane > 0 ? before : TA(0);
+                row_tot[q] = __shfl_sync(kFullMask, inc, 31);
+            }
+        };
+        scan_group(0);
+        __syncthreads();  // the prefix is in shared memory
         if (s_fail[k & 1]) {
             failed = true;
             fail_at = k;
             break;
         }
         TA base = s_prefix[k & 1] + wp_cur;
-        const size_t seg = (size_t)t * kWTile + (size_t)warp * SEG;
+        const size_t seg = (size_t)t * TILE + (size_t)warp * SEG;
         const bool full = full_tile(k);
+#pragma unroll 1
+        for (int g = 0; g < VPT / GRP; ++g) {
+            if (g > 0) scan_group(g);
 #pragma unroll
-        for (int j = 0; j < VPT; ++j) {
-            TA r = base + row_excl[j];
-            TA y[EPV];
-#pragma unroll
-            for (int e = 0; e < EPV; ++e) {
+            for (int q = 0; q < GRP; ++q) {
+                TA y0, y1;
+                const TA r = base + row_excl[q];
                 if (INCLUSIVE) {
-                    r += v[j][e];
-                    y[e] = r;
+                    y0 = r + v[q][0];
+                    y1 = y0 + v[q][1];
                 } else {
-                    y[e] = r;
-                    r += v[j][e];
+                    y0 = r;
+                    y1 = r + v[q][0];
+                }
+                base += row_tot[q];
+                const size_t i0 = seg + (size_t)(32 * (g * GRP + q) + lane) * EPV;
+                if (full) {
+                    st_v2_u64(out + i0, acc_bits<TA>(y0), acc_bits<TA>(y1));
+                } else {
+                    if (i0 < n) out[i0] = y0;
+                    if (i0 + 1 < n) out[i0 + 1] = y1;
                 }
             }
-            base += row_tot[j];
-            const size_t i0 = seg + (size_t)(32 * j + lane) * EPV;
-            if (full) {
-                st_v2_u64(out + i0, acc_bits<TA>(y[0]), acc_bits<TA>(y[1]));
-            } else {
-#pragma unroll
-                for (int e = 0; e < EPV; ++e)
-                    if (i0 + e < n) out[i0 + e] = y[e];
-            }
+        }
+        __syncthreads();  // tile k read by everyone
+        if (threadIdx.x == 0) {
+            consumed = k + 1;
+            if (k + STAGES < count) issue(k + STAGES);
         }
         wp_cur = wp_next;
         agg_cur = agg_next;
@@ -303,7 +322,8 @@ k_scan_wide(const TI* in, TA* out, size_t n, uint32_t num_tiles, bool fast, Look
 
 template <typename TI, typename TA, bool INCL>
 static cudaError_t launch_wide(const void* in, void* out, size_t n, const LookbackWs& ws, cudaStream_t s) {
-    constexpr size_t SMEM = 3 * (size_t)kWTile * sizeof(TI);
+    constexpr uint32_t TILE = wide_tile<TI>();
+    constexpr size_t SMEM = 3 * (size_t)TILE * sizeof(TI);
     auto kern = k_scan_wide<TI, TA, INCL>;
     static int sms = 0;
     if (sms == 0) {
@@ -315,7 +335,7 @@ static cudaError_t launch_wide(const void* in, void* out, size_t n, const Lookba
         cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
         sms = v > 0 ? v : 1;
     }
-    const uint32_t tiles = (uint32_t)((n + kWTile - 1) / kWTile);
+    const uint32_t tiles = (uint32_t)((n + TILE - 1) / TILE);
     const uint32_t grid = tiles < (uint32_t)sms ? tiles : (uint32_t)sms;
     const bool fast = ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) & 15u) == 0;
     LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};

@@ -53,7 +53,7 @@ def test_scan_timeout_is_reported_and_recovered(ss, dead_tile):
 
 def test_compaction_timeout_is_reported_and_recovered(ss):
     import torch
-    n = 50 * TILE
+    n = 50 * 65536 + 17  # tile 7 exists for every compaction tile size (4096 to 65536)
     keys, flags = si.workload_compaction(n, 0.5, seed=3)
     d_k = torch.from_numpy(keys.view(np.int32)).to("cuda:0")
     d_f = torch.from_numpy(flags).to("cuda:0")

@@ -92,8 +92,8 @@ def check(ss, kind, inclusive, x, **kw):
 
 @pytest.mark.parametrize("kind", list(KINDS))
 @pytest.mark.parametrize("inclusive", [True, False])
-@pytest.mark.parametrize("n", [1, 2, 3, 7, 8191, 8192, 8193, 3 * 8192 + 5, 152 * 8192, 152 * 8192 + 1,
-                               1_000_003])
+@pytest.mark.parametrize("n", [1, 2, 3, 7, 8191, 8192, 8193, 16383, 16384, 16385, 3 * 8192 + 5, 152 * 8192,
+                               152 * 8192 + 1, 152 * 16384 + 3, 1_000_003])
 def test_sizes(ss, kind, inclusive, n):
     check(ss, kind, inclusive, wide_input(kind, n))
 
