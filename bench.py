@@ -47,7 +47,7 @@ WORKLOAD = ("device-wide scan, n=1e8 per launch; one step = int32 exclusive + in
 KERNEL_SOURCES = ["stream_compaction_pass_gb300/csrc/scan_pipe.cu", "stream_compaction_pass_gb300/csrc/scan.cu",
                   "stream_compaction_pass_gb300/csrc/scan_body.cuh", "stream_compaction_pass_gb300/csrc/tile.cuh",
                   "stream_compaction_pass_gb300/csrc/lookback.cuh", "stream_compaction_pass_gb300/csrc/bulk.cuh"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "k_scan_lookback_pipe_n1e8.md")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "k_scan_lookback_pipe_sb_n1e8.md")
 
 
 def dist_env():
@@ -453,7 +453,7 @@ def run_ours(args) -> None:
     mean_launch_ms = statistics.fmean(launch_ms)
     achieved = BYTES_PER_ELEM * N / (mean_launch_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": recorded_traffic(), "kernel": "k_scan_lookback_pipe",
+                "frac": achieved / peak, "traffic": recorded_traffic(), "kernel": "k_scan_lookback_pipe_sb",
                 "bytes_per_launch": BYTES_PER_ELEM * N, "mean_launch_ms": mean_launch_ms,
                 "median_launch_ms": statistics.median(launch_ms), "peak_source": peak_src,
                 "frac_of_nominal_8TBs": achieved / 8000.0}
@@ -478,7 +478,8 @@ def run_ours(args) -> None:
     e2e_s = time.perf_counter() - t0
     e2e = {"value": 4 * N * e2e_steps / e2e_s / 1e9, "unit": UNIT,
            "h2d_bytes_per_step": 4 * N * 4, "d2h_bytes_per_step": 4 * N * 4,
-           "steps": e2e_steps, "api": "ss_scan_host (chunked H2D / seeded scan / D2H pipeline)"}
+           "steps": e2e_steps, "api": "ss_scan_host on pinned host buffers: the scan kernel reads and writes them directly "
+                  "(NVLink-C2C), no staging copies"}
 
     rows = {} if args.no_rows else row_rates(torch, ss, stream, dev, xs_d, xf_d, out_i)
     cpu = None if args.no_cpu else cpu_baseline(xs, xf, budget_s=args.cpu_budget)

@@ -676,12 +676,14 @@ static cudaError_t dispatch_pipe(int config, const void* in, void* out, size_t n
         case 3: return launch_pipe<T, INCL, 512, 8, 3, 1, TRACE, true>(in, out, n, ws, ci, co, tr, s);
         case 4: return launch_pipe<T, INCL, 512, 4, 3, 1, TRACE>(in, out, n, ws, ci, co, tr, s);
         case 6: return launch_pipe<T, INCL, 512, 8, 3, 1, TRACE, false, true>(in, out, n, ws, ci, co, tr, s);
-        default:  // 2: the double register buffer spills for fp32 exclusive; that case takes the
-                  // single-buffer kernel with the same 16384-element tiles (and a third stage)
+        case 7:  // the double register buffer spills for fp32 exclusive; that case takes the
+                 // single-buffer kernel with the same 16384-element tiles (and a third stage)
             if constexpr (std::is_same<T, float>::value && !INCL)
                 return launch_pipe<T, INCL, 512, 8, 3, 1, TRACE, true>(in, out, n, ws, ci, co, tr, s);
             else
                 return launch_pipe<T, INCL, 512, 8, 2, 1, TRACE>(in, out, n, ws, ci, co, tr, s);
+        default:  // 2: single register buffer, 18432-element tiles, three 72 KB stages
+            return launch_pipe<T, INCL, 512, 9, 3, 1, TRACE, true>(in, out, n, ws, ci, co, tr, s);
     }
 }
 

@@ -163,9 +163,9 @@ def test_in_place(ss, kind):
         assert_equal(got, ref.astype(got.dtype) if kind == "f32" else ref)
 
 
-@pytest.mark.parametrize("config", range(7))
+@pytest.mark.parametrize("config", range(8))
 def test_every_tile_configuration(ss, config):
-    assert ss.ss_scan_config_count() == 7
+    assert ss.ss_scan_config_count() == 8
     default = ss.ss_scan_tile_elems()
     ss.ss_set_scan_config(config)
     try:
@@ -233,7 +233,7 @@ def test_nondefault_stream(ss):
     assert_equal(got, sweep_reference(SWEEP_MAX)[:n])
 
 
-@pytest.mark.parametrize("config", [0, 1, 2, 3, 4, 5, 6])
+@pytest.mark.parametrize("config", [0, 1, 2, 3, 4, 5, 6, 7])
 def test_trace_build_scans_and_records(ss, config):
     import torch
     n = 10_000_000 + 123
