@@ -325,7 +325,17 @@ def row_rates(torch, ss, stream, dev, xs_d, xf_d, out_d):
         off_e = torch.empty(257, dtype=torch.int32, device=dev)
         ms = time_region(torch, stream, lambda: ss.ss_moe_counts_offsets(
             ids, 256, 64, cnt_e, off_e, stream=stream.cuda_stream), 100)
-        rows[f"moe_counts_offsets_t{tokens}_k8_e256"] = {"us": ms * 1e3, "GB/s_on_ids": gbs(4 * tokens * 8, ms)}
+        # the same call captured once in a CUDA graph and replayed: the GPU's time per call
+        # without the per-call host work
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            ss.ss_moe_counts_offsets(ids, 256, 64, cnt_e, off_e, stream=stream.cuda_stream)
+        ms_g = time_region(torch, stream, graph.replay, 100)
+        rows[f"moe_counts_offsets_t{tokens}_k8_e256"] = {
+            "us": ms * 1e3, "us_graph_replay": ms_g * 1e3, "ids_MB": 4 * tokens * 8 / 1e6,
+            "GB/s_on_ids_graph": gbs(4 * tokens * 8, ms_g),
+            "note": "ids stay in L2 (129 MB) across replays; 'us' includes the per-call host work"}
+        del graph
         del ids
     # scans with 64-bit sums at n = 1e8: uint32 -> uint64 (4 + 8 B per element) and int64 / fp64 (8 + 8)
     w_in = torch.from_numpy(si.uniform_u32(N, seed=60).view(np.int32)).to(dev)

@@ -35,7 +35,9 @@
  *     descriptors, a tile counter, the status word), about 8 bytes per 4096
  *     elements, grown on demand with stream-ordered allocation and freed
  *     by ss_shutdown().  Size it before capturing a stream into a CUDA
- *     graph by making one call of the largest n on that stream first.
+ *     graph by making one call of the largest n on that stream first; a
+ *     captured graph may then be replayed any number of times up to 2^29
+ *     (the device-side launch epoch separates the replays).
  */
 #ifndef STREAMSCAN_H
 #define STREAMSCAN_H
