@@ -343,6 +343,252 @@ static cudaError_t launch_wide(const void* in, void* out, size_t n, const Lookba
     return cudaGetLastError();
 }
 
+// fp64 form.  GB300 keeps little FP64 throughput (about two DADD per clock
+// per SM), so the fp64 scan is bound by its adds, not by HBM.  This form
+// needs about 2.4 adds per element, against 6.6 for the form above:
+//  - Each lane owns 16 consecutive elements (blocked, not striped across
+//    the warp).  It scans them in sequence (15 adds) while the tile is
+//    summed, so the tile's aggregate is the last lane prefix of the block,
+//    with no separate reduction.  One warp scan covers 16 elements.
+//  - The lane's 16 prefixes stay in registers until the tile's output (the
+//    next iteration), so a tile leaves the ring as soon as it is summed, and
+//    two stages suffice.
+//  - Outputs add the tile/warp/lane offset (one add each).  They go through
+//    a per-warp 4 KB area of shared memory, which is read back by 16-byte
+//    lanes, so every global store of a warp covers 512 contiguous bytes.
+//    The lane-blocked shared-memory accesses (128 bytes per lane) conflict
+//    8 ways.  They use the load/store pipe, which idles while the adds
+//    bound the kernel.
+template <bool INCLUSIVE>
+__global__ void __launch_bounds__(kWThreads, 1)
+k_scan_f64_blocked(const double* in, double* out, size_t n, uint32_t num_tiles, bool fast, LookbackCtx ctx) {
+    constexpr int STAGES = 2;
+    constexpr uint32_t TILE = 8192;
+    constexpr int EPT = 16;                                // elements per thread
+    constexpr uint32_t SEG = 32u * EPT;                    // 512 elements per warp
+    constexpr uint32_t IN_BYTES = TILE * 8;
+    static_assert(SEG * kWWarps == TILE, "tile geometry");
+
+    extern __shared__ __align__(128) unsigned char smem_raw[];  // STAGES x 64 KB ring, then 64 KB output area
+    double* ring = reinterpret_cast<double*>(smem_raw);
+    double* stage_out = ring + (size_t)STAGES * TILE;
+    __shared__ __align__(8) uint64_t bars[STAGES];
+    __shared__ double s_wtot[2][kWWarps];   // warp totals, then their exclusive scan, by tile parity
+    __shared__ double s_agg[2];
+    __shared__ double s_prefix[2];
+    __shared__ uint32_t s_fail[2], s_rank, s_epoch;
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const uint32_t G = gridDim.x;
+    const uint64_t policy = policy_evict_first();
+
+    if (threadIdx.x == 0) {
+        uint32_t rank, epoch;
+        claim_tile(ctx.counter, G, &rank, &epoch);
+        s_rank = rank;
+        s_epoch = epoch;
+        for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
+        fence_async_shared();
+    }
+    __syncthreads();
+    const uint32_t rank = s_rank;
+    const uint32_t epoch = s_epoch;
+    if (rank >= G) {
+        if (threadIdx.x == 0) record_error(ctx.status, kErrCounter, rank);
+        return;
+    }
+    const uint32_t count = rank < num_tiles ? (num_tiles - rank + G - 1) / G : 0;
+    uint32_t issued = 0, consumed = 0;  // thread 0
+
+    auto full_tile = [&](uint32_t k) { return fast && (size_t)(rank + k * G) * TILE + TILE <= n; };
+    auto issue = [&](uint32_t k) {
+        const int s = (int)(k % STAGES);
+        if (full_tile(k)) {
+            fence_async_shared();
+            mbar_arrive_expect_tx(&bars[s], IN_BYTES);
+            bulk_load(ring + (size_t)s * TILE, in + (size_t)(rank + k * G) * TILE, IN_BYTES, &bars[s], policy);
+        } else {
+            mbar_arrive(&bars[s]);  // read from global with bounds checks instead
+        }
+        issued = k + 1;
+    };
+    // Waits for tile k, scans this lane's 16 elements into p, the lane
+    // totals across the warp into *lane_excl, and (warp 0) the warp totals;
+    // warp 0 publishes the tile's aggregate.  The tile's stage is free on
+    // return.  False if the copy did not arrive.
+    auto scan_in = [&](uint32_t k, double (&p)[EPT], double* lane_excl) -> bool {
+        const uint32_t t = rank + k * G;
+        const bool ok = mbar_wait_bounded(&bars[k % STAGES], (k / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
+        if (__syncthreads_or(!ok)) {
+            if (threadIdx.x == 0) record_error(ctx.status, kErrBulkTimeout, t);
+            return false;
+        }
+        const size_t e0 = (size_t)t * TILE + (size_t)threadIdx.x * EPT;
+        if (full_tile(k)) {
+            const double* src = ring + (size_t)(k % STAGES) * TILE + (size_t)threadIdx.x * EPT;
+#pragma unroll
+            for (int q = 0; q < EPT; q += 2) {
+                double a, b;
+                asm volatile("ld.shared.v2.f64 {%0, %1}, [%2];" : "=d"(a), "=d"(b) : "r"(smem_u32(src + q)));
+                p[q] = a;
+                p[q + 1] = b;
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < EPT; ++q) p[q] = e0 + q < n ? in[e0 + q] : 0.0;
+        }
+#pragma unroll
+        for (int q = 1; q < EPT; ++q) p[q] += p[q - 1];
+        const double inc = warp_inclusive_scan<double>(p[EPT - 1], lane);
+        const double before = __shfl_up_sync(kFullMask, inc, 1);
+        *lane_excl = lane > 0 ? before : 0.0;
+        if (lane == 31) s_wtot[k & 1][warp] = inc;
+        __syncthreads();  // warp totals are in; the stage has been read by everyone
+        if (threadIdx.x == 0 && k + STAGES < count) issue(k + STAGES);
+        if (warp == 0) {
+            const double w = lane < kWWarps ? s_wtot[k & 1][lane] : 0.0;
+            const double winc = warp_inclusive_scan<double>(w, lane);
+            const double agg = __shfl_sync(kFullMask, winc, kWWarps - 1);
+            if (lane < kWWarps) s_wtot[k & 1][lane] = winc - w;  // exclusive; read after later barriers
+            if (lane == 0) {
+                s_agg[k & 1] = agg;
+                if ((int64_t)t != ctx.fault_tile) {
+                    if (t == 0) {
+                        if (num_tiles > 1)
+                            st_relaxed_desc16(ctx.desc, pack_desc16(epoch, kStateP, acc_bits<double>(agg)));
+                    } else {
+                        st_relaxed_desc16(ctx.desc + 2 * (size_t)t, pack_desc16(epoch, kStateA, acc_bits<double>(agg)));
+                    }
+                }
+            }
+            compiler_fence();  // the aggregate is published before this warp's look-back
+        }
+        return true;
+    };
+
+    double pc[EPT], pn[EPT];
+    double lx_cur = 0.0, lx_next = 0.0, prev_incl = 0.0;
+    bool failed = false;
+    uint32_t fail_at = 0;
+    if (threadIdx.x == 0)
+        for (uint32_t k = 0; k < count && k < (uint32_t)STAGES; ++k) issue(k);
+    if (count > 0 && !scan_in(0, pc, &lx_cur)) failed = true;
+
+    // One iteration: scan tile k+1 into pn, look back for tile k, write tile k from pc.
+    auto step = [&](uint32_t k, double (&p_cur)[EPT], double lx, double (&p_next)[EPT], double* lx_nx) -> bool {
+        const uint32_t t = rank + k * G;
+        if (k + 1 < count && !scan_in(k + 1, p_next, lx_nx)) {
+            fail_at = k;
+            return false;
+        }
+        if (warp == 0) {
+            const double agg = s_agg[k & 1];
+            double excl = 0.0;
+            bool lb_failed = false;
+            const bool dead = (int64_t)t == ctx.fault_tile;  // test hook only
+            if (t == 0) {
+                lb_failed = dead;
+            } else if (dead) {
+                lb_failed = true;
+            } else {
+                const int64_t floor = k > 0 ? (int64_t)t - (int64_t)G : -1;
+                excl = lookback_wide<double>(ctx.desc, ctx, t, epoch, lane, &lb_failed, floor, prev_incl);
+                if (lane == 0) {
+                    if (!lb_failed) {
+                        st_relaxed_desc16(ctx.desc + 2 * (size_t)t,
+                                          pack_desc16(epoch, kStateP, acc_bits<double>(excl + agg)));
+                    } else {
+                        st_relaxed_desc16(ctx.desc + 2 * (size_t)t, pack_desc16(epoch, kStatePoison, 0ull));
+                        record_error(ctx.status, kErrLookbackTimeout, t);
+                    }
+                }
+            }
+            prev_incl = excl + agg;
+            if (lane == 0) {
+                s_prefix[k & 1] = excl;
+                s_fail[k & 1] = lb_failed ? 1u : 0u;
+            }
+        }
+        __syncthreads();  // the prefix and tile k's warp offsets are in shared memory
+        if (s_fail[k & 1]) {
+            fail_at = k;
+            return false;
+        }
+        const double base = (s_prefix[k & 1] + s_wtot[k & 1][warp]) + lx;
+        double y[EPT];
+#pragma unroll
+        for (int q = 0; q < EPT; ++q) {
+            if (INCLUSIVE) y[q] = base + p_cur[q];
+            else y[q] = q == 0 ? base : base + p_cur[q - 1];
+        }
+        const size_t e0 = (size_t)t * TILE + (size_t)threadIdx.x * EPT;
+        if (full_tile(k)) {
+            double* mine = stage_out + (size_t)threadIdx.x * EPT;
+#pragma unroll
+            for (int q = 0; q < EPT; q += 2)
+                asm volatile("st.shared.v2.f64 [%0], {%1, %2};" ::"r"(smem_u32(mine + q)), "d"(y[q]), "d"(y[q + 1])
+                             : "memory");
+            __syncwarp();
+            const double* wsrc = stage_out + (size_t)warp * SEG;
+            double* wdst = out + (size_t)t * TILE + (size_t)warp * SEG;
+#pragma unroll
+            for (int j = 0; j < EPT / 2; ++j) {
+                const uint32_t off = (uint32_t)(j * 32 + lane) * 2;  // 16 bytes per lane, contiguous per warp
+                double a, b;
+                asm volatile("ld.shared.v2.f64 {%0, %1}, [%2];" : "=d"(a), "=d"(b) : "r"(smem_u32(wsrc + off)));
+                st_v2_u64(wdst + off, acc_bits<double>(a), acc_bits<double>(b));
+            }
+            __syncwarp();  // the area is read before this warp's next tile writes it
+        } else {
+#pragma unroll
+            for (int q = 0; q < EPT; ++q)
+                if (e0 + q < n) out[e0 + q] = y[q];
+        }
+        return true;
+    };
+
+    for (uint32_t k = 0; !failed && k < count; k += 2) {
+        if (!step(k, pc, lx_cur, pn, &lx_next)) failed = true;
+        else if (k + 1 < count && !step(k + 1, pn, lx_next, pc, &lx_cur)) failed = true;
+    }
+
+    if (failed && threadIdx.x == 0) {
+        consumed = issued;  // every issued copy is waited for below
+        for (uint32_t j = fail_at + 1; j < count; ++j) {
+            const uint32_t tt = rank + j * G;
+            if ((int64_t)tt != ctx.fault_tile)
+                st_relaxed_desc16(ctx.desc + 2 * (size_t)tt, pack_desc16(epoch, kStatePoison, 0ull));
+        }
+        for (uint32_t j = fail_at + 1; j < issued; ++j)
+            mbar_wait_bounded(&bars[j % STAGES], (j / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
+    }
+    (void)consumed;
+}
+
+template <bool INCL>
+static cudaError_t launch_f64_blocked(const void* in, void* out, size_t n, const LookbackWs& ws, cudaStream_t s) {
+    constexpr uint32_t TILE = 8192;
+    constexpr size_t SMEM = 3 * (size_t)TILE * 8;  // two ring stages and the output area
+    auto kern = k_scan_f64_blocked<INCL>;
+    static int sms = 0;
+    if (sms == 0) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
+        if (e != cudaSuccess) return e;
+        int dev = 0, v = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        sms = v > 0 ? v : 1;
+    }
+    const uint32_t tiles = (uint32_t)((n + TILE - 1) / TILE);
+    const uint32_t grid = tiles < (uint32_t)sms ? tiles : (uint32_t)sms;
+    const bool fast = ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) & 15u) == 0;
+    LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};
+    kern<<<grid, kWThreads, SMEM, s>>>(static_cast<const double*>(in), static_cast<double*>(out), n, tiles, fast,
+                                       ctx);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_scan_wide(WideType type, bool inclusive, const void* in, void* out, size_t n,
                              const LookbackWs& ws, cudaStream_t s) {
     using u64 = unsigned long long;
@@ -357,8 +603,7 @@ cudaError_t launch_scan_wide(WideType type, bool inclusive, const void* in, void
             return inclusive ? launch_wide<u64, u64, true>(in, out, n, ws, s)
                              : launch_wide<u64, u64, false>(in, out, n, ws, s);
         default:
-            return inclusive ? launch_wide<double, double, true>(in, out, n, ws, s)
-                             : launch_wide<double, double, false>(in, out, n, ws, s);
+            return inclusive ? launch_f64_blocked<true>(in, out, n, ws, s) : launch_f64_blocked<false>(in, out, n, ws, s);
     }
 }
 

@@ -69,12 +69,13 @@ def run_wide(ss, kind: str, inclusive: bool, x: np.ndarray, offset: int = 0, inp
 
 
 def f64_bound(n: int) -> float:
-    # Every output is a sum whose add tree has depth at most 16 (a lane's
-    # elements) + 5 (warp scan) + 16 (warp totals) + 7 per tile of the
-    # look-back chain (one add to the predecessor's prefix, a 5-level warp
-    # reduction of a window, one add of the window sums), so the normalised
-    # error is at most (7 * tiles + 37) * u (first order), plus the oracle's
-    # own rounding of about u.
+    # Every output is a sum whose add tree has depth at most 16 (a lane's 16
+    # elements, in sequence) + 5 (warp scan) + 5 (scan of the 16 warp
+    # totals) + 3 (tile, warp and lane offsets) + 7 per tile of the look-back
+    # chain (one add to the predecessor's prefix, a 5-level warp reduction of
+    # a window, one add of the window sums).  So the normalised error is at
+    # most (7 * tiles + 29) * u (first order), plus the oracle's own rounding
+    # of about u; 64 leaves room.
     tiles = max(1, math.ceil(n / TILE))
     return (7 * tiles + 64) * U
 
