@@ -41,3 +41,26 @@ def test_ranges_and_moments():
 def test_structured_patterns():
     assert si.structured_period4(8).tolist() == [1, 1, 1, 2, 1, 1, 1, 2]
     assert si.structured_i_mod_8(10).tolist() == [1, 2, 3, 4, 5, 6, 7, 8, 1, 2]
+
+
+def test_positive_f32_fraction_and_range():
+    n = 1 << 20
+    for p in (0.01, 0.5, 0.99):
+        x = si.workload_positive_f32(n, p, seed=5)
+        assert x.dtype == np.float32
+        assert x.min() >= -(1 - p) - 1e-6 and x.max() < p + 1e-6
+        assert abs(float((x > 0).mean()) - p) < 0.01
+
+
+def test_topk_ids_are_distinct_uniform_and_reproducible():
+    ids = si.topk_ids(20_000, 8, 64, seed=6)
+    assert ids.shape == (20_000, 8) and ids.dtype == np.int32
+    assert ids.min() == 0 and ids.max() == 63
+    srt = np.sort(ids, axis=1)
+    assert (np.diff(srt, axis=1) > 0).all(), "an expert repeats within a row"
+    counts = np.bincount(ids.ravel(), minlength=64)
+    assert counts.min() > 0.9 * counts.mean() and counts.max() < 1.1 * counts.mean()
+    assert np.array_equal(ids, si.topk_ids(20_000, 8, 64, seed=6))
+    # top_k = E: every row is a permutation
+    full = si.topk_ids(100, 5, 5, seed=7)
+    assert (np.sort(full, axis=1) == np.arange(5)).all()
