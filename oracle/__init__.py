@@ -54,6 +54,12 @@ def _declare(lib):
         f.restype = None
     lib.oracle_abs_prefix_rows_f32.argtypes = [p, p, sz, sz]
     lib.oracle_abs_prefix_rows_f32.restype = None
+    for name in ("oracle_scan_segments_i32", "oracle_scan_segments_u32", "oracle_scan_segments_f32"):
+        f = getattr(lib, name)
+        f.argtypes = [p, p, sz, p, sz, i]
+        f.restype = None
+    lib.oracle_abs_prefix_segments_f32.argtypes = [p, p, sz, p, sz]
+    lib.oracle_abs_prefix_segments_f32.restype = None
     lib.oracle_compact_u32.argtypes = [p, p, p, sz]
     lib.oracle_compact_u32.restype = u64
     for name in ("oracle_compact_positive_f32", "oracle_compact_positive_i32", "oracle_compact_positive_u32"):
@@ -166,6 +172,35 @@ def abs_prefix_rows_f32(x: np.ndarray, lib=None) -> np.ndarray:
     rows, cols = x.shape
     y = np.empty((rows, cols), dtype=np.float64)
     (lib or load()).oracle_abs_prefix_rows_f32(_ptr(x), _ptr(y), rows, cols)
+    return y
+
+
+def _check_offsets(offsets, n):
+    offsets = np.ascontiguousarray(offsets, dtype=np.uint64)
+    assert offsets.size >= 2 and offsets[0] == 0 and offsets[-1] == n, "offsets must run from 0 to n"
+    assert (np.diff(offsets.astype(np.int64)) >= 0).all(), "offsets must not decrease"
+    return offsets
+
+
+def scan_segments(x: np.ndarray, offsets: np.ndarray, inclusive: bool, lib=None) -> np.ndarray:
+    """Every segment [offsets[s], offsets[s+1]) of a 1-D int32 / uint32 / fp32
+    array scanned on its own (fp32 in float64)."""
+    x = np.ascontiguousarray(x)
+    offsets = _check_offsets(offsets, x.size)
+    kinds = {np.dtype(np.int32): ("oracle_scan_segments_i32", np.int32),
+             np.dtype(np.uint32): ("oracle_scan_segments_u32", np.uint32),
+             np.dtype(np.float32): ("oracle_scan_segments_f32", np.float64)}
+    fn, out_dt = kinds[x.dtype]
+    y = np.empty(x.size, dtype=out_dt)
+    getattr(lib or load(), fn)(_ptr(x), _ptr(y), x.size, _ptr(offsets), offsets.size - 1, int(bool(inclusive)))
+    return y
+
+
+def abs_prefix_segments_f32(x: np.ndarray, offsets: np.ndarray, lib=None) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    offsets = _check_offsets(offsets, x.size)
+    y = np.empty(x.size, dtype=np.float64)
+    (lib or load()).oracle_abs_prefix_segments_f32(_ptr(x), _ptr(y), x.size, _ptr(offsets), offsets.size - 1)
     return y
 
 

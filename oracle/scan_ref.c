@@ -227,6 +227,43 @@ void oracle_abs_prefix_rows_f32(const float *x, double *y, size_t rows, size_t c
         oracle_abs_prefix_f32(x + r * cols, y + r * cols, cols);
 }
 
+/*
+ * Segmented scans: segment s is [offsets[s], offsets[s+1]) for s < S, with
+ * offsets[0] = 0, offsets[S] = n and offsets non-decreasing (empty segments
+ * allowed); every segment is scanned on its own, from zero.  Batched rows are
+ * the case offsets[s] = s * cols.
+ */
+void oracle_scan_segments_i32(const int32_t *x, int32_t *y, size_t n, const uint64_t *offsets, size_t S,
+                              int inclusive)
+{
+    (void)n;
+    for (size_t s = 0; s < S; ++s)
+        oracle_scan_i32(x + offsets[s], y + offsets[s], (size_t)(offsets[s + 1] - offsets[s]), inclusive);
+}
+
+void oracle_scan_segments_u32(const uint32_t *x, uint32_t *y, size_t n, const uint64_t *offsets, size_t S,
+                              int inclusive)
+{
+    (void)n;
+    for (size_t s = 0; s < S; ++s)
+        oracle_scan_u32(x + offsets[s], y + offsets[s], (size_t)(offsets[s + 1] - offsets[s]), inclusive);
+}
+
+void oracle_scan_segments_f32(const float *x, double *y, size_t n, const uint64_t *offsets, size_t S,
+                              int inclusive)
+{
+    (void)n;
+    for (size_t s = 0; s < S; ++s)
+        oracle_scan_f32(x + offsets[s], y + offsets[s], (size_t)(offsets[s + 1] - offsets[s]), inclusive);
+}
+
+void oracle_abs_prefix_segments_f32(const float *x, double *y, size_t n, const uint64_t *offsets, size_t S)
+{
+    (void)n;
+    for (size_t s = 0; s < S; ++s)
+        oracle_abs_prefix_f32(x + offsets[s], y + offsets[s], (size_t)(offsets[s + 1] - offsets[s]));
+}
+
 
 /*
  * Order-preserving compaction: copy keys[i] for every i with flags[i] != 0,

@@ -59,6 +59,9 @@ MUTANTS = [
     ("scan_ref.c", "        oracle_scan_i32(x + r * cols, y + r * cols, cols, inclusive);",
      "        oracle_scan_i32(x + r * cols, y + r * cols, cols, !inclusive);",
      "batched int32 scan flips inclusive"),
+    ("scan_ref.c", "oracle_scan_i32(x + offsets[s], y + offsets[s], (size_t)(offsets[s + 1] - offsets[s]), inclusive);",
+     "oracle_scan_i32(x + offsets[s], y + offsets[s], (size_t)(offsets[s + 1] - offsets[s]) - (s + 1 == S), inclusive);",
+     "segmented scan drops the last element"),
     ("tile_model.c", "return i + i / 32 + i / 1024;", "return i + i / 32 + i / 512;", "two-term padding uses /512"),
     ("tile_model.c", "return i + i / 32;\n", "return i + i / 16;\n", "one-term padding uses /16"),
     ("tile_model.c", "total += 2 * level;", "total += level;", "model counts one sweep"),
@@ -150,6 +153,10 @@ def _checks(lib):
     pin("rows_i32", lambda: oracle.scan_rows(xr, True, lib=lib).tolist() == [[3, 4, 11, 11], [4, 5, 11, 14]])
     pin("rows_u32", lambda: oracle.scan_rows(xr.astype(np.uint32), False, lib=lib).tolist()
         == [[0, 3, 4, 11], [0, 4, 5, 11]])
+
+    xs = np.array([3, 1, 7, 0, 4, 1, 6, 3], dtype=np.int32)
+    pin("segments_i32", lambda: oracle.scan_segments(xs, [0, 3, 3, 8], True, lib=lib).tolist()
+        == [3, 4, 11, 0, 4, 5, 11, 14])
 
     pin("model_plain", lambda: oracle.blelloch_requests(4096, oracle.LAYOUT_PLAIN, lib=lib) == 1534)
     pin("model_pad32", lambda: oracle.blelloch_requests(4096, oracle.LAYOUT_PAD32, lib=lib) == 294)

@@ -23,6 +23,9 @@ Which pin covers which oracle function:
 * scan_rows / abs_prefix_rows_f32: a worked example by hand, all-ones rows
   restart at every row, brute force with Python integers, each row equal to
   the pinned one-dimensional scan.
+* scan_segments / abs_prefix_segments_f32: a worked example by hand with an
+  empty segment, one segment = the flat scan, unit segments, equal lengths =
+  the batched rows, brute force with Python integers.
 * moe_counts_offsets: a worked example by hand, the histogram against
   numpy's bincount, tile size 1 against the (pinned) exclusive scan, the
   rounding invariants, one-expert and out-of-range cases.
@@ -524,3 +527,43 @@ def test_rows_brute_force_and_one_row_is_the_flat_scan():
     for r in range(4):
         assert np.array_equal(oracle.scan_rows(xf, True)[r], oracle.scan_f32(xf[r], True))
         assert np.array_equal(oracle.abs_prefix_rows_f32(xf)[r], oracle.abs_prefix_f32(xf[r]))
+
+
+# ---- segmented scans ----
+
+def test_segments_worked_example():
+    x = np.array([3, 1, 7, 0, 4, 1, 6, 3], dtype=np.int32)
+    # segments [0,3), [3,3) (empty), [3,8)
+    assert oracle.scan_segments(x, [0, 3, 3, 8], True).tolist() == [3, 4, 11, 0, 4, 5, 11, 14]
+    assert oracle.scan_segments(x, [0, 3, 3, 8], False).tolist() == [0, 3, 4, 0, 0, 4, 5, 11]
+
+
+def test_segments_special_cases():
+    x = si.workload_int_pm1000(1000, seed=2)
+    assert np.array_equal(oracle.scan_segments(x, [0, 1000], True), oracle.scan_i32(x, True))
+    unit = np.arange(1001, dtype=np.uint64)  # every element its own segment
+    assert np.array_equal(oracle.scan_segments(x, unit, True), x)
+    assert (oracle.scan_segments(x, unit, False) == 0).all()
+    rows = np.arange(0, 1001, 100, dtype=np.uint64)  # equal lengths: the batched rows
+    assert np.array_equal(oracle.scan_segments(x, rows, False), oracle.scan_rows(x.reshape(10, 100), False).ravel())
+
+
+@pytest.mark.parametrize("inclusive", [True, False])
+def test_segments_brute_force(inclusive):
+    n = 300
+    x = si.uniform_int32(n, -(2**31), 2**31 - 1, seed=91)
+    offsets = si.segment_offsets(n, 7.0, seed=92, empty_frac=0.2)
+    got = oracle.scan_segments(x, offsets, inclusive)
+    want = np.empty(n, dtype=np.int64)
+    for s in range(offsets.size - 1):
+        acc = 0
+        for i in range(int(offsets[s]), int(offsets[s + 1])):
+            if inclusive:
+                acc += int(x[i])
+                want[i] = acc
+            else:
+                want[i] = acc
+                acc += int(x[i])
+    assert got.tolist() == [((v + 2**31) % 2**32) - 2**31 for v in want.tolist()]
+    xf = si.uniform_f32(n, seed=93)
+    assert np.array_equal(oracle.abs_prefix_segments_f32(xf, offsets), oracle.scan_segments(xf, offsets, True))
