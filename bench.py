@@ -360,6 +360,19 @@ def row_rates(torch, ss, stream, dev, xs_d, xf_d, out_d):
         rows[f"scan_rows_f32_{r_}x{c_}"] = {"ms": ms, "GB/s": gbs(8 * r_ * c_, ms),
                                             "frac": gbs(8 * r_ * c_, ms) / peak}
         del xr, orr
+    # segmented scans, fp32 inclusive, n = 1e8: top-p-length segments and short ones
+    xs_seg = torch.from_numpy(si.uniform_f32(N, seed=96)).to(dev)
+    os_seg = torch.empty_like(xs_seg)
+    for mean in (128256.0, 100.0):
+        off_np = si.segment_offsets(N, mean, seed=98)
+        off = torch.from_numpy(off_np.astype(np.int64)).to(dev)
+        ms = time_region(torch, stream, lambda: ss.ss_scan_segments(ss.SS_F32, True, xs_seg, os_seg, off,
+                                                                    stream=stream.cuda_stream), 20)
+        rows[f"scan_segments_f32_1e8_mean{int(mean)}"] = {"ms": ms, "segments": int(off_np.size - 1),
+                                                          "GB/s_on_2n": gbs(8 * N, ms),
+                                                          "frac_on_2n": gbs(8 * N, ms) / peak}
+        del off
+    del xs_seg, os_seg
     # context only: torch.cumsum on the same int32 input, timed the same way
     def cumsum():
         with torch.cuda.stream(stream):  # torch ops run on torch's current stream

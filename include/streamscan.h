@@ -197,6 +197,28 @@ ss_status ss_scan_rows(ss_dtype dtype, int inclusive, const void *in, void *out,
                        ss_stream_t stream);
 
 /*
+ * Segmented scans: every segment [offsets[s], offsets[s+1]) of a flat array
+ * scanned on its own, from zero; the general form of ss_scan_rows, for rows
+ * of different lengths.  Same element types, wraparound and fp32 rules as the
+ * flat scans.
+ *   in, out       device, n elements each; out == in is allowed, any other
+ *                 overlap is SS_ERR_INVALID_ARG.
+ *   d_offsets     device, num_segments + 1 uint64: offsets[0] = 0,
+ *                 non-decreasing, offsets[num_segments] = n (empty segments
+ *                 are fine).  Only the starts offsets[0 .. num_segments-1]
+ *                 are read, and the scan restarts at each start below n (so
+ *                 with offsets as described the result is the definition
+ *                 above).
+ *   num_segments  0 means one segment, the whole array.
+ * Two launches on the stream: a pass that marks the segment starts in a
+ * workspace bitmask (n / 8 bytes), then the single-pass scan with a
+ * segmented add, in which a tile holding a segment start publishes its
+ * inclusive prefix at once.
+ */
+ss_status ss_scan_segments(ss_dtype dtype, int inclusive, const void *in, void *out, size_t n,
+                           const uint64_t *d_offsets, size_t num_segments, ss_stream_t stream);
+
+/*
  * MoE token counts and expert offsets aligned to GEMM tiles ("Prefix sum and
  * other parallel patterns", In LLMs: MoE token dispatch, steps 1-2, and
  * Exercise 2: a histogram of the router's expert ids, then an exclusive

@@ -213,18 +213,20 @@ def topk_ids(num_tokens: int, top_k: int, num_experts: int, seed: int = 6) -> np
 
 
 def segment_offsets(n: int, mean_len: float, seed: int = 90, empty_frac: float = 0.0) -> np.ndarray:
-    """Offsets (uint64, from 0 to n) of segments whose lengths are Poisson-like
-    around mean_len: lengths 1 + Poisson(mean_len - 1), a fraction empty_frac
-    of them set to 0.  The last segment ends at n."""
+    """Offsets (uint64, from 0 to n) of segments with lengths uniform in
+    [1, 2 * mean_len - 1] (mean mean_len; all 1 when mean_len <= 1), a
+    fraction empty_frac of them set to 0.  The last segment ends at n."""
+    hi = int(min(max(2.0 * mean_len - 1.0, 1.0), 2.0 ** 31 - 1))
     m = int(n / max(mean_len, 1.0)) + 16
-    lens = (poisson_u32(m, max(mean_len - 1.0, 0.0), seed).astype(np.int64) + 1
-            if mean_len > 1.0 else np.ones(m, dtype=np.int64))
+    lens = uniform_int32(m, 1, hi, seed).astype(np.int64)
     if empty_frac > 0.0:
         lens[bernoulli_flags(m, empty_frac, seed + 1) != 0] = 0
     ends = np.cumsum(lens)
+    while ends[-1] < n:  # rare: draw more until the lengths cover n
+        lens = np.concatenate([lens, uniform_int32(m, 1, hi, seed + len(lens)).astype(np.int64)])
+        ends = np.cumsum(lens)
     k = int(np.searchsorted(ends, n, side="left"))
-    offsets = np.concatenate([[0], np.minimum(ends[:k], n), [n]]).astype(np.uint64)
-    return offsets
+    return np.concatenate([[0], ends[:k], [n]]).astype(np.uint64)
 
 
 def workload_poisson_counts(n: int, lam: float = 8.0, seed: int = 4) -> np.ndarray:

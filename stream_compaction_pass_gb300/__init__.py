@@ -78,6 +78,7 @@ def _declare(lib):
         "scan_exclusive_f64": [P, P, SZ, P],
         "ss_scan_wide": [I, I, P, P, SZ, P],
         "ss_scan_rows": [I, I, P, P, SZ, SZ, P],
+        "ss_scan_segments": [I, I, P, P, SZ, P, SZ, P],
         "ss_set_host_mode": [I],
         "ss_scan": [I, I, I, P, P, SZ, P],
         "ss_scan_seeded": [I, I, P, P, SZ, P, P, P],
@@ -262,6 +263,16 @@ def ss_scan_wide(wide_type: int, inclusive: bool, inp, out, n=None, stream=None)
 def ss_scan_rows(dtype: int, inclusive: bool, inp, out, rows: int, cols: int, stream=None):
     _check(lib().ss_scan_rows(dtype, int(bool(inclusive)), _addr(inp), _addr(out), rows, cols,
                               _stream(stream, inp, out)), "ss_scan_rows")
+
+
+def ss_scan_segments(dtype: int, inclusive: bool, inp, out, offsets, num_segments=None, n=None, stream=None):
+    """offsets: device uint64/int64 tensor of num_segments + 1 entries."""
+    if n is None:
+        n = _numel(inp)
+    if num_segments is None:
+        num_segments = _numel(offsets) - 1
+    _check(lib().ss_scan_segments(dtype, int(bool(inclusive)), _addr(inp), _addr(out), n, _addr(offsets),
+                                  num_segments, _stream(stream, inp, out)), "ss_scan_segments")
 
 
 def ss_moe_counts_offsets(topk_ids, num_experts: int, align: int, counts, offsets, m=None, stream=None):

@@ -466,6 +466,32 @@ ss_status ss_scan_rows(ss_dtype dtype, int inclusive, const void* in, void* out,
     return e == cudaSuccess ? SS_OK : cuda_fail(e, "batched scan launch");
 }
 
+ss_status ss_scan_segments(ss_dtype dtype, int inclusive, const void* in, void* out, size_t n,
+                           const uint64_t* d_offsets, size_t num_segments, ss_stream_t stream) {
+    if (!valid_dtype(dtype)) return fail(SS_ERR_UNSUPPORTED, "unknown dtype");
+    cudaStream_t s = (cudaStream_t)stream;
+    ss_status st = check_scan_args(in, out, n, ss::kMinScanTile);
+    if (st != SS_OK) return st;
+    if (n == 0) return SS_OK;
+    if (num_segments > 0 && d_offsets == nullptr) return fail(SS_ERR_INVALID_ARG, "d_offsets is null");
+    if (reinterpret_cast<uintptr_t>(d_offsets) & 7u) return fail(SS_ERR_INVALID_ARG, "d_offsets must be 8-byte aligned");
+    if (num_segments > ((size_t)1 << 40)) return fail(SS_ERR_INVALID_ARG, "too many segments");
+    if (num_segments > 0 && overlaps(d_offsets, (num_segments + 1) * 8, out, n * 4))
+        return fail(SS_ERR_INVALID_ARG, "d_offsets overlaps out");
+    const size_t tiles = (n + ss::kSegTile - 1) / ss::kSegTile;
+    Workspace* w = nullptr;
+    st = get_workspace(s, &w);
+    if (st != SS_OK) return st;
+    st = ensure_desc(w, tiles);
+    if (st != SS_OK) return st;
+    st = ensure_totals(w, ((n + 31) / 32) * 4);
+    if (st != SS_OK) return st;
+    cudaError_t e = ss::launch_scan_segments(to_dtype(dtype), inclusive != 0, in, out, n,
+                                             reinterpret_cast<const unsigned long long*>(d_offsets), num_segments,
+                                             static_cast<uint32_t*>(w->totals), make_ws(w), s);
+    return e == cudaSuccess ? SS_OK : cuda_fail(e, "segmented scan launch");
+}
+
 ss_status ss_moe_counts_offsets(const int32_t* topk_ids, size_t m, int32_t num_experts, uint32_t align,
                                 uint32_t* d_counts, uint32_t* d_offsets, ss_stream_t stream) {
     cudaStream_t s = (cudaStream_t)stream;

@@ -118,6 +118,14 @@ constexpr size_t kRowsPipeMin = 16384;
 cudaError_t launch_scan_rows(Dtype dt, bool inclusive, const void* in, void* out, size_t rows, size_t cols,
                              const LookbackWs& ws, cudaStream_t s);
 
+// Segmented scans (scan_segments.cu): `bits` is a workspace bitmask of
+// ceil(n / 32) words that the call zeroes and fills with the segment starts
+// (offsets[0 .. num_segments-1]) before the scan.
+constexpr size_t kSegTile = 16384;
+cudaError_t launch_scan_segments(Dtype dt, bool inclusive, const void* in, void* out, size_t n,
+                                 const unsigned long long* offsets, size_t num_segments, uint32_t* bits,
+                                 const LookbackWs& ws, cudaStream_t s);
+
 // MoE token counts and tile-aligned offsets (moe.cu).  `acc` holds
 // num_experts uint32 and `ticket` one; both are zero on entry and the launch
 // leaves them zero.

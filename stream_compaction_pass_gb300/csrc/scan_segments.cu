@@ -1,0 +1,372 @@
+// scan_segments.cu -- segmented scans: every segment [offsets[s],
+// offsets[s+1]) of a flat array scanned on its own.  This is the general form
+// of the batched (per-row) scans: variable-length rows, as in a batch of
+// sequences of different lengths ("Prefix sum and other parallel patterns",
+// In LLMs: MoE token dispatch, last paragraph, the per-row cumulative sums).
+//
+// Two launches:
+//   1. k_segment_heads marks every segment start in a bitmask over the
+//      elements (one bit per element, zeroed just before on the stream).
+//   2. k_scan_segments runs the persistent single-pass scan (the schedule of
+//      scan_pipe.cu's single-register-buffer kernel) with a segmented add.
+//      The segmented add works on pairs (f, s): f says whether a segment
+//      starts in the span, s is the sum since the last start in it, or over
+//      the whole span if none.  (fa, sa) then (fb, sb) gives
+//      (fa | fb, fb ? sb : sa + sb).  It replaces the plain add in the lane,
+//      warp, row and block steps.  A tile publishes the s of its whole span:
+//      - a tile that contains a start publishes it at once as its inclusive
+//        prefix (P), because what follows its last start depends on no
+//        predecessor;
+//      - any other tile publishes it as its aggregate (A) and looks back as
+//        usual.
+//      So look-backs stop at the nearest tile holding a segment start.  The
+//      prefix found by the look-back applies only up to the tile's first
+//      start.
+// The array's first element always starts a segment.
+#include "bulk.cuh"
+#include "internal.h"
+#include "tile.cuh"
+
+namespace ss {
+
+namespace {
+
+constexpr int kSThreads = 512;
+constexpr int kSWarps = kSThreads / 32;
+constexpr int kSVpt = 8;                                        // rows of 4 elements per lane
+constexpr uint32_t kSSeg = 32u * kSVpt * 4;                     // 1024 elements per warp
+constexpr uint32_t kSTile = kSSeg * kSWarps;                    // 16384
+static_assert(kSTile == kSegTile, "tile size shared with the host side");
+
+template <typename T>
+struct SegPair {
+    uint32_t f;
+    T s;
+};
+
+// (a) then (b), in element order.
+template <typename T>
+__device__ __forceinline__ SegPair<T> seg_add(SegPair<T> a, SegPair<T> b) {
+    return SegPair<T>{a.f | b.f, b.f ? b.s : a.s + b.s};
+}
+
+// Inclusive segmented scan across the 32 lanes of a warp.
+template <typename T>
+__device__ __forceinline__ SegPair<T> warp_seg_scan(SegPair<T> p, int lane) {
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const T s_up = __shfl_up_sync(kFullMask, p.s, off);
+        const uint32_t f_up = __shfl_up_sync(kFullMask, p.f, off);
+        if (lane >= off) {
+            if (!p.f) p.s += s_up;
+            p.f |= f_up;
+        }
+    }
+    return p;
+}
+
+}  // namespace
+
+__global__ void k_segment_heads(const unsigned long long* offsets, size_t num_segments, size_t n, uint32_t* bits) {
+    for (size_t s = (size_t)blockIdx.x * blockDim.x + threadIdx.x; s < num_segments;
+         s += (size_t)gridDim.x * blockDim.x) {
+        const unsigned long long pos = offsets[s];
+        if (pos < n) atomicOr(bits + (pos >> 5), 1u << (pos & 31u));
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0 && n > 0) atomicOr(bits, 1u);  // the first element starts a segment
+}
+
+template <typename T, bool INCLUSIVE>
+__global__ void __launch_bounds__(kSThreads, 1)
+k_scan_segments(const T* in, T* out, size_t n, const uint32_t* bits, uint32_t num_tiles, bool fast,
+                LookbackCtx ctx) {
+    constexpr int STAGES = 3;
+    constexpr uint32_t TILE_BYTES = kSTile * (uint32_t)sizeof(T);
+    constexpr int VPT = kSVpt;
+
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    T* ring = reinterpret_cast<T*>(smem_raw);
+    __shared__ __align__(8) uint64_t bars[STAGES];
+    __shared__ T s_ws[2][kSWarps];         // warp summaries, by tile parity
+    __shared__ uint32_t s_wf[2][kSWarps];
+    __shared__ uint32_t s_hw[2][kSThreads];  // the tile's head-bit words (512 x 32 = 16384), by tile parity
+    __shared__ T s_prefix[2];
+    __shared__ uint32_t s_fail[2], s_rank, s_epoch;
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const uint32_t G = gridDim.x;
+    const uint64_t policy = policy_evict_first();
+
+    if (threadIdx.x == 0) {
+        uint32_t rank, epoch;
+        claim_tile(ctx.counter, G, &rank, &epoch);
+        s_rank = rank;
+        s_epoch = epoch;
+        for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
+        fence_async_shared();
+    }
+    __syncthreads();
+    const uint32_t rank = s_rank;
+    const uint32_t epoch = s_epoch;
+    if (rank >= G) {
+        if (threadIdx.x == 0) record_error(ctx.status, kErrCounter, rank);
+        return;
+    }
+    const uint32_t count = rank < num_tiles ? (num_tiles - rank + G - 1) / G : 0;
+    uint32_t issued = 0, consumed = 0;  // thread 0
+
+    auto full_tile = [&](uint32_t k) { return fast && (size_t)(rank + k * G) * kSTile + kSTile <= n; };
+    auto issue = [&](uint32_t k) {
+        const int s = (int)(k % STAGES);
+        if (full_tile(k)) {
+            fence_async_shared();
+            mbar_arrive_expect_tx(&bars[s], TILE_BYTES);
+            bulk_load(ring + (size_t)s * kSTile, in + (size_t)(rank + k * G) * kSTile, TILE_BYTES, &bars[s], policy);
+        } else {
+            mbar_arrive(&bars[s]);  // read from global with bounds checks instead
+        }
+        issued = k + 1;
+    };
+    // This lane's rows of tile k.
+    auto read_rows = [&](uint32_t k, T (&v)[VPT][4]) {
+        const size_t tile_base = (size_t)(rank + k * G) * kSTile;
+        const size_t seg = tile_base + (size_t)warp * kSSeg;
+        if (full_tile(k)) {
+            const T* src = ring + (size_t)(k % STAGES) * kSTile + (size_t)warp * kSSeg + (size_t)lane * 4;
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const uint4 r = lds_vec(src + 128 * j);
+                v[j][0] = from_bits<T>(r.x);
+                v[j][1] = from_bits<T>(r.y);
+                v[j][2] = from_bits<T>(r.z);
+                v[j][3] = from_bits<T>(r.w);
+            }
+        } else {
+            load_rows<T, VPT>(in, n, seg, lane, false, v);
+        }
+    };
+    // The lane's segmented summary of its row-j vector.
+    auto lane_pair = [&](const T (&x)[4], uint32_t h) {
+        T r = T(0);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if ((h >> e) & 1u) r = T(0);
+            r += x[e];
+        }
+        return SegPair<T>{h != 0u ? 1u : 0u, r};
+    };
+    // Waits for tile k, forms its warp summaries and its own; publishes the
+    // tile's s as P (a segment starts in it) or A.  Leaves the warp
+    // summaries in s_ws/s_wf[k & 1]; returns the tile summary and this
+    // lane's head bits (nibble j = row j).  A warp with no segment start in
+    // its span sums plainly.
+    auto reduce_publish = [&](uint32_t k, SegPair<T>* tile_pair, uint32_t* hb_out) -> bool {
+        const uint32_t t = rank + k * G;
+        const size_t wbase = ((size_t)t * kSTile) >> 5;  // one head word per thread, coalesced
+        s_hw[k & 1][threadIdx.x] = wbase + threadIdx.x < (n + 31) / 32 ? bits[wbase + threadIdx.x] : 0u;
+        const bool ok = mbar_wait_bounded(&bars[k % STAGES], (k / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
+        if (__syncthreads_or(!ok)) {
+            if (threadIdx.x == 0) record_error(ctx.status, kErrBulkTimeout, t);
+            return false;
+        }
+        uint32_t hb = 0;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const uint32_t p = warp * kSSeg + (32u * j + lane) * 4;  // element index in the tile
+            hb |= ((s_hw[k & 1][p >> 5] >> (p & 31u)) & 15u) << (4 * j);
+        }
+        *hb_out = hb;
+        T v[VPT][4];
+        read_rows(k, v);
+        SegPair<T> w{0u, T(0)};
+        if (__any_sync(kFullMask, hb != 0u)) {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const SegPair<T> row = warp_seg_scan<T>(lane_pair(v[j], (hb >> (4 * j)) & 15u), lane);
+                const SegPair<T> tot{__shfl_sync(kFullMask, row.f, 31), __shfl_sync(kFullMask, row.s, 31)};
+                w = seg_add(w, tot);
+            }
+        } else {
+            T x = T(0);
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) x += ((v[j][0] + v[j][1]) + v[j][2]) + v[j][3];
+            w.s = warp_sum(x);
+        }
+        if (lane == 0) {
+            s_ws[k & 1][warp] = w.s;
+            s_wf[k & 1][warp] = w.f;
+        }
+        __syncthreads();
+        SegPair<T> tp{0u, T(0)};
+#pragma unroll
+        for (int q = 0; q < kSWarps; ++q) tp = seg_add(tp, SegPair<T>{s_wf[k & 1][q], s_ws[k & 1][q]});
+        *tile_pair = tp;
+        if (threadIdx.x == 0 && (int64_t)t != ctx.fault_tile) {
+            if (tp.f || t == 0) {
+                if (num_tiles > 1) st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStateP, to_bits<T>(tp.s)));
+            } else {
+                st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStateA, to_bits<T>(tp.s)));
+            }
+        }
+        compiler_fence();  // the summary just published stays ahead of the look-back
+        return true;
+    };
+
+    SegPair<T> tp_cur{0u, T(0)}, tp_next{0u, T(0)};
+    uint32_t hb_cur = 0, hb_next = 0;
+    T prev_incl = T(0);
+    bool failed = false;
+    uint32_t fail_at = 0;
+    if (threadIdx.x == 0)
+        for (uint32_t k = 0; k < count && k < (uint32_t)STAGES; ++k) issue(k);
+    if (count > 0 && !reduce_publish(0, &tp_cur, &hb_cur)) failed = true;
+
+    for (uint32_t k = 0; !failed && k < count; ++k) {
+        const uint32_t t = rank + k * G;
+        if (k + 1 < count && !reduce_publish(k + 1, &tp_next, &hb_next)) {
+            failed = true;
+            fail_at = k;
+            break;
+        }
+        if (warp == 0) {
+            T excl = T(0);
+            bool lb_failed = false;
+            const bool dead = (int64_t)t == ctx.fault_tile;  // test hook only
+            if (t == 0) {
+                lb_failed = dead;
+            } else if (dead) {
+                lb_failed = true;
+            } else {
+                const int64_t floor = k > 0 ? (int64_t)t - (int64_t)G : -1;
+                excl = lookback<T, 1>(ctx, t, epoch, lane, &lb_failed, nullptr, floor, prev_incl);
+                if (lane == 0) {
+                    if (lb_failed) {
+                        st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStatePoison, 0u));
+                        record_error(ctx.status, kErrLookbackTimeout, t);
+                    } else if (!tp_cur.f) {  // a tile holding a start published its P already
+                        st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStateP, to_bits<T>(excl + tp_cur.s)));
+                    }
+                }
+            }
+            prev_incl = tp_cur.f ? tp_cur.s : excl + tp_cur.s;
+            if (lane == 0) {
+                s_prefix[k & 1] = excl;
+                s_fail[k & 1] = lb_failed ? 1u : 0u;
+            }
+        }
+        // Tile k's rows: lane summaries, segmented warp scans per row (or
+        // plain ones where this warp's span holds no segment start).
+        T v[VPT][4];
+        read_rows(k, v);
+        const uint32_t hb = hb_cur;
+        const bool seg_warp = __any_sync(kFullMask, hb != 0u);
+        SegPair<T> ex[VPT], rt[VPT];  // per row: what the lanes before hold, and the row's total
+        if (seg_warp) {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const SegPair<T> inc = warp_seg_scan<T>(lane_pair(v[j], (hb >> (4 * j)) & 15u), lane);
+                const T s_b = __shfl_up_sync(kFullMask, inc.s, 1);
+                const uint32_t f_b = __shfl_up_sync(kFullMask, inc.f, 1);
+                ex[j] = lane > 0 ? SegPair<T>{f_b, s_b} : SegPair<T>{0u, T(0)};
+                rt[j] = SegPair<T>{__shfl_sync(kFullMask, inc.f, 31), __shfl_sync(kFullMask, inc.s, 31)};
+            }
+        } else {  // no start in this warp's span: plain scans, the flags all 0
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const T inc = warp_inclusive_scan<T>(((v[j][0] + v[j][1]) + v[j][2]) + v[j][3], lane);
+                const T s_b = __shfl_up_sync(kFullMask, inc, 1);
+                ex[j] = SegPair<T>{0u, lane > 0 ? s_b : T(0)};
+                rt[j] = SegPair<T>{0u, __shfl_sync(kFullMask, inc, 31)};
+            }
+        }
+        __syncthreads();  // tile k read by everyone; the prefix is in shared memory
+        if (threadIdx.x == 0) {
+            consumed = k + 1;
+            if (k + STAGES < count) issue(k + STAGES);
+        }
+        if (s_fail[k & 1]) {
+            failed = true;
+            fail_at = k;
+            break;
+        }
+        // What comes before this warp's segment: the warps before it, in order.
+        SegPair<T> run{0u, T(0)};
+        for (int q = 0; q < warp; ++q) run = seg_add(run, SegPair<T>{s_wf[k & 1][q], s_ws[k & 1][q]});
+        const T excl = s_prefix[k & 1];
+        const size_t tile_base = (size_t)t * kSTile;
+        {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const SegPair<T> before = seg_add(run, ex[j]);
+                T r = before.f ? before.s : excl + before.s;
+                const uint32_t h = (hb >> (4 * j)) & 15u;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if ((h >> e) & 1u) r = T(0);
+                    const T x = v[j][e];
+                    if (INCLUSIVE) {
+                        r += x;
+                        v[j][e] = r;
+                    } else {
+                        v[j][e] = r;
+                        r += x;
+                    }
+                }
+                run = seg_add(run, rt[j]);
+            }
+        }
+        store_rows<T, VPT>(out, n, tile_base + (size_t)warp * kSSeg, lane, full_tile(k), v);
+        tp_cur = tp_next;
+        hb_cur = hb_next;
+    }
+
+    if (failed && threadIdx.x == 0) {
+        for (uint32_t j = fail_at + 1; j < count; ++j) {
+            const uint32_t tt = rank + j * G;
+            if ((int64_t)tt != ctx.fault_tile) st_relaxed_u64(ctx.desc + tt, pack_desc(epoch, kStatePoison, 0u));
+        }
+        for (uint32_t j = consumed; j < issued; ++j)
+            mbar_wait_bounded(&bars[j % STAGES], (j / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
+    }
+}
+
+template <typename T, bool INCL>
+static cudaError_t launch_segments(const void* in, void* out, size_t n, const uint32_t* bits,
+                                   const LookbackWs& ws, cudaStream_t s) {
+    constexpr size_t SMEM = 3 * (size_t)kSTile * sizeof(T);
+    auto kern = k_scan_segments<T, INCL>;
+    static int sms = 0;
+    if (sms == 0) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
+        if (e != cudaSuccess) return e;
+        int dev = 0, v = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        sms = v > 0 ? v : 1;
+    }
+    const uint32_t tiles = (uint32_t)((n + kSTile - 1) / kSTile);
+    const uint32_t grid = tiles < (uint32_t)sms ? tiles : (uint32_t)sms;
+    const bool fast = ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) & 15u) == 0;
+    LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};
+    kern<<<grid, kSThreads, SMEM, s>>>(static_cast<const T*>(in), static_cast<T*>(out), n, bits, tiles, fast, ctx);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scan_segments(Dtype dt, bool inclusive, const void* in, void* out, size_t n,
+                                 const unsigned long long* offsets, size_t num_segments, uint32_t* bits,
+                                 const LookbackWs& ws, cudaStream_t s) {
+    cudaError_t e = cudaMemsetAsync(bits, 0, ((n + 31) / 32) * 4, s);
+    if (e != cudaSuccess) return e;
+    const size_t blocks = (num_segments + 255) / 256;
+    const unsigned grid = (unsigned)(blocks == 0 ? 1 : (blocks < 4096 ? blocks : 4096));
+    k_segment_heads<<<grid, 256, 0, s>>>(offsets, num_segments, n, bits);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (dt == Dtype::F32)
+        return inclusive ? launch_segments<float, true>(in, out, n, bits, ws, s)
+                         : launch_segments<float, false>(in, out, n, bits, ws, s);
+    return inclusive ? launch_segments<uint32_t, true>(in, out, n, bits, ws, s)
+                     : launch_segments<uint32_t, false>(in, out, n, bits, ws, s);
+}
+
+}  // namespace ss

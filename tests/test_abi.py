@@ -94,6 +94,17 @@ def test_rows_scan_arguments(lib):
     assert lib.ss_scan_rows(7, 0, 0x10000, 0x20000, 4, 4, None) == ss.SS_ERR_UNSUPPORTED
 
 
+def test_segments_arguments(lib):
+    inv = ss.SS_ERR_INVALID_ARG
+    f = lib.ss_scan_segments
+    assert f(ss.SS_I32, 1, None, None, 0, None, 0, None) == ss.SS_OK                 # empty
+    assert f(ss.SS_I32, 1, 0x10000, 0x20000, 64, None, 3, None) == inv               # no offsets
+    assert f(ss.SS_I32, 1, 0x10000, 0x20000, 64, 0x30004, 3, None) == inv            # offsets misaligned
+    assert f(ss.SS_I32, 1, 0x10000, 0x20000, 64, 0x20010, 3, None) == inv            # offsets overlap out
+    assert f(ss.SS_I32, 1, 0x10000, 0x10004, 64, 0x30000, 3, None) == inv            # in/out partial overlap
+    assert f(9, 1, 0x10000, 0x20000, 64, 0x30000, 3, None) == ss.SS_ERR_UNSUPPORTED
+
+
 def test_moe_arguments(lib):
     inv = ss.SS_ERR_INVALID_ARG
     f = lib.ss_moe_counts_offsets
