@@ -565,6 +565,27 @@ def profile_compaction(n: int, p: float) -> None:
     print(f"compaction ok at n={n}, p={p}, kept {c}")
 
 
+def profile_f64(n: int) -> None:
+    """Two launches of the fp64 inclusive scan at n elements (seeded, values
+    24-bit fractions scaled over 2^-10 .. 2^10), for a profiler to capture;
+    checks the result against the oracle within the fp64 bound."""
+    import torch
+    import seeded_inputs as si
+    import stream_compaction_pass_gb300 as ss
+    import oracle as orc
+    x = (si.uniform_f32(n, seed=64).astype(np.float64) - 0.5) * np.exp2(
+        si.uniform_int32(n, -10, 10, seed=65).astype(np.float64))
+    d = torch.from_numpy(x).cuda()
+    o = torch.empty_like(d)
+    for _ in range(2):
+        ss.scan_inclusive_f64(d, o)
+    torch.cuda.synchronize()
+    err = float(np.max(np.abs(o.cpu().numpy() - orc.scan_f64(x, True)) / np.maximum(1.0, orc.abs_prefix_f64(x))))
+    bound = (7 * ((n + 8191) // 8192) + 64) * 2.0 ** -53
+    assert err <= bound, f"fp64 error {err} above {bound}"
+    print(f"fp64 scan ok at n={n}, normalised error {err:.2e}")
+
+
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -583,7 +604,12 @@ def main() -> None:
     ap.add_argument("--profile-compaction", type=int, default=0, metavar="N",
                     help="only run the default compaction twice at n=N (for a profiler) and exit")
     ap.add_argument("--keep-p", type=float, default=0.5, help="keep probability for --profile-compaction")
+    ap.add_argument("--profile-f64", type=int, default=0, metavar="N",
+                    help="only run the fp64 inclusive scan twice at n=N (for a profiler) and exit")
     args = ap.parse_args()
+    if args.profile_f64:
+        profile_f64(args.profile_f64)
+        return
     if args.profile_compaction:
         profile_compaction(args.profile_compaction, args.keep_p)
         return
