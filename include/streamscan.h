@@ -103,7 +103,7 @@ ss_status scan_exclusive_f32(const float *in, float *out, size_t n, ss_stream_t 
  *   f64      fp64 in and out, IEEE round-to-nearest adds in an order the
  *            caller does not control (as for fp32).
  *   in   device, n elements, aligned to the element size (16-byte aligned
- *        in and out take the bulk-copy path).
+ *        in and out take the bulk-copy path; for f64, the tensor-copy path).
  *   out  device, n 8-byte elements.  out == in is allowed for i64 and f64;
  *        any other overlap is SS_ERR_INVALID_ARG.
  *   n    0 <= n < 2^31 * 8192.

@@ -240,7 +240,8 @@ ss_status scan_wide(ss::WideType type, bool inclusive, const void* in, void* out
     if (!(in_size == 8 && in == out) && overlaps(in, n * in_size, out, n * 8))
         return fail(SS_ERR_INVALID_ARG, in_size == 8 ? "in and out partially overlap"
                                                      : "a widened scan cannot overlap its input");
-    const size_t tiles = (n + ss::kWideTile - 1) / ss::kWideTile;
+    const size_t tile = type == ss::WideType::F64 ? ss::kWideTileF64 : ss::kWideTile;
+    const size_t tiles = (n + tile - 1) / tile;
     Workspace* w = nullptr;
     ss_status st = get_workspace(s, &w);
     if (st != SS_OK) return st;

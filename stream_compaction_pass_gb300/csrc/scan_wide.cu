@@ -33,6 +33,7 @@
 #include "bulk.cuh"
 #include "internal.h"
 #include "lookback_wide.cuh"
+#include "tensor_copy.cuh"
 
 namespace ss {
 
@@ -343,9 +344,10 @@ static cudaError_t launch_wide(const void* in, void* out, size_t n, const Lookba
     return cudaGetLastError();
 }
 
-// fp64 form.  GB300 keeps little FP64 throughput (about two DADD per clock
-// per SM), so the fp64 scan is bound by its adds, not by HBM.  This form
-// needs about 2.4 adds per element, against 6.6 for the form above:
+// fp64 form.  GB300 keeps little FP64 throughput (measured: about 528 G
+// DADD/s for the chip, 1.7 per clock per SM; one warp per sub-partition
+// already reaches it), so the fp64 scan is bound by its adds, not by HBM.
+// This form needs about 2.3 adds per element, against 6.6 for the form above:
 //  - Each lane owns 16 consecutive elements (blocked, not striped across
 //    the warp).  It scans them in sequence (15 adds) while the tile is
 //    summed, so the tile's aggregate is the last lane prefix of the block,
@@ -353,29 +355,41 @@ static cudaError_t launch_wide(const void* in, void* out, size_t n, const Lookba
 //  - The lane's 16 prefixes stay in registers until the tile's output (the
 //    next iteration), so a tile leaves the ring as soon as it is summed, and
 //    two stages suffice.
-//  - Outputs add the tile/warp/lane offset (one add each).  They go through
-//    a per-warp 4 KB area of shared memory, which is read back by 16-byte
-//    lanes, so every global store of a warp covers 512 contiguous bytes.
-//    The lane-blocked shared-memory accesses (128 bytes per lane) conflict
-//    8 ways.  They use the load/store pipe, which idles while the adds
-//    bound the kernel.
-template <bool INCLUSIVE>
-__global__ void __launch_bounds__(kWThreads, 1)
-k_scan_f64_blocked(const double* in, double* out, size_t n, uint32_t num_tiles, bool fast, LookbackCtx ctx) {
+//  - Outputs add the tile/warp/lane offset (one add each; warp 0 folds the
+//    tile's prefix into the warp offsets).  They go through
+//    a per-warp 4 KB area of shared memory, which one tensor store per warp
+//    writes to global memory.
+//  - A lane's 16 elements are one 128-byte row of shared memory.  Read or
+//    written 16 bytes at a time in plain row-major order, the 8 lanes of a
+//    quarter-warp would all hit the same 4 banks.  So the ring and the
+//    output areas hold the rows with the 128-byte swizzle of the tensor
+//    copies (chunk index XOR row index mod 8): tensor loads write the ring
+//    that way and tensor stores read the output areas that way, and every
+//    lane's 16-byte access of a quarter-warp falls in its own banks.
+//  - Two 256-thread CTAs per SM (4096-element tiles): while one waits at a
+//    barrier for its look-back, the other's adds keep the FP64 pipe busy.
+template <bool INCLUSIVE, int THREADS>
+__global__ void __launch_bounds__(THREADS, THREADS <= 128 ? 4 : (THREADS <= 256 ? 2 : 1))
+k_scan_f64_blocked(const double* in, double* out, size_t n, uint32_t num_tiles, bool fast, LookbackCtx ctx,
+                   const __grid_constant__ CUtensorMap map_in, const __grid_constant__ CUtensorMap map_out) {
     constexpr int STAGES = 2;
-    constexpr uint32_t TILE = 8192;
     constexpr int EPT = 16;                                // elements per thread
+    constexpr int WARPS = THREADS / 32;
+    constexpr uint32_t TILE = (uint32_t)THREADS * EPT;
     constexpr uint32_t SEG = 32u * EPT;                    // 512 elements per warp
     constexpr uint32_t IN_BYTES = TILE * 8;
-    static_assert(SEG * kWWarps == TILE, "tile geometry");
+    constexpr uint32_t ROWS = TILE / 16;                   // 128-byte rows per tile, one per thread
+    constexpr uint32_t BOX_ROWS = ROWS < 256 ? ROWS : 256;  // rows per tensor load (at most 256)
+    static_assert(SEG * WARPS == TILE && ROWS == THREADS && ROWS % BOX_ROWS == 0, "tile geometry");
 
-    extern __shared__ __align__(128) unsigned char smem_raw[];  // STAGES x 64 KB ring, then 64 KB output area
-    double* ring = reinterpret_cast<double*>(smem_raw);
+    // STAGES x 64 KB ring, then the 64 KB output area; the swizzled copies
+    // want 1024-byte aligned areas.
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    double* ring = reinterpret_cast<double*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
     double* stage_out = ring + (size_t)STAGES * TILE;
     __shared__ __align__(8) uint64_t bars[STAGES];
-    __shared__ double s_wtot[2][kWWarps];   // warp totals, then their exclusive scan, by tile parity
+    __shared__ double s_wtot[2][WARPS];  // warp totals, their exclusive scan, then + the tile's prefix; by parity
     __shared__ double s_agg[2];
-    __shared__ double s_prefix[2];
     __shared__ uint32_t s_fail[2], s_rank, s_epoch;
 
     const int lane = threadIdx.x & 31;
@@ -407,7 +421,11 @@ k_scan_f64_blocked(const double* in, double* out, size_t n, uint32_t num_tiles, 
         if (full_tile(k)) {
             fence_async_shared();
             mbar_arrive_expect_tx(&bars[s], IN_BYTES);
-            bulk_load(ring + (size_t)s * TILE, in + (size_t)(rank + k * G) * TILE, IN_BYTES, &bars[s], policy);
+            const int32_t row0 = (int32_t)((size_t)(rank + k * G) * ROWS);
+#pragma unroll
+            for (uint32_t b = 0; b < ROWS / BOX_ROWS; ++b)
+                tensor_load_2d(ring + (size_t)s * TILE + b * BOX_ROWS * 16, &map_in, 0, row0 + (int32_t)(b * BOX_ROWS),
+                               &bars[s], policy);
         } else {
             mbar_arrive(&bars[s]);  // read from global with bounds checks instead
         }
@@ -426,11 +444,13 @@ k_scan_f64_blocked(const double* in, double* out, size_t n, uint32_t num_tiles, 
         }
         const size_t e0 = (size_t)t * TILE + (size_t)threadIdx.x * EPT;
         if (full_tile(k)) {
-            const double* src = ring + (size_t)(k % STAGES) * TILE + (size_t)threadIdx.x * EPT;
+            const uint32_t stage = smem_u32(ring + (size_t)(k % STAGES) * TILE);
 #pragma unroll
             for (int q = 0; q < EPT; q += 2) {
                 double a, b;
-                asm volatile("ld.shared.v2.f64 {%0, %1}, [%2];" : "=d"(a), "=d"(b) : "r"(smem_u32(src + q)));
+                asm volatile("ld.shared.v2.f64 {%0, %1}, [%2];"
+                             : "=d"(a), "=d"(b)
+                             : "r"(stage + swizzle128_offset(threadIdx.x, (uint32_t)q / 2)));
                 p[q] = a;
                 p[q + 1] = b;
             }
@@ -447,10 +467,10 @@ k_scan_f64_blocked(const double* in, double* out, size_t n, uint32_t num_tiles, 
         __syncthreads();  // warp totals are in; the stage has been read by everyone
         if (threadIdx.x == 0 && k + STAGES < count) issue(k + STAGES);
         if (warp == 0) {
-            const double w = lane < kWWarps ? s_wtot[k & 1][lane] : 0.0;
+            const double w = lane < WARPS ? s_wtot[k & 1][lane] : 0.0;
             const double winc = warp_inclusive_scan<double>(w, lane);
-            const double agg = __shfl_sync(kFullMask, winc, kWWarps - 1);
-            if (lane < kWWarps) s_wtot[k & 1][lane] = winc - w;  // exclusive; read after later barriers
+            const double agg = __shfl_sync(kFullMask, winc, WARPS - 1);
+            if (lane < WARPS) s_wtot[k & 1][lane] = winc - w;  // exclusive; read after later barriers
             if (lane == 0) {
                 s_agg[k & 1] = agg;
                 if ((int64_t)t != ctx.fault_tile) {
@@ -505,17 +525,15 @@ k_scan_f64_blocked(const double* in, double* out, size_t n, uint32_t num_tiles, 
                 }
             }
             prev_incl = excl + agg;
-            if (lane == 0) {
-                s_prefix[k & 1] = excl;
-                s_fail[k & 1] = lb_failed ? 1u : 0u;
-            }
+            if (lane == 0) s_fail[k & 1] = lb_failed ? 1u : 0u;
+            if (lane < WARPS) s_wtot[k & 1][lane] = excl + s_wtot[k & 1][lane];  // each warp's offset in the scan
         }
-        __syncthreads();  // the prefix and tile k's warp offsets are in shared memory
+        __syncthreads();  // tile k's warp offsets, prefix included, are in shared memory
         if (s_fail[k & 1]) {
             fail_at = k;
             return false;
         }
-        const double base = (s_prefix[k & 1] + s_wtot[k & 1][warp]) + lx;
+        const double base = s_wtot[k & 1][warp] + lx;
         double y[EPT];
 #pragma unroll
         for (int q = 0; q < EPT; ++q) {
@@ -524,22 +542,21 @@ k_scan_f64_blocked(const double* in, double* out, size_t n, uint32_t num_tiles, 
         }
         const size_t e0 = (size_t)t * TILE + (size_t)threadIdx.x * EPT;
         if (full_tile(k)) {
-            double* mine = stage_out + (size_t)threadIdx.x * EPT;
+            const double* area = stage_out + (size_t)warp * SEG;  // 32 rows, 1024-byte aligned
+            if (lane == 0) bulk_wait_group_read0();  // this warp's previous store has read the area
+            __syncwarp();
+            const uint32_t mine = smem_u32(area);
 #pragma unroll
             for (int q = 0; q < EPT; q += 2)
-                asm volatile("st.shared.v2.f64 [%0], {%1, %2};" ::"r"(smem_u32(mine + q)), "d"(y[q]), "d"(y[q + 1])
+                asm volatile("st.shared.v2.f64 [%0], {%1, %2};" ::"r"(mine + swizzle128_offset(lane, (uint32_t)q / 2)),
+                             "d"(y[q]), "d"(y[q + 1])
                              : "memory");
+            fence_async_shared();
             __syncwarp();
-            const double* wsrc = stage_out + (size_t)warp * SEG;
-            double* wdst = out + (size_t)t * TILE + (size_t)warp * SEG;
-#pragma unroll
-            for (int j = 0; j < EPT / 2; ++j) {
-                const uint32_t off = (uint32_t)(j * 32 + lane) * 2;  // 16 bytes per lane, contiguous per warp
-                double a, b;
-                asm volatile("ld.shared.v2.f64 {%0, %1}, [%2];" : "=d"(a), "=d"(b) : "r"(smem_u32(wsrc + off)));
-                st_v2_u64(wdst + off, acc_bits<double>(a), acc_bits<double>(b));
+            if (lane == 0) {
+                tensor_store_2d(&map_out, 0, (int32_t)((size_t)t * ROWS + (size_t)warp * 32), area);
+                bulk_commit_group();
             }
-            __syncwarp();  // the area is read before this warp's next tile writes it
         } else {
 #pragma unroll
             for (int q = 0; q < EPT; ++q)
@@ -563,29 +580,45 @@ k_scan_f64_blocked(const double* in, double* out, size_t n, uint32_t num_tiles, 
         for (uint32_t j = fail_at + 1; j < issued; ++j)
             mbar_wait_bounded(&bars[j % STAGES], (j / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
     }
+    if (lane == 0) bulk_wait_group0();  // this warp's output stores are complete before the CTA leaves
     (void)consumed;
 }
 
-template <bool INCL>
+constexpr int kF64Threads = 256;
+static_assert(kF64Threads * 16 == (int)kWideTileF64, "fp64 tile size shared with the host side");
+
+template <bool INCL, int THREADS>
 static cudaError_t launch_f64_blocked(const void* in, void* out, size_t n, const LookbackWs& ws, cudaStream_t s) {
-    constexpr uint32_t TILE = 8192;
-    constexpr size_t SMEM = 3 * (size_t)TILE * 8;  // two ring stages and the output area
-    auto kern = k_scan_f64_blocked<INCL>;
+    constexpr uint32_t TILE = (uint32_t)THREADS * 16;
+    constexpr size_t SMEM = 3 * (size_t)TILE * 8 + 1024;  // two ring stages, the output area, alignment slack
+    auto kern = k_scan_f64_blocked<INCL, THREADS>;
     static int sms = 0;
     if (sms == 0) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
         if (e != cudaSuccess) return e;
-        int dev = 0, v = 0;
+        int dev = 0, v = 0, per_sm = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        sms = v > 0 ? v : 1;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, THREADS, SMEM);
+        if (e != cudaSuccess) return e;
+        sms = (v > 0 ? v : 1) * (per_sm > 0 ? per_sm : 1);  // resident CTAs: the persistent grid
     }
     const uint32_t tiles = (uint32_t)((n + TILE - 1) / TILE);
     const uint32_t grid = tiles < (uint32_t)sms ? tiles : (uint32_t)sms;
-    const bool fast = ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) & 15u) == 0;
+    // Full tiles go through the tensor copies: both buffers 16-byte aligned,
+    // and every row coordinate within the copies' signed 32-bit range.
+    const uint64_t rows = n / 16;
+    const bool fast = ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) & 15u) == 0 &&
+                      n >= TILE && rows <= (uint64_t)INT32_MAX;
+    CUtensorMap map_in{}, map_out{};
+    if (fast) {
+        cudaError_t e = encode_rows128_f64(&map_in, in, rows, THREADS < 256 ? THREADS : 256);
+        if (e == cudaSuccess) e = encode_rows128_f64(&map_out, out, rows, 32);
+        if (e != cudaSuccess) return e;
+    }
     LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};
-    kern<<<grid, kWThreads, SMEM, s>>>(static_cast<const double*>(in), static_cast<double*>(out), n, tiles, fast,
-                                       ctx);
+    kern<<<grid, THREADS, SMEM, s>>>(static_cast<const double*>(in), static_cast<double*>(out), n, tiles, fast, ctx,
+                                       map_in, map_out);
     return cudaGetLastError();
 }
 
@@ -603,7 +636,8 @@ cudaError_t launch_scan_wide(WideType type, bool inclusive, const void* in, void
             return inclusive ? launch_wide<u64, u64, true>(in, out, n, ws, s)
                              : launch_wide<u64, u64, false>(in, out, n, ws, s);
         default:
-            return inclusive ? launch_f64_blocked<true>(in, out, n, ws, s) : launch_f64_blocked<false>(in, out, n, ws, s);
+            return inclusive ? launch_f64_blocked<true, kF64Threads>(in, out, n, ws, s)
+                             : launch_f64_blocked<false, kF64Threads>(in, out, n, ws, s);
     }
 }
 

@@ -108,3 +108,22 @@ def test_wide_scan_timeout_is_reported_and_recovered(ss):
     ss.scan_inclusive_i64(d, o)
     assert ss.ss_stream_status() == (ss.SS_OK, -1)
     assert_equal(o.cpu().numpy(), oracle.scan_i64(x, True))
+
+
+def test_f64_scan_timeout_is_reported_and_recovered(ss):
+    # the fp64 kernel has its own tiles (4096 elements) and look-back loop
+    import torch
+    n = 80 * 4096 + 3
+    x = si.uniform_int32(n, -1000, 1000, seed=2).astype(np.float64)
+    d = torch.from_numpy(x).to("cuda:0")
+    o = torch.empty_like(d)
+    ss.ss_debug_set_lookback_fault(9, 2_000_000)
+    try:
+        ss.scan_exclusive_f64(d, o)
+        st, tile = ss.ss_stream_status()
+    finally:
+        ss.ss_debug_set_lookback_fault(-1, 0)
+    assert st == ss.SS_ERR_LOOKBACK_TIMEOUT and tile > 9
+    ss.scan_exclusive_f64(d, o)
+    assert ss.ss_stream_status() == (ss.SS_OK, -1)
+    assert_equal(o.cpu().numpy(), oracle.scan_f64(x, False))

@@ -18,7 +18,8 @@ from gpu_helpers import SENTINEL, Guarded, assert_equal
 
 pytestmark = pytest.mark.gpu
 
-TILE = 8192
+TILE = 8192      # integer kinds
+TILE_F64 = 4096  # fp64: two 256-thread CTAs per SM, 16 elements per lane
 U = 2.0 ** -53
 
 KINDS = {
@@ -70,13 +71,13 @@ def run_wide(ss, kind: str, inclusive: bool, x: np.ndarray, offset: int = 0, inp
 
 def f64_bound(n: int) -> float:
     # Every output is a sum whose add tree has depth at most 16 (a lane's 16
-    # elements, in sequence) + 5 (warp scan) + 5 (scan of the 16 warp
-    # totals) + 3 (tile, warp and lane offsets) + 7 per tile of the look-back
-    # chain (one add to the predecessor's prefix, a 5-level warp reduction of
-    # a window, one add of the window sums).  So the normalised error is at
-    # most (7 * tiles + 29) * u (first order), plus the oracle's own rounding
-    # of about u; 64 leaves room.
-    tiles = max(1, math.ceil(n / TILE))
+    # elements, in sequence) + 5 (warp scan) + 5 (scan of the 8 warp totals)
+    # + 2 (the tile's prefix into the warp offset, then the lane offset) + 7
+    # per tile of the look-back chain (one add to the predecessor's prefix, a
+    # 5-level warp reduction of a window, one add of the window sums).  So
+    # the normalised error is at most (7 * tiles + 28) * u (first order),
+    # plus the oracle's own rounding of about u; 64 leaves room.
+    tiles = max(1, math.ceil(n / TILE_F64))
     return (7 * tiles + 64) * U
 
 
@@ -93,7 +94,8 @@ def check(ss, kind, inclusive, x, **kw):
 
 @pytest.mark.parametrize("kind", list(KINDS))
 @pytest.mark.parametrize("inclusive", [True, False])
-@pytest.mark.parametrize("n", [1, 2, 3, 7, 8191, 8192, 8193, 16383, 16384, 16385, 3 * 8192 + 5, 152 * 8192,
+@pytest.mark.parametrize("n", [1, 2, 3, 7, 4095, 4096, 4097, 8191, 8192, 8193, 16383, 16384, 16385, 3 * 8192 + 5,
+                               152 * 8192,
                                152 * 8192 + 1, 152 * 16384 + 3, 1_000_003])
 def test_sizes(ss, kind, inclusive, n):
     check(ss, kind, inclusive, wide_input(kind, n))
