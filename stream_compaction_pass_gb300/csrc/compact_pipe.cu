@@ -1,9 +1,9 @@
 // compact_pipe.cu -- the fused order-preserving compaction as a persistent
 // kernel fed by the bulk-copy engine.
 //
-// Same result as compact.cu (keep keys[i] where flags[i] != 0, or where a
-// built-in predicate of keys[i] holds, in order; "Prefix sum and other
-// parallel patterns", Stream compaction and Exercise 1), on the schedule of
+// Same result as compact.cu (keep keys[i] where flags[i] != 0, in order;
+// "Prefix sum and other parallel patterns", Stream compaction and Exercise
+// 1; the built-in predicates run in compact_pred.cu), on the schedule of
 // the persistent scan (scan_pipe.cu): each CTA takes a rank from the
 // workspace counter and handles tiles rank, rank + G, ...; a shared-memory
 // ring receives each tile's keys and flags with two bulk copies (the keys
@@ -824,18 +824,8 @@ void set_compact_kernel(int k) { g_compact_kernel = k; }
 
 cudaError_t launch_compact_pipe(KeepRule rule, const uint32_t* keys, const uint8_t* flags, uint32_t* out,
                                 unsigned long long* d_count, size_t n, const LookbackWs& ws, cudaStream_t s) {
-    switch (rule) {  // a predicate needs every key, so its keys come through the ring
-        case KeepRule::PositiveF32:
-            return launch_compact_persistent<512, 8, 3, false, KeepRule::PositiveF32>(keys, flags, out, d_count, n,
-                                                                                       ws, s);
-        case KeepRule::PositiveI32:
-            return launch_compact_persistent<512, 8, 3, false, KeepRule::PositiveI32>(keys, flags, out, d_count, n,
-                                                                                       ws, s);
-        case KeepRule::PositiveU32:
-            return launch_compact_persistent<512, 8, 3, false, KeepRule::PositiveU32>(keys, flags, out, d_count, n,
-                                                                                       ws, s);
-        default: break;
-    }
+    // A predicate needs every key: its own kernel streams them all through the ring.
+    if (rule != KeepRule::Flags) return launch_compact_pred(rule, keys, out, d_count, n, ws, s);
     if (g_compact_kernel == 0)
         return launch_compact_persistent<512, 8, 2, false>(keys, flags, out, d_count, n, ws, s);
     if (g_compact_kernel == 2 && n > (size_t)65536)

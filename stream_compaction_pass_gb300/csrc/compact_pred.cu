@@ -1,0 +1,407 @@
+// compact_pred.cu -- order-preserving compaction under a built-in predicate
+// (keep keys[i] where keys[i] > 0 in its element type; no flag array).
+// "Prefix sum and other parallel patterns", Stream compaction: compact.cu
+// keeps v > 0; Exercise 1 fuses the flag pass into the compaction.
+//
+// A persistent CTA per SM takes a rank from the workspace counter and owns
+// tiles rank, rank + G, ... (16384 keys each), which a three-stage
+// shared-memory ring receives by bulk copies.  The CTA has 16 compute warps
+// and one look-back warp:
+//  - compute warps, iteration k: count the kept keys of tile k+1 and publish
+//    the count (the tile's aggregate, one iteration early); rank tile k's
+//    kept keys (per-row keep masks, the rows' counts packed one byte per row
+//    and scanned across the warp, popc inside a vector); take tile k's
+//    prefix from the look-back warp; scatter.
+//  - look-back warp: for each tile, as soon as its aggregate is known, walks
+//    the predecessors' descriptors (no further than this CTA's previous
+//    tile) and publishes the inclusive count.  That is a whole iteration
+//    before the compute warps need the prefix, so the look-back's L2 round
+//    trips run beside their work instead of in front of a barrier.
+//  - scatter: a warp's kept keys form one contiguous run of the output.  Each
+//    warp writes them, half a segment at a time, into its own staging area
+//    at the output's 16-byte phase, then stores the run as aligned 16-byte
+//    vectors (partial vectors at the two ends element by element).  Every
+//    store instruction of a warp then covers 512 contiguous bytes, instead
+//    of one 4-byte slot in every 16 bytes.
+// Named barriers carry the aggregate to the look-back warp and the prefix
+// back.  Each has two ids, by tile parity; each side must pass the other's
+// barrier of tile k before it can arrive at the barrier of tile k + 2 with
+// the same id, so neither side laps the other.
+#include "bulk.cuh"
+#include "internal.h"
+#include "keep.cuh"
+#include "tile.cuh"
+
+namespace ss {
+
+namespace {
+
+constexpr int kPredComputeWarps = 16;
+constexpr int kPredComputeThreads = kPredComputeWarps * 32;  // 512
+constexpr int kPredThreads = kPredComputeThreads + 32;       // + the look-back warp
+constexpr int kPredVpt = 8;                                  // 16-byte key vectors per lane per tile
+constexpr int kPredStages = 3;
+constexpr uint32_t kPredTile = (uint32_t)kPredComputeThreads * kPredVpt * 4;  // 16384
+constexpr uint32_t kPredStageBytes = kPredTile * 4;
+constexpr uint32_t kPredHalf = 32u * kPredVpt * 2;  // keys per staging pass: 4 rows of a warp segment
+constexpr uint32_t kPredStgWords = kPredHalf + 4;   // + up to 3 words of phase, rounded to 16 bytes
+constexpr size_t kPredSmem = (size_t)kPredStages * kPredStageBytes + (size_t)kPredComputeWarps * kPredStgWords * 4;
+static_assert(kPredTile >= kCompactTile, "descriptors are sized for kCompactTile-element tiles");
+
+// Named barriers (id 0 is __syncthreads).
+constexpr uint32_t kBarCompute = 1;  // compute warps only
+constexpr uint32_t kBarAgg = 2;      // + tile parity: the aggregate is in shared memory
+constexpr uint32_t kBarPre = 4;      // + tile parity: the prefix is in shared memory
+
+__device__ __forceinline__ void bar_sync_n(uint32_t id, uint32_t threads) {
+    asm volatile("barrier.cta.sync.aligned %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ void bar_arrive_n(uint32_t id, uint32_t threads) {
+    asm volatile("barrier.cta.arrive.aligned %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Barrier among `threads` threads that returns whether any of them passed true.
+__device__ __forceinline__ bool bar_any_n(uint32_t id, uint32_t threads, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "barrier.cta.red.or.aligned.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(threads)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void st_global_v4(uint32_t* p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t vec_elem(const uint4& v, int s) {
+    return s == 0 ? v.x : s == 1 ? v.y : s == 2 ? v.z : v.w;
+}
+
+}  // namespace
+
+template <KeepRule RULE>
+__global__ void __launch_bounds__(kPredThreads, 1)
+k_compact_pred(const uint32_t* keys, uint32_t* out, unsigned long long* d_count, size_t n, uint32_t num_tiles,
+               LookbackCtx ctx) {
+    constexpr int VPT = kPredVpt;
+    constexpr int STAGES = kPredStages;
+    constexpr int CW = kPredComputeWarps;
+    constexpr uint32_t CT = kPredComputeThreads;
+    constexpr uint32_t ALL = kPredThreads;
+    constexpr uint32_t TILE = kPredTile;
+    constexpr uint32_t SEG = 32u * VPT * 4;  // keys per warp segment
+    static_assert(VPT == 8, "two packed count words of four rows, one staging pass each");
+
+    extern __shared__ __align__(128) unsigned char smem_raw[];  // ring, then the staging areas
+    __shared__ __align__(8) uint64_t bars[STAGES];
+    __shared__ uint32_t s_wsum[2][CW];  // warp counts, by tile parity
+    __shared__ uint32_t s_agg[2], s_stop[2], s_prefix[2], s_fail[2], s_rank, s_epoch;
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const uint32_t G = gridDim.x;
+
+    if (threadIdx.x == 0) {
+        uint32_t rank, epoch;
+        claim_tile(ctx.counter, G, &rank, &epoch);  // one claim per CTA; the last resets the counter
+        s_rank = rank;
+        s_epoch = epoch;
+        for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
+        fence_async_shared();
+    }
+    __syncthreads();
+    const uint32_t rank = s_rank;
+    const uint32_t epoch = s_epoch;
+    if (rank >= G) {
+        if (threadIdx.x == 0) record_error(ctx.status, kErrCounter, rank);
+        return;
+    }
+    const uint32_t count = rank < num_tiles ? (num_tiles - rank + G - 1) / G : 0;
+
+    if (warp == CW) {
+        // ---- look-back warp ----
+        uint32_t prev_incl = 0;  // inclusive count through this CTA's previous tile
+        for (uint32_t k = 0; k < count; ++k) {
+            const uint32_t t = rank + k * G;
+            bar_sync_n(kBarAgg + (k & 1), ALL);
+            if (s_stop[k & 1]) break;  // the compute warps stopped before this tile: nothing awaits its prefix
+            const uint32_t agg = s_agg[k & 1];
+            uint32_t excl = 0;
+            bool lb_failed = false;
+            const bool dead = (int64_t)t == ctx.fault_tile;  // test hook only
+            if (t == 0) {
+                lb_failed = dead;
+            } else if (dead) {
+                lb_failed = true;  // it publishes nothing, so its successors' waits run out
+            } else {
+                const int64_t floor = k > 0 ? (int64_t)t - (int64_t)G : -1;
+                excl = lookback<uint32_t, 1>(ctx, t, epoch, lane, &lb_failed, nullptr, floor, prev_incl);
+                if (lane == 0) {
+                    if (!lb_failed) {
+                        st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStateP, excl + agg));
+                    } else {
+                        st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStatePoison, 0u));
+                        record_error(ctx.status, kErrLookbackTimeout, t);
+                    }
+                }
+            }
+            prev_incl = excl + agg;
+            if (lane == 0) {
+                s_prefix[k & 1] = excl;
+                s_fail[k & 1] = lb_failed ? 1u : 0u;
+                if (!lb_failed && t == num_tiles - 1) *d_count = (unsigned long long)excl + agg;
+            }
+            bar_arrive_n(kBarPre + (k & 1), ALL);
+            if (lb_failed) {
+                // The compute warps stop after this tile; they have already
+                // arrived (or will, before they wait for this prefix) with
+                // the next tile's aggregate.  Take that arrival, then leave.
+                if (k + 1 < count) bar_sync_n(kBarAgg + ((k + 1) & 1), ALL);
+                break;
+            }
+        }
+        return;
+    }
+
+    // ---- compute warps ----
+    const uint64_t policy = policy_evict_first();
+    uint32_t issued = 0, consumed = 0;  // thread 0
+    unsigned char* const ring = smem_raw;
+    uint32_t* const stg = reinterpret_cast<uint32_t*>(smem_raw + (size_t)STAGES * kPredStageBytes) +
+                          (size_t)warp * kPredStgWords;
+
+    auto full = [&](uint32_t k) { return (size_t)(rank + k * G) * TILE + TILE <= n; };
+    auto issue = [&](uint32_t k) {  // thread 0
+        const int s = (int)(k % STAGES);
+        if (full(k)) {
+            fence_async_shared();
+            mbar_arrive_expect_tx(&bars[s], kPredStageBytes);
+            bulk_load(ring + (size_t)s * kPredStageBytes, keys + (size_t)(rank + k * G) * TILE, kPredStageBytes,
+                      &bars[s], policy);
+        } else {
+            mbar_arrive(&bars[s]);  // ragged last tile: read from global with bounds checks
+        }
+        issued = k + 1;
+    };
+    // This lane's keys of tile k and their keep masks (bit e of m[j]: element e
+    // of row j is kept).  Row j of a lane is the 16-byte vector j * 32 + lane
+    // of its warp's segment.
+    auto load_tile = [&](uint32_t k, uint32_t (&key)[VPT][4], uint32_t (&m)[VPT]) {
+        const size_t seg = (size_t)(rank + k * G) * TILE + (size_t)warp * SEG;
+        if (full(k)) {
+            const unsigned char* kb =
+                ring + (size_t)(k % STAGES) * kPredStageBytes + ((size_t)warp * SEG + (size_t)lane * 4) * 4;
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const uint4 r = lds_vec(kb + 512 * j);
+                key[j][0] = r.x;
+                key[j][1] = r.y;
+                key[j][2] = r.z;
+                key[j][3] = r.w;
+                m[j] = keep_mask4<RULE>(key[j]);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                m[j] = 0;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const size_t i = seg + (size_t)(32 * j + lane) * 4 + e;
+                    key[j][e] = i < n ? keys[i] : 0u;
+                    if (i < n && keep_bits<RULE>(key[j][e])) m[j] |= 1u << e;
+                }
+            }
+        }
+    };
+    // Waits for tile k, counts its kept keys, publishes the count and hands
+    // it to the look-back warp.  *wp: this warp's offset inside the tile.
+    // False if the tile's copy did not arrive (then the look-back warp is
+    // told to stop).  Always arrives at the tile's aggregate barrier.
+    auto count_tile = [&](uint32_t k, uint32_t* wp) -> bool {
+        const uint32_t t = rank + k * G;
+        const bool ok = mbar_wait_bounded(&bars[k % STAGES], (k / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
+        if (bar_any_n(kBarCompute, CT, !ok)) {
+            if (threadIdx.x == 0) {
+                record_error(ctx.status, kErrBulkTimeout, t);
+                s_stop[k & 1] = 1u;
+            }
+            bar_arrive_n(kBarAgg + (k & 1), ALL);
+            return false;
+        }
+        uint32_t key[VPT][4], m[VPT];
+        load_tile(k, key, m);
+        uint32_t c = 0;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) c += (uint32_t)__popc(m[j]);
+        c = warp_sum(c);
+        if (lane == 0) s_wsum[k & 1][warp] = c;
+        bar_sync_n(kBarCompute, CT);
+        const uint32_t w = lane < CW ? s_wsum[k & 1][lane] : 0u;
+        const uint32_t inc = warp_inclusive_scan<uint32_t>(w, lane);
+        *wp = __shfl_sync(kFullMask, inc - w, warp);
+        const uint32_t agg = __shfl_sync(kFullMask, inc, CW - 1);
+        if (threadIdx.x == 0) {
+            if ((int64_t)t != ctx.fault_tile) {
+                if (t == 0) {
+                    if (num_tiles > 1) st_relaxed_u64(ctx.desc, pack_desc(epoch, kStateP, agg));
+                } else {
+                    st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStateA, agg));
+                }
+            }
+            s_agg[k & 1] = agg;
+            s_stop[k & 1] = 0u;
+        }
+        bar_arrive_n(kBarAgg + (k & 1), ALL);
+        return true;
+    };
+    // Writes this warp's kept keys of tile k, already ranked: row_run[j] is
+    // the position of the lane's first kept key of row j in the warp's run,
+    // c0 the count of rows 0..3, `start` the run's first output index.  Two
+    // passes of four rows through the staging area; in each, key number i of
+    // the pass goes to staging word i + a, where a puts the words at the
+    // 16-byte phase of their output slots, so every full 16-byte vector of
+    // the staging area is one aligned vector of the output.
+    auto scatter = [&](const uint32_t (&key)[VPT][4], const uint32_t (&m)[VPT], const uint32_t (&row_run)[VPT],
+                       uint32_t c0, uint32_t c_all, uint32_t start) {
+        const uint32_t out_phase = (uint32_t)(reinterpret_cast<uintptr_t>(out) >> 2) & 3u;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t first = h == 0 ? 0u : c0;                 // run position where the pass starts
+            const uint32_t cnt = h == 0 ? c0 : c_all - c0;           // keys in the pass (warp-uniform)
+            const size_t d0 = (size_t)start + first;                 // output index of the pass's first key
+            const uint32_t a = (uint32_t)(d0 + out_phase) & 3u;      // its 16-byte phase, in words
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int j = 4 * h + q;
+                const uint32_t base = row_run[j] - first + a;
+                const uint32_t mj = m[j];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint32_t idx = base + (uint32_t)__popc(mj & ((1u << e) - 1u));
+                    if ((mj >> e) & 1u) stg[idx] = key[j][e];
+                }
+            }
+            __syncwarp();
+            const uint32_t tot = a + cnt;          // staging words in use, from word a
+            uint32_t* const gbase = out + d0 - a;  // output slot of staging word 0 (16-byte aligned)
+            for (uint32_t v = (uint32_t)lane; 4 * v < tot; v += 32) {
+                const uint4 x = lds_vec(stg + 4 * v);
+                if (4 * v >= a && 4 * v + 4 <= tot) {
+                    st_global_v4(gbase + 4 * v, x);
+                } else {
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) {
+                        const uint32_t w = 4 * v + (uint32_t)s;
+                        if (w >= a && w < tot) gbase[w] = vec_elem(x, s);
+                    }
+                }
+            }
+            __syncwarp();  // the area is read before the next pass writes it
+        }
+    };
+
+    if (threadIdx.x == 0)
+        for (uint32_t k = 0; k < count && k < (uint32_t)STAGES; ++k) issue(k);
+
+    uint32_t wp_cur = 0;
+    bool failed = false;
+    uint32_t poison_from = 0;  // first of this CTA's tiles (by k) left for thread 0 to poison on failure
+    if (count > 0 && !count_tile(0, &wp_cur)) failed = true;
+
+    for (uint32_t k = 0; !failed && k < count; ++k) {
+        uint32_t wp_next = 0;
+        bool next_ok = true;
+        if (k + 1 < count) next_ok = count_tile(k + 1, &wp_next);
+
+        // Rank tile k's kept keys.
+        uint32_t key[VPT][4], m[VPT];
+        load_tile(k, key, m);
+        uint32_t row_run[VPT];
+        uint32_t run = 0, c0 = 0;
+#pragma unroll
+        for (int w = 0; w < VPT / 4; ++w) {
+            uint32_t packed = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) packed |= (uint32_t)__popc(m[4 * w + q]) << (8 * q);
+            const uint32_t inc = warp_inclusive_scan<uint32_t>(packed, lane);
+            const uint32_t exc = inc - packed;  // bytewise, no borrows (each byte <= 128)
+            const uint32_t rows = __shfl_sync(kFullMask, inc, 31);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                row_run[4 * w + q] = run + ((exc >> (8 * q)) & 0xffu);
+                run += (rows >> (8 * q)) & 0xffu;
+            }
+            if (w == 0) c0 = run;
+        }
+
+        bar_sync_n(kBarPre + (k & 1), ALL);  // tile k's prefix; every compute warp has read tile k
+        const bool lb_failed = s_fail[k & 1] != 0;
+        const uint32_t prefix = s_prefix[k & 1];
+        if (threadIdx.x == 0) {
+            consumed = k + 1;
+            if (!lb_failed && next_ok && k + STAGES < count) issue(k + STAGES);
+        }
+        if (lb_failed) {  // the look-back warp poisoned tile k
+            failed = true;
+            poison_from = k + 1;
+            break;
+        }
+        scatter(key, m, row_run, c0, run, prefix + wp_cur);
+        if (!next_ok) {
+            failed = true;
+            poison_from = k + 1;
+            break;
+        }
+        wp_cur = wp_next;
+    }
+
+    if (failed && threadIdx.x == 0) {
+        // Later tiles of this CTA publish nothing else: poison them so that
+        // their successors stop at once, then wait for the copies in flight.
+        for (uint32_t k = poison_from; k < count; ++k) {
+            const uint32_t t = rank + k * G;
+            if ((int64_t)t != ctx.fault_tile) st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStatePoison, 0u));
+        }
+        for (uint32_t k = consumed; k < issued; ++k)
+            mbar_wait_bounded(&bars[k % STAGES], (k / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
+    }
+}
+
+template <KeepRule RULE>
+static cudaError_t launch_pred(const uint32_t* keys, uint32_t* out, unsigned long long* d_count, size_t n,
+                               const LookbackWs& ws, cudaStream_t s) {
+    auto kern = k_compact_pred<RULE>;
+    static int sms = 0;
+    if (sms == 0) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPredSmem);
+        if (e != cudaSuccess) return e;
+        int dev = 0, v = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        sms = v > 0 ? v : 1;
+    }
+    const uint32_t tiles = (uint32_t)((n + kPredTile - 1) / kPredTile);
+    const uint32_t grid = tiles < (uint32_t)sms ? tiles : (uint32_t)sms;
+    LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};
+    kern<<<grid, kPredThreads, kPredSmem, s>>>(keys, out, d_count, n, tiles, ctx);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_compact_pred(KeepRule rule, const uint32_t* keys, uint32_t* out, unsigned long long* d_count,
+                                size_t n, const LookbackWs& ws, cudaStream_t s) {
+    switch (rule) {
+        case KeepRule::PositiveF32: return launch_pred<KeepRule::PositiveF32>(keys, out, d_count, n, ws, s);
+        case KeepRule::PositiveI32: return launch_pred<KeepRule::PositiveI32>(keys, out, d_count, n, ws, s);
+        case KeepRule::PositiveU32: return launch_pred<KeepRule::PositiveU32>(keys, out, d_count, n, ws, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace ss

@@ -91,6 +91,12 @@ cudaError_t launch_compact(KeepRule rule, const uint32_t* keys, const uint8_t* f
 // (and flags), n above one 16384-element tile.
 cudaError_t launch_compact_pipe(KeepRule rule, const uint32_t* keys, const uint8_t* flags, uint32_t* out,
                                 unsigned long long* d_count, size_t n, const LookbackWs& ws, cudaStream_t s);
+
+// Predicate compaction (compact_pred.cu): keys kept where the rule holds
+// (PositiveF32/I32/U32), with a dedicated look-back warp and staged 16-byte
+// stores; keys 16-byte aligned, n > 16384.
+cudaError_t launch_compact_pred(KeepRule rule, const uint32_t* keys, uint32_t* out, unsigned long long* d_count,
+                                size_t n, const LookbackWs& ws, cudaStream_t s);
 int compact_kernel_count();
 void set_compact_kernel(int k);
 

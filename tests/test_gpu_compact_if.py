@@ -120,6 +120,17 @@ def test_positive_misaligned(ss, ioff, ooff):
     assert_equal(got, expected_bits("f32", x))
 
 
+@pytest.mark.parametrize("p", [0.02, 0.5, 0.99])
+@pytest.mark.parametrize("ooff", [1, 2, 3])
+def test_positive_output_phase(ss, p, ooff):
+    # aligned keys take the persistent kernel; the output starts 4, 8 or 12
+    # bytes past a 16-byte boundary, so every staged run has a ragged head
+    n = 9 * 16384 + 77
+    x = positive_input(n, p, "f32")
+    got, c = run_positive(ss, "f32", x, out_offset=ooff)
+    assert_equal(got, expected_bits("f32", x))
+
+
 def test_positive_zero_length(ss):
     import torch
     cnt = torch.full((1,), 77, dtype=torch.int64, device="cuda:0")
