@@ -7,24 +7,26 @@
 // tiles rank, rank + G, ... (16384 keys each), which a three-stage
 // shared-memory ring receives by bulk copies.  The CTA has 16 compute warps
 // and one look-back warp:
-//  - compute warps, iteration k: count the kept keys of tile k+1 and publish
-//    the count (the tile's aggregate, one iteration early); rank tile k's
-//    kept keys (per-row keep masks, the rows' counts packed one byte per row
-//    and scanned across the warp, popc inside a vector); take tile k's
-//    prefix from the look-back warp; scatter.
-//  - look-back warp: for each tile, as soon as its aggregate is known, walks
-//    the predecessors' descriptors (no further than this CTA's previous
-//    tile) and publishes the inclusive count.  That is a whole iteration
-//    before the compute warps need the prefix, so the look-back's L2 round
-//    trips run beside their work instead of in front of a barrier.
+//  - compute warps, iteration k: count the kept keys of tile k+1 (each warp
+//    its own segment, no barrier: the last warp to finish adds the counts up
+//    and publishes the tile's aggregate, one iteration early) and hand it to
+//    the look-back warp; rank tile k's kept keys (per-row keep masks, the
+//    rows' counts packed one byte per row and scanned across the warp, popc
+//    inside a vector); take tile k's offsets from the look-back warp;
+//    scatter.
+//  - look-back warp: for each tile, as soon as it is handed over, walks the
+//    predecessors' descriptors (no further than this CTA's previous tile),
+//    publishes the inclusive count, and works out each warp's output
+//    offset.  That is an iteration before the compute warps need them, so
+//    the look-back's L2 round trips run beside their work instead of in
+//    front of a barrier.
 //  - scatter: a warp's kept keys form one contiguous run of the output.  Each
 //    warp writes them, half a segment at a time, into its own staging area
 //    at the output's 16-byte phase, then stores the run as aligned 16-byte
 //    vectors (partial vectors at the two ends element by element).  Every
 //    store instruction of a warp then covers 512 contiguous bytes, instead
 //    of one 4-byte slot in every 16 bytes.
-// Named barriers carry the aggregate to the look-back warp and the prefix
-// back.  Each has two ids, by tile parity; each side must pass the other's
+// Named barriers hand each tile to the look-back warp and its offsets back.  Each has two ids, by tile parity; each side must pass the other's
 // barrier of tile k before it can arrive at the barrier of tile k + 2 with
 // the same id, so neither side laps the other.
 #include "bulk.cuh"
@@ -41,6 +43,7 @@ constexpr int kPredComputeThreads = kPredComputeWarps * 32;  // 512
 constexpr int kPredThreads = kPredComputeThreads + 32;       // + the look-back warp
 constexpr int kPredVpt = 8;                                  // 16-byte key vectors per lane per tile
 constexpr int kPredStages = 3;
+constexpr int kPredLookbackK = 1;  // descriptors per lane per look-back round
 constexpr uint32_t kPredTile = (uint32_t)kPredComputeThreads * kPredVpt * 4;  // 16384
 constexpr uint32_t kPredStageBytes = kPredTile * 4;
 constexpr uint32_t kPredHalf = 32u * kPredVpt * 2;  // keys per staging pass: 4 rows of a warp segment
@@ -59,20 +62,6 @@ __device__ __forceinline__ void bar_sync_n(uint32_t id, uint32_t threads) {
 
 __device__ __forceinline__ void bar_arrive_n(uint32_t id, uint32_t threads) {
     asm volatile("barrier.cta.arrive.aligned %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
-// Barrier among `threads` threads that returns whether any of them passed true.
-__device__ __forceinline__ bool bar_any_n(uint32_t id, uint32_t threads, bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "barrier.cta.red.or.aligned.pred q, %2, %3, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)v), "r"(id), "r"(threads)
-        : "memory");
-    return r != 0;
 }
 
 __device__ __forceinline__ void st_global_v4(uint32_t* p, uint4 v) {
@@ -101,8 +90,13 @@ k_compact_pred(const uint32_t* keys, uint32_t* out, unsigned long long* d_count,
 
     extern __shared__ __align__(128) unsigned char smem_raw[];  // ring, then the staging areas
     __shared__ __align__(8) uint64_t bars[STAGES];
-    __shared__ uint32_t s_wsum[2][CW];  // warp counts, by tile parity
-    __shared__ uint32_t s_agg[2], s_stop[2], s_prefix[2], s_fail[2], s_rank, s_epoch;
+    // By tile parity: the warps' counts; the counting warps' arrival tally and
+    // timeout bits (reset by the last of them); the aggregate and the stop
+    // flag (written once per tile by the last counting warp); each warp's
+    // output offset, prefix included, and the look-back's failure flag
+    // (written by the look-back warp).
+    __shared__ uint32_t s_wsum[2][CW], s_base[2][CW];
+    __shared__ uint32_t s_arrive[2], s_bad[2], s_agg[2], s_stop[2], s_fail[2], s_rank, s_epoch;
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -115,6 +109,7 @@ k_compact_pred(const uint32_t* keys, uint32_t* out, unsigned long long* d_count,
         s_epoch = epoch;
         for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
         fence_async_shared();
+        for (int q = 0; q < 2; ++q) s_arrive[q] = s_bad[q] = s_stop[q] = s_fail[q] = 0u;
     }
     __syncthreads();
     const uint32_t rank = s_rank;
@@ -131,8 +126,10 @@ k_compact_pred(const uint32_t* keys, uint32_t* out, unsigned long long* d_count,
         for (uint32_t k = 0; k < count; ++k) {
             const uint32_t t = rank + k * G;
             bar_sync_n(kBarAgg + (k & 1), ALL);
-            if (s_stop[k & 1]) break;  // the compute warps stopped before this tile: nothing awaits its prefix
+            if (s_stop[k & 1]) break;  // tile k's copy never arrived: the compute warps stop before its scatter
             const uint32_t agg = s_agg[k & 1];
+            const uint32_t wc = lane < CW ? s_wsum[k & 1][lane] : 0u;
+            const uint32_t wexcl = warp_inclusive_scan<uint32_t>(wc, lane) - wc;  // warp offsets inside the tile
             uint32_t excl = 0;
             bool lb_failed = false;
             const bool dead = (int64_t)t == ctx.fault_tile;  // test hook only
@@ -142,7 +139,7 @@ k_compact_pred(const uint32_t* keys, uint32_t* out, unsigned long long* d_count,
                 lb_failed = true;  // it publishes nothing, so its successors' waits run out
             } else {
                 const int64_t floor = k > 0 ? (int64_t)t - (int64_t)G : -1;
-                excl = lookback<uint32_t, 1>(ctx, t, epoch, lane, &lb_failed, nullptr, floor, prev_incl);
+                excl = lookback<uint32_t, kPredLookbackK>(ctx, t, epoch, lane, &lb_failed, nullptr, floor, prev_incl);
                 if (lane == 0) {
                     if (!lb_failed) {
                         st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStateP, excl + agg));
@@ -153,16 +150,16 @@ k_compact_pred(const uint32_t* keys, uint32_t* out, unsigned long long* d_count,
                 }
             }
             prev_incl = excl + agg;
+            if (lane < CW) s_base[k & 1][lane] = excl + wexcl;
             if (lane == 0) {
-                s_prefix[k & 1] = excl;
                 s_fail[k & 1] = lb_failed ? 1u : 0u;
                 if (!lb_failed && t == num_tiles - 1) *d_count = (unsigned long long)excl + agg;
             }
             bar_arrive_n(kBarPre + (k & 1), ALL);
             if (lb_failed) {
-                // The compute warps stop after this tile; they have already
-                // arrived (or will, before they wait for this prefix) with
-                // the next tile's aggregate.  Take that arrival, then leave.
+                // The compute warps stop after this tile; they handed over
+                // the next tile before they waited for this one's offsets.
+                // Take that arrival, then leave.
                 if (k + 1 < count) bar_sync_n(kBarAgg + ((k + 1) & 1), ALL);
                 break;
             }
@@ -220,46 +217,55 @@ k_compact_pred(const uint32_t* keys, uint32_t* out, unsigned long long* d_count,
             }
         }
     };
-    // Waits for tile k, counts its kept keys, publishes the count and hands
-    // it to the look-back warp.  *wp: this warp's offset inside the tile.
-    // False if the tile's copy did not arrive (then the look-back warp is
-    // told to stop).  Always arrives at the tile's aggregate barrier.
-    auto count_tile = [&](uint32_t k, uint32_t* wp) -> bool {
+    // Waits for tile k and counts this warp's kept keys.  The last warp to
+    // finish adds the counts up and publishes the tile's aggregate (or, if a
+    // warp's copy wait ran out, publishes nothing and sets the tile's stop
+    // flag).  No barrier: the warps meet through an arrival tally in shared
+    // memory.
+    auto count_tile = [&](uint32_t k) {
         const uint32_t t = rank + k * G;
-        const bool ok = mbar_wait_bounded(&bars[k % STAGES], (k / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
-        if (bar_any_n(kBarCompute, CT, !ok)) {
-            if (threadIdx.x == 0) {
-                record_error(ctx.status, kErrBulkTimeout, t);
-                s_stop[k & 1] = 1u;
-            }
-            bar_arrive_n(kBarAgg + (k & 1), ALL);
-            return false;
-        }
-        uint32_t key[VPT][4], m[VPT];
-        load_tile(k, key, m);
+        const int par = (int)(k & 1);
+        const bool ok = __all_sync(kFullMask, mbar_wait_bounded(&bars[k % STAGES], (k / STAGES) & 1u,
+                                                                ctx.max_polls, ctx.timeout_ns));
         uint32_t c = 0;
+        if (ok) {
+            uint32_t key[VPT][4], m[VPT];
+            load_tile(k, key, m);
 #pragma unroll
-        for (int j = 0; j < VPT; ++j) c += (uint32_t)__popc(m[j]);
-        c = warp_sum(c);
-        if (lane == 0) s_wsum[k & 1][warp] = c;
-        bar_sync_n(kBarCompute, CT);
-        const uint32_t w = lane < CW ? s_wsum[k & 1][lane] : 0u;
-        const uint32_t inc = warp_inclusive_scan<uint32_t>(w, lane);
-        *wp = __shfl_sync(kFullMask, inc - w, warp);
-        const uint32_t agg = __shfl_sync(kFullMask, inc, CW - 1);
-        if (threadIdx.x == 0) {
-            if ((int64_t)t != ctx.fault_tile) {
-                if (t == 0) {
-                    if (num_tiles > 1) st_relaxed_u64(ctx.desc, pack_desc(epoch, kStateP, agg));
-                } else {
-                    st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStateA, agg));
-                }
-            }
-            s_agg[k & 1] = agg;
-            s_stop[k & 1] = 0u;
+            for (int j = 0; j < VPT; ++j) c += (uint32_t)__popc(m[j]);
         }
-        bar_arrive_n(kBarAgg + (k & 1), ALL);
-        return true;
+        c = warp_sum(c);
+        uint32_t last = 0;
+        if (lane == 0) {
+            s_wsum[par][warp] = c;
+            if (!ok) {
+                atomicOr(&s_bad[par], 1u);
+                record_error(ctx.status, kErrBulkTimeout, t);
+            }
+            __threadfence_block();  // the count (and bit) before the tally
+            last = atomicAdd(&s_arrive[par], 1u) == (uint32_t)(CW - 1) ? 1u : 0u;
+        }
+        last = __shfl_sync(kFullMask, last, 0);
+        if (last) {
+            __syncwarp();
+            __threadfence_block();  // every warp's count after the tally
+            const uint32_t w = lane < CW ? *(volatile uint32_t*)&s_wsum[par][lane] : 0u;
+            const uint32_t agg = warp_sum(w);
+            if (lane == 0) {
+                const uint32_t bad = *(volatile uint32_t*)&s_bad[par];
+                if (!bad && (int64_t)t != ctx.fault_tile) {
+                    if (t == 0) {
+                        if (num_tiles > 1) st_relaxed_u64(ctx.desc, pack_desc(epoch, kStateP, agg));
+                    } else {
+                        st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStateA, agg));
+                    }
+                }
+                s_agg[par] = agg;
+                s_stop[par] = bad;
+                s_bad[par] = 0u;
+                s_arrive[par] = 0u;
+            }
+        }
     };
     // Writes this warp's kept keys of tile k, already ranked: row_run[j] is
     // the position of the lane's first kept key of row j in the warp's run,
@@ -310,15 +316,23 @@ k_compact_pred(const uint32_t* keys, uint32_t* out, unsigned long long* d_count,
     if (threadIdx.x == 0)
         for (uint32_t k = 0; k < count && k < (uint32_t)STAGES; ++k) issue(k);
 
-    uint32_t wp_cur = 0;
     bool failed = false;
     uint32_t poison_from = 0;  // first of this CTA's tiles (by k) left for thread 0 to poison on failure
-    if (count > 0 && !count_tile(0, &wp_cur)) failed = true;
+    if (count > 0) {
+        count_tile(0);
+        bar_arrive_n(kBarAgg, ALL);  // tile 0 to the look-back warp
+    }
+    bar_sync_n(kBarCompute, CT);  // tile 0's stop flag is in shared memory
+    if (count > 0 && s_stop[0]) {  // tile 0's copy did not arrive
+        failed = true;
+        poison_from = 0;
+    }
 
     for (uint32_t k = 0; !failed && k < count; ++k) {
-        uint32_t wp_next = 0;
-        bool next_ok = true;
-        if (k + 1 < count) next_ok = count_tile(k + 1, &wp_next);
+        if (k + 1 < count) {  // count tile k+1 and hand it to the look-back warp
+            count_tile(k + 1);
+            bar_arrive_n(kBarAgg + ((k + 1) & 1), ALL);
+        }
 
         // Rank tile k's kept keys.
         uint32_t key[VPT][4], m[VPT];
@@ -341,25 +355,26 @@ k_compact_pred(const uint32_t* keys, uint32_t* out, unsigned long long* d_count,
             if (w == 0) c0 = run;
         }
 
-        bar_sync_n(kBarPre + (k & 1), ALL);  // tile k's prefix; every compute warp has read tile k
+        bar_sync_n(kBarPre + (k & 1), ALL);  // tile k's offsets; every compute warp has read tile k
         const bool lb_failed = s_fail[k & 1] != 0;
-        const uint32_t prefix = s_prefix[k & 1];
+        const uint32_t base = s_base[k & 1][warp];
         if (threadIdx.x == 0) {
             consumed = k + 1;
-            if (!lb_failed && next_ok && k + STAGES < count) issue(k + STAGES);
+            const bool next_stops = k + 1 < count && s_stop[(k + 1) & 1] != 0;
+            if (!lb_failed && !next_stops && k + STAGES < count) issue(k + STAGES);
         }
+        const bool next_stops = k + 1 < count && s_stop[(k + 1) & 1] != 0;
         if (lb_failed) {  // the look-back warp poisoned tile k
             failed = true;
             poison_from = k + 1;
             break;
         }
-        scatter(key, m, row_run, c0, run, prefix + wp_cur);
-        if (!next_ok) {
+        scatter(key, m, row_run, c0, run, base);
+        if (next_stops) {  // tile k+1's copy did not arrive; the look-back warp stops there too
             failed = true;
             poison_from = k + 1;
             break;
         }
-        wp_cur = wp_next;
     }
 
     if (failed && threadIdx.x == 0) {
