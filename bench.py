@@ -543,14 +543,29 @@ def profile_ablations(n: int) -> None:
     print(f"ablations ok at n={n}")
 
 
-def profile_compaction(n: int, p: float) -> None:
+def profile_compaction(n: int, p: float, predicate: bool = False) -> None:
     """Two launches of the default (flag) compaction at n keys, keep
     probability p (the compaction workload's generators), for a profiler to
-    capture; checks the result against the oracle."""
+    capture; checks the result against the oracle.  With `predicate`, the
+    fp32 `v > 0` compaction of the predicate workload instead."""
     import torch
     import seeded_inputs as si
     import stream_compaction_pass_gb300 as ss
     import oracle as orc
+    if predicate:
+        x = si.workload_positive_f32(n, p, seed=5)
+        ref = orc.compact_positive_f32(x)
+        dx = torch.from_numpy(x).cuda()
+        do = torch.empty_like(dx)
+        cnt = torch.zeros(1, dtype=torch.int64, device="cuda")
+        for _ in range(2):
+            ss.compact_positive_f32(dx, do, cnt)
+        torch.cuda.synchronize()
+        c = int(cnt.item())
+        assert c == ref.size and np.array_equal(do[:c].cpu().numpy().view(np.uint32), ref.view(np.uint32)), \
+            "predicate compaction mismatch"
+        print(f"predicate compaction ok at n={n}, p={p}, kept {c}")
+        return
     keys, flags = si.workload_compaction(n, p, seed=3)
     ref = orc.compact_u32(keys, flags)
     dk = torch.from_numpy(keys.view(np.int32)).cuda()
@@ -604,6 +619,8 @@ def main() -> None:
     ap.add_argument("--profile-compaction", type=int, default=0, metavar="N",
                     help="only run the default compaction twice at n=N (for a profiler) and exit")
     ap.add_argument("--keep-p", type=float, default=0.5, help="keep probability for --profile-compaction")
+    ap.add_argument("--predicate", action="store_true",
+                    help="with --profile-compaction: the fp32 v > 0 compaction instead of the flag form")
     ap.add_argument("--profile-f64", type=int, default=0, metavar="N",
                     help="only run the fp64 inclusive scan twice at n=N (for a profiler) and exit")
     args = ap.parse_args()
@@ -611,7 +628,7 @@ def main() -> None:
         profile_f64(args.profile_f64)
         return
     if args.profile_compaction:
-        profile_compaction(args.profile_compaction, args.keep_p)
+        profile_compaction(args.profile_compaction, args.keep_p, args.predicate)
         return
     if args.profile_ablations:
         profile_ablations(args.profile_ablations)

@@ -26,9 +26,10 @@
 //    vectors (partial vectors at the two ends element by element).  Every
 //    store instruction of a warp then covers 512 contiguous bytes, instead
 //    of one 4-byte slot in every 16 bytes.
-// Named barriers hand each tile to the look-back warp and its offsets back.  Each has two ids, by tile parity; each side must pass the other's
-// barrier of tile k before it can arrive at the barrier of tile k + 2 with
-// the same id, so neither side laps the other.
+// Named barriers hand each tile to the look-back warp and its offsets back.
+// Each has two ids, by tile parity; each side must pass the other's barrier
+// of tile k before it can arrive at the barrier of tile k + 2 with the same
+// id, so neither side laps the other.
 #include "bulk.cuh"
 #include "internal.h"
 #include "keep.cuh"
