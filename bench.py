@@ -580,6 +580,31 @@ def profile_compaction(n: int, p: float, predicate: bool = False) -> None:
     print(f"compaction ok at n={n}, p={p}, kept {c}")
 
 
+def profile_segments(n: int, mean: float) -> None:
+    """Two launches of the fp32 inclusive segmented scan at n elements with
+    segments of mean length `mean` (the segment workload's generators), for
+    a profiler to capture; checks sampled segments against the oracle."""
+    import torch
+    import seeded_inputs as si
+    import stream_compaction_pass_gb300 as ss
+    import oracle as orc
+    x = si.uniform_f32(n, seed=96)
+    off = si.segment_offsets(n, mean, seed=98)
+    dx = torch.from_numpy(x).cuda()
+    do = torch.empty_like(dx)
+    doff = torch.from_numpy(off.astype(np.int64)).cuda()
+    for _ in range(2):
+        ss.ss_scan_segments(ss.SS_F32, True, dx, do, doff)
+    torch.cuda.synchronize()
+    got = do.cpu().numpy()
+    for s_ in np.linspace(0, off.size - 2, 5).astype(np.int64):  # whole segments, checked one by one
+        a, b = int(off[s_]), int(off[s_ + 1])
+        ref = orc.scan_f32(x[a:b], True)
+        err = orc.fp32_normalised_error(got[a:b], ref, x[a:b]) if b > a else 0.0
+        assert err <= 1e-4, f"segment {s_} error {err}"
+    print(f"segmented scan ok at n={n}, mean {mean}, {off.size - 1} segments")
+
+
 def profile_f64(n: int) -> None:
     """Two launches of the fp64 inclusive scan at n elements (seeded, values
     24-bit fractions scaled over 2^-10 .. 2^10), for a profiler to capture;
@@ -621,9 +646,15 @@ def main() -> None:
     ap.add_argument("--keep-p", type=float, default=0.5, help="keep probability for --profile-compaction")
     ap.add_argument("--predicate", action="store_true",
                     help="with --profile-compaction: the fp32 v > 0 compaction instead of the flag form")
+    ap.add_argument("--profile-segments", type=int, default=0, metavar="N",
+                    help="only run the fp32 segmented scan twice at n=N (for a profiler) and exit")
+    ap.add_argument("--mean", type=float, default=128256.0, help="mean segment length for --profile-segments")
     ap.add_argument("--profile-f64", type=int, default=0, metavar="N",
                     help="only run the fp64 inclusive scan twice at n=N (for a profiler) and exit")
     args = ap.parse_args()
+    if args.profile_segments:
+        profile_segments(args.profile_segments, args.mean)
+        return
     if args.profile_f64:
         profile_f64(args.profile_f64)
         return

@@ -82,14 +82,17 @@ k_scan_segments(const T* in, T* out, size_t n, const uint32_t* bits, uint32_t nu
                 LookbackCtx ctx) {
     constexpr int STAGES = 3;
     constexpr uint32_t TILE_BYTES = kSTile * (uint32_t)sizeof(T);
+    constexpr uint32_t HEAD_WORDS = kSTile / 32;  // the tile's head bits, one word per 32 elements
     constexpr int VPT = kSVpt;
 
+    // The element ring, then one head-bit area per stage: a full tile's
+    // elements and head words arrive by two bulk copies on one barrier.
     extern __shared__ __align__(128) unsigned char smem_raw[];
     T* ring = reinterpret_cast<T*>(smem_raw);
+    uint32_t* heads = reinterpret_cast<uint32_t*>(smem_raw + (size_t)STAGES * TILE_BYTES);
     __shared__ __align__(8) uint64_t bars[STAGES];
     __shared__ T s_ws[2][kSWarps];         // warp summaries, by tile parity
     __shared__ uint32_t s_wf[2][kSWarps];
-    __shared__ uint32_t s_hw[2][kSThreads];  // the tile's head-bit words (512 x 32 = 16384), by tile parity
     __shared__ T s_prefix[2];
     __shared__ uint32_t s_fail[2], s_rank, s_epoch;
 
@@ -120,9 +123,11 @@ k_scan_segments(const T* in, T* out, size_t n, const uint32_t* bits, uint32_t nu
     auto issue = [&](uint32_t k) {
         const int s = (int)(k % STAGES);
         if (full_tile(k)) {
+            const size_t t = rank + k * G;
             fence_async_shared();
-            mbar_arrive_expect_tx(&bars[s], TILE_BYTES);
-            bulk_load(ring + (size_t)s * kSTile, in + (size_t)(rank + k * G) * kSTile, TILE_BYTES, &bars[s], policy);
+            mbar_arrive_expect_tx(&bars[s], TILE_BYTES + HEAD_WORDS * 4);
+            bulk_load(ring + (size_t)s * kSTile, in + t * kSTile, TILE_BYTES, &bars[s], policy);
+            bulk_load(heads + (size_t)s * HEAD_WORDS, bits + t * HEAD_WORDS, HEAD_WORDS * 4, &bars[s], policy);
         } else {
             mbar_arrive(&bars[s]);  // read from global with bounds checks instead
         }
@@ -163,18 +168,21 @@ k_scan_segments(const T* in, T* out, size_t n, const uint32_t* bits, uint32_t nu
     // its span sums plainly.
     auto reduce_publish = [&](uint32_t k, SegPair<T>* tile_pair, uint32_t* hb_out) -> bool {
         const uint32_t t = rank + k * G;
-        const size_t wbase = ((size_t)t * kSTile) >> 5;  // one head word per thread, coalesced
-        s_hw[k & 1][threadIdx.x] = wbase + threadIdx.x < (n + 31) / 32 ? bits[wbase + threadIdx.x] : 0u;
         const bool ok = mbar_wait_bounded(&bars[k % STAGES], (k / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
         if (__syncthreads_or(!ok)) {
             if (threadIdx.x == 0) record_error(ctx.status, kErrBulkTimeout, t);
             return false;
         }
         uint32_t hb = 0;
+        const bool full = full_tile(k);
+        const uint32_t* hw = heads + (size_t)(k % STAGES) * HEAD_WORDS;
+        const size_t wbase = (size_t)t * HEAD_WORDS;  // the tile's first head word in `bits`
+        const size_t nwords = (n + 31) / 32;
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
             const uint32_t p = warp * kSSeg + (32u * j + lane) * 4;  // element index in the tile
-            hb |= ((s_hw[k & 1][p >> 5] >> (p & 31u)) & 15u) << (4 * j);
+            const uint32_t word = full ? hw[p >> 5] : (wbase + (p >> 5) < nwords ? bits[wbase + (p >> 5)] : 0u);
+            hb |= ((word >> (p & 31u)) & 15u) << (4 * j);
         }
         *hb_out = hb;
         T v[VPT][4];
@@ -334,7 +342,7 @@ k_scan_segments(const T* in, T* out, size_t n, const uint32_t* bits, uint32_t nu
 template <typename T, bool INCL>
 static cudaError_t launch_segments(const void* in, void* out, size_t n, const uint32_t* bits,
                                    const LookbackWs& ws, cudaStream_t s) {
-    constexpr size_t SMEM = 3 * (size_t)kSTile * sizeof(T);
+    constexpr size_t SMEM = 3 * (size_t)kSTile * sizeof(T) + 3 * (size_t)(kSTile / 32) * 4;  // + head words
     auto kern = k_scan_segments<T, INCL>;
     static int sms = 0;
     if (sms == 0) {
@@ -347,7 +355,8 @@ static cudaError_t launch_segments(const void* in, void* out, size_t n, const ui
     }
     const uint32_t tiles = (uint32_t)((n + kSTile - 1) / kSTile);
     const uint32_t grid = tiles < (uint32_t)sms ? tiles : (uint32_t)sms;
-    const bool fast = ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) & 15u) == 0;
+    const bool fast = ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out) |
+                        reinterpret_cast<uintptr_t>(bits)) & 15u) == 0;
     LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};
     kern<<<grid, kSThreads, SMEM, s>>>(static_cast<const T*>(in), static_cast<T*>(out), n, bits, tiles, fast, ctx);
     return cudaGetLastError();
