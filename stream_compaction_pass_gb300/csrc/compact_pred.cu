@@ -218,19 +218,47 @@ k_compact_pred(const uint32_t* keys, uint32_t* out, unsigned long long* d_count,
             }
         }
     };
+    // The lane's key vectors of tile k that hold a kept key (rows with none
+    // are left unread), given the masks from its count.
+    auto load_kept = [&](uint32_t k, const uint32_t (&m)[VPT], uint32_t (&key)[VPT][4]) {
+        const size_t seg = (size_t)(rank + k * G) * TILE + (size_t)warp * SEG;
+        if (full(k)) {
+            const unsigned char* kb =
+                ring + (size_t)(k % STAGES) * kPredStageBytes + ((size_t)warp * SEG + (size_t)lane * 4) * 4;
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                uint4 r = make_uint4(0u, 0u, 0u, 0u);
+                if (m[j]) r = lds_vec(kb + 512 * j);
+                key[j][0] = r.x;
+                key[j][1] = r.y;
+                key[j][2] = r.z;
+                key[j][3] = r.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const size_t i = seg + (size_t)(32 * j + lane) * 4 + e;
+                    key[j][e] = ((m[j] >> e) & 1u) ? keys[i] : 0u;
+                }
+        }
+    };
     // Waits for tile k and counts this warp's kept keys.  The last warp to
     // finish adds the counts up and publishes the tile's aggregate (or, if a
     // warp's copy wait ran out, publishes nothing and sets the tile's stop
     // flag).  No barrier: the warps meet through an arrival tally in shared
     // memory.
-    auto count_tile = [&](uint32_t k) {
+    auto count_tile = [&](uint32_t k, uint32_t (&m)[VPT]) {
         const uint32_t t = rank + k * G;
         const int par = (int)(k & 1);
         const bool ok = __all_sync(kFullMask, mbar_wait_bounded(&bars[k % STAGES], (k / STAGES) & 1u,
                                                                 ctx.max_polls, ctx.timeout_ns));
         uint32_t c = 0;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) m[j] = 0u;
         if (ok) {
-            uint32_t key[VPT][4], m[VPT];
+            uint32_t key[VPT][4];
             load_tile(k, key, m);
 #pragma unroll
             for (int j = 0; j < VPT; ++j) c += (uint32_t)__popc(m[j]);
@@ -319,8 +347,11 @@ k_compact_pred(const uint32_t* keys, uint32_t* out, unsigned long long* d_count,
 
     bool failed = false;
     uint32_t poison_from = 0;  // first of this CTA's tiles (by k) left for thread 0 to poison on failure
+    uint32_t m_cur[VPT], m_next[VPT];  // keep masks of tiles k and k+1, from their counts
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) m_cur[j] = m_next[j] = 0u;
     if (count > 0) {
-        count_tile(0);
+        count_tile(0, m_cur);
         bar_arrive_n(kBarAgg, ALL);  // tile 0 to the look-back warp
     }
     bar_sync_n(kBarCompute, CT);  // tile 0's stop flag is in shared memory
@@ -331,13 +362,16 @@ k_compact_pred(const uint32_t* keys, uint32_t* out, unsigned long long* d_count,
 
     for (uint32_t k = 0; !failed && k < count; ++k) {
         if (k + 1 < count) {  // count tile k+1 and hand it to the look-back warp
-            count_tile(k + 1);
+            count_tile(k + 1, m_next);
             bar_arrive_n(kBarAgg + ((k + 1) & 1), ALL);
         }
 
-        // Rank tile k's kept keys.
+        // Rank tile k's kept keys (masks from its count; only vectors with a
+        // kept key are read again).
         uint32_t key[VPT][4], m[VPT];
-        load_tile(k, key, m);
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) m[j] = m_cur[j];
+        load_kept(k, m, key);
         uint32_t row_run[VPT];
         uint32_t run = 0, c0 = 0;
 #pragma unroll
@@ -376,6 +410,8 @@ k_compact_pred(const uint32_t* keys, uint32_t* out, unsigned long long* d_count,
             poison_from = k + 1;
             break;
         }
+#pragma unroll
+        for (int j2 = 0; j2 < VPT; ++j2) m_cur[j2] = m_next[j2];
     }
 
     if (failed && threadIdx.x == 0) {
