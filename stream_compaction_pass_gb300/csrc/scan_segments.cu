@@ -67,11 +67,44 @@ __device__ __forceinline__ SegPair<T> warp_seg_scan(SegPair<T> p, int lane) {
 
 }  // namespace
 
+// One bit per segment start.  Each thread takes four consecutive offsets
+// (two 16-byte loads when the array is 16-byte aligned, so that more loads
+// are in flight), ORs together the starts that share a 32-bit word (the
+// offsets are sorted, so they are neighbours) and makes one atomic OR per
+// word.
 __global__ void k_segment_heads(const unsigned long long* offsets, size_t num_segments, size_t n, uint32_t* bits) {
-    for (size_t s = (size_t)blockIdx.x * blockDim.x + threadIdx.x; s < num_segments;
-         s += (size_t)gridDim.x * blockDim.x) {
-        const unsigned long long pos = offsets[s];
-        if (pos < n) atomicOr(bits + (pos >> 5), 1u << (pos & 31u));
+    const size_t quads = (num_segments + 3) / 4;
+    const bool vec = (reinterpret_cast<uintptr_t>(offsets) & 15u) == 0;
+    for (size_t q = (size_t)blockIdx.x * blockDim.x + threadIdx.x; q < quads; q += (size_t)gridDim.x * blockDim.x) {
+        const size_t s0 = q * 4;
+        unsigned long long p[4];
+        if (vec && s0 + 4 <= num_segments) {
+            const ulonglong2 a = __ldg(reinterpret_cast<const ulonglong2*>(offsets + s0));
+            const ulonglong2 b = __ldg(reinterpret_cast<const ulonglong2*>(offsets + s0 + 2));
+            p[0] = a.x;
+            p[1] = a.y;
+            p[2] = b.x;
+            p[3] = b.y;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) p[e] = s0 + e < num_segments ? offsets[s0 + e] : (unsigned long long)n;
+        }
+        unsigned long long word = ~0ull;
+        uint32_t acc = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (p[e] >= n) continue;
+            const unsigned long long w = p[e] >> 5;
+            const uint32_t b = 1u << (p[e] & 31u);
+            if (w == word) {
+                acc |= b;
+            } else {
+                if (acc) atomicOr(bits + word, acc);
+                word = w;
+                acc = b;
+            }
+        }
+        if (acc) atomicOr(bits + word, acc);
     }
     if (blockIdx.x == 0 && threadIdx.x == 0 && n > 0) atomicOr(bits, 1u);  // the first element starts a segment
 }
@@ -367,7 +400,7 @@ cudaError_t launch_scan_segments(Dtype dt, bool inclusive, const void* in, void*
                                  const LookbackWs& ws, cudaStream_t s) {
     cudaError_t e = cudaMemsetAsync(bits, 0, ((n + 31) / 32) * 4, s);
     if (e != cudaSuccess) return e;
-    const size_t blocks = (num_segments + 255) / 256;
+    const size_t blocks = ((num_segments + 3) / 4 + 255) / 256;
     const unsigned grid = (unsigned)(blocks == 0 ? 1 : (blocks < 4096 ? blocks : 4096));
     k_segment_heads<<<grid, 256, 0, s>>>(offsets, num_segments, n, bits);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
