@@ -93,6 +93,25 @@ def test_unaligned(ss, offset):
     check(ss, "i32", True, seg_input("i32", n), si.segment_offsets(n, 900.0, seed=99), offset=offset)
 
 
+@pytest.mark.parametrize("mean", [3.5, 40.0])
+def test_offsets_not_16_byte_aligned(ss, mean):
+    # the offsets array starts 8 bytes past a 16-byte boundary: the start
+    # marking reads it element by element instead of in 16-byte pairs
+    import torch
+    n = 300_007
+    x = seg_input("i32", n)
+    offsets = si.segment_offsets(n, mean, seed=101, empty_frac=0.1)
+    buf = torch.zeros(offsets.size + 1, dtype=torch.int64, device="cuda")
+    buf[1:] = torch.from_numpy(offsets.astype(np.int64)).cuda()
+    d_off = buf[1:]
+    assert d_off.data_ptr() % 16 == 8
+    src = torch.from_numpy(x).cuda()
+    dst = torch.empty_like(src)
+    ss.ss_scan_segments(ss.SS_I32, True, src, dst, d_off)
+    assert ss.ss_stream_status()[0] == ss.SS_OK
+    assert_equal(dst.cpu().numpy(), oracle.scan_segments(x, offsets, True), tile=16384)
+
+
 def test_in_place(ss):
     n = 700_001
     check(ss, "u32", False, seg_input("u32", n), si.segment_offsets(n, 2000.0, seed=100), inplace=True)
