@@ -196,10 +196,12 @@ k_scan_rows_warp(const T* in, T* out, size_t rows, size_t cols, bool vec) {
     }
 }
 
-// Persistent form for long rows (at least one 16384-element tile, row
-// starts 16-byte aligned).  It uses the single-register-buffer schedule of
-// the flat scan (scan_pipe.cu): a rank per CTA, tiles rank + k*G, a
-// three-stage bulk-copy ring, and the aggregate one iteration early.
+// Persistent form for long rows (at least 16384 elements, row starts
+// 16-byte aligned).  It uses the single-register-buffer schedule of the flat
+// scan (scan_pipe.cu): a rank per CTA, tiles rank + k*G, a three-stage
+// bulk-copy ring, and the aggregate one iteration early.  A tile is VPT
+// 16-byte vectors per lane (10240 to 18432 elements); the launcher picks VPT
+// per call from the row length.
 // Tiles are numbered row by row, and none crosses a row boundary:
 //  - a row's last tile is shorter, and is fetched by a shorter bulk copy
 //    (its byte count is a multiple of 16 because the row length is a
@@ -209,14 +211,13 @@ k_scan_rows_warp(const T* in, T* out, size_t rows, size_t cols, bool vec) {
 //  - every other tile looks back no further than the row's first tile, or
 //    than this CTA's previous tile when that lies in the same row (its
 //    inclusive prefix is then in hand).
-template <typename T, bool INCLUSIVE>
+template <typename T, bool INCLUSIVE, int VPT>
 __global__ void __launch_bounds__(kRPThreads, 1)
 k_scan_rows_pipe(const T* in, T* out, size_t cols, uint32_t tiles_per_row, uint32_t num_tiles, LookbackCtx ctx) {
     constexpr int STAGES = 3;
-    constexpr int VPT = 8;
     constexpr int WARPS = kRPThreads / 32;
     constexpr uint32_t TILE = (uint32_t)kRPThreads * VPT * 4;
-    static_assert(TILE == kRowsPipeTile, "tile geometry");
+    static_assert(TILE >= kRowsTile, "descriptors are sized for kRowsTile-element tiles");
     constexpr uint32_t SEG = 32u * VPT * 4;
 
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -389,11 +390,12 @@ k_scan_rows_pipe(const T* in, T* out, size_t cols, uint32_t tiles_per_row, uint3
     }
 }
 
-template <typename T, bool INCL>
+template <typename T, bool INCL, int VPT>
 static cudaError_t launch_rows_pipe(const T* in, T* out, size_t rows, size_t cols, const LookbackWs& ws,
                                    cudaStream_t s) {
-    constexpr size_t SMEM = 3 * (size_t)kRowsPipeTile * sizeof(T);
-    auto kern = k_scan_rows_pipe<T, INCL>;
+    constexpr size_t TILE = (size_t)kRPThreads * VPT * 4;
+    constexpr size_t SMEM = 3 * TILE * sizeof(T);
+    auto kern = k_scan_rows_pipe<T, INCL, VPT>;
     static int sms = 0;
     if (sms == 0) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
@@ -403,7 +405,7 @@ static cudaError_t launch_rows_pipe(const T* in, T* out, size_t rows, size_t col
         cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
         sms = v > 0 ? v : 1;
     }
-    const uint32_t tpr = (uint32_t)((cols + kRowsPipeTile - 1) / kRowsPipeTile);
+    const uint32_t tpr = (uint32_t)((cols + TILE - 1) / TILE);
     const uint32_t tiles = (uint32_t)(rows * tpr);
     const uint32_t grid = tiles < (uint32_t)sms ? tiles : (uint32_t)sms;
     LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};
@@ -433,7 +435,18 @@ static cudaError_t launch_rows(const void* in, void* out, size_t rows, size_t co
     }
     if (cols >= kRowsPipeMin && cols % 4 == 0 &&
         ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) & 15u) == 0)
-        return launch_rows_pipe<T, INCL>(pin, pout, rows, cols, ws, s);
+    {
+        // Tiles of 10240, 14336, 16384 or 18432 elements (5, 7, 8 or 9 key
+        // vectors per lane): the fewest tiles per row (fewer look-backs),
+        // and among those the smallest tile (the least padding in a row's
+        // short last tile, so less time per tile).
+        auto tiles_of = [&](size_t vpt) { const size_t tile = (size_t)kRPThreads * vpt * 4; return (cols + tile - 1) / tile; };
+        const size_t fewest = tiles_of(9);
+        if (tiles_of(5) == fewest) return launch_rows_pipe<T, INCL, 5>(pin, pout, rows, cols, ws, s);
+        if (tiles_of(7) == fewest) return launch_rows_pipe<T, INCL, 7>(pin, pout, rows, cols, ws, s);
+        if (tiles_of(8) == fewest) return launch_rows_pipe<T, INCL, 8>(pin, pout, rows, cols, ws, s);
+        return launch_rows_pipe<T, INCL, 9>(pin, pout, rows, cols, ws, s);
+    }
     const uint32_t tpr = (uint32_t)((cols + kRowsTile - 1) / kRowsTile);
     const uint32_t tiles = (uint32_t)(rows * tpr);
     LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};
