@@ -57,8 +57,11 @@ def check(ss, kind, inclusive, x, **kw):
 
 SHAPES = [(1, 1), (1, 5), (3, 7), (1000, 1), (17, 128), (5, 2047), (5, 2048), (5, 2049), (3, 4096),
           (3, 4097), (100, 4095), (64, 32000), (4, 128256), (2, 1_000_003), (1000, 100), (4096, 256),
-          # persistent long-row kernel: one tile per row, a short last tile, many rows per CTA
-          (3, 16384), (5, 16388), (7, 32772), (1, 1 << 20), (300, 20000), (153, 16384 * 3)]
+          # persistent long-row kernel: one tile per row, a short last tile, many rows per CTA;
+          # its tile is chosen from the row length: 10240 (20000), 14336 (40000, 27000),
+          # 16384 (32000, 49152) or 18432 (16388, 32772, 128256, 2^20) elements
+          (3, 16384), (5, 16388), (7, 32772), (1, 1 << 20), (300, 20000), (153, 16384 * 3),
+          (5, 40000), (11, 27000)]
 
 
 @pytest.mark.parametrize("kind", ["i32", "u32", "f32"])
