@@ -245,6 +245,23 @@ def time_region(torch, stream, fn, reps: int, warmup: int = 3) -> float:
     return a.elapsed_time(b) / reps
 
 
+def time_flushed(torch, stream, fn, scratch, reps: int) -> float:
+    """Mean ms of fn() on `stream` with L2 flushed before each call: the
+    scratch buffer (larger than L2) is written between calls, and only fn()
+    is inside the CUDA events."""
+    fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    with torch.cuda.stream(stream):
+        for a, b in ev:
+            scratch.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in ev) / reps
+
+
 def row_rates(torch, ss, stream, dev, xs_d, xf_d, out_d):
     """Secondary rows: every other hot-path row at its own workload, each
     timed with CUDA events (mean of 20 after 3 warm-ups)."""
@@ -318,6 +335,35 @@ def row_rates(torch, ss, stream, dev, xs_d, xf_d, out_d):
                                                    "unordered_frac_on_4n+4k": gbs(alg, ms_u) / peak}
         del xp
     del kout
+    # the small configurations: int32 n = 4096, an inclusive and an exclusive scan per step
+    # (launch latency, not bandwidth), per call from Python and per replay of a captured
+    # graph; fp32 n = 1e6 and 1e7, which fit in L2, warm (back to back) and with L2 flushed
+    x_small = torch.from_numpy(si.workload_int_0_100(4096, seed=0)).to(dev)
+    o_small = torch.empty_like(x_small)
+
+    def small_step():
+        ss.scan_inclusive_i32(x_small, o_small, stream=stream.cuda_stream)
+        ss.scan_exclusive_i32(x_small, o_small, stream=stream.cuda_stream)
+    ms = time_region(torch, stream, small_step, 200)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        small_step()
+    ms_g = time_region(torch, stream, graph.replay, 200)
+    rows["scan_i32_4096_incl_and_excl"] = {"us_per_step": ms * 1e3, "us_per_graph_replay": ms_g * 1e3,
+                                           "note": "two launches per step; bound by launch latency"}
+    del graph, x_small, o_small
+    scratch = torch.empty(80_000_000, dtype=torch.int32, device=dev)  # 320 MB, over twice the L2
+    for nf in (1_000_000, 10_000_000):
+        xf_s = torch.from_numpy(si.workload_f32_unit(nf, seed=1)).to(dev)
+        of_s = torch.empty_like(xf_s)
+        fn = lambda: ss.scan_inclusive_f32(xf_s, of_s, stream=stream.cuda_stream)  # noqa: E731
+        ms_w = time_region(torch, stream, fn, 50)
+        ms_f = time_flushed(torch, stream, fn, scratch, 20)
+        rows[f"scan_f32_incl_{nf}"] = {"ms_warm": ms_w, "ms_l2_flushed": ms_f,
+                                       "GB/s_warm": gbs(8 * nf, ms_w), "GB/s_l2_flushed": gbs(8 * nf, ms_f),
+                                       "frac_l2_flushed": gbs(8 * nf, ms_f) / peak}
+        del xf_s, of_s
+    del scratch
     # MoE counts and 64-aligned offsets: 256 experts, top-8, decode and prefill batch sizes
     for tokens in (4096, 65536, 1 << 20):
         ids = torch.from_numpy(si.topk_ids(tokens, 8, 256, seed=6)).to(dev)

@@ -325,14 +325,18 @@ const char *ss_status_string(ss_status status);
 const char *ss_last_error_detail(void);
 
 /* Elements per tile of the single-pass scan under the current tile
- * configuration, and the number of configurations that can be selected. */
+ * configuration (under the automatic choice, of the row used for large n),
+ * and the number of configurations that can be selected. */
 size_t ss_scan_tile_elems(void);
 int ss_scan_config_count(void);
 
 /* Selects the single-pass scan's tile configuration for later calls in this
  * process (ss_scan_config_count() rows: one CTA per tile, or a persistent
- * grid streaming tiles through a shared-memory ring).  Results do not depend
- * on it, except for the rounding of fp32 sums. */
+ * grid streaming tiles through a shared-memory ring).  -1 (the initial
+ * setting) chooses per call by size: row 7 (16384-element tiles) below 5e7
+ * elements, row 2 (18432) from there on.  Results do not depend on it,
+ * except for the rounding of fp32 sums.  SS_ERR_INVALID_ARG below -1 or
+ * from ss_scan_config_count() on. */
 ss_status ss_set_scan_config(int config);
 
 /* Selects the persistent compaction kernel used for 16-byte aligned inputs

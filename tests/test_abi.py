@@ -135,8 +135,11 @@ def test_config_table(lib):
     for c in range(n):
         ss.ss_set_scan_config(c)
         tiles.append(ss.ss_scan_tile_elems())
-    ss.ss_set_scan_config(2)  # the library's default row
     assert tiles[0] == 4096 and all(t % 128 == 0 for t in tiles)
+    # -1: chosen per call by size; the tile reported is the large-n row's (2)
+    assert lib.ss_set_scan_config(-2) == ss.SS_ERR_INVALID_ARG
+    ss.ss_set_scan_config(-1)
+    assert ss.ss_scan_tile_elems() == tiles[2]
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):

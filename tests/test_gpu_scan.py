@@ -256,3 +256,29 @@ def test_trace_build_scans_and_records(ss, config):
     assert (np.diff(t, axis=1) >= 0).all()        # begin <= aggregate <= published <= resolved <= end
     assert (rec[1:, 5] >= 1).all()                # every tile after the first read a window
     assert (rec[0, 5] == 0)
+
+
+@pytest.mark.parametrize("n", [3_000_017, 49_999_999, 50_000_000, 60_000_001])
+def test_automatic_configuration(ss, n):
+    # the initial setting (-1) picks the 16384-element-tile row below 5e7
+    # elements and the 18432 row from there on; both sides of the switch,
+    # int32 exclusive and fp32 inclusive and exclusive
+    import torch
+    ss.ss_set_scan_config(-1)
+    try:
+        x = sweep_input(SWEEP_MAX)[:n]
+        d_in = torch.from_numpy(x).to("cuda:0")
+        d_out = torch.empty_like(d_in)
+        ss.scan_exclusive_i32(d_in, d_out)
+        assert ss.ss_stream_status()[0] == ss.SS_OK
+        assert_equal(d_out.cpu().numpy(), sweep_reference(SWEEP_MAX)[:n], 16384)
+        f = si.workload_f32_unit(n, seed=1)
+        d_f = torch.from_numpy(f).to("cuda:0")
+        d_g = torch.empty_like(d_f)
+        for inclusive in (True, False):
+            (ss.scan_inclusive_f32 if inclusive else ss.scan_exclusive_f32)(d_f, d_g)
+            assert ss.ss_stream_status()[0] == ss.SS_OK
+            err = oracle.fp32_normalised_error(d_g.cpu().numpy(), oracle.scan_f32(f, inclusive), f)
+            assert err <= 1e-4, f"fp32 error {err:.3e} (inclusive={inclusive})"
+    finally:
+        ss.ss_set_scan_config(DEFAULT_CONFIG)
