@@ -364,6 +364,20 @@ def row_rates(torch, ss, stream, dev, xs_d, xf_d, out_d):
                                        "frac_l2_flushed": gbs(8 * nf, ms_f) / peak}
         del xf_s, of_s
     del scratch
+    # int32 exclusive across sizes, 2^20 .. 2^30 (inputs from a seeded on-device generator, in
+    # [-1000, 1000]: integer adds take the same time whatever the values)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(2)
+    sweep = {}
+    for lg in (20, 24, 27, 30):
+        ns = 1 << lg
+        xi = torch.randint(-1000, 1001, (ns,), dtype=torch.int32, device=dev, generator=gen)
+        oi = torch.empty_like(xi)
+        ms = time_region(torch, stream, lambda: ss.scan_exclusive_i32(xi, oi, stream=stream.cuda_stream),
+                         20 if lg < 30 else 5)
+        sweep[f"2^{lg}"] = {"ms": ms, "G-elem/s": ns / ms / 1e6, "frac": gbs(8 * ns, ms) / peak}
+        del xi, oi
+    rows["scan_i32_excl_size_sweep"] = sweep
     # MoE counts and 64-aligned offsets: 256 experts, top-8, decode and prefill batch sizes
     for tokens in (4096, 65536, 1 << 20):
         ids = torch.from_numpy(si.topk_ids(tokens, 8, 256, seed=6)).to(dev)
