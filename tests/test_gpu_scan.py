@@ -282,3 +282,24 @@ def test_automatic_configuration(ss, n):
             assert err <= 1e-4, f"fp32 error {err:.3e} (inclusive={inclusive})"
     finally:
         ss.ss_set_scan_config(DEFAULT_CONFIG)
+
+
+def test_automatic_configuration_carries_between_chunks(ss):
+    # under the automatic choice, chunks below the switch take the
+    # 16384-element-tile row: a carried prefix must chain through it
+    import torch
+    ss.ss_set_scan_config(-1)
+    try:
+        n = 7_000_003
+        x = sweep_input(SWEEP_MAX)[:n]
+        d_in = torch.from_numpy(x).to("cuda:0")
+        d_out = torch.empty_like(d_in)
+        carry = torch.zeros(1, dtype=torch.int32, device="cuda:0")
+        bounds = [0, 1_000_001, 4_500_000, n]
+        for a, b in zip(bounds[:-1], bounds[1:]):
+            ss.ss_scan_seeded(ss.SS_I32, False, d_in[a:b], d_out[a:b], carry, carry)
+        assert ss.ss_stream_status()[0] == ss.SS_OK
+        assert_equal(d_out.cpu().numpy(), sweep_reference(SWEEP_MAX)[:n], 16384)
+        assert int(carry.item()) == int(oracle.scan_i32(x, True)[-1])
+    finally:
+        ss.ss_set_scan_config(DEFAULT_CONFIG)
