@@ -60,7 +60,6 @@ template <> __device__ __forceinline__ unsigned long long widen<unsigned long lo
     unsigned long long x) {
     return x;
 }
-template <> __device__ __forceinline__ double widen<double, double>(double x) { return x; }
 
 // A lane's two consecutive input elements from shared memory.
 template <typename TI>
@@ -382,9 +381,10 @@ k_scan_f64_blocked(const double* in, double* out, size_t n, uint32_t num_tiles, 
     constexpr uint32_t BOX_ROWS = ROWS < 256 ? ROWS : 256;  // rows per tensor load (at most 256)
     static_assert(SEG * WARPS == TILE && ROWS == THREADS && ROWS % BOX_ROWS == 0, "tile geometry");
 
-    // STAGES x 64 KB ring, then the 64 KB output area; the swizzled copies
-    // want 1024-byte aligned areas.
-    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // STAGES x 64 KB ring, then the 64 KB output area.  The swizzled copies
+    // want 1024-byte aligned areas: the start is rounded up here, into the
+    // 1 KB of slack the launch adds.
+    extern __shared__ __align__(128) unsigned char smem_raw[];
     double* ring = reinterpret_cast<double*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
     double* stage_out = ring + (size_t)STAGES * TILE;
     __shared__ __align__(8) uint64_t bars[STAGES];
