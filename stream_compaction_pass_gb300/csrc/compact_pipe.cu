@@ -35,6 +35,17 @@ __device__ __forceinline__ uint32_t byte_keep_mask(uint32_t w) {
            ((w & 0x00ff0000u) ? 4u : 0u) | ((w & 0xff000000u) ? 8u : 0u);
 }
 
+// A 16-byte key vector through the read-only path: no L1 allocation, and a
+// 256-byte L2 fetch around the miss (neighbouring vectors are usually wanted
+// too when the flags are dense).
+__device__ __forceinline__ uint4 ld_key_vec(const uint4* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t lds_u32(const void* p) {
     uint32_t r;
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(smem_u32(p)) : "memory");
@@ -592,7 +603,7 @@ k_compact_chunked(const uint32_t* keys, const uint8_t* flags, uint32_t* out, uns
 #pragma unroll
             for (int j = 0; j < VPT; ++j) {
                 uint4 r = make_uint4(0u, 0u, 0u, 0u);
-                if (m[j]) r = ld_vec(kp + 32 * j);
+                if (m[j]) r = ld_key_vec(kp + 32 * j);
                 key[j][0] = r.x;
                 key[j][1] = r.y;
                 key[j][2] = r.z;
