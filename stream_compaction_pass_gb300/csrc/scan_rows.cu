@@ -153,6 +153,7 @@ k_scan_rows_warp(const T* in, T* out, size_t rows, size_t cols, bool vec) {
             T v[kRSteps][4];
 #pragma unroll
             for (int u = 0; u < kRSteps; ++u) {
+                if (c0 + (size_t)u * 128 >= cols) break;  // past the row's end: a short row's last steps
                 const size_t b = c0 + (size_t)u * 128 + (size_t)lane * 4;
                 if (vec && b + 4 <= cols) {
                     const uint4 q = ld_vec(reinterpret_cast<const uint4*>(rin + b));
@@ -167,6 +168,7 @@ k_scan_rows_warp(const T* in, T* out, size_t rows, size_t cols, bool vec) {
             }
 #pragma unroll
             for (int u = 0; u < kRSteps; ++u) {
+                if (c0 + (size_t)u * 128 >= cols) break;
                 const T s = ((v[u][0] + v[u][1]) + v[u][2]) + v[u][3];
                 const T inc = warp_inclusive_scan<T>(s, lane);
                 T run = carry + (inc - s);
