@@ -14,11 +14,12 @@
 //     tile publishes its inclusive prefix at once; the others look back no
 //     further than it (the floor is the row's start, with prefix 0).  So the
 //     rows' chains are independent, and one launch covers every row.
-//   - Shorter rows take one warp each.  The warp walks its row in steps of
-//     512 elements (four 128-element chunks, one 16-byte vector per lane
-//     each).  Each chunk is a lane-local scan of 4 and a shuffle scan across
-//     the warp; the running total carries from chunk to chunk.  No workspace
-//     and no look-back.
+//   - Rows of up to kRowsWarpMax elements take one warp each.  The warp
+//     walks its row in steps of 512 elements (four 128-element chunks, one
+//     16-byte vector per lane each).  Each chunk is a lane-local scan of 4
+//     and a shuffle scan across the warp; the running total carries from
+//     chunk to chunk.  Rows of at most 64 elements share a warp several at a
+//     time instead (k_scan_rows_packed).  No workspace and no look-back.
 // Rows whose start is not 16-byte aligned (cols not a multiple of 4, or an
 // unaligned base) are read and written element by element with bounds checks.
 #include "bulk.cuh"
@@ -194,6 +195,65 @@ k_scan_rows_warp(const T* in, T* out, size_t rows, size_t cols, bool vec) {
                         if (b + e < cols) rout[b + e] = y[e];
                 }
             }
+        }
+    }
+}
+
+// Rows of at most 64 elements, packed: a row gets L lanes (L = cols / 4
+// rounded up to a power of two, at most 16), each holding one vector of 4
+// consecutive elements, and a warp takes 32 / L consecutive rows per step
+// (they are contiguous in memory, so its loads stay coalesced).  The lane
+// scan and a shuffle scan of width L inside each lane group give every
+// output; no carry, since a row fits in one step.
+template <typename T, bool INCLUSIVE, int L>
+__global__ void __launch_bounds__(kRThreads)
+k_scan_rows_packed(const T* in, T* out, size_t rows, size_t cols, bool vec) {
+    constexpr int R = 32 / L;  // rows per warp step
+    const int lane = threadIdx.x & 31;
+    const int li = lane % L;   // lane inside its row's group
+    const size_t gw = ((size_t)blockIdx.x * kRThreads + threadIdx.x) >> 5;
+    const size_t nw = ((size_t)gridDim.x * kRThreads) >> 5;
+    for (size_t rg = gw; rg * R < rows; rg += nw) {  // warp-uniform
+        const size_t r = rg * R + (size_t)(lane / L);
+        const bool live = r < rows;
+        const size_t b = (size_t)li * 4;  // first element of this lane in its row
+        T v[4];
+        if (live && vec && b + 4 <= cols) {
+            const uint4 q = ld_vec(reinterpret_cast<const uint4*>(in + r * cols + b));
+            v[0] = from_bits<T>(q.x);
+            v[1] = from_bits<T>(q.y);
+            v[2] = from_bits<T>(q.z);
+            v[3] = from_bits<T>(q.w);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[e] = live && b + e < cols ? in[r * cols + b + e] : T(0);
+        }
+        const T sum = ((v[0] + v[1]) + v[2]) + v[3];
+        T inc = sum;
+#pragma unroll
+        for (int d = 1; d < L; d <<= 1) {
+            const T t = __shfl_up_sync(kFullMask, inc, d, L);
+            if (li >= d) inc += t;
+        }
+        T run = inc - sum;
+        T y[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (INCLUSIVE) {
+                run += v[e];
+                y[e] = run;
+            } else {
+                y[e] = run;
+                run += v[e];
+            }
+        }
+        if (live && vec && b + 4 <= cols) {
+            st_vec(reinterpret_cast<uint4*>(out + r * cols + b),
+                   make_uint4(to_bits<T>(y[0]), to_bits<T>(y[1]), to_bits<T>(y[2]), to_bits<T>(y[3])));
+        } else if (live) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (b + e < cols) out[r * cols + b + e] = y[e];
         }
     }
 }
@@ -429,8 +489,21 @@ static cudaError_t launch_rows(const void* in, void* out, size_t rows, size_t co
     T* pout = static_cast<T*>(out);
     if (cols <= kRowsWarpMax) {
         const bool vec = cols % 4 == 0 && ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) & 15u) == 0;
-        const size_t want = (rows + kRWarps - 1) / kRWarps;
         const size_t cap = (size_t)sms * (2048 / kRThreads);
+        if (cols <= 64) {  // several rows per warp
+            const int L = cols <= 4 ? 1 : cols <= 8 ? 2 : cols <= 16 ? 4 : cols <= 32 ? 8 : 16;
+            const size_t want = (rows + (size_t)kRWarps * (32 / L) - 1) / ((size_t)kRWarps * (32 / L));
+            const unsigned grid = (unsigned)(want < cap ? want : cap);
+            switch (L) {
+                case 1: k_scan_rows_packed<T, INCL, 1><<<grid, kRThreads, 0, s>>>(pin, pout, rows, cols, vec); break;
+                case 2: k_scan_rows_packed<T, INCL, 2><<<grid, kRThreads, 0, s>>>(pin, pout, rows, cols, vec); break;
+                case 4: k_scan_rows_packed<T, INCL, 4><<<grid, kRThreads, 0, s>>>(pin, pout, rows, cols, vec); break;
+                case 8: k_scan_rows_packed<T, INCL, 8><<<grid, kRThreads, 0, s>>>(pin, pout, rows, cols, vec); break;
+                default: k_scan_rows_packed<T, INCL, 16><<<grid, kRThreads, 0, s>>>(pin, pout, rows, cols, vec); break;
+            }
+            return cudaGetLastError();
+        }
+        const size_t want = (rows + kRWarps - 1) / kRWarps;
         const unsigned grid = (unsigned)(want < cap ? want : cap);
         k_scan_rows_warp<T, INCL><<<grid, kRThreads, 0, s>>>(pin, pout, rows, cols, vec);
         return cudaGetLastError();

@@ -61,7 +61,11 @@ SHAPES = [(1, 1), (1, 5), (3, 7), (1000, 1), (17, 128), (5, 2047), (5, 2048), (5
           # its tile is chosen from the row length: 10240 (20000), 14336 (40000, 27000),
           # 16384 (32000, 49152) or 18432 (16388, 32772, 128256, 2^20) elements
           (3, 16384), (5, 16388), (7, 32772), (1, 1 << 20), (300, 20000), (153, 16384 * 3),
-          (5, 40000), (11, 27000)]
+          (5, 40000), (11, 27000),
+          # rows of at most 64 elements, several to a warp (lanes per row 1, 2, 4, 8, 16),
+          # lengths that are and are not multiples of 4, row counts that leave a warp's
+          # last group short
+          (5001, 4), (3001, 3), (2001, 8), (999, 17), (1000, 33), (777, 64), (4097, 61), (70001, 2)]
 
 
 @pytest.mark.parametrize("kind", ["i32", "u32", "f32"])
@@ -78,7 +82,7 @@ def test_bench_shapes(ss, shape):
     check(ss, "i32", False, rows_input("i32", *shape))
 
 
-@pytest.mark.parametrize("shape", [(9, 5000), (33, 300), (7, 2051), (5, 40000)])
+@pytest.mark.parametrize("shape", [(9, 5000), (33, 300), (7, 2051), (5, 40000), (1001, 20), (513, 64)])
 @pytest.mark.parametrize("offset", [1, 3])
 def test_unaligned(ss, shape, offset):
     check(ss, "i32", True, rows_input("i32", *shape), offset=offset)
