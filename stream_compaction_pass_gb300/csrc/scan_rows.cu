@@ -18,8 +18,9 @@
 //     walks its row in steps of 512 elements (four 128-element chunks, one
 //     16-byte vector per lane each).  Each chunk is a lane-local scan of 4
 //     and a shuffle scan across the warp; the running total carries from
-//     chunk to chunk.  Rows of at most 64 elements share a warp several at a
-//     time instead (k_scan_rows_packed).  No workspace and no look-back.
+//     chunk to chunk.  Rows of at most 224 elements take one step instead,
+//     several rows to a warp up to 128 elements (k_scan_rows_packed).  No
+//     workspace and no look-back.
 // Rows whose start is not 16-byte aligned (cols not a multiple of 4, or an
 // unaligned base) are read and written element by element with bounds checks.
 #include "bulk.cuh"
@@ -199,15 +200,16 @@ k_scan_rows_warp(const T* in, T* out, size_t rows, size_t cols, bool vec) {
     }
 }
 
-// Rows of at most 64 elements, packed: a row gets L lanes (L = cols / 4
-// rounded up to a power of two, at most 16), each holding one vector of 4
-// consecutive elements, and a warp takes 32 / L consecutive rows per step
-// (they are contiguous in memory, so its loads stay coalesced).  The lane
-// scan and a shuffle scan of width L inside each lane group give every
-// output; no carry, since a row fits in one step.
-template <typename T, bool INCLUSIVE, int L>
+// Rows of at most 224 elements, packed: a row gets L lanes, each holding
+// EPL consecutive elements (one or two 16-byte vectors), with L * EPL the
+// smallest power of two that covers the row; a warp takes 32 / L consecutive
+// rows per step (they are contiguous in memory, so its loads stay
+// coalesced).  The lane scan and a shuffle scan of width L inside each lane
+// group give every output; no carry, since a row fits in one step.
+template <typename T, bool INCLUSIVE, int L, int EPL>
 __global__ void __launch_bounds__(kRThreads)
 k_scan_rows_packed(const T* in, T* out, size_t rows, size_t cols, bool vec) {
+    static_assert(EPL == 4 || EPL == 8, "one or two 16-byte vectors per lane");
     constexpr int R = 32 / L;  // rows per warp step
     const int lane = threadIdx.x & 31;
     const int li = lane % L;   // lane inside its row's group
@@ -216,19 +218,25 @@ k_scan_rows_packed(const T* in, T* out, size_t rows, size_t cols, bool vec) {
     for (size_t rg = gw; rg * R < rows; rg += nw) {  // warp-uniform
         const size_t r = rg * R + (size_t)(lane / L);
         const bool live = r < rows;
-        const size_t b = (size_t)li * 4;  // first element of this lane in its row
-        T v[4];
-        if (live && vec && b + 4 <= cols) {
-            const uint4 q = ld_vec(reinterpret_cast<const uint4*>(in + r * cols + b));
-            v[0] = from_bits<T>(q.x);
-            v[1] = from_bits<T>(q.y);
-            v[2] = from_bits<T>(q.z);
-            v[3] = from_bits<T>(q.w);
-        } else {
+        const size_t b = (size_t)li * EPL;  // first element of this lane in its row
+        T v[EPL];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) v[e] = live && b + e < cols ? in[r * cols + b + e] : T(0);
+        for (int h = 0; h < EPL / 4; ++h) {
+            const size_t bh = b + 4 * h;
+            if (live && vec && bh + 4 <= cols) {
+                const uint4 q = ld_vec(reinterpret_cast<const uint4*>(in + r * cols + bh));
+                v[4 * h + 0] = from_bits<T>(q.x);
+                v[4 * h + 1] = from_bits<T>(q.y);
+                v[4 * h + 2] = from_bits<T>(q.z);
+                v[4 * h + 3] = from_bits<T>(q.w);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) v[4 * h + e] = live && bh + e < cols ? in[r * cols + bh + e] : T(0);
+            }
         }
-        const T sum = ((v[0] + v[1]) + v[2]) + v[3];
+        T sum = T(0);
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) sum += v[e];
         T inc = sum;
 #pragma unroll
         for (int d = 1; d < L; d <<= 1) {
@@ -236,9 +244,9 @@ k_scan_rows_packed(const T* in, T* out, size_t rows, size_t cols, bool vec) {
             if (li >= d) inc += t;
         }
         T run = inc - sum;
-        T y[4];
+        T y[EPL];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
+        for (int e = 0; e < EPL; ++e) {
             if (INCLUSIVE) {
                 run += v[e];
                 y[e] = run;
@@ -247,13 +255,18 @@ k_scan_rows_packed(const T* in, T* out, size_t rows, size_t cols, bool vec) {
                 run += v[e];
             }
         }
-        if (live && vec && b + 4 <= cols) {
-            st_vec(reinterpret_cast<uint4*>(out + r * cols + b),
-                   make_uint4(to_bits<T>(y[0]), to_bits<T>(y[1]), to_bits<T>(y[2]), to_bits<T>(y[3])));
-        } else if (live) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (b + e < cols) out[r * cols + b + e] = y[e];
+        for (int h = 0; h < EPL / 4; ++h) {
+            const size_t bh = b + 4 * h;
+            if (live && vec && bh + 4 <= cols) {
+                st_vec(reinterpret_cast<uint4*>(out + r * cols + bh),
+                       make_uint4(to_bits<T>(y[4 * h]), to_bits<T>(y[4 * h + 1]), to_bits<T>(y[4 * h + 2]),
+                                  to_bits<T>(y[4 * h + 3])));
+            } else if (live) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (bh + e < cols) out[r * cols + bh + e] = y[4 * h + e];
+            }
         }
     }
 }
@@ -490,16 +503,27 @@ static cudaError_t launch_rows(const void* in, void* out, size_t rows, size_t co
     if (cols <= kRowsWarpMax) {
         const bool vec = cols % 4 == 0 && ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) & 15u) == 0;
         const size_t cap = (size_t)sms * (2048 / kRThreads);
-        if (cols <= 64) {  // several rows per warp
-            const int L = cols <= 4 ? 1 : cols <= 8 ? 2 : cols <= 16 ? 4 : cols <= 32 ? 8 : 16;
-            const size_t want = (rows + (size_t)kRWarps * (32 / L) - 1) / ((size_t)kRWarps * (32 / L));
+        if (cols <= 224) {  // one step per row: several rows per warp up to 128 elements
+            // lanes per row and elements per lane: 4 per lane up to 64 elements, then 8.
+            // From about 224 elements the warp kernel's two full 512-byte steps per
+            // row beat one step whose stores cover 16 bytes in every 32.
+            const int L = cols <= 4 ? 1 : cols <= 8 ? 2 : cols <= 16 ? 4 : cols <= 32 ? 8 : cols <= 64 ? 16
+                        : cols <= 128 ? 16 : 32;
+            const size_t per_cta = (size_t)kRWarps * (32 / L);
+            const size_t want = (rows + per_cta - 1) / per_cta;
             const unsigned grid = (unsigned)(want < cap ? want : cap);
-            switch (L) {
-                case 1: k_scan_rows_packed<T, INCL, 1><<<grid, kRThreads, 0, s>>>(pin, pout, rows, cols, vec); break;
-                case 2: k_scan_rows_packed<T, INCL, 2><<<grid, kRThreads, 0, s>>>(pin, pout, rows, cols, vec); break;
-                case 4: k_scan_rows_packed<T, INCL, 4><<<grid, kRThreads, 0, s>>>(pin, pout, rows, cols, vec); break;
-                case 8: k_scan_rows_packed<T, INCL, 8><<<grid, kRThreads, 0, s>>>(pin, pout, rows, cols, vec); break;
-                default: k_scan_rows_packed<T, INCL, 16><<<grid, kRThreads, 0, s>>>(pin, pout, rows, cols, vec); break;
+            if (cols <= 64) {
+                switch (L) {
+                    case 1: k_scan_rows_packed<T, INCL, 1, 4><<<grid, kRThreads, 0, s>>>(pin, pout, rows, cols, vec); break;
+                    case 2: k_scan_rows_packed<T, INCL, 2, 4><<<grid, kRThreads, 0, s>>>(pin, pout, rows, cols, vec); break;
+                    case 4: k_scan_rows_packed<T, INCL, 4, 4><<<grid, kRThreads, 0, s>>>(pin, pout, rows, cols, vec); break;
+                    case 8: k_scan_rows_packed<T, INCL, 8, 4><<<grid, kRThreads, 0, s>>>(pin, pout, rows, cols, vec); break;
+                    default: k_scan_rows_packed<T, INCL, 16, 4><<<grid, kRThreads, 0, s>>>(pin, pout, rows, cols, vec); break;
+                }
+            } else if (L == 16) {
+                k_scan_rows_packed<T, INCL, 16, 8><<<grid, kRThreads, 0, s>>>(pin, pout, rows, cols, vec);
+            } else {
+                k_scan_rows_packed<T, INCL, 32, 8><<<grid, kRThreads, 0, s>>>(pin, pout, rows, cols, vec);
             }
             return cudaGetLastError();
         }

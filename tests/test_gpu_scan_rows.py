@@ -65,7 +65,11 @@ SHAPES = [(1, 1), (1, 5), (3, 7), (1000, 1), (17, 128), (5, 2047), (5, 2048), (5
           # rows of at most 64 elements, several to a warp (lanes per row 1, 2, 4, 8, 16),
           # lengths that are and are not multiples of 4, row counts that leave a warp's
           # last group short
-          (5001, 4), (3001, 3), (2001, 8), (999, 17), (1000, 33), (777, 64), (4097, 61), (70001, 2)]
+          (5001, 4), (3001, 3), (2001, 8), (999, 17), (1000, 33), (777, 64), (4097, 61), (70001, 2),
+          # rows of 65-224 elements take one step each with two vectors per lane; 225 and
+          # longer go back to one warp per row
+          (2001, 65), (999, 128), (1001, 129), (777, 200), (501, 224), (502, 225), (333, 250),
+          (1000, 255)]
 
 
 @pytest.mark.parametrize("kind", ["i32", "u32", "f32"])
