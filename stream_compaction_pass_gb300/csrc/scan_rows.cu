@@ -201,72 +201,81 @@ k_scan_rows_warp(const T* in, T* out, size_t rows, size_t cols, bool vec) {
 }
 
 // Rows of at most 224 elements, packed: a row gets L lanes, each holding
-// EPL consecutive elements (one or two 16-byte vectors), with L * EPL the
-// smallest power of two that covers the row; a warp takes 32 / L consecutive
-// rows per step (they are contiguous in memory, so its loads stay
-// coalesced).  The lane scan and a shuffle scan of width L inside each lane
-// group give every output; no carry, since a row fits in one step.
+// EPL / 4 16-byte vectors, with L * EPL the smallest power of two that
+// covers the row; a warp takes 32 / L consecutive rows per step (they are
+// contiguous in memory, so its loads stay coalesced).  Vector h of lane i in
+// a group holds elements h * 4L + 4i .. h * 4L + 4i + 3, so that each load
+// and store instruction covers whole 4L-element runs of a row.  The lane
+// scan and a shuffle scan of width L per vector give every output, the
+// first vector's group total carried into the second; no carry between
+// steps, since a row fits in one step.
 template <typename T, bool INCLUSIVE, int L, int EPL>
 __global__ void __launch_bounds__(kRThreads)
 k_scan_rows_packed(const T* in, T* out, size_t rows, size_t cols, bool vec) {
     static_assert(EPL == 4 || EPL == 8, "one or two 16-byte vectors per lane");
-    constexpr int R = 32 / L;  // rows per warp step
+    constexpr int R = 32 / L;   // rows per warp step
+    constexpr int H = EPL / 4;  // vectors per lane
     const int lane = threadIdx.x & 31;
-    const int li = lane % L;   // lane inside its row's group
+    const int li = lane % L;    // lane inside its row's group
     const size_t gw = ((size_t)blockIdx.x * kRThreads + threadIdx.x) >> 5;
     const size_t nw = ((size_t)gridDim.x * kRThreads) >> 5;
     for (size_t rg = gw; rg * R < rows; rg += nw) {  // warp-uniform
         const size_t r = rg * R + (size_t)(lane / L);
         const bool live = r < rows;
-        const size_t b = (size_t)li * EPL;  // first element of this lane in its row
-        T v[EPL];
+        T v[H][4];
 #pragma unroll
-        for (int h = 0; h < EPL / 4; ++h) {
-            const size_t bh = b + 4 * h;
+        for (int h = 0; h < H; ++h) {
+            const size_t bh = (size_t)h * 4 * L + (size_t)li * 4;  // first element of vector h in its row
             if (live && vec && bh + 4 <= cols) {
                 const uint4 q = ld_vec(reinterpret_cast<const uint4*>(in + r * cols + bh));
-                v[4 * h + 0] = from_bits<T>(q.x);
-                v[4 * h + 1] = from_bits<T>(q.y);
-                v[4 * h + 2] = from_bits<T>(q.z);
-                v[4 * h + 3] = from_bits<T>(q.w);
+                v[h][0] = from_bits<T>(q.x);
+                v[h][1] = from_bits<T>(q.y);
+                v[h][2] = from_bits<T>(q.z);
+                v[h][3] = from_bits<T>(q.w);
             } else {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) v[4 * h + e] = live && bh + e < cols ? in[r * cols + bh + e] : T(0);
+                for (int e = 0; e < 4; ++e) v[h][e] = live && bh + e < cols ? in[r * cols + bh + e] : T(0);
             }
         }
-        T sum = T(0);
+        T sum[H], inc[H];
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) sum += v[e];
-        T inc = sum;
+        for (int h = 0; h < H; ++h) {
+            sum[h] = ((v[h][0] + v[h][1]) + v[h][2]) + v[h][3];
+            inc[h] = sum[h];
+        }
 #pragma unroll
         for (int d = 1; d < L; d <<= 1) {
-            const T t = __shfl_up_sync(kFullMask, inc, d, L);
-            if (li >= d) inc += t;
-        }
-        T run = inc - sum;
-        T y[EPL];
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) {
-            if (INCLUSIVE) {
-                run += v[e];
-                y[e] = run;
-            } else {
-                y[e] = run;
-                run += v[e];
+            for (int h = 0; h < H; ++h) {
+                const T t = __shfl_up_sync(kFullMask, inc[h], d, L);
+                if (li >= d) inc[h] += t;
             }
         }
+        T carry = T(0);
 #pragma unroll
-        for (int h = 0; h < EPL / 4; ++h) {
-            const size_t bh = b + 4 * h;
+        for (int h = 0; h < H; ++h) {
+            T run = carry + (inc[h] - sum[h]);
+            T y[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (INCLUSIVE) {
+                    run += v[h][e];
+                    y[e] = run;
+                } else {
+                    y[e] = run;
+                    run += v[h][e];
+                }
+            }
+            const size_t bh = (size_t)h * 4 * L + (size_t)li * 4;
             if (live && vec && bh + 4 <= cols) {
                 st_vec(reinterpret_cast<uint4*>(out + r * cols + bh),
-                       make_uint4(to_bits<T>(y[4 * h]), to_bits<T>(y[4 * h + 1]), to_bits<T>(y[4 * h + 2]),
-                                  to_bits<T>(y[4 * h + 3])));
+                       make_uint4(to_bits<T>(y[0]), to_bits<T>(y[1]), to_bits<T>(y[2]), to_bits<T>(y[3])));
             } else if (live) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    if (bh + e < cols) out[r * cols + bh + e] = y[4 * h + e];
+                    if (bh + e < cols) out[r * cols + bh + e] = y[e];
             }
+            if (h + 1 < H) carry += __shfl_sync(kFullMask, inc[h], L - 1, L);  // the group's total of vector h
         }
     }
 }
@@ -505,8 +514,7 @@ static cudaError_t launch_rows(const void* in, void* out, size_t rows, size_t co
         const size_t cap = (size_t)sms * (2048 / kRThreads);
         if (cols <= 224) {  // one step per row: several rows per warp up to 128 elements
             // lanes per row and elements per lane: 4 per lane up to 64 elements, then 8.
-            // From about 224 elements the warp kernel's two full 512-byte steps per
-            // row beat one step whose stores cover 16 bytes in every 32.
+            // From about 224 elements on, the warp kernel is as fast.
             const int L = cols <= 4 ? 1 : cols <= 8 ? 2 : cols <= 16 ? 4 : cols <= 32 ? 8 : cols <= 64 ? 16
                         : cols <= 128 ? 16 : 32;
             const size_t per_cta = (size_t)kRWarps * (32 / L);
