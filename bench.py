@@ -40,10 +40,8 @@ BYTES_PER_ELEM = 8  # one 4-byte read + one 4-byte write
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 VARIANTS = [("i32", False), ("i32", True), ("f32", False), ("f32", True)]
-DATA = ("synthetic: seeded SplitMix64 counter streams; int32 uniform in [-1000, 1000] "
-        "(seed 2) and fp32 uniform in [0, 1) (seed 1)")
-WORKLOAD = ("device-wide scan, n=1e8 per launch; one step = int32 exclusive + inclusive "
-            "and fp32 exclusive + inclusive (4 launches)")
+DATA = "synthetic, seeded SplitMix64: int32 U[-1000,1000] (seed 2), fp32 U[0,1) (seed 1)"
+WORKLOAD = "scan n=1e8; step = int32 excl+incl, fp32 excl+incl (4 launches)"
 KERNEL_SOURCES = ["stream_compaction_pass_gb300/csrc/scan_pipe.cu", "stream_compaction_pass_gb300/csrc/scan.cu",
                   "stream_compaction_pass_gb300/csrc/scan_body.cuh", "stream_compaction_pass_gb300/csrc/tile.cuh",
                   "stream_compaction_pass_gb300/csrc/lookback.cuh", "stream_compaction_pass_gb300/csrc/bulk.cuh"]
@@ -74,7 +72,7 @@ def whole_job_rate(elems_per_rank: int, world: int, max_elapsed_ms: float) -> fl
 
 
 def emit(obj) -> None:
-    print(json.dumps(obj), flush=True)
+    print(json.dumps(obj, separators=(",", ":")), flush=True)
 
 
 # --------------------------------------------------------------------------
@@ -85,7 +83,7 @@ def measured_hbm_peak():
     try:
         with open(path) as f:
             v = float(json.load(f)["hbm_gbs"])
-        return v, "measured (MEASURED_PEAKS.json hbm_gbs, burst copy)"
+        return v, "measured (MEASURED_PEAKS.json hbm_gbs)"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 copy measurement)"
 
@@ -113,16 +111,44 @@ def recorded_traffic():
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    """SM clock and clock-event (throttle) reasons, sampled every ~1 ms by a
+    thread while the timed region runs.  Reads NVML directly (read-only
+    queries; the timed region is a few ms, shorter than nvidia-smi's first
+    sample); falls back to nvidia-smi at 100 ms if NVML cannot be loaded."""
 
+    # NVML clock-event reason bits (nvmlClocksEventReason*)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_id: str | None):
+        import threading
         self.proc = None
+        self.nvml = None
+        self.samples = []  # (sm_mhz, reasons bitmask)
+        self.max_mhz = None
         if gpu_id is None:
             return
+        try:
+            import ctypes
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByUUID(gpu_id.encode(), ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle for this GPU")
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # NVML_CLOCK_SM
+                self.max_mhz = float(mx.value)
+            self.nvml, self.handle = nv, h
+            self.stop_flag = threading.Event()
+            self.thread = threading.Thread(target=self._run_nvml, daemon=True)
+            self.thread.start()
+            return
+        except Exception:
+            self.nvml = None
         try:
             import tempfile
             fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
@@ -133,10 +159,31 @@ class ClockSampler:
         except Exception:
             self.proc = None
 
+    def _run_nvml(self):
+        import ctypes
+        clk, rsn = ctypes.c_uint(), ctypes.c_ulonglong()
+        get_reasons = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self.stop_flag.is_set():
+            if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(clk)) == 0 and \
+                    get_reasons(self.handle, ctypes.byref(rsn)) == 0:
+                self.samples.append((float(clk.value), int(rsn.value)))
+            time.sleep(0.001)
+
     def stop(self):
+        if self.nvml is not None:
+            self.stop_flag.set()
+            self.thread.join(timeout=5)
+            reasons = set()
+            for _mhz, bits in self.samples:
+                for bit, name in self.REASONS.items():
+                    if bits & bit:
+                        reasons.add(name)
+            sm = [m for m, _b in self.samples]
+            return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                    "reasons": sorted(reasons), "samples": len(sm), "source": "nvml"}
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
-                    "note": "nvidia-smi unavailable"}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -161,7 +208,7 @@ class ClockSampler:
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "source": "nvidia-smi"}
 
 
 def gpu_uuid(torch, dev) -> str | None:
@@ -195,9 +242,8 @@ def cpu_baseline(xs, xf, budget_s: float = 10.0):
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
-    return {"value": 4 * m * reps / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{reps} full steps (4 sequential scans of the same 1e8-element inputs) "
-                      f"in {dt:.1f} s on one host core"}
+    return {"value": _sig(4 * m * reps / dt / 1e9), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{reps} full steps (4 scans of 1e8) in {dt:.1f} s, one core"}
 
 
 def run_reference(args) -> None:
@@ -262,183 +308,192 @@ def time_flushed(torch, stream, fn, scratch, reps: int) -> float:
     return sum(a.elapsed_time(b) for a, b in ev) / reps
 
 
-def row_rates(torch, ss, stream, dev, xs_d, xf_d, out_d):
-    """Secondary rows: every other hot-path row at its own workload, each
-    timed with CUDA events (mean of 20 after 3 warm-ups)."""
+def _sig(v: float, digits: int = 4) -> float:
+    """v rounded to `digits` significant digits (keeps the JSON line short)."""
+    if v == 0 or not np.isfinite(v):
+        return float(v)
+    return float(f"{v:.{digits}g}")
+
+
+def sweep_sizes():
+    """The int32 size sweep: 2^10 .. 2^30, 2^k - 1 and 2^k + 1 around the
+    tile-sized and large powers, and 10^3 .. 10^9."""
+    sizes = {1 << k for k in range(10, 31)}
+    for k in (10, 12, 13, 16, 20, 24, 27, 30):
+        sizes |= {(1 << k) - 1, (1 << k) + 1}
+    sizes |= {10 ** k for k in range(3, 10)}
+    return sorted(sizes)
+
+
+def size_label(n: int) -> str:
+    for k in range(10, 31):
+        for d, tag in ((0, ""), (-1, "-1"), (1, "+1")):
+            if n == (1 << k) + d:
+                return f"2^{k}{tag}"
+    for k in range(3, 10):
+        if n == 10 ** k:
+            return f"1e{k}"
+    return str(n)
+
+
+def row_rates(torch, ss, stream, dev, xs_d, xf_d, out_d, launch_ms_by_variant):
+    """Secondary rows, one short entry each: [ms per call, fraction of the
+    measured HBM peak on the row's algorithmic bytes] (CUDA events, mean of
+    20 after 3 warm-ups; L2 flushed before every call where the data would
+    fit in L2)."""
     import seeded_inputs as si
     rows = {}
     peak, _ = measured_hbm_peak()
+    sh = stream.cuda_stream
+    scratch = torch.empty(80_000_000, dtype=torch.int32, device=dev)  # 320 MB, over twice the L2
 
-    def gbs(bytes_, ms):
-        return bytes_ / (ms * 1e-3) / 1e9
+    def entry(bytes_, ms):
+        return [_sig(ms), round(bytes_ / (ms * 1e-3) / 1e9 / peak, 3)]
 
-    # copy probe with the scan's loader: the practical roofline of this access pattern
-    ms = time_region(torch, stream, lambda: ss.ss_copy_u32(xs_d, out_d, N, stream=stream.cuda_stream), 20)
-    rows["copy_probe_u32_1e8"] = {"ms": ms, "GB/s": gbs(8 * N, ms), "frac": gbs(8 * N, ms) / peak}
-    # ablations at the same int32 workload
-    for name, algo, traffic in (("reduce_then_scan", ss.SS_ALGO_REDUCE_THEN_SCAN, 12),
-                                ("rts_blelloch_plain", ss.SS_ALGO_RTS_BLELLOCH, 12),
-                                ("rts_blelloch_pad32", ss.SS_ALGO_RTS_BLELLOCH_PAD32, 12),
-                                ("rts_blelloch_pad2", ss.SS_ALGO_RTS_BLELLOCH_PAD2, 12)):
-        ms = time_region(torch, stream, lambda a=algo: ss.ss_scan(ss.SS_I32, False, a, xs_d, out_d,
-                                                                  stream=stream.cuda_stream), 20)
-        rows[f"{name}_i32_1e8"] = {"ms": ms, "G-elem/s": N / ms / 1e6,
-                                   "GB/s_on_2n": gbs(8 * N, ms), "frac_on_2n": gbs(8 * N, ms) / peak,
-                                   "GB/s_moved": gbs(traffic * N, ms)}
-    # uint32 Poisson(8) counts, n = 2^27, in place and out of place
-    nc = 1 << 27
-    cnt = torch.from_numpy(si.workload_poisson_counts(nc, seed=4).view(np.int32)).to(dev)
-    cnt_out = torch.empty_like(cnt)
-    ms = time_region(torch, stream, lambda: ss.scan_exclusive_u32(cnt, cnt_out, stream=stream.cuda_stream), 20)
-    rows["u32_poisson_2p27_out_of_place"] = {"ms": ms, "GB/s": gbs(8 * nc, ms), "frac": gbs(8 * nc, ms) / peak}
-    ms = time_region(torch, stream, lambda: ss.scan_exclusive_u32(cnt_out, cnt_out, stream=stream.cuda_stream), 20)
-    rows["u32_poisson_2p27_in_place"] = {"ms": ms, "GB/s": gbs(8 * nc, ms), "frac": gbs(8 * nc, ms) / peak}
-    del cnt, cnt_out
-    # compaction, n = 2^28, p in {0.01, 0.5, 0.99}
-    nk = 1 << 28
-    keys = torch.from_numpy(si.uniform_u32(nk, 6).view(np.int32)).to(dev)
-    kout = torch.empty_like(keys)
-    dcount = torch.zeros(1, dtype=torch.int64, device=dev)
-    for p in (0.01, 0.5, 0.99):
-        flags_np = si.bernoulli_flags(nk, p, 7)
-        flags = torch.from_numpy(flags_np).to(dev)
-        kept = int(flags_np.sum(dtype=np.int64))
-        ms = time_region(torch, stream, lambda: ss.compact_u32(keys, flags, kout, dcount, stream=stream.cuda_stream), 20)
-        alg = nk * 5 + 4 * kept + 8
-        # key bytes a reader that skips 32-byte sectors without a kept key must fetch
-        sectors = int(np.count_nonzero(flags_np.reshape(-1, 8).any(axis=1)))
-        minimal = nk + 32 * sectors + 4 * kept + 8
-        rows[f"compact_2p28_p{p}"] = {"ms": ms, "G-elem/s": nk / ms / 1e6, "kept": kept,
-                                      "GB/s_on_5n+4k": gbs(alg, ms), "frac_on_5n+4k": gbs(alg, ms) / peak,
-                                      "GB/s_on_sector_minimum": gbs(minimal, ms),
-                                      "frac_on_sector_minimum": gbs(minimal, ms) / peak}
-        ms_u = time_region(torch, stream, lambda: ss.ss_compact_u32_unordered(
-            keys, flags, kout, dcount, stream=stream.cuda_stream), 20)
-        rows[f"compact_unordered_2p28_p{p}"] = {"ms": ms_u, "frac_on_5n+4k": gbs(alg, ms_u) / peak}
-        del flags
-    del keys
-    # predicate compaction (keep v > 0, fp32, no flag array), n = 2^28, ordered and unordered
-    for p in (0.01, 0.5, 0.99):
-        xp = torch.from_numpy(si.workload_positive_f32(nk, p, seed=5)).to(dev)
-        pout = kout.view(torch.float32)
-        ss.compact_positive_f32(xp, pout, dcount, stream=stream.cuda_stream)
-        stream.synchronize()
-        kept = int(dcount.item())
-        alg = nk * 4 + 4 * kept + 8
-        ms = time_region(torch, stream, lambda: ss.compact_positive_f32(xp, pout, dcount, stream=stream.cuda_stream),
-                         20)
-        ms_u = time_region(torch, stream, lambda: ss.ss_compact_positive_unordered(
-            ss.SS_F32, xp, pout, dcount, stream=stream.cuda_stream), 20)
-        rows[f"compact_positive_f32_2p28_p{p}"] = {"ms": ms, "kept": kept, "GB/s_on_4n+4k": gbs(alg, ms),
-                                                   "frac_on_4n+4k": gbs(alg, ms) / peak,
-                                                   "unordered_ms": ms_u,
-                                                   "unordered_frac_on_4n+4k": gbs(alg, ms_u) / peak}
-        del xp
-    del kout
-    # the small configurations: int32 n = 4096, an inclusive and an exclusive scan per step
-    # (launch latency, not bandwidth), per call from Python and per replay of a captured
-    # graph; fp32 n = 1e6 and 1e7, which fit in L2, warm (back to back) and with L2 flushed
+    def timed(fn, nbytes, reps=20):
+        # inputs that fit in L2 twice over get a flush before every call
+        if nbytes < 2 * L2_BYTES:
+            return time_flushed(torch, stream, fn, scratch, reps)
+        return time_region(torch, stream, fn, reps)
+
+    # C2 at n = 1e8 and the headline variants, from the step's own per-launch events
+    for (kind, incl), ms in launch_ms_by_variant.items():
+        rows[f"{kind}{'i' if incl else 'x'}_1e8"] = entry(8 * N, ms)
+    # C2: fp32 inclusive and exclusive at 1e6 and 1e7 (L2 flushed)
+    for nf in (1_000_000, 10_000_000):
+        xf_s = torch.from_numpy(si.workload_f32_unit(nf, seed=1)).to(dev)
+        of_s = torch.empty_like(xf_s)
+        for incl in (True, False):
+            fn = (lambda: ss.scan_inclusive_f32(xf_s, of_s, stream=sh)) if incl else \
+                 (lambda: ss.scan_exclusive_f32(xf_s, of_s, stream=sh))
+            rows[f"f32{'i' if incl else 'x'}_{nf:.0e}".replace("+0", "")] = entry(8 * nf, timed(fn, 8 * nf))
+        del xf_s, of_s
+    # C1: int32 n = 4096, an inclusive and an exclusive scan per step, per call from
+    # Python and per replay of a captured graph (launch latency, not bandwidth): [us, us]
     x_small = torch.from_numpy(si.workload_int_0_100(4096, seed=0)).to(dev)
     o_small = torch.empty_like(x_small)
 
     def small_step():
-        ss.scan_inclusive_i32(x_small, o_small, stream=stream.cuda_stream)
-        ss.scan_exclusive_i32(x_small, o_small, stream=stream.cuda_stream)
+        ss.scan_inclusive_i32(x_small, o_small, stream=sh)
+        ss.scan_exclusive_i32(x_small, o_small, stream=sh)
     ms = time_region(torch, stream, small_step, 200)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         small_step()
     ms_g = time_region(torch, stream, graph.replay, 200)
-    rows["scan_i32_4096_incl_and_excl"] = {"us_per_step": ms * 1e3, "us_per_graph_replay": ms_g * 1e3,
-                                           "note": "two launches per step; bound by launch latency"}
+    rows["c1_4096_us"] = [_sig(ms * 1e3, 3), _sig(ms_g * 1e3, 3)]
     del graph, x_small, o_small
-    scratch = torch.empty(80_000_000, dtype=torch.int32, device=dev)  # 320 MB, over twice the L2
-    for nf in (1_000_000, 10_000_000):
-        xf_s = torch.from_numpy(si.workload_f32_unit(nf, seed=1)).to(dev)
-        of_s = torch.empty_like(xf_s)
-        fn = lambda: ss.scan_inclusive_f32(xf_s, of_s, stream=stream.cuda_stream)  # noqa: E731
-        ms_w = time_region(torch, stream, fn, 50)
-        ms_f = time_flushed(torch, stream, fn, scratch, 20)
-        rows[f"scan_f32_incl_{nf}"] = {"ms_warm": ms_w, "ms_l2_flushed": ms_f,
-                                       "GB/s_warm": gbs(8 * nf, ms_w), "GB/s_l2_flushed": gbs(8 * nf, ms_f),
-                                       "frac_l2_flushed": gbs(8 * nf, ms_f) / peak}
-        del xf_s, of_s
-    del scratch
-    # int32 exclusive across sizes, 2^20 .. 2^30 (inputs from a seeded on-device generator, in
-    # [-1000, 1000]: integer adds take the same time whatever the values)
+    # C3: int32 exclusive over the whole size sweep, us per call (the fraction is
+    # 8n bytes / time / peak); prefixes of one seeded input in [-1000, 1000]
+    top = sweep_sizes()[-1]
     gen = torch.Generator(device=dev)
     gen.manual_seed(2)
+    xi = torch.randint(-1000, 1001, (top,), dtype=torch.int32, device=dev, generator=gen)
+    oi = torch.empty_like(xi)
     sweep = {}
-    for lg in (20, 24, 27, 30):
-        ns = 1 << lg
-        xi = torch.randint(-1000, 1001, (ns,), dtype=torch.int32, device=dev, generator=gen)
-        oi = torch.empty_like(xi)
-        ms = time_region(torch, stream, lambda: ss.scan_exclusive_i32(xi, oi, stream=stream.cuda_stream),
-                         20 if lg < 30 else 5)
-        sweep[f"2^{lg}"] = {"ms": ms, "G-elem/s": ns / ms / 1e6, "frac": gbs(8 * ns, ms) / peak}
-        del xi, oi
-    rows["scan_i32_excl_size_sweep"] = sweep
-    # MoE counts and 64-aligned offsets: 256 experts, top-8, decode and prefill batch sizes
+    for ns in sweep_sizes():
+        a, o = xi[:ns], oi[:ns]
+        ms = timed(lambda: ss.scan_exclusive_i32(a, o, stream=sh), 8 * ns, 20 if ns < (1 << 29) else 5)
+        sweep[size_label(ns)] = _sig(ms * 1e3, 3)
+    # 2^k - 1 and 2^k + 1 sit beside 2^k: "2^k": [us(2^k), us(2^k - 1), us(2^k + 1)]
+    for lbl in [k for k in sweep if k.startswith("2^") and k[-2:] not in ("-1", "+1")]:
+        if lbl + "-1" in sweep:
+            sweep[lbl] = [sweep[lbl], sweep.pop(lbl + "-1"), sweep.pop(lbl + "+1")]
+    rows["i32x_sweep_us"] = sweep
+    del xi, oi
+    # copy probe with the scan's loader: the practical roofline of this access pattern
+    ms = time_region(torch, stream, lambda: ss.ss_copy_u32(xs_d, out_d, N, stream=sh), 20)
+    rows["copy_1e8"] = entry(8 * N, ms)
+    # ablations (reduce-then-scan, three kernels) at the same int32 workload, on 2n bytes
+    for name, algo in (("rts", ss.SS_ALGO_REDUCE_THEN_SCAN), ("rts_bl", ss.SS_ALGO_RTS_BLELLOCH),
+                       ("rts_bl32", ss.SS_ALGO_RTS_BLELLOCH_PAD32), ("rts_bl2", ss.SS_ALGO_RTS_BLELLOCH_PAD2)):
+        ms = time_region(torch, stream, lambda a=algo: ss.ss_scan(ss.SS_I32, False, a, xs_d, out_d, stream=sh), 20)
+        rows[f"{name}_1e8"] = entry(8 * N, ms)
+    # C5: uint32 Poisson(8) counts, n = 2^27, out of place and in place
+    nc = 1 << 27
+    cnt = torch.from_numpy(si.workload_poisson_counts(nc, seed=4).view(np.int32)).to(dev)
+    cnt_out = torch.empty_like(cnt)
+    rows["pois"] = entry(8 * nc, time_region(torch, stream, lambda: ss.scan_exclusive_u32(cnt, cnt_out, stream=sh), 20))
+    rows["pois_inpl"] = entry(8 * nc, time_region(
+        torch, stream, lambda: ss.scan_exclusive_u32(cnt_out, cnt_out, stream=sh), 20))
+    del cnt, cnt_out
+    # C4: flag compaction, n = 2^28, p in {0.01, 0.5, 0.99}, on 5n + 4k bytes; and the
+    # unordered (warp-aggregated atomics) ablation on the same inputs, ms only
+    nk = 1 << 28
+    keys = torch.from_numpy(si.uniform_u32(nk, 6).view(np.int32)).to(dev)
+    kout = torch.empty_like(keys)
+    dcount = torch.zeros(1, dtype=torch.int64, device=dev)
+    unord = []
+    for p in (0.01, 0.5, 0.99):
+        flags_np = si.bernoulli_flags(nk, p, 7)
+        flags = torch.from_numpy(flags_np).to(dev)
+        kept = int(flags_np.sum(dtype=np.int64))
+        ms = time_region(torch, stream, lambda: ss.compact_u32(keys, flags, kout, dcount, stream=sh), 20)
+        rows[f"cmp_p{p}"] = entry(nk * 5 + 4 * kept + 8, ms)
+        unord.append(_sig(time_region(torch, stream, lambda: ss.ss_compact_u32_unordered(
+            keys, flags, kout, dcount, stream=sh), 20)))
+        del flags
+    rows["cmp_unord_ms"] = unord
+    del keys
+    # predicate compaction (keep v > 0, fp32, no flag array), on 4n + 4k bytes; unordered ms
+    unord = []
+    for p in (0.01, 0.5, 0.99):
+        xp = torch.from_numpy(si.workload_positive_f32(nk, p, seed=5)).to(dev)
+        pout = kout.view(torch.float32)
+        ss.compact_positive_f32(xp, pout, dcount, stream=sh)
+        stream.synchronize()
+        kept = int(dcount.item())
+        ms = time_region(torch, stream, lambda: ss.compact_positive_f32(xp, pout, dcount, stream=sh), 20)
+        rows[f"pos_p{p}"] = entry(nk * 4 + 4 * kept + 8, ms)
+        unord.append(_sig(time_region(torch, stream, lambda: ss.ss_compact_positive_unordered(
+            ss.SS_F32, xp, pout, dcount, stream=sh), 20)))
+        del xp
+    rows["pos_unord_ms"] = unord
+    del kout
+    # MoE counts and 64-aligned offsets, 256 experts, top-8: [us per call, us per graph replay]
     for tokens in (4096, 65536, 1 << 20):
         ids = torch.from_numpy(si.topk_ids(tokens, 8, 256, seed=6)).to(dev)
         cnt_e = torch.empty(256, dtype=torch.int32, device=dev)
         off_e = torch.empty(257, dtype=torch.int32, device=dev)
-        ms = time_region(torch, stream, lambda: ss.ss_moe_counts_offsets(
-            ids, 256, 64, cnt_e, off_e, stream=stream.cuda_stream), 100)
-        # the same call captured once in a CUDA graph and replayed: the GPU's time per call
-        # without the per-call host work
+        ms = time_region(torch, stream, lambda: ss.ss_moe_counts_offsets(ids, 256, 64, cnt_e, off_e, stream=sh), 100)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
-            ss.ss_moe_counts_offsets(ids, 256, 64, cnt_e, off_e, stream=stream.cuda_stream)
+            ss.ss_moe_counts_offsets(ids, 256, 64, cnt_e, off_e, stream=sh)
         ms_g = time_region(torch, stream, graph.replay, 100)
-        rows[f"moe_counts_offsets_t{tokens}_k8_e256"] = {
-            "us": ms * 1e3, "us_graph_replay": ms_g * 1e3, "ids_MB": 4 * tokens * 8 / 1e6,
-            "GB/s_on_ids_graph": gbs(4 * tokens * 8, ms_g),
-            "note": "ids stay in L2 (129 MB) across replays; 'us' includes the per-call host work"}
-        del graph
-        del ids
-    # scans with 64-bit sums at n = 1e8: uint32 -> uint64 (4 + 8 B per element) and int64 / fp64 (8 + 8)
+        rows[f"moe_t{tokens}_us"] = [_sig(ms * 1e3, 3), _sig(ms_g * 1e3, 3)]
+        del graph, ids
+    # scans with 64-bit sums at n = 1e8: uint32 -> uint64 (12 B per element), int64 and fp64 (16 B)
     w_in = torch.from_numpy(si.uniform_u32(N, seed=60).view(np.int32)).to(dev)
     w_64 = torch.from_numpy(si.uniform_f32(N, seed=64).astype(np.float64)).to(dev)
     w_out = torch.empty(N, dtype=torch.float64, device=dev)
     for name, fn, per in (
-            ("u32_u64_incl", lambda: ss.ss_scan_wide(ss.SS_WIDE_U32_U64, True, w_in, w_out,
-                                                     stream=stream.cuda_stream), 12),
-            ("i64_incl", lambda: ss.ss_scan_wide(ss.SS_WIDE_I64, True, w_64.view(torch.int64), w_out,
-                                                 stream=stream.cuda_stream), 16),
-            ("f64_incl", lambda: ss.ss_scan_wide(ss.SS_WIDE_F64, True, w_64, w_out, stream=stream.cuda_stream), 16)):
-        ms = time_region(torch, stream, fn, 20)
-        rows[f"scan_{name}_1e8"] = {"ms": ms, "G-elem/s": N / ms / 1e6, "GB/s": gbs(per * N, ms),
-                                    "frac": gbs(per * N, ms) / peak}
+            ("u32_u64", lambda: ss.ss_scan_wide(ss.SS_WIDE_U32_U64, True, w_in, w_out, stream=sh), 12),
+            ("i64", lambda: ss.ss_scan_wide(ss.SS_WIDE_I64, True, w_64.view(torch.int64), w_out, stream=sh), 16),
+            ("f64", lambda: ss.ss_scan_wide(ss.SS_WIDE_F64, True, w_64, w_out, stream=sh), 16)):
+        rows[f"{name}_1e8"] = entry(per * N, time_region(torch, stream, fn, 20))
     del w_in, w_64, w_out
-    # batched per-row scans, fp32 inclusive: top-p over a 128,256-entry vocabulary, and short rows
+    # batched per-row fp32 inclusive scans: top-p over a 128,256-entry vocabulary, and short rows
     for r_, c_ in ((512, 128256), (262144, 256), (16384, 4096)):
         xr = torch.from_numpy(si.uniform_f32(r_ * c_, seed=82)).to(dev)
         orr = torch.empty_like(xr)
-        ms = time_region(torch, stream, lambda: ss.ss_scan_rows(ss.SS_F32, True, xr, orr, r_, c_,
-                                                                stream=stream.cuda_stream), 20)
-        rows[f"scan_rows_f32_{r_}x{c_}"] = {"ms": ms, "GB/s": gbs(8 * r_ * c_, ms),
-                                            "frac": gbs(8 * r_ * c_, ms) / peak}
+        rows[f"rows_{r_}x{c_}"] = entry(8 * r_ * c_, time_region(
+            torch, stream, lambda: ss.ss_scan_rows(ss.SS_F32, True, xr, orr, r_, c_, stream=sh), 20))
         del xr, orr
-    # segmented scans, fp32 inclusive, n = 1e8: top-p-length segments and short ones
+    # segmented fp32 inclusive scans, n = 1e8, by mean segment length, on 2n bytes
     xs_seg = torch.from_numpy(si.uniform_f32(N, seed=96)).to(dev)
     os_seg = torch.empty_like(xs_seg)
-    for mean in (128256.0, 100.0):
-        off_np = si.segment_offsets(N, mean, seed=98)
-        off = torch.from_numpy(off_np.astype(np.int64)).to(dev)
-        ms = time_region(torch, stream, lambda: ss.ss_scan_segments(ss.SS_F32, True, xs_seg, os_seg, off,
-                                                                    stream=stream.cuda_stream), 20)
-        rows[f"scan_segments_f32_1e8_mean{int(mean)}"] = {"ms": ms, "segments": int(off_np.size - 1),
-                                                          "GB/s_on_2n": gbs(8 * N, ms),
-                                                          "frac_on_2n": gbs(8 * N, ms) / peak}
+    for mean in (128256.0, 100.0, 4.0):
+        off = torch.from_numpy(si.segment_offsets(N, mean, seed=98).astype(np.int64)).to(dev)
+        rows[f"seg_mean{int(mean)}"] = entry(8 * N, time_region(
+            torch, stream, lambda: ss.ss_scan_segments(ss.SS_F32, True, xs_seg, os_seg, off, stream=sh), 20))
         del off
-    del xs_seg, os_seg
+    del xs_seg, os_seg, scratch
+
     # context only: torch.cumsum on the same int32 input, timed the same way
     def cumsum():
         with torch.cuda.stream(stream):  # torch ops run on torch's current stream
             torch.cumsum(xs_d, 0, dtype=torch.int32, out=out_d)
-    ms = time_region(torch, stream, cumsum, 20)
-    rows["context_torch_cumsum_i32_1e8"] = {"ms": ms, "G-elem/s": N / ms / 1e6}
+    rows["cumsum_1e8"] = entry(8 * N, time_region(torch, stream, cumsum, 20))
     return rows
 
 
@@ -535,11 +590,13 @@ def run_ours(args) -> None:
     peak, peak_src = measured_hbm_peak()
     mean_launch_ms = statistics.fmean(launch_ms)
     achieved = BYTES_PER_ELEM * N / (mean_launch_ms * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": recorded_traffic(), "kernel": "k_scan_lookback_pipe_sb",
-                "bytes_per_launch": BYTES_PER_ELEM * N, "mean_launch_ms": mean_launch_ms,
-                "median_launch_ms": statistics.median(launch_ms), "peak_source": peak_src,
-                "frac_of_nominal_8TBs": achieved / 8000.0}
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(), "kernel": "k_scan_lookback_pipe_sb",
+                "mean_launch_ms": _sig(mean_launch_ms, 5), "peak_source": peak_src,
+                "frac_of_nominal_8TBs": round(achieved / 8000.0, 4)}
+    by_variant = {}
+    for j, v in enumerate(VARIANTS):
+        by_variant[v] = statistics.fmean(launch_ms[j::len(launches)])
 
     # end to end through the host-memory API: pinned host in, pinned host out
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
@@ -559,25 +616,24 @@ def run_ours(args) -> None:
     for _ in range(e2e_steps):
         e2e_step()
     e2e_s = time.perf_counter() - t0
-    e2e = {"value": 4 * N * e2e_steps / e2e_s / 1e9, "unit": UNIT,
-           "h2d_bytes_per_step": 4 * N * 4, "d2h_bytes_per_step": 4 * N * 4,
-           "steps": e2e_steps, "api": "ss_scan_host on pinned host buffers: the scan kernel reads and writes them directly "
-                  "(NVLink-C2C), no staging copies"}
+    e2e = {"value": _sig(4 * N * e2e_steps / e2e_s / 1e9), "unit": UNIT,
+           "h2d_bytes_per_step": 4 * N * 4, "d2h_bytes_per_step": 4 * N * 4, "steps": e2e_steps,
+           "api": "ss_scan_host, pinned host buffers"}
 
-    rows = {} if args.no_rows else row_rates(torch, ss, stream, dev, xs_d, xf_d, out_i)
+    rows = {} if args.no_rows else row_rates(torch, ss, stream, dev, xs_d, xf_d, out_i, by_variant)
     cpu = None if args.no_cpu else cpu_baseline(xs, xf, budget_s=args.cpu_budget)
 
-    emit({"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-          "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+    emit({"metric": METRIC, "value": _sig(value, 5), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+          "warmup": args.warmup, "ms_per_step": _sig(ms_per_step, 5), "higher_is_better": True,
           "scaling": "weak", "vs_baseline": None, "dtype": "int32/fp32", "data": DATA,
-          "config": {"workload": WORKLOAD, "n": N, "elements_per_step": len(launches) * N,
-                     "l2": "inputs larger than L2 (400 MB per array vs 129 MB), no flush",
+          "config": {"workload": WORKLOAD, "n": N, "l2": "no flush: inputs > L2",
                      "parallelism": "replicas" if world > 1 else "single GPU",
                      "tile_elems": ss.ss_scan_tile_elems(),
                      "scan_config": "library default" if args.config is None else args.config},
           "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
           "gpu_launches": len(launches) * args.steps, "clocks": clocks,
-          "GB/s": value * BYTES_PER_ELEM, "rows": rows})
+          "rows_unit": "[ms, frac of HBM peak] unless named _us/_ms",
+          "rows": rows})
     if world > 1:
         torch.distributed.destroy_process_group()
 

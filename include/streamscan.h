@@ -252,6 +252,19 @@ ss_status ss_scan(ss_dtype dtype, int inclusive, ss_algo algo, const void *in, v
                   size_t n, ss_stream_t stream);
 
 /*
+ * Sum of all n elements of `in`, written to *d_total (device, one element of
+ * dtype's type, 4-byte aligned) -- the first step of a scan split over
+ * several devices ("Prefix sum and other parallel patterns", A device-level
+ * scan: scan then propagate -- the part totals are scanned and each part is
+ * offset by the sum of the parts before it).  int32 and uint32 wrap modulo
+ * 2^32; fp32 adds in an order that is fixed for a fixed n and device (so the
+ * same input gives the same bits on every run).  n == 0 writes 0.  in is
+ * 4-byte aligned (16-byte aligned takes the vector path); *d_total must not
+ * overlap in.  One launch; uses the stream's workspace.
+ */
+ss_status ss_reduce_sum(ss_dtype dtype, const void *in, void *d_total, size_t n, ss_stream_t stream);
+
+/*
  * Single-pass scan seeded with a carry: the prefix before in[0] is
  * *d_carry_in (device, one element of the scan's type; NULL means 0), and
  * the inclusive total including the seed is written to *d_carry_out (device,
@@ -334,9 +347,10 @@ int ss_scan_config_count(void);
  * process (ss_scan_config_count() rows: one CTA per tile, or a persistent
  * grid streaming tiles through a shared-memory ring).  -1 (the initial
  * setting) chooses per call by size: row 7 (16384-element tiles) below 5e7
- * elements, row 2 (18432) from there on.  Results do not depend on it,
- * except for the rounding of fp32 sums.  SS_ERR_INVALID_ARG below -1 or
- * from ss_scan_config_count() on. */
+ * elements, row 8 (18432-element tiles, each claimed from the tile counter
+ * as its copy starts, so that faster SMs take more tiles) from there on.
+ * Results do not depend on it, except for the rounding of fp32 sums.
+ * SS_ERR_INVALID_ARG below -1 or from ss_scan_config_count() on. */
 ss_status ss_set_scan_config(int config);
 
 /* Selects the persistent compaction kernel used for 16-byte aligned inputs
@@ -376,6 +390,9 @@ ss_status ss_debug_set_lookback_fault(int64_t tile, uint64_t timeout_ns);
  * every GPU loading the library holds until the process exits.
  *   dtype, inclusive, in, out, stream: as for ss_scan (SS_ALGO_LOOKBACK);
  *        out == in is allowed.  The caller passes inputs and outputs.
+ *        `stream` must belong to the current device (the array used is the
+ *        current device's); a stream of another device returns
+ *        SS_ERR_INVALID_ARG.
  *   n    0 <= n <= 2^30; larger n returns SS_ERR_INVALID_ARG.
  * The first call on a device sets up that device: it looks up the array's
  * device address and zeroes it, which synchronises the device; make that
@@ -389,6 +406,16 @@ ss_status ss_debug_set_lookback_fault(int64_t tile, uint64_t timeout_ns);
  */
 ss_status ss_scan_noalloc(ss_dtype dtype, int inclusive, const void *in, void *out, size_t n,
                           ss_stream_t stream);
+
+/*
+ * Test hooks for ss_scan_noalloc's periodic descriptor clear: the clear runs
+ * on the current device's call that makes the count of calls a multiple of
+ * ss_debug_noalloc_clear_period() (2^29), before its launch.
+ * ss_debug_set_noalloc_calls sets the count of calls made so far on the
+ * current device, so that a test reaches a clear in a few calls.
+ */
+ss_status ss_debug_set_noalloc_calls(uint64_t calls);
+uint64_t ss_debug_noalloc_clear_period(void);
 
 #ifdef __cplusplus
 }

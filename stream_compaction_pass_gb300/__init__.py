@@ -82,6 +82,7 @@ def _declare(lib):
         "ss_set_host_mode": [I],
         "ss_scan": [I, I, I, P, P, SZ, P],
         "ss_scan_seeded": [I, I, P, P, SZ, P, P, P],
+        "ss_reduce_sum": [I, P, P, SZ, P],
         "ss_scan_host": [I, I, P, P, SZ, P],
         "ss_copy_u32": [P, P, SZ, P],
         "ss_scan_trace": [I, P, P, SZ, P, P],
@@ -90,6 +91,7 @@ def _declare(lib):
         "ss_set_compact_config": [I],
         "ss_debug_set_lookback_fault": [I64, U64],
         "ss_scan_noalloc": [I, I, P, P, SZ, P],
+        "ss_debug_set_noalloc_calls": [U64],
     }
     for name, args in sigs.items():
         f = getattr(lib, name)
@@ -105,6 +107,8 @@ def _declare(lib):
     lib.ss_scan_config_count.restype = I
     lib.ss_shutdown.argtypes = []
     lib.ss_shutdown.restype = None
+    lib.ss_debug_noalloc_clear_period.argtypes = []
+    lib.ss_debug_noalloc_clear_period.restype = U64
     return lib
 
 
@@ -298,6 +302,14 @@ def ss_scan_seeded(dtype: int, inclusive: bool, inp, out, carry_in=None, carry_o
            "ss_scan_seeded")
 
 
+def ss_reduce_sum(dtype: int, inp, d_total, n=None, stream=None):
+    """Sum of `inp` (device) into d_total (device, one element)."""
+    if n is None:
+        n = _numel(inp)
+    _check(lib().ss_reduce_sum(dtype, _addr(inp), _addr(d_total), n, _stream(stream, inp, d_total)),
+           "ss_reduce_sum")
+
+
 def ss_scan_host(dtype: int, inclusive: bool, h_in, h_out, n=None, stream=None):
     if n is None:
         n = _numel(h_in)
@@ -363,6 +375,14 @@ def ss_shutdown() -> None:
 
 def ss_debug_set_lookback_fault(tile: int, timeout_ns: int = 0) -> None:
     _check(lib().ss_debug_set_lookback_fault(tile, timeout_ns), "ss_debug_set_lookback_fault")
+
+
+def ss_debug_set_noalloc_calls(calls: int) -> None:
+    _check(lib().ss_debug_set_noalloc_calls(calls), "ss_debug_set_noalloc_calls")
+
+
+def ss_debug_noalloc_clear_period() -> int:
+    return int(lib().ss_debug_noalloc_clear_period())
 
 
 def ss_scan_noalloc(dtype: int, inclusive: bool, inp, out, n=None, stream=None):

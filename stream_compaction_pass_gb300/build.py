@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libstreamscan.so")
 SOURCES = ["scan.cu", "scan_pipe.cu", "scan_ws.cu", "compact.cu", "compact_pipe.cu", "ablations.cu", "api.cu",
-           "noalloc.cu", "compact_unordered.cu", "moe.cu", "scan_wide.cu", "scan_rows.cu", "scan_segments.cu", "compact_pred.cu"]
+           "noalloc.cu", "compact_unordered.cu", "moe.cu", "scan_wide.cu", "scan_rows.cu", "scan_segments.cu", "compact_pred.cu", "reduce.cu", "launch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          "--expt-relaxed-constexpr"]

@@ -24,8 +24,8 @@ thread_local std::string g_detail;
 std::atomic<int> g_config{-1};
 
 // Below this many elements the 16384-element-tile row (7) beats the default
-// row (2): its shorter tiles fill and drain the persistent pipeline sooner
-// (measured at 1e6 .. 3e7 elements; the two are level at 1e8).
+// row (8): its shorter tiles fill and drain the persistent pipeline sooner
+// (measured at 1e6 .. 3e7 elements; from 1e8 on row 8 is ahead).
 constexpr size_t kAutoSmallScan = 50'000'000;
 
 int effective_config(size_t n) {
@@ -68,7 +68,7 @@ struct Workspace {
     int device = 0;
     cudaStream_t stream = nullptr;
     // Header: [0] tile counter (u64), [8] status words (2 x u32), [16] carry (8 B),
-    // [24] MoE ticket (u32).
+    // [24] MoE ticket (u32), [28] reduction ticket (u32).
     unsigned char* header = nullptr;
     unsigned long long* desc = nullptr;
     size_t desc_cap = 0;  // descriptors
@@ -88,6 +88,7 @@ unsigned long long* ws_counter(Workspace* w) { return reinterpret_cast<unsigned 
 uint32_t* ws_status(Workspace* w) { return reinterpret_cast<uint32_t*>(w->header + 8); }
 void* ws_carry(Workspace* w) { return w->header + 16; }
 uint32_t* ws_ticket(Workspace* w) { return reinterpret_cast<uint32_t*>(w->header + 24); }
+uint32_t* ws_reduce_ticket(Workspace* w) { return reinterpret_cast<uint32_t*>(w->header + 28); }
 
 ss_status get_workspace(cudaStream_t s, Workspace** out) {
     int dev = 0;
@@ -389,6 +390,29 @@ ss_status ss_scan_seeded(ss_dtype dtype, int inclusive, const void* in, void* ou
     }
     return scan_lookback(to_dtype(dtype), inclusive != 0, in, out, n, d_carry_in, d_carry_out,
                          (cudaStream_t)stream);
+}
+
+ss_status ss_reduce_sum(ss_dtype dtype, const void* in, void* d_total, size_t n, ss_stream_t stream) {
+    if (!valid_dtype(dtype)) return fail(SS_ERR_UNSUPPORTED, "unknown dtype");
+    if (d_total == nullptr) return fail(SS_ERR_INVALID_ARG, "null total");
+    if (reinterpret_cast<uintptr_t>(d_total) & 3u) return fail(SS_ERR_INVALID_ARG, "total must be 4-byte aligned");
+    cudaStream_t s = (cudaStream_t)stream;
+    if (n == 0) {
+        cudaError_t e = cudaMemsetAsync(d_total, 0, 4, s);
+        return e == cudaSuccess ? SS_OK : cuda_fail(e, "total clear");
+    }
+    if (in == nullptr) return fail(SS_ERR_INVALID_ARG, "null pointer with n > 0");
+    if (reinterpret_cast<uintptr_t>(in) & 3u) return fail(SS_ERR_INVALID_ARG, "in must be 4-byte aligned");
+    if (n > SIZE_MAX / 8) return fail(SS_ERR_INVALID_ARG, "n too large");
+    if (overlaps(in, n * 4, d_total, 4)) return fail(SS_ERR_INVALID_ARG, "the total overlaps the input");
+    Workspace* w = nullptr;
+    ss_status st = get_workspace(s, &w);
+    if (st != SS_OK) return st;
+    const uint32_t grid = ss::reduce_grid(device_sms(w->device));
+    st = ensure_totals(w, (size_t)grid * 4);
+    if (st != SS_OK) return st;
+    cudaError_t e = ss::launch_reduce_sum(to_dtype(dtype), in, n, w->totals, ws_reduce_ticket(w), d_total, grid, s);
+    return e == cudaSuccess ? SS_OK : cuda_fail(e, "reduction launch");
 }
 
 ss_status compact_u32(const uint32_t* keys, const uint8_t* flags, uint32_t* out, uint64_t* d_count,

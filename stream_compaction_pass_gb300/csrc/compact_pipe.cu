@@ -782,21 +782,11 @@ static cudaError_t launch_compact_persistent(const uint32_t* keys, const uint8_t
         if constexpr (SELECTIVE) return k_compact_sel<THREADS, VPT, STAGES>;
         else return k_compact_pipe<THREADS, VPT, STAGES, RULE>;
     }();
-    static int blocks_per_sm = -1;
-    static int sms = 0;
-    if (blocks_per_sm < 0) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
-        if (e != cudaSuccess) return e;
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        int b = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, THREADS, SMEM);
-        if (e != cudaSuccess) return e;
-        blocks_per_sm = b > 0 ? b : 1;
-    }
+    KernelSetup su;
+    cudaError_t e = kernel_setup(reinterpret_cast<const void*>(kern), THREADS, SMEM, &su);
+    if (e != cudaSuccess) return e;
     const uint32_t tiles = (uint32_t)((n + TILE - 1) / TILE);
-    const size_t resident = (size_t)sms * (size_t)blocks_per_sm;
+    const size_t resident = (size_t)su.sms * (size_t)su.blocks_per_sm;
     const uint32_t grid = (uint32_t)(tiles < resident ? tiles : resident);
     LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};
     kern<<<grid, THREADS, SMEM, s>>>(keys, flags, out, d_count, n, tiles, ctx);
@@ -816,17 +806,11 @@ static cudaError_t launch_compact_chunked(const uint32_t* keys, const uint8_t* f
     constexpr size_t TILE = 65536;
     constexpr size_t SMEM = STAGES * TILE;
     auto kern = k_compact_chunked<THREADS, STAGES>;
-    static int sms = 0;
-    if (sms == 0) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
-        if (e != cudaSuccess) return e;
-        int dev = 0, v = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        sms = v > 0 ? v : 1;
-    }
+    KernelSetup su;
+    cudaError_t e = kernel_setup(reinterpret_cast<const void*>(kern), THREADS, SMEM, &su);
+    if (e != cudaSuccess) return e;
     const uint32_t tiles = (uint32_t)((n + TILE - 1) / TILE);
-    const uint32_t grid = tiles < (uint32_t)sms ? tiles : (uint32_t)sms;
+    const uint32_t grid = tiles < (uint32_t)su.sms ? tiles : (uint32_t)su.sms;
     LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};
     kern<<<grid, THREADS, SMEM, s>>>(keys, flags, out, d_count, n, tiles, ctx);
     return cudaGetLastError();

@@ -430,17 +430,11 @@ template <KeepRule RULE>
 static cudaError_t launch_pred(const uint32_t* keys, uint32_t* out, unsigned long long* d_count, size_t n,
                                const LookbackWs& ws, cudaStream_t s) {
     auto kern = k_compact_pred<RULE>;
-    static int sms = 0;
-    if (sms == 0) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPredSmem);
-        if (e != cudaSuccess) return e;
-        int dev = 0, v = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        sms = v > 0 ? v : 1;
-    }
+    KernelSetup su;
+    cudaError_t e = kernel_setup(reinterpret_cast<const void*>(kern), kPredThreads, kPredSmem, &su);
+    if (e != cudaSuccess) return e;
     const uint32_t tiles = (uint32_t)((n + kPredTile - 1) / kPredTile);
-    const uint32_t grid = tiles < (uint32_t)sms ? tiles : (uint32_t)sms;
+    const uint32_t grid = tiles < (uint32_t)su.sms ? tiles : (uint32_t)su.sms;
     LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};
     kern<<<grid, kPredThreads, kPredSmem, s>>>(keys, out, d_count, n, tiles, ctx);
     return cudaGetLastError();

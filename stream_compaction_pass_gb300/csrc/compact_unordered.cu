@@ -126,20 +126,19 @@ k_compact_unordered(const uint32_t* keys, const uint8_t* flags, uint32_t* out, u
 template <KeepRule RULE>
 static cudaError_t launch_unordered(const uint32_t* keys, const uint8_t* flags, uint32_t* out,
                                     unsigned long long* d_count, size_t n, cudaStream_t s) {
-    static int sms = 0;
-    if (sms == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (sms <= 0) sms = 1;
-    }
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (sms <= 0) sms = 1;
     const bool vec = (reinterpret_cast<uintptr_t>(keys) & 15u) == 0 &&
                      (RULE != KeepRule::Flags || (reinterpret_cast<uintptr_t>(flags) & 3u) == 0);
     const size_t steps = vec ? (n + kUBatch - 1) / kUBatch : (n + 31) / 32;  // warp steps
     const size_t want = (steps + kUThreads / 32 - 1) / (kUThreads / 32);
     const size_t cap = (size_t)sms * (2048 / kUThreads);  // one full wave of 256-thread CTAs
     const unsigned grid = (unsigned)(want < cap ? (want > 0 ? want : 1) : cap);
-    cudaError_t e = cudaMemsetAsync(d_count, 0, sizeof(unsigned long long), s);
+    e = cudaMemsetAsync(d_count, 0, sizeof(unsigned long long), s);
     if (e != cudaSuccess) return e;
     k_compact_unordered<RULE><<<grid, kUThreads, 0, s>>>(keys, flags, out, d_count, n, vec);
     return cudaGetLastError();

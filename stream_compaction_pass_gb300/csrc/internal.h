@@ -25,6 +25,15 @@ struct LookbackWs {
     int64_t fault_tile = -1;                // test hook: tile that never publishes
 };
 
+// Launch set-up of a kernel on the current device: SM count and resident CTAs
+// per SM at `max_smem` bytes of dynamic shared memory, whose limit it also
+// raises (launch.cu).  Done once per (kernel, device); thread-safe.
+struct KernelSetup {
+    int sms = 1;
+    int blocks_per_sm = 1;
+};
+cudaError_t kernel_setup(const void* kern, int threads, size_t max_smem, KernelSetup* out);
+
 // A single-pass scan configuration: which kernel, its tile geometry and
 // its look-back window.
 struct ScanConfig {
@@ -142,6 +151,13 @@ cudaError_t launch_moe_counts_offsets(const int32_t* ids, size_t m, int32_t num_
                                       uint32_t* counts, uint32_t* offsets, uint32_t* acc, uint32_t* ticket,
                                       uint32_t grid, cudaStream_t s);
 uint32_t moe_grid(size_t m, int sms);
+
+// Sum of a whole array (reduce.cu): int32/uint32 wrap modulo 2^32, fp32 in
+// an order fixed by n and the grid.  `partials` holds `grid` values and
+// `ticket` is zero on entry; the launch leaves it zero.
+uint32_t reduce_grid(int sms);
+cudaError_t launch_reduce_sum(Dtype dt, const void* in, size_t n, void* partials, uint32_t* ticket, void* total,
+                              uint32_t grid, cudaStream_t s);
 
 // Ablations (reduce-then-scan, three kernels).  `totals` holds one value
 // per 4096-element tile.  tile_scan: 0 = register/shuffle tile scan,

@@ -125,13 +125,12 @@ k_moe_counts_offsets(const int32_t* ids, size_t m, int32_t num_experts, uint32_t
 cudaError_t launch_moe_counts_offsets(const int32_t* ids, size_t m, int32_t num_experts, uint32_t align,
                                       uint32_t* counts, uint32_t* offsets, uint32_t* acc, uint32_t* ticket,
                                       uint32_t grid, cudaStream_t s) {
-    static int smem_set = 0;
     const size_t smem = (size_t)num_experts * 4;
-    if (smem > 48 * 1024 && smem_set < (int)smem) {
-        cudaError_t e = cudaFuncSetAttribute(k_moe_counts_offsets, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
+    if (smem > 48 * 1024) {  // the limit is raised once per device, to the largest expert count
+        KernelSetup su;
+        cudaError_t e = kernel_setup(reinterpret_cast<const void*>(k_moe_counts_offsets), kMoeThreads,
+                                     (size_t)kMoeMaxExperts * 4, &su);
         if (e != cudaSuccess) return e;
-        smem_set = (int)smem;
     }
     size_t chunk = (m + grid - 1) / grid;
     chunk = (chunk + 3) / 4 * 4;

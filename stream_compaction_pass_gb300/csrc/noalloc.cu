@@ -51,6 +51,21 @@ ss_status na_fail(ss_status st, const char* why) {
 
 }  // namespace
 
+// Test hook: sets the number of calls made so far on the current device, so
+// that a test can reach the periodic descriptor clear without 2^29 calls.
+extern "C" ss_status ss_debug_set_noalloc_calls(uint64_t calls) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return na_fail(SS_ERR_CUDA, cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return na_fail(SS_ERR_UNSUPPORTED, "device index too large");
+    std::lock_guard<std::mutex> lk(g_na_mu);
+    g_na_calls[dev] = calls;
+    return SS_OK;
+}
+
+// The number of calls after which the descriptors are cleared (for tests).
+extern "C" uint64_t ss_debug_noalloc_clear_period(void) { return kClearEvery; }
+
 extern "C" ss_status ss_scan_noalloc(ss_dtype dtype, int inclusive, const void* in, void* out, size_t n,
                                      ss_stream_t stream) {
     if (dtype != SS_I32 && dtype != SS_U32 && dtype != SS_F32)
@@ -71,6 +86,13 @@ extern "C" ss_status ss_scan_noalloc(ss_dtype dtype, int inclusive, const void* 
     if (e != cudaSuccess) return na_fail(SS_ERR_CUDA, cudaGetErrorString(e));
     if (dev < 0 || dev >= kMaxDevices) return na_fail(SS_ERR_UNSUPPORTED, "device index too large");
     cudaStream_t s = (cudaStream_t)stream;
+    // The scratch array is picked by the current device, so the stream must
+    // belong to that device: a stream of another device would pair this
+    // device's array with the other device's launch.
+    int stream_dev = dev;
+    e = cudaStreamGetDevice(s, &stream_dev);
+    if (e != cudaSuccess) return na_fail(SS_ERR_CUDA, cudaGetErrorString(e));
+    if (stream_dev != dev) return na_fail(SS_ERR_INVALID_ARG, "the stream belongs to another device than the current one");
 
     unsigned long long* scratch;
     {

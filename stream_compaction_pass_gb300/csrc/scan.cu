@@ -75,15 +75,17 @@ k_copy_probe(const uint32_t* in, uint32_t* out, size_t n, bool aligned) {
 static const ScanConfig kConfigs[] = {
     {0, 256, 16, 0, 1},  // 0: one CTA per 4096-element tile (the allocation-free entry point's kernel)
     {0, 256, 32, 0, 1},  // 1: one CTA per 8192-element tile (the fallback for unaligned or small inputs)
-    {1, 512, 36, 3, 1},  // 2: persistent, 18432-element tiles, 3-stage ring (216 KB), single register buffer -- the default
+    {1, 512, 36, 3, 1},  // 2: persistent, 18432-element tiles, 3-stage ring (216 KB), single register buffer
     {1, 512, 32, 3, 1},  // 3: persistent, 16384, 3 stages (192 KB), single register buffer
     {1, 512, 16, 3, 1},  // 4: persistent, 8192, 3 stages (96 KB, two CTAs per SM)
     {2, 512, 32, 3, 1},  // 5: persistent and warp-specialised, 16384, 3 stages, look-back one tile late
     {1, 512, 32, 3, 1},  // 6: persistent, lean iteration (one barrier), 16384, 3 stages
     {1, 512, 32, 2, 1},  // 7: persistent, 16384, 2-stage ring (128 KB), double register buffer
+    {1, 512, 36, 3, 1},  // 8: as row 2, each tile claimed from the counter when its copy starts -- the default
+    {1, 512, 32, 3, 1},  // 9: as row 8 with 16384-element tiles
 };
 constexpr int kNumConfigs = sizeof(kConfigs) / sizeof(kConfigs[0]);
-constexpr int kDefaultConfig = 2;
+constexpr int kDefaultConfig = 8;
 
 int scan_config_count() { return kNumConfigs; }
 ScanConfig scan_config(int idx) { return kConfigs[(idx >= 0 && idx < kNumConfigs) ? idx : 0]; }

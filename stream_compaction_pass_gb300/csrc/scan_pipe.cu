@@ -246,7 +246,20 @@ k_scan_lookback_pipe(const T* in, T* out, size_t n, uint32_t num_tiles, Lookback
 // the ring needs three stages.  Same arithmetic and look-back as above; it
 // exists because the double register buffer does not fit 128 registers for
 // every element type without spilling.
-template <typename T, bool INCLUSIVE, int THREADS, int VPT, int STAGES, int K, bool TRACE>
+//
+// DYN selects how tiles reach CTAs.  false: the fixed stride above (rank +
+// k*G).  true: thread 0 claims each tile from the workspace counter when it
+// starts that tile's copy, STAGES tiles ahead of its scan.  Claims are
+// handed out in increasing order, so a CTA still processes its tiles in
+// increasing order and its previous tile still bounds its look-back; what
+// changes is that an SM that streams faster takes more tiles, instead of
+// the look-back chain pacing every CTA at the slowest one's rate.  Each CTA
+// stops at its first claim past the last tile, so a launch makes exactly
+// num_tiles + G claims and the one that makes the last claim resets the
+// counter for the next launch.  Every wait still ends: the CTA owning the
+// smallest unfinished tile has claimed it, has finished its own earlier
+// tiles, and finds every tile below it finished.
+template <typename T, bool INCLUSIVE, int THREADS, int VPT, int STAGES, int K, bool TRACE, bool DYN>
 __global__ void __launch_bounds__(THREADS, 1)
 k_scan_lookback_pipe_sb(const T* in, T* out, size_t n, uint32_t num_tiles, LookbackCtx ctx,
                         const T* carry_in, T* carry_out, unsigned long long* trace) {
@@ -255,50 +268,81 @@ k_scan_lookback_pipe_sb(const T* in, T* out, size_t n, uint32_t num_tiles, Lookb
     constexpr uint32_t TILE = (uint32_t)THREADS * VPT * 4;
     constexpr uint32_t TILE_BYTES = TILE * (uint32_t)sizeof(T);
     constexpr uint32_t SEG = 32u * VPT * 4;
+    constexpr uint32_t kNoTile = 0xffffffffu;
 
     extern __shared__ __align__(128) unsigned char smem_raw[];
     T* ring = reinterpret_cast<T*>(smem_raw);
     __shared__ __align__(8) uint64_t bars[STAGES];
     __shared__ ScanSmem<T, WARPS> sm;
     __shared__ uint32_t s_rank, s_epoch;
+    __shared__ uint32_t s_tile[STAGES];  // DYN: the tile in each stage, kNoTile past the last
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const uint32_t G = gridDim.x;
     const uint64_t policy = policy_evict_first();
 
+    uint32_t issued = 0, consumed = 0;  // thread 0: copies started / stages read
+    bool claims_done = false;           // thread 0 (DYN): a claim has come back past the last tile
+
+    // DYN, thread 0: the next tile id from the counter, or kNoTile.
+    auto claim_next = [&]() -> uint32_t {
+        if (claims_done) return kNoTile;
+        uint32_t id, ep;
+        claim_tile(ctx.counter, num_tiles + G, &id, &ep);
+        s_epoch = ep;
+        if (id < num_tiles) return id;
+        claims_done = true;
+        return kNoTile;
+    };
+
     if (threadIdx.x == 0) {
-        uint32_t rank, epoch;
-        claim_tile(ctx.counter, G, &rank, &epoch);
-        s_rank = rank;
-        s_epoch = epoch;
+        if (!DYN) {
+            uint32_t rank, epoch;
+            claim_tile(ctx.counter, G, &rank, &epoch);
+            s_rank = rank;
+            s_epoch = epoch;
+        } else {
+            s_rank = 0;
+        }
         for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
         fence_async_shared();
     }
-    __syncthreads();
-    const uint32_t rank = s_rank;
-    const uint32_t epoch = s_epoch;
-    if (rank >= G) {
+    if (!DYN) __syncthreads();
+    const uint32_t rank = DYN ? 0u : s_rank;
+    if (!DYN && rank >= G) {
         if (threadIdx.x == 0) record_error(ctx.status, kErrCounter, rank);
         return;
     }
-    const uint32_t count = rank < num_tiles ? (num_tiles - rank + G - 1) / G : 0;
-    uint32_t issued = 0, consumed = 0;  // thread 0
+    const uint32_t count = DYN ? 0u : (rank < num_tiles ? (num_tiles - rank + G - 1) / G : 0);
 
-    auto issue = [&](uint32_t k) {
+    // The tile in this CTA's k-th slot.  DYN reads the id thread 0 stored
+    // when it started that slot's copy; every reader is past a barrier that
+    // follows the store, and the slot is only rewritten after a barrier that
+    // follows every read.
+    auto tile_of = [&](uint32_t k) -> uint32_t {
+        if constexpr (DYN) return s_tile[k % STAGES];
+        else return k < count ? rank + k * G : kNoTile;
+    };
+
+    auto issue = [&](uint32_t k) {  // thread 0
         const int s = (int)(k % STAGES);
-        const size_t base = (size_t)(rank + k * G) * TILE;
-        if (base + TILE <= n) {
-            fence_async_shared();
-            mbar_arrive_expect_tx(&bars[s], TILE_BYTES);
-            bulk_load(ring + (size_t)s * TILE, in + base, TILE_BYTES, &bars[s], policy);
-        } else {
-            mbar_arrive(&bars[s]);
+        const uint32_t t = DYN ? claim_next() : rank + k * G;
+        if (DYN) s_tile[s] = t;
+        if (t != kNoTile) {
+            const size_t base = (size_t)t * TILE;
+            if (base + TILE <= n) {
+                fence_async_shared();
+                mbar_arrive_expect_tx(&bars[s], TILE_BYTES);
+                bulk_load(ring + (size_t)s * TILE, in + base, TILE_BYTES, &bars[s], policy);
+            } else {
+                mbar_arrive(&bars[s]);
+            }
         }
         issued = k + 1;
     };
-    auto read_rows = [&](uint32_t k, T (&v)[VPT][4]) {
-        const size_t tile_base = (size_t)(rank + k * G) * TILE;
+    auto read_rows = [&](uint32_t k, uint32_t t, T (&v)[VPT][4]) {
+        const size_t tile_base = (size_t)t * TILE;
         if (tile_base + TILE <= n) {
             const T* src = ring + (size_t)(k % STAGES) * TILE + (size_t)warp * SEG + (size_t)lane * 4;
 #pragma unroll
@@ -313,9 +357,8 @@ k_scan_lookback_pipe_sb(const T* in, T* out, size_t n, uint32_t num_tiles, Lookb
             load_rows<T, VPT>(in, n, tile_base + (size_t)warp * SEG, lane, false, v);
         }
     };
-    // Waits for tile k, sums it, publishes its aggregate; false if the copy did not arrive.
-    auto reduce_publish = [&](uint32_t k, T* wp, T* agg) -> bool {
-        const uint32_t t = rank + k * G;
+    // Waits for slot k (tile t), sums it, publishes its aggregate; false if the copy did not arrive.
+    auto reduce_publish = [&](uint32_t k, uint32_t t, T* wp, T* agg) -> bool {
         if (TRACE && threadIdx.x == 0) trace[(size_t)t * kTraceWords] = globaltimer_ns();
         const bool ok = mbar_wait_bounded(&bars[k % STAGES], (k / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
         if (__syncthreads_or(!ok)) {
@@ -323,7 +366,7 @@ k_scan_lookback_pipe_sb(const T* in, T* out, size_t n, uint32_t num_tiles, Lookb
             return false;
         }
         T v[VPT][4];
-        read_rows(k, v);
+        read_rows(k, t, v);
         T x = T(0);
 #pragma unroll
         for (int j = 0; j < VPT; ++j) x += ((v[j][0] + v[j][1]) + v[j][2]) + v[j][3];
@@ -331,10 +374,10 @@ k_scan_lookback_pipe_sb(const T* in, T* out, size_t n, uint32_t num_tiles, Lookb
         if (threadIdx.x == 0 && (int64_t)t != ctx.fault_tile) {
             if (t == 0) {
                 if (num_tiles > 1)
-                    st_relaxed_u64(ctx.desc, pack_desc(epoch, kStateP,
+                    st_relaxed_u64(ctx.desc, pack_desc(s_epoch, kStateP,
                                                        to_bits<T>((carry_in ? *carry_in : T(0)) + *agg)));
             } else {
-                st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStateA, to_bits<T>(*agg)));
+                st_relaxed_u64(ctx.desc + t, pack_desc(s_epoch, kStateA, to_bits<T>(*agg)));
             }
             if (TRACE) trace[(size_t)t * kTraceWords + 1] = trace[(size_t)t * kTraceWords + 2] = globaltimer_ns();
         }
@@ -342,17 +385,27 @@ k_scan_lookback_pipe_sb(const T* in, T* out, size_t n, uint32_t num_tiles, Lookb
         return true;
     };
 
+    if (threadIdx.x == 0) {
+        if (DYN)
+            for (uint32_t k = 0; k < (uint32_t)STAGES; ++k) issue(k);
+        else
+            for (uint32_t k = 0; k < count && k < (uint32_t)STAGES; ++k) issue(k);
+    }
+    if (DYN) __syncthreads();  // the first slots' tile ids and the epoch
+    const uint32_t epoch = s_epoch;
+
     T wp_cur = T(0), agg_cur = T(0), prev_incl = T(0);
+    int64_t prev_tile = -1;  // warp 0: this CTA's previous tile, whose inclusive prefix is prev_incl
     bool failed = false;
     uint32_t fail_at = 0;
-    if (threadIdx.x == 0)
-        for (uint32_t k = 0; k < count && k < (uint32_t)STAGES; ++k) issue(k);
-    if (count > 0 && !reduce_publish(0, &wp_cur, &agg_cur)) failed = true;
+    uint32_t t = tile_of(0);
+    if (t != kNoTile && !reduce_publish(0, t, &wp_cur, &agg_cur)) failed = true;
 
-    for (uint32_t k = 0; !failed && k < count; ++k) {
-        const uint32_t t = rank + k * G;
+    uint32_t k = 0;
+    for (; !failed && t != kNoTile; ++k) {
+        const uint32_t tn = tile_of(k + 1);
         T wp_next = T(0), agg_next = T(0);
-        if (k + 1 < count && !reduce_publish(k + 1, &wp_next, &agg_next)) {
+        if (tn != kNoTile && !reduce_publish(k + 1, tn, &wp_next, &agg_next)) {
             failed = true;
             fail_at = k;
             break;
@@ -368,8 +421,7 @@ k_scan_lookback_pipe_sb(const T* in, T* out, size_t n, uint32_t num_tiles, Lookb
             } else if (dead) {
                 lb_failed = true;
             } else {
-                const int64_t floor = k > 0 ? (int64_t)t - (int64_t)G : -1;
-                excl = lookback<T, K, TRACE>(ctx, t, epoch, lane, &lb_failed, &stats, floor, prev_incl);
+                excl = lookback<T, K, TRACE>(ctx, t, epoch, lane, &lb_failed, &stats, prev_tile, prev_incl);
                 if (lane == 0) {
                     if (!lb_failed) {
                         st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStateP, to_bits<T>(excl + agg_cur)));
@@ -380,6 +432,7 @@ k_scan_lookback_pipe_sb(const T* in, T* out, size_t n, uint32_t num_tiles, Lookb
                 }
             }
             prev_incl = excl + agg_cur;
+            prev_tile = t;
             if (lane == 0) {
                 sm.prefix[k & 1] = excl;
                 sm.fail[k & 1] = lb_failed ? 1u : 0u;
@@ -393,13 +446,13 @@ k_scan_lookback_pipe_sb(const T* in, T* out, size_t n, uint32_t num_tiles, Lookb
             }
         }
         T v[VPT][4];
-        read_rows(k, v);
+        read_rows(k, t, v);
         T pre[VPT];
         warp_rows_scan<T, VPT>(v, lane, pre);
         __syncthreads();  // tile k read by everyone; the prefix is in shared memory
         if (threadIdx.x == 0) {
             consumed = k + 1;
-            if (k + STAGES < count) issue(k + STAGES);
+            if (DYN || k + STAGES < count) issue(k + STAGES);
         }
         if (sm.fail[k & 1]) {
             failed = true;
@@ -413,15 +466,25 @@ k_scan_lookback_pipe_sb(const T* in, T* out, size_t n, uint32_t num_tiles, Lookb
         if (TRACE && threadIdx.x == 0) trace[(size_t)t * kTraceWords + 4] = globaltimer_ns();
         wp_cur = wp_next;
         agg_cur = agg_next;
+        t = tn;
     }
 
     if (failed && threadIdx.x == 0) {
-        for (uint32_t k = fail_at + 1; k < count; ++k) {
-            const uint32_t t = rank + k * G;
-            if ((int64_t)t != ctx.fault_tile) st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStatePoison, 0u));
+        // Leaving early: poison this CTA's later tiles (DYN: the ones it has
+        // claimed, then every claim up to its first one past the last tile,
+        // which keeps the launch's claim count exact), and let its copies in
+        // flight land before the shared memory goes away (bounded waits).
+        for (uint32_t j = fail_at + 1; j < (DYN ? issued : count); ++j) {
+            const uint32_t tt = DYN ? s_tile[j % STAGES] : rank + j * G;
+            if (tt != kNoTile && (int64_t)tt != ctx.fault_tile)
+                st_relaxed_u64(ctx.desc + tt, pack_desc(epoch, kStatePoison, 0u));
         }
-        for (uint32_t k = consumed; k < issued; ++k)
-            mbar_wait_bounded(&bars[k % STAGES], (k / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
+        if (DYN)
+            for (uint32_t tt = claim_next(); tt != kNoTile; tt = claim_next())
+                if ((int64_t)tt != ctx.fault_tile) st_relaxed_u64(ctx.desc + tt, pack_desc(epoch, kStatePoison, 0u));
+        for (uint32_t j = consumed; j < issued; ++j)
+            if (!DYN || s_tile[j % STAGES] != kNoTile)
+                mbar_wait_bounded(&bars[j % STAGES], (j / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
     }
 }
 
@@ -636,7 +699,7 @@ k_scan_lookback_lean(const T* in, T* out, size_t n, uint32_t num_tiles, Lookback
 }
 
 template <typename T, bool INCL, int THREADS, int VPT, int STAGES, int K, bool TRACE, bool SB = false,
-          bool LEAN = false>
+          bool LEAN = false, bool DYN = false>
 static cudaError_t launch_pipe(const void* in, void* out, size_t n, const LookbackWs& ws,
                                const void* carry_in, void* carry_out, unsigned long long* trace,
                                cudaStream_t s) {
@@ -644,24 +707,14 @@ static cudaError_t launch_pipe(const void* in, void* out, size_t n, const Lookba
     constexpr size_t SMEM = (size_t)STAGES * TILE * sizeof(T);
     auto kern = [] {
         if constexpr (LEAN) return k_scan_lookback_lean<T, INCL, THREADS, VPT, STAGES, K, TRACE>;
-        else if constexpr (SB) return k_scan_lookback_pipe_sb<T, INCL, THREADS, VPT, STAGES, K, TRACE>;
+        else if constexpr (SB) return k_scan_lookback_pipe_sb<T, INCL, THREADS, VPT, STAGES, K, TRACE, DYN>;
         else return k_scan_lookback_pipe<T, INCL, THREADS, VPT, STAGES, K, TRACE>;
     }();
-    static int blocks_per_sm = -1;  // per instantiation; one device model in a process
-    static int sms = 0;
-    if (blocks_per_sm < 0) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
-        if (e != cudaSuccess) return e;
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        int b = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, THREADS, SMEM);
-        if (e != cudaSuccess) return e;
-        blocks_per_sm = b > 0 ? b : 1;
-    }
+    KernelSetup su;
+    cudaError_t e = kernel_setup(reinterpret_cast<const void*>(kern), THREADS, SMEM, &su);
+    if (e != cudaSuccess) return e;
     const uint32_t tiles = (uint32_t)((n + TILE - 1) / TILE);
-    const size_t resident = (size_t)sms * (size_t)blocks_per_sm;
+    const size_t resident = (size_t)su.sms * (size_t)su.blocks_per_sm;
     const uint32_t grid = (uint32_t)(tiles < resident ? tiles : resident);
     LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};
     kern<<<grid, THREADS, SMEM, s>>>(static_cast<const T*>(in), static_cast<T*>(out), n, tiles, ctx,
@@ -682,6 +735,10 @@ static cudaError_t dispatch_pipe(int config, const void* in, void* out, size_t n
                 return launch_pipe<T, INCL, 512, 8, 3, 1, TRACE, true>(in, out, n, ws, ci, co, tr, s);
             else
                 return launch_pipe<T, INCL, 512, 8, 2, 1, TRACE>(in, out, n, ws, ci, co, tr, s);
+        case 8:  // 18432-element tiles claimed one at a time from the counter
+            return launch_pipe<T, INCL, 512, 9, 3, 1, TRACE, true, false, true>(in, out, n, ws, ci, co, tr, s);
+        case 9:  // the same with 16384-element tiles
+            return launch_pipe<T, INCL, 512, 8, 3, 1, TRACE, true, false, true>(in, out, n, ws, ci, co, tr, s);
         default:  // 2: single register buffer, 18432-element tiles, three 72 KB stages
             return launch_pipe<T, INCL, 512, 9, 3, 1, TRACE, true>(in, out, n, ws, ci, co, tr, s);
     }

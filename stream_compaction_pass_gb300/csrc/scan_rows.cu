@@ -480,18 +480,12 @@ static cudaError_t launch_rows_pipe(const T* in, T* out, size_t rows, size_t col
     constexpr size_t TILE = (size_t)kRPThreads * VPT * 4;
     constexpr size_t SMEM = 3 * TILE * sizeof(T);
     auto kern = k_scan_rows_pipe<T, INCL, VPT>;
-    static int sms = 0;
-    if (sms == 0) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
-        if (e != cudaSuccess) return e;
-        int dev = 0, v = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        sms = v > 0 ? v : 1;
-    }
+    KernelSetup su;
+    cudaError_t e = kernel_setup(reinterpret_cast<const void*>(kern), kRPThreads, SMEM, &su);
+    if (e != cudaSuccess) return e;
     const uint32_t tpr = (uint32_t)((cols + TILE - 1) / TILE);
     const uint32_t tiles = (uint32_t)(rows * tpr);
-    const uint32_t grid = tiles < (uint32_t)sms ? tiles : (uint32_t)sms;
+    const uint32_t grid = tiles < (uint32_t)su.sms ? tiles : (uint32_t)su.sms;
     LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};
     kern<<<grid, kRPThreads, SMEM, s>>>(in, out, cols, tpr, tiles, ctx);
     return cudaGetLastError();
@@ -500,13 +494,12 @@ static cudaError_t launch_rows_pipe(const T* in, T* out, size_t rows, size_t col
 template <typename T, bool INCL>
 static cudaError_t launch_rows(const void* in, void* out, size_t rows, size_t cols, const LookbackWs& ws,
                                cudaStream_t s) {
-    static int sms = 0;
-    if (sms == 0) {
-        int dev = 0, v = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        sms = v > 0 ? v : 1;
-    }
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (sms <= 0) sms = 1;
     const T* pin = static_cast<const T*>(in);
     T* pout = static_cast<T*>(out);
     if (cols <= kRowsWarpMax) {

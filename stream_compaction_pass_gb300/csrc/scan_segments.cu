@@ -377,17 +377,11 @@ static cudaError_t launch_segments(const void* in, void* out, size_t n, const ui
                                    const LookbackWs& ws, cudaStream_t s) {
     constexpr size_t SMEM = 3 * (size_t)kSTile * sizeof(T) + 3 * (size_t)(kSTile / 32) * 4;  // + head words
     auto kern = k_scan_segments<T, INCL>;
-    static int sms = 0;
-    if (sms == 0) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
-        if (e != cudaSuccess) return e;
-        int dev = 0, v = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        sms = v > 0 ? v : 1;
-    }
+    KernelSetup su;
+    cudaError_t e = kernel_setup(reinterpret_cast<const void*>(kern), kSThreads, SMEM, &su);
+    if (e != cudaSuccess) return e;
     const uint32_t tiles = (uint32_t)((n + kSTile - 1) / kSTile);
-    const uint32_t grid = tiles < (uint32_t)sms ? tiles : (uint32_t)sms;
+    const uint32_t grid = tiles < (uint32_t)su.sms ? tiles : (uint32_t)su.sms;
     const bool fast = ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out) |
                         reinterpret_cast<uintptr_t>(bits)) & 15u) == 0;
     LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};

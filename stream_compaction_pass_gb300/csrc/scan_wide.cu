@@ -325,18 +325,11 @@ static cudaError_t launch_wide(const void* in, void* out, size_t n, const Lookba
     constexpr uint32_t TILE = wide_tile<TI>();
     constexpr size_t SMEM = 3 * (size_t)TILE * sizeof(TI);
     auto kern = k_scan_wide<TI, TA, INCL>;
-    static int sms = 0;
-    if (sms == 0) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
-        if (e != cudaSuccess) return e;
-        int dev = 0;
-        cudaGetDevice(&dev);
-        int v = 0;
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        sms = v > 0 ? v : 1;
-    }
+    KernelSetup su;
+    cudaError_t e = kernel_setup(reinterpret_cast<const void*>(kern), kWThreads, SMEM, &su);
+    if (e != cudaSuccess) return e;
     const uint32_t tiles = (uint32_t)((n + TILE - 1) / TILE);
-    const uint32_t grid = tiles < (uint32_t)sms ? tiles : (uint32_t)sms;
+    const uint32_t grid = tiles < (uint32_t)su.sms ? tiles : (uint32_t)su.sms;
     const bool fast = ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) & 15u) == 0;
     LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};
     kern<<<grid, kWThreads, SMEM, s>>>(static_cast<const TI*>(in), static_cast<TA*>(out), n, tiles, fast, ctx);
@@ -592,19 +585,12 @@ static cudaError_t launch_f64_blocked(const void* in, void* out, size_t n, const
     constexpr uint32_t TILE = (uint32_t)THREADS * 16;
     constexpr size_t SMEM = 3 * (size_t)TILE * 8 + 1024;  // two ring stages, the output area, alignment slack
     auto kern = k_scan_f64_blocked<INCL, THREADS>;
-    static int sms = 0;
-    if (sms == 0) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
-        if (e != cudaSuccess) return e;
-        int dev = 0, v = 0, per_sm = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, THREADS, SMEM);
-        if (e != cudaSuccess) return e;
-        sms = (v > 0 ? v : 1) * (per_sm > 0 ? per_sm : 1);  // resident CTAs: the persistent grid
-    }
+    KernelSetup su;
+    cudaError_t e = kernel_setup(reinterpret_cast<const void*>(kern), THREADS, SMEM, &su);
+    if (e != cudaSuccess) return e;
+    const uint32_t resident = (uint32_t)(su.sms * su.blocks_per_sm);  // the persistent grid
     const uint32_t tiles = (uint32_t)((n + TILE - 1) / TILE);
-    const uint32_t grid = tiles < (uint32_t)sms ? tiles : (uint32_t)sms;
+    const uint32_t grid = tiles < resident ? tiles : resident;
     // Full tiles go through the tensor copies: both buffers 16-byte aligned,
     // and every row coordinate within the copies' signed 32-bit range.
     const uint64_t rows = n / 16;
@@ -612,7 +598,7 @@ static cudaError_t launch_f64_blocked(const void* in, void* out, size_t n, const
                       n >= TILE && rows <= (uint64_t)INT32_MAX;
     CUtensorMap map_in{}, map_out{};
     if (fast) {
-        cudaError_t e = encode_rows128_f64(&map_in, in, rows, THREADS < 256 ? THREADS : 256);
+        e = encode_rows128_f64(&map_in, in, rows, THREADS < 256 ? THREADS : 256);
         if (e == cudaSuccess) e = encode_rows128_f64(&map_out, out, rows, 32);
         if (e != cudaSuccess) return e;
     }

@@ -316,21 +316,11 @@ static cudaError_t launch_ws(const void* in, void* out, size_t n, const Lookback
     constexpr size_t TILE = (size_t)DWARPS * 32 * VPT * 4;
     constexpr size_t SMEM = (size_t)STAGES * TILE * sizeof(T);
     auto kern = k_scan_ws<T, INCL, DWARPS, VPT, STAGES, K, LAG, TRACE>;
-    static int blocks_per_sm = -1;  // per instantiation; one device model in a process
-    static int sms = 0;
-    if (blocks_per_sm < 0) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
-        if (e != cudaSuccess) return e;
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        int b = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, THREADS, SMEM);
-        if (e != cudaSuccess) return e;
-        blocks_per_sm = b > 0 ? b : 1;
-    }
+    KernelSetup su;
+    cudaError_t e = kernel_setup(reinterpret_cast<const void*>(kern), THREADS, SMEM, &su);
+    if (e != cudaSuccess) return e;
     const uint32_t tiles = (uint32_t)((n + TILE - 1) / TILE);
-    const size_t resident = (size_t)sms * (size_t)blocks_per_sm;
+    const size_t resident = (size_t)su.sms * (size_t)su.blocks_per_sm;
     const uint32_t grid = (uint32_t)(tiles < resident ? tiles : resident);
     LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};
     kern<<<grid, THREADS, SMEM, s>>>(static_cast<const T*>(in), static_cast<T*>(out), n, tiles, ctx,

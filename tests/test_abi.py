@@ -136,10 +136,10 @@ def test_config_table(lib):
         ss.ss_set_scan_config(c)
         tiles.append(ss.ss_scan_tile_elems())
     assert tiles[0] == 4096 and all(t % 128 == 0 for t in tiles)
-    # -1: chosen per call by size; the tile reported is the large-n row's (2)
+    # -1: chosen per call by size; the tile reported is the large-n row's (8)
     assert lib.ss_set_scan_config(-2) == ss.SS_ERR_INVALID_ARG
     ss.ss_set_scan_config(-1)
-    assert ss.ss_scan_tile_elems() == tiles[2]
+    assert ss.ss_scan_tile_elems() == tiles[8]
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):

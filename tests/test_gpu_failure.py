@@ -17,13 +17,14 @@ pytestmark = pytest.mark.gpu
 TILE = 4096
 
 
-@pytest.fixture(scope="module", params=[0, 2, 5, 6], ids=["one-cta-per-tile", "persistent", "warp-specialised", "lean"])
+@pytest.fixture(scope="module", params=[0, 2, 5, 6, 8],
+                ids=["one-cta-per-tile", "persistent", "warp-specialised", "lean", "claimed-tiles"])
 def ss(request):
     import stream_compaction_pass_gb300 as m
     m.ss_set_scan_config(request.param)
     yield m
     m.ss_debug_set_lookback_fault(-1, 0)
-    m.ss_set_scan_config(2)
+    m.ss_set_scan_config(-1)  # the library's initial, automatic setting
 
 
 def _scan(ss, x):
