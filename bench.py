@@ -38,6 +38,12 @@ UNIT = "G-elem/s"
 N = 100_000_000
 BYTES_PER_ELEM = 8  # one 4-byte read + one 4-byte write
 L2_BYTES = 129 * 1024 * 1024
+# fp64 scan roofline: GB300's nominal FP64 rate is 1.25 TFLOP/s counting an FMA as two
+# operations, i.e. 625e9 FP64 adds per second; the lane-blocked fp64 kernel makes about 2.3
+# adds per element (15 in-lane adds per 16 elements, ~4 warp-scan adds per lane, and one
+# add per output).
+FP64_DADD_PER_S = 625e9
+FP64_ADDS_PER_ELEM = 2.3
 FALLBACK_HBM_GBS = 6800.0
 VARIANTS = [("i32", False), ("i32", True), ("f32", False), ("f32", True)]
 DATA = "synthetic, seeded SplitMix64: int32 U[-1000,1000] (seed 2), fp32 U[0,1) (seed 1)"
@@ -470,7 +476,11 @@ def row_rates(torch, ss, stream, dev, xs_d, xf_d, out_d, launch_ms_by_variant):
             ("u32_u64", lambda: ss.ss_scan_wide(ss.SS_WIDE_U32_U64, True, w_in, w_out, stream=sh), 12),
             ("i64", lambda: ss.ss_scan_wide(ss.SS_WIDE_I64, True, w_64.view(torch.int64), w_out, stream=sh), 16),
             ("f64", lambda: ss.ss_scan_wide(ss.SS_WIDE_F64, True, w_64, w_out, stream=sh), 16)):
-        rows[f"{name}_1e8"] = entry(per * N, time_region(torch, stream, fn, 20))
+        ms = time_region(torch, stream, fn, 20)
+        rows[f"{name}_1e8"] = entry(per * N, ms)
+    # fp64 is bound by FP64 adds on this GPU: a third number, the fraction of the nominal
+    # FP64 add rate (FP64_DADD_PER_S) at the kernel's FP64_ADDS_PER_ELEM adds per element
+    rows["f64_1e8"].append(round(FP64_ADDS_PER_ELEM * N / (rows["f64_1e8"][0] * 1e-3) / FP64_DADD_PER_S, 3))
     del w_in, w_64, w_out
     # batched per-row fp32 inclusive scans: top-p over a 128,256-entry vocabulary, and short rows
     for r_, c_ in ((512, 128256), (262144, 256), (16384, 4096)):

@@ -316,9 +316,9 @@ ss_status ss_copy_u32(const uint32_t *in, uint32_t *out, size_t n, ss_stream_t s
  *   [2] aggregate published   [3] look-back resolved   [4] outputs issued
  *   [5] descriptor windows read   [6] polls that found an unpublished tile
  *   [7] SM id (low 32 bits) | CTA index << 32
- * Rows 0 and 1 and every persistent row have traced builds; others return
- * SS_ERR_UNSUPPORTED.  A persistent row needs 16-byte aligned in/out and
- * n above one tile.  The scan result is the same as scan_exclusive_u32's.
+ * Every row has a traced build (rows 10-12, with the two-level look-back,
+ * record [5] = 1).  A persistent row needs 16-byte aligned in/out and n
+ * above one tile.  The scan result is the same as scan_exclusive_u32's.
  */
 ss_status ss_scan_trace(int config, const uint32_t *in, uint32_t *out, size_t n, uint64_t *d_trace,
                         ss_stream_t stream);
@@ -346,9 +346,10 @@ int ss_scan_config_count(void);
 /* Selects the single-pass scan's tile configuration for later calls in this
  * process (ss_scan_config_count() rows: one CTA per tile, or a persistent
  * grid streaming tiles through a shared-memory ring).  -1 (the initial
- * setting) chooses per call by size: row 7 (16384-element tiles) below 5e7
- * elements, row 8 (18432-element tiles, each claimed from the tile counter
- * as its copy starts, so that faster SMs take more tiles) from there on.
+ * setting) chooses per call by size: row 7 (16384-element tiles) from 2e6
+ * to 5e7 elements, row 8 (18432-element tiles, each claimed from the tile
+ * counter as its copy starts, so that faster SMs take more tiles) below and
+ * above.
  * Results do not depend on it, except for the rounding of fp32 sums.
  * SS_ERR_INVALID_ARG below -1 or from ss_scan_config_count() on. */
 ss_status ss_set_scan_config(int config);

@@ -23,15 +23,18 @@ thread_local std::string g_detail;
 // The scan's configuration row; -1 = chosen per call by size.
 std::atomic<int> g_config{-1};
 
-// Below this many elements the 16384-element-tile row (7) beats the default
-// row (8): its shorter tiles fill and drain the persistent pipeline sooner
-// (measured at 1e6 .. 3e7 elements; from 1e8 on row 8 is ahead).
-constexpr size_t kAutoSmallScan = 50'000'000;
+// Between these sizes the 16384-element-tile row (7) beats the default row
+// (8): its shorter tiles fill and drain the persistent pipeline sooner
+// (measured with L2 flushed at 3e6 .. 3e7 elements).  Below, there are fewer
+// tiles than SMs and row 8's claims win (1e6: 11.9 against 12.6 us); from
+// 1e8 on row 8 is ahead.
+constexpr size_t kAutoMidLow = 2'000'000;
+constexpr size_t kAutoMidHigh = 50'000'000;
 
 int effective_config(size_t n) {
     const int c = g_config.load();
     if (c >= 0) return c;
-    return n < kAutoSmallScan ? 7 : ss::scan_default_config();
+    return (n >= kAutoMidLow && n < kAutoMidHigh) ? 7 : ss::scan_default_config();
 }
 
 std::atomic<int64_t> g_fault_tile{-1};
@@ -222,6 +225,14 @@ ss_status check_scan_args(const void* in, const void* out, size_t n, size_t tile
     return SS_OK;
 }
 
+// Descriptors a single-pass scan of n elements may use: one per tile of the
+// smallest tile any row uses, and one per group of 32 tiles (the two-level
+// look-back of rows 10-12 puts its group descriptors after the tiles').
+size_t scan_desc_count(size_t n) {
+    const size_t tiles = (n + ss::kMinScanTile - 1) / ss::kMinScanTile;
+    return tiles + (tiles + 31) / 32;
+}
+
 ss_status scan_lookback(Dtype dt, bool inclusive, const void* in, void* out, size_t n,
                         const void* carry_in, void* carry_out, cudaStream_t s) {
     const int cfg = effective_config(n);
@@ -233,7 +244,7 @@ ss_status scan_lookback(Dtype dt, bool inclusive, const void* in, void* out, siz
     if (tiles > 1 || g_fault_tile.load() >= 0) {
         st = get_workspace(s, &w);
         if (st != SS_OK) return st;
-        st = ensure_desc(w, tiles);
+        st = ensure_desc(w, scan_desc_count(n));
         if (st != SS_OK) return st;
     }
     cudaError_t e = ss::launch_scan_lookback(dt, inclusive, cfg, in, out, n, make_ws(w), carry_in,
@@ -597,13 +608,12 @@ ss_status ss_scan_trace(int config, const uint32_t* in, uint32_t* out, size_t n,
     if (d_trace == nullptr || (reinterpret_cast<uintptr_t>(d_trace) & 7u))
         return fail(SS_ERR_INVALID_ARG, "trace must be a non-null, 8-byte aligned device pointer");
     const ss::ScanConfig c = ss::scan_config(config);
-    if (!c.persistent && config > 1) return fail(SS_ERR_UNSUPPORTED, "no traced build of this configuration");
     if (c.persistent && (n <= c.tile() || ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) & 15u)))
         return fail(SS_ERR_INVALID_ARG, "a persistent trace needs 16-byte aligned in/out and more than one tile");
     Workspace* w = nullptr;
     st = get_workspace(s, &w);
     if (st != SS_OK) return st;
-    st = ensure_desc(w, (n + ss::kMinScanTile - 1) / ss::kMinScanTile);
+    st = ensure_desc(w, scan_desc_count(n));
     if (st != SS_OK) return st;
     cudaError_t e = ss::launch_scan_trace(config, in, out, n, make_ws(w),
                                           reinterpret_cast<unsigned long long*>(d_trace), s);

@@ -64,8 +64,8 @@ cudaError_t launch_scan_lookback_pipe(Dtype dt, bool inclusive, int config, cons
                                       void* carry_out, cudaStream_t s);
 
 // Exclusive uint32 scan with a per-tile timing trace (8 x uint64 per tile,
-// layout in scan_body.cuh).  Rows 0, 1 and the persistent rows have traced
-// builds; others return cudaErrorInvalidValue.
+// layout in scan_body.cuh).  Every row of the configuration table has a
+// traced build.
 cudaError_t launch_scan_trace(int config, const void* in, void* out, size_t n, const LookbackWs& ws,
                               unsigned long long* trace, cudaStream_t s);
 cudaError_t launch_scan_trace_pipe(int config, const void* in, void* out, size_t n,

@@ -29,7 +29,7 @@ cudaError_t kernel_setup(const void* kern, int threads, size_t max_smem, KernelS
         return cudaSuccess;
     }
     KernelSetup k;
-    if (max_smem > 48 * 1024) {
+    if (max_smem > 0) {  // also at 48 KB and below: static shared memory counts against the default limit
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
         if (e != cudaSuccess) return e;
     }

@@ -118,8 +118,9 @@ __device__ __forceinline__ void record_error(uint32_t* status, uint32_t bits, ui
 
 // Look-back for tile `tile` > 0, run by all 32 lanes of one warp after the
 // tile's aggregate A was published.  Each poll reads a window of 32*K
-// predecessors' descriptors (lane l reads tiles pred - K*l - q, q = 0..K-1,
-// so lane order is distance order), waits while any descriptor up to the
+// predecessors' descriptors in K coalesced loads: load q of lane l reads the
+// tile at distance 32q + l + 1 (so each load instruction covers 32
+// consecutive descriptors, 256 bytes), waits while any descriptor up to the
 // nearest P is still X, and sums values back to and including that P; with
 // no P in the window it sums the whole window and moves 32*K tiles further
 // back.  Returns the tile's exclusive prefix in every lane; sets *failed
@@ -147,7 +148,7 @@ __device__ __forceinline__ LookbackWindow<K> lookback_prefetch(const LookbackCtx
     const int64_t pred = (int64_t)tile - 1;
 #pragma unroll
     for (int q = 0; q < K; ++q) {
-        const int64_t idx = pred - (int64_t)lane * K - q;
+        const int64_t idx = pred - 32 * q - lane;
         w.d[q] = idx > floor ? ld_relaxed_u64(c.desc + idx) : floor_desc;
     }
     return w;
@@ -175,7 +176,6 @@ __device__ __forceinline__ T lookback(const LookbackCtx& c, uint32_t tile, uint3
     *failed = false;
     while (true) {
         unsigned long long d[K];
-        uint32_t st[K];
         if (use_window) {
 #pragma unroll
             for (int q = 0; q < K; ++q) d[q] = window->d[q];
@@ -183,28 +183,32 @@ __device__ __forceinline__ T lookback(const LookbackCtx& c, uint32_t tile, uint3
         } else {
 #pragma unroll
             for (int q = 0; q < K; ++q) {
-                const int64_t idx = pred - (int64_t)lane * K - q;
+                const int64_t idx = pred - 32 * q - lane;
                 d[q] = idx > floor ? ld_relaxed_u64(c.desc + idx) : floor_desc;
             }
         }
+        // Nearest stop (P or POISON) in distance order: load q, then lane.
+        int qstop = K;     // load holding the nearest stop, K if none
+        int first = 31;    // its lane
+        bool x_before = false;  // an unpublished descriptor nearer than the stop
 #pragma unroll
         for (int q = 0; q < K; ++q) {
             const uint32_t hi = (uint32_t)(d[q] >> 32);
-            st[q] = ((hi & ~3u) == tag) ? (hi & 3u) : kStateX;
+            const uint32_t st = ((hi & ~3u) == tag) ? (hi & 3u) : kStateX;
+            const uint32_t stops = __ballot_sync(kFullMask, st == kStateP || st == kStatePoison);
+            const uint32_t xs = __ballot_sync(kFullMask, st == kStateX);
+            if (qstop == K) {
+                if (stops) {
+                    qstop = q;
+                    first = __ffs(stops) - 1;
+                    if (xs & ((1u << first) - 1u)) x_before = true;
+                } else if (xs) {
+                    x_before = true;
+                }
+            }
         }
-        int qs = K;  // this lane's nearest stop (P or POISON), K if none
-#pragma unroll
-        for (int q = K - 1; q >= 0; --q)
-            if (st[q] == kStateP || st[q] == kStatePoison) qs = q;
-        bool lane_x = false;  // an unpublished descriptor before this lane's stop
-#pragma unroll
-        for (int q = 0; q < K; ++q)
-            if (q < qs && st[q] == kStateX) lane_x = true;
         if (TRACE) stats->windows += 1;
-        const uint32_t stop_mask = __ballot_sync(kFullMask, qs < K);
-        const int first = stop_mask ? __ffs(stop_mask) - 1 : 31;
-        const uint32_t upto = (first == 31) ? kFullMask : ((2u << first) - 1u);
-        if (__ballot_sync(kFullMask, lane_x) & upto) {
+        if (x_before) {
             // A predecessor up to the nearest P has not published yet: wait.
             ++polls;
             if (TRACE) stats->waits += 1;
@@ -218,27 +222,100 @@ __device__ __forceinline__ T lookback(const LookbackCtx& c, uint32_t tile, uint3
             }
             continue;
         }
-        if (stop_mask) {
-            bool poisoned = false;
-#pragma unroll
-            for (int q = 0; q < K; ++q)
-                if (q == qs && st[q] == kStatePoison) poisoned = true;
-            if ((__ballot_sync(kFullMask, poisoned) >> first) & 1u) {
-                *failed = true;
-                return T(0);
-            }
-        }
         T v = T(0);
-        const bool whole = (stop_mask == 0) || lane < first;
-        const bool part = (stop_mask != 0) && lane == first;
+        bool poisoned = false;
 #pragma unroll
-        for (int q = 0; q < K; ++q)
-            if (whole || (part && q <= qs)) v += from_bits<T>((uint32_t)d[q]);
+        for (int q = 0; q < K; ++q) {
+            if (q < qstop || (q == qstop && lane <= first)) v += from_bits<T>((uint32_t)d[q]);
+            if (q == qstop && lane == first && (uint32_t)(d[q] >> 32) == (tag | kStatePoison)) poisoned = true;
+        }
+        if (__any_sync(kFullMask, poisoned)) {
+            *failed = true;
+            return T(0);
+        }
         acc += warp_sum(v);
-        if (stop_mask) return acc;
+        if (qstop < K) return acc;
         pred -= 32 * K;
         polls = 0;
     }
+}
+
+// Two-level look-back, for kernels that run one CTA per tile: tiles form
+// groups of 32 consecutive tiles, and group g has its own descriptor
+// gdesc[g], published by the group's last tile -- first as A (the group's
+// total), then as P (the inclusive prefix through the group).  A tile reads
+// the descriptors of the tiles before it in its group (one load per lane):
+// if one of them holds a P, the tile's prefix is that P plus the aggregates
+// after it; otherwise their aggregates give the tile's offset inside the
+// group, and a look-back over the group descriptors gives the group's
+// prefix.  Tile t therefore needs about two round trips whatever t is,
+// where the one-level look-back walks back t/32 windows while the tiles
+// before it are still being resolved.  `agg` is the tile's aggregate (used
+// for the group descriptors).  Returns the exclusive prefix in every lane;
+// sets *failed (warp uniform) if a wait ran out or a predecessor was
+// poisoned.  Tile 0 is not handled here (its prefix is the seed).
+template <typename T>
+__device__ __forceinline__ T lookback_two_level(const LookbackCtx& c, unsigned long long* gdesc, uint32_t tile,
+                                                uint32_t num_tiles, uint32_t epoch, int lane, T agg,
+                                                bool* failed) {
+    const uint32_t tag = epoch << 2;
+    const uint32_t g = tile >> 5;
+    const uint32_t mate = (g << 5) + (uint32_t)lane;  // this lane's tile in the group
+    const bool valid = mate < tile;
+    const bool last_of_group = (tile & 31u) == 31u;
+    *failed = false;
+    uint32_t polls = 0;
+    uint64_t t0 = 0;
+    T in_group = T(0);
+    bool have_p = false;
+    while (true) {
+        const unsigned long long d = valid ? ld_relaxed_u64(c.desc + mate) : 0ull;
+        const uint32_t hi = (uint32_t)(d >> 32);
+        const uint32_t st = ((hi & ~3u) == tag) ? (hi & 3u) : kStateX;
+        const uint32_t pm = __ballot_sync(kFullMask, valid && (st == kStateP || st == kStatePoison));
+        const int p = pm ? 31 - __clz(pm) : -1;                          // nearest stop: the highest such lane
+        const uint32_t after = p >= 0 ? ~((2u << p) - 1u) : kFullMask;   // lanes nearer than the stop
+        if (__ballot_sync(kFullMask, valid && st == kStateX) & after) {
+            ++polls;
+            if (polls == 1) t0 = globaltimer_ns();
+            if (polls > 4) __nanosleep(polls < 16 ? 32 : (polls < 64 ? 128 : 256));
+            bool give_up = polls >= c.max_polls || (globaltimer_ns() - t0) > c.timeout_ns;
+            give_up = __shfl_sync(kFullMask, give_up, 0);
+            if (give_up) {
+                *failed = true;
+                if (last_of_group && lane == 0) st_relaxed_u64(gdesc + g, pack_desc(epoch, kStatePoison, 0u));
+                return T(0);
+            }
+            continue;
+        }
+        if (p >= 0 && __shfl_sync(kFullMask, st, p) == kStatePoison) {
+            *failed = true;
+            if (last_of_group && lane == 0) st_relaxed_u64(gdesc + g, pack_desc(epoch, kStatePoison, 0u));
+            return T(0);
+        }
+        const bool take = valid && (int)lane >= p;
+        in_group = warp_sum(take ? from_bits<T>((uint32_t)d) : T(0));
+        have_p = p >= 0;
+        break;
+    }
+    T excl = in_group;
+    if (!have_p) {
+        // No inclusive prefix before this tile in its group (g > 0: tile 0
+        // always publishes one): in_group is the tile's offset in the group.
+        if (last_of_group && lane == 0) st_relaxed_u64(gdesc + g, pack_desc(epoch, kStateA, to_bits<T>(in_group + agg)));
+        compiler_fence();
+        LookbackCtx gc = c;
+        gc.desc = gdesc;
+        const T gp = lookback<T, 1>(gc, g, epoch, lane, failed);
+        if (*failed) {
+            if (last_of_group && lane == 0) st_relaxed_u64(gdesc + g, pack_desc(epoch, kStatePoison, 0u));
+            return T(0);
+        }
+        excl = gp + in_group;
+    }
+    if (last_of_group && lane == 0 && tile + 1 < num_tiles)
+        st_relaxed_u64(gdesc + g, pack_desc(epoch, kStateP, to_bits<T>(excl + agg)));
+    return excl;
 }
 
 }  // namespace ss

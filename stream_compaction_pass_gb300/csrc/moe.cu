@@ -126,7 +126,7 @@ cudaError_t launch_moe_counts_offsets(const int32_t* ids, size_t m, int32_t num_
                                       uint32_t* counts, uint32_t* offsets, uint32_t* acc, uint32_t* ticket,
                                       uint32_t grid, cudaStream_t s) {
     const size_t smem = (size_t)num_experts * 4;
-    if (smem > 48 * 1024) {  // the limit is raised once per device, to the largest expert count
+    if (smem > 0) {  // the limit is raised once per device, to the largest expert count
         KernelSetup su;
         cudaError_t e = kernel_setup(reinterpret_cast<const void*>(k_moe_counts_offsets), kMoeThreads,
                                      (size_t)kMoeMaxExperts * 4, &su);

@@ -19,7 +19,7 @@
 
 namespace ss {
 
-template <typename T, bool INCLUSIVE, int THREADS, int VPT, int K, bool TRACE>
+template <typename T, bool INCLUSIVE, int THREADS, int VPT, int K, bool TRACE, bool GROUPED>
 __global__ void __launch_bounds__(THREADS)
 k_scan_lookback(const T* in, T* out, size_t n, uint32_t num_tiles, LookbackCtx ctx, bool aligned,
                 const T* carry_in, T* carry_out, unsigned long long* trace) {
@@ -53,8 +53,8 @@ k_scan_lookback(const T* in, T* out, size_t n, uint32_t num_tiles, LookbackCtx c
     const bool fast = aligned && (seg + SEG <= n);
     T v[VPT][4];
     load_rows<T, VPT>(in, n, seg, lane, fast, v);
-    scan_tile_body<T, INCLUSIVE, THREADS, VPT, K, TRACE>(v, out, n, seg, fast, tile, num_tiles, epoch,
-                                                         ctx, carry_in, carry_out, sm, rec);
+    scan_tile_body<T, INCLUSIVE, THREADS, VPT, K, TRACE, GROUPED>(v, out, n, seg, fast, tile, num_tiles, epoch,
+                                                                  ctx, carry_in, carry_out, sm, rec);
 }
 
 template <int THREADS, int VPT>
@@ -83,6 +83,9 @@ static const ScanConfig kConfigs[] = {
     {1, 512, 32, 2, 1},  // 7: persistent, 16384, 2-stage ring (128 KB), double register buffer
     {1, 512, 36, 3, 1},  // 8: as row 2, each tile claimed from the counter when its copy starts -- the default
     {1, 512, 32, 3, 1},  // 9: as row 8 with 16384-element tiles
+    {0, 256, 16, 0, 1},  // 10: one CTA per 4096-element tile, two-level look-back (groups of 32 tiles)
+    {0, 256, 32, 0, 1},  // 11: the same with 8192-element tiles
+    {0, 512, 16, 0, 1},  // 12: the same with 8192-element tiles of 512 threads
 };
 constexpr int kNumConfigs = sizeof(kConfigs) / sizeof(kConfigs[0]);
 constexpr int kDefaultConfig = 8;
@@ -95,14 +98,14 @@ static bool aligned16(const void* a, const void* b) {
     return ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b)) & 15u) == 0;
 }
 
-template <typename T, bool INCL, int THREADS, int VPT, int K, bool TRACE = false>
+template <typename T, bool INCL, int THREADS, int VPT, int K, bool TRACE = false, bool GROUPED = false>
 static cudaError_t launch_one(const void* in, void* out, size_t n, const LookbackWs& ws,
                              const void* carry_in, void* carry_out, cudaStream_t s,
                              unsigned long long* trace = nullptr) {
     const size_t tile = (size_t)THREADS * VPT * 4;
     const uint32_t tiles = (uint32_t)((n + tile - 1) / tile);
     LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};
-    k_scan_lookback<T, INCL, THREADS, VPT, K, TRACE><<<tiles, THREADS, 0, s>>>(
+    k_scan_lookback<T, INCL, THREADS, VPT, K, TRACE, GROUPED><<<tiles, THREADS, 0, s>>>(
         static_cast<const T*>(in), static_cast<T*>(out), n, tiles, ctx, aligned16(in, out),
         static_cast<const T*>(carry_in), static_cast<T*>(carry_out), trace);
     return cudaGetLastError();
@@ -111,8 +114,13 @@ static cudaError_t launch_one(const void* in, void* out, size_t n, const Lookbac
 template <typename T, bool INCL>
 static cudaError_t dispatch_config(int config, const void* in, void* out, size_t n,
                                    const LookbackWs& ws, const void* ci, void* co, cudaStream_t s) {
-    if (config == 1) return launch_one<T, INCL, 256, 8, 1>(in, out, n, ws, ci, co, s);
-    return launch_one<T, INCL, 256, 4, 1>(in, out, n, ws, ci, co, s);
+    switch (config) {
+        case 1: return launch_one<T, INCL, 256, 8, 1>(in, out, n, ws, ci, co, s);
+        case 10: return launch_one<T, INCL, 256, 4, 1, false, true>(in, out, n, ws, ci, co, s);
+        case 11: return launch_one<T, INCL, 256, 8, 1, false, true>(in, out, n, ws, ci, co, s);
+        case 12: return launch_one<T, INCL, 512, 4, 1, false, true>(in, out, n, ws, ci, co, s);
+        default: return launch_one<T, INCL, 256, 4, 1>(in, out, n, ws, ci, co, s);
+    }
 }
 
 // The persistent kernel needs 16-byte aligned in/out (bulk copies) and at
@@ -152,7 +160,10 @@ cudaError_t launch_scan_trace(int config, const void* in, void* out, size_t n, c
     switch (config) {
         case 1: return launch_one<uint32_t, false, 256, 8, 1, true>(in, out, n, ws, nullptr, nullptr, s, trace);
         case 0: return launch_one<uint32_t, false, 256, 4, 1, true>(in, out, n, ws, nullptr, nullptr, s, trace);
-        default: return cudaErrorInvalidValue;  // traced builds exist for rows 0, 1 and the persistent rows
+        case 10: return launch_one<uint32_t, false, 256, 4, 1, true, true>(in, out, n, ws, nullptr, nullptr, s, trace);
+        case 11: return launch_one<uint32_t, false, 256, 8, 1, true, true>(in, out, n, ws, nullptr, nullptr, s, trace);
+        case 12: return launch_one<uint32_t, false, 512, 4, 1, true, true>(in, out, n, ws, nullptr, nullptr, s, trace);
+        default: return cudaErrorInvalidValue;  // every row has a traced build
     }
 }
 

@@ -44,7 +44,7 @@ __device__ __forceinline__ uint32_t sm_id() {
 // (CTA-uniform) if the look-back failed; the tile's outputs are then not
 // written and an error has been recorded.  With TRACE, thread 0 fills
 // rec[1..7] (rec[0] is the caller's).
-template <typename T, bool INCLUSIVE, int THREADS, int VPT, int K, bool TRACE = false>
+template <typename T, bool INCLUSIVE, int THREADS, int VPT, int K, bool TRACE = false, bool GROUPED = false>
 __device__ __forceinline__ bool scan_tile_body(const T (&v)[VPT][4], T* out, size_t n, size_t seg,
                                                bool full, uint32_t tile, uint32_t num_tiles,
                                                uint32_t epoch, const LookbackCtx& ctx,
@@ -79,7 +79,14 @@ __device__ __forceinline__ bool scan_tile_body(const T (&v)[VPT][4], T* out, siz
                 st_relaxed_u64(ctx.desc + tile, pack_desc(epoch, kStateA, to_bits<T>(block_total)));
             compiler_fence();  // publish before looking back
             if (TRACE && lane == 0) rec[2] = globaltimer_ns();
-            excl = lookback<T, K, TRACE>(ctx, tile, epoch, lane, &failed, &stats);
+            if constexpr (GROUPED) {
+                // group descriptors follow the launch's tile descriptors
+                excl = lookback_two_level<T>(ctx, ctx.desc + num_tiles, tile, num_tiles, epoch, lane, block_total,
+                                             &failed);
+                if (TRACE) stats.windows = 1;
+            } else {
+                excl = lookback<T, K, TRACE>(ctx, tile, epoch, lane, &failed, &stats);
+            }
             if (lane == 0) {
                 if (!failed) {
                     st_relaxed_u64(ctx.desc + tile,

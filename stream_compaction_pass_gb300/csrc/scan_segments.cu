@@ -8,7 +8,8 @@
 //   1. k_segment_heads marks every segment start in a bitmask over the
 //      elements (one bit per element, zeroed just before on the stream).
 //   2. k_scan_segments runs the persistent single-pass scan (the schedule of
-//      scan_pipe.cu's single-register-buffer kernel) with a segmented add.
+//      scan_pipe.cu's single-register-buffer kernel, with each tile claimed
+//      from the counter when its copy starts) with a segmented add.
 //      The segmented add works on pairs (f, s): f says whether a segment
 //      starts in the span, s is the sum since the last start in it, or over
 //      the whole span if none.  (fa, sa) then (fb, sb) gives
@@ -127,50 +128,65 @@ k_scan_segments(const T* in, T* out, size_t n, const uint32_t* bits, uint32_t nu
     __shared__ T s_ws[2][kSWarps];         // warp summaries, by tile parity
     __shared__ uint32_t s_wf[2][kSWarps];
     __shared__ T s_prefix[2];
-    __shared__ uint32_t s_fail[2], s_rank, s_epoch;
+    __shared__ uint32_t s_fail[2], s_epoch;
+    __shared__ uint32_t s_tile[STAGES];  // the tile in each stage, kNoTile past the last
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const uint32_t G = gridDim.x;
     const uint64_t policy = policy_evict_first();
+    constexpr uint32_t kNoTile = 0xffffffffu;
 
-    if (threadIdx.x == 0) {
-        uint32_t rank, epoch;
-        claim_tile(ctx.counter, G, &rank, &epoch);
-        s_rank = rank;
-        s_epoch = epoch;
-        for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
-        fence_async_shared();
-    }
-    __syncthreads();
-    const uint32_t rank = s_rank;
-    const uint32_t epoch = s_epoch;
-    if (rank >= G) {
-        if (threadIdx.x == 0) record_error(ctx.status, kErrCounter, rank);
-        return;
-    }
-    const uint32_t count = rank < num_tiles ? (num_tiles - rank + G - 1) / G : 0;
+    // Tiles are claimed one at a time, when their copy starts (the scheme of
+    // scan_pipe.cu's default row): claims come out in increasing order, each
+    // CTA stops at its first claim past the last tile, so a launch makes
+    // num_tiles + G claims and the last one resets the counter.
     uint32_t issued = 0, consumed = 0;  // thread 0
-
-    auto full_tile = [&](uint32_t k) { return fast && (size_t)(rank + k * G) * kSTile + kSTile <= n; };
-    auto issue = [&](uint32_t k) {
+    bool claims_done = false;           // thread 0
+    auto claim_next = [&]() -> uint32_t {
+        if (claims_done) return kNoTile;
+        uint32_t id, ep;
+        claim_tile(ctx.counter, num_tiles + G, &id, &ep);
+        s_epoch = ep;
+        if (id < num_tiles) return id;
+        claims_done = true;
+        return kNoTile;
+    };
+    auto full_tile = [&](uint32_t t) { return fast && (size_t)t * kSTile + kSTile <= n; };
+    auto issue = [&](uint32_t k) {  // thread 0
         const int s = (int)(k % STAGES);
-        if (full_tile(k)) {
-            const size_t t = rank + k * G;
-            fence_async_shared();
-            mbar_arrive_expect_tx(&bars[s], TILE_BYTES + HEAD_WORDS * 4);
-            bulk_load(ring + (size_t)s * kSTile, in + t * kSTile, TILE_BYTES, &bars[s], policy);
-            bulk_load(heads + (size_t)s * HEAD_WORDS, bits + t * HEAD_WORDS, HEAD_WORDS * 4, &bars[s], policy);
-        } else {
-            mbar_arrive(&bars[s]);  // read from global with bounds checks instead
+        const uint32_t t = claim_next();
+        s_tile[s] = t;
+        if (t != kNoTile) {
+            if (full_tile(t)) {
+                fence_async_shared();
+                mbar_arrive_expect_tx(&bars[s], TILE_BYTES + HEAD_WORDS * 4);
+                bulk_load(ring + (size_t)s * kSTile, in + (size_t)t * kSTile, TILE_BYTES, &bars[s], policy);
+                bulk_load(heads + (size_t)s * HEAD_WORDS, bits + (size_t)t * HEAD_WORDS, HEAD_WORDS * 4, &bars[s],
+                          policy);
+            } else {
+                mbar_arrive(&bars[s]);  // read from global with bounds checks instead
+            }
         }
         issued = k + 1;
     };
-    // This lane's rows of tile k.
-    auto read_rows = [&](uint32_t k, T (&v)[VPT][4]) {
-        const size_t tile_base = (size_t)(rank + k * G) * kSTile;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
+        fence_async_shared();
+        for (uint32_t k = 0; k < (uint32_t)STAGES; ++k) issue(k);
+    }
+    __syncthreads();  // the barriers, the first slots' tile ids and the epoch
+    const uint32_t epoch = s_epoch;
+    // The tile in this CTA's k-th slot: thread 0 stored it when it started
+    // the slot's copy; every reader is past a barrier that follows the store,
+    // and the slot is only rewritten after a barrier that follows every read.
+    auto tile_of = [&](uint32_t k) -> uint32_t { return s_tile[k % STAGES]; };
+
+    // This lane's rows of slot k (tile t).
+    auto read_rows = [&](uint32_t k, uint32_t t, T (&v)[VPT][4]) {
+        const size_t tile_base = (size_t)t * kSTile;
         const size_t seg = tile_base + (size_t)warp * kSSeg;
-        if (full_tile(k)) {
+        if (full_tile(t)) {
             const T* src = ring + (size_t)(k % STAGES) * kSTile + (size_t)warp * kSSeg + (size_t)lane * 4;
 #pragma unroll
             for (int j = 0; j < VPT; ++j) {
@@ -199,15 +215,14 @@ k_scan_segments(const T* in, T* out, size_t n, const uint32_t* bits, uint32_t nu
     // summaries in s_ws/s_wf[k & 1]; returns the tile summary and this
     // lane's head bits (nibble j = row j).  A warp with no segment start in
     // its span sums plainly.
-    auto reduce_publish = [&](uint32_t k, SegPair<T>* tile_pair, uint32_t* hb_out) -> bool {
-        const uint32_t t = rank + k * G;
+    auto reduce_publish = [&](uint32_t k, uint32_t t, SegPair<T>* tile_pair, uint32_t* hb_out) -> bool {
         const bool ok = mbar_wait_bounded(&bars[k % STAGES], (k / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
         if (__syncthreads_or(!ok)) {
             if (threadIdx.x == 0) record_error(ctx.status, kErrBulkTimeout, t);
             return false;
         }
         uint32_t hb = 0;
-        const bool full = full_tile(k);
+        const bool full = full_tile(t);
         const uint32_t* hw = heads + (size_t)(k % STAGES) * HEAD_WORDS;
         const size_t wbase = (size_t)t * HEAD_WORDS;  // the tile's first head word in `bits`
         const size_t nwords = (n + 31) / 32;
@@ -219,7 +234,7 @@ k_scan_segments(const T* in, T* out, size_t n, const uint32_t* bits, uint32_t nu
         }
         *hb_out = hb;
         T v[VPT][4];
-        read_rows(k, v);
+        read_rows(k, t, v);
         SegPair<T> w{0u, T(0)};
         if (__any_sync(kFullMask, hb != 0u)) {
 #pragma unroll
@@ -257,15 +272,15 @@ k_scan_segments(const T* in, T* out, size_t n, const uint32_t* bits, uint32_t nu
     SegPair<T> tp_cur{0u, T(0)}, tp_next{0u, T(0)};
     uint32_t hb_cur = 0, hb_next = 0;
     T prev_incl = T(0);
+    int64_t prev_tile = -1;  // warp 0: this CTA's previous tile, whose inclusive prefix is prev_incl
     bool failed = false;
     uint32_t fail_at = 0;
-    if (threadIdx.x == 0)
-        for (uint32_t k = 0; k < count && k < (uint32_t)STAGES; ++k) issue(k);
-    if (count > 0 && !reduce_publish(0, &tp_cur, &hb_cur)) failed = true;
+    uint32_t t = tile_of(0);
+    if (t != kNoTile && !reduce_publish(0, t, &tp_cur, &hb_cur)) failed = true;
 
-    for (uint32_t k = 0; !failed && k < count; ++k) {
-        const uint32_t t = rank + k * G;
-        if (k + 1 < count && !reduce_publish(k + 1, &tp_next, &hb_next)) {
+    for (uint32_t k = 0; !failed && t != kNoTile; ++k) {
+        const uint32_t tn = tile_of(k + 1);
+        if (tn != kNoTile && !reduce_publish(k + 1, tn, &tp_next, &hb_next)) {
             failed = true;
             fail_at = k;
             break;
@@ -279,8 +294,7 @@ k_scan_segments(const T* in, T* out, size_t n, const uint32_t* bits, uint32_t nu
             } else if (dead) {
                 lb_failed = true;
             } else {
-                const int64_t floor = k > 0 ? (int64_t)t - (int64_t)G : -1;
-                excl = lookback<T, 1>(ctx, t, epoch, lane, &lb_failed, nullptr, floor, prev_incl);
+                excl = lookback<T, 1>(ctx, t, epoch, lane, &lb_failed, nullptr, prev_tile, prev_incl);
                 if (lane == 0) {
                     if (lb_failed) {
                         st_relaxed_u64(ctx.desc + t, pack_desc(epoch, kStatePoison, 0u));
@@ -291,6 +305,7 @@ k_scan_segments(const T* in, T* out, size_t n, const uint32_t* bits, uint32_t nu
                 }
             }
             prev_incl = tp_cur.f ? tp_cur.s : excl + tp_cur.s;
+            prev_tile = t;
             if (lane == 0) {
                 s_prefix[k & 1] = excl;
                 s_fail[k & 1] = lb_failed ? 1u : 0u;
@@ -299,7 +314,7 @@ k_scan_segments(const T* in, T* out, size_t n, const uint32_t* bits, uint32_t nu
         // Tile k's rows: lane summaries, segmented warp scans per row (or
         // plain ones where this warp's span holds no segment start).
         T v[VPT][4];
-        read_rows(k, v);
+        read_rows(k, t, v);
         const uint32_t hb = hb_cur;
         const bool seg_warp = __any_sync(kFullMask, hb != 0u);
         SegPair<T> ex[VPT], rt[VPT];  // per row: what the lanes before hold, and the row's total
@@ -324,7 +339,7 @@ k_scan_segments(const T* in, T* out, size_t n, const uint32_t* bits, uint32_t nu
         __syncthreads();  // tile k read by everyone; the prefix is in shared memory
         if (threadIdx.x == 0) {
             consumed = k + 1;
-            if (k + STAGES < count) issue(k + STAGES);
+            issue(k + STAGES);
         }
         if (s_fail[k & 1]) {
             failed = true;
@@ -357,18 +372,26 @@ k_scan_segments(const T* in, T* out, size_t n, const uint32_t* bits, uint32_t nu
                 run = seg_add(run, rt[j]);
             }
         }
-        store_rows<T, VPT>(out, n, tile_base + (size_t)warp * kSSeg, lane, full_tile(k), v);
+        store_rows<T, VPT>(out, n, tile_base + (size_t)warp * kSSeg, lane, full_tile(t), v);
         tp_cur = tp_next;
         hb_cur = hb_next;
+        t = tn;
     }
 
     if (failed && threadIdx.x == 0) {
-        for (uint32_t j = fail_at + 1; j < count; ++j) {
-            const uint32_t tt = rank + j * G;
-            if ((int64_t)tt != ctx.fault_tile) st_relaxed_u64(ctx.desc + tt, pack_desc(epoch, kStatePoison, 0u));
+        // Leaving early: poison the tiles this CTA has claimed and every later
+        // claim up to its first one past the last tile (which keeps the
+        // launch's claim count exact); let copies in flight land.
+        for (uint32_t j = fail_at + 1; j < issued; ++j) {
+            const uint32_t tt = s_tile[j % STAGES];
+            if (tt != kNoTile && (int64_t)tt != ctx.fault_tile)
+                st_relaxed_u64(ctx.desc + tt, pack_desc(epoch, kStatePoison, 0u));
         }
+        for (uint32_t tt = claim_next(); tt != kNoTile; tt = claim_next())
+            if ((int64_t)tt != ctx.fault_tile) st_relaxed_u64(ctx.desc + tt, pack_desc(epoch, kStatePoison, 0u));
         for (uint32_t j = consumed; j < issued; ++j)
-            mbar_wait_bounded(&bars[j % STAGES], (j / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
+            if (s_tile[j % STAGES] != kNoTile)
+                mbar_wait_bounded(&bars[j % STAGES], (j / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
     }
 }
 

@@ -17,8 +17,8 @@ pytestmark = pytest.mark.gpu
 TILE = 4096
 
 
-@pytest.fixture(scope="module", params=[0, 2, 5, 6, 8],
-                ids=["one-cta-per-tile", "persistent", "warp-specialised", "lean", "claimed-tiles"])
+@pytest.fixture(scope="module", params=[0, 2, 5, 6, 8, 10],
+                ids=["one-cta-per-tile", "persistent", "warp-specialised", "lean", "claimed-tiles", "two-level"])
 def ss(request):
     import stream_compaction_pass_gb300 as m
     m.ss_set_scan_config(request.param)

@@ -194,7 +194,7 @@ def test_in_place(ss, kind):
         assert_equal(got, ref.astype(got.dtype) if kind == "f32" else ref)
 
 
-NUM_CONFIGS = 10
+NUM_CONFIGS = 13
 
 
 @pytest.mark.parametrize("config", range(NUM_CONFIGS))
@@ -292,11 +292,12 @@ def test_trace_build_scans_and_records(ss, config):
     assert (rec[0, 5] == 0)
 
 
-@pytest.mark.parametrize("n", [3_000_017, 49_999_999, 50_000_000, 60_000_001])
+@pytest.mark.parametrize("n", [1_000_003, 1_999_999, 2_000_000, 3_000_017, 49_999_999, 50_000_000, 60_000_001])
 def test_automatic_configuration(ss, n):
-    # the initial setting (-1) picks the 16384-element-tile row below 5e7
-    # elements and the 18432 row from there on; both sides of the switch,
-    # int32 exclusive and fp32 inclusive and exclusive
+    # the initial setting (-1) picks the 16384-element-tile row from 2e6 to
+    # 5e7 elements and the 18432 row (tiles claimed from the counter) below
+    # and above; both sides of each switch, int32 exclusive and fp32
+    # inclusive and exclusive
     import torch
     ss.ss_set_scan_config(-1)
     try:
@@ -319,8 +320,9 @@ def test_automatic_configuration(ss, n):
 
 
 def test_automatic_configuration_carries_between_chunks(ss):
-    # under the automatic choice, chunks below the switch take the
-    # 16384-element-tile row: a carried prefix must chain through it
+    # under the automatic choice the first chunk (1e6) takes the 18432 row
+    # and the others the 16384-element-tile row: a carried prefix must chain
+    # through both
     import torch
     ss.ss_set_scan_config(-1)
     try:
