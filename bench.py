@@ -562,8 +562,9 @@ def run_ours(args) -> None:
     st, _ = ss.ss_stream_status(sh)
     assert st == ss.SS_OK
 
-    # per-launch events inside the timed region
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(launches) + 1)] for _ in range(args.steps)]
+    # The timed region: K steps between two events on the launching stream.  No event sits
+    # between launches (each one adds ~2 us of gap), so the mean launch duration of the scan
+    # kernel is the region's time over its launches, inter-launch gaps included.
     sampler = ClockSampler(gpu_uuid(torch, dev)) if rank == 0 else None
     if world > 1:
         torch.distributed.barrier()
@@ -571,11 +572,9 @@ def run_ours(args) -> None:
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
-    for k in range(args.steps):
-        ev[k][0].record(stream)
-        for j, f in enumerate(launches):
+    for _ in range(args.steps):
+        for f in launches:
             f()
-            ev[k][j + 1].record(stream)
     t_end.record(stream)
     t_end.synchronize()
     torch.cuda.synchronize()
@@ -583,7 +582,7 @@ def run_ours(args) -> None:
         torch.distributed.barrier()
     clocks = sampler.stop() if sampler else None
     elapsed_ms = t_start.elapsed_time(t_end)
-    launch_ms = [ev[k][j].elapsed_time(ev[k][j + 1]) for k in range(args.steps) for j in range(len(launches))]
+    mean_launch_ms = elapsed_ms / (len(launches) * args.steps)
     st, tile = ss.ss_stream_status(sh)
     assert st == ss.SS_OK, f"device status {st} at tile {tile}"
 
@@ -598,15 +597,15 @@ def run_ours(args) -> None:
 
     # roofline of the dominant kernel (the look-back scan: every launch of the step)
     peak, peak_src = measured_hbm_peak()
-    mean_launch_ms = statistics.fmean(launch_ms)
     achieved = BYTES_PER_ELEM * N / (mean_launch_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": recorded_traffic(), "kernel": "k_scan_lookback_pipe_sb",
                 "mean_launch_ms": _sig(mean_launch_ms, 5), "peak_source": peak_src,
                 "frac_of_nominal_8TBs": round(achieved / 8000.0, 4)}
+    # the four variants one by one (after the timed region): each repeated back to back
     by_variant = {}
-    for j, v in enumerate(VARIANTS):
-        by_variant[v] = statistics.fmean(launch_ms[j::len(launches)])
+    for v, f in zip(VARIANTS, launches):
+        by_variant[v] = time_region(torch, stream, f, 10)
 
     # end to end through the host-memory API: pinned host in, pinned host out
     e2e_steps = max(1, min(args.steps, args.e2e_steps))

@@ -30,9 +30,19 @@ namespace ss {
 
 namespace {
 
+// Bit 7 of each byte of the result is set iff that byte of w is nonzero:
+// adding 0x7f to the low seven bits of a byte carries into bit 7 iff they are
+// not all zero (and never out of the byte), and OR-ing w adds the byte's own
+// bit 7.  Four flags in five operations.
+__device__ __forceinline__ uint32_t nonzero_byte_bits(uint32_t w) {
+    return (((w & 0x7f7f7f7fu) + 0x7f7f7f7fu) | w) & 0x80808080u;
+}
+// The keep mask of four flag bytes: bit e set iff byte e is nonzero.  The
+// multiply by 2^21 + 2^14 + 2^7 + 1 moves bits 7, 15, 23 and 31 to bits 28..31
+// (no other partial product reaches those bits, and none overlap below them,
+// so nothing carries in).
 __device__ __forceinline__ uint32_t byte_keep_mask(uint32_t w) {
-    return ((w & 0x000000ffu) ? 1u : 0u) | ((w & 0x0000ff00u) ? 2u : 0u) |
-           ((w & 0x00ff0000u) ? 4u : 0u) | ((w & 0xff000000u) ? 8u : 0u);
+    return (nonzero_byte_bits(w) * 0x00204081u) >> 28;
 }
 
 // A 16-byte key vector through the read-only path: no L1 allocation, and a
@@ -631,11 +641,18 @@ k_compact_chunked(const uint32_t* keys, const uint8_t* flags, uint32_t* out, uns
         }
 #pragma unroll
         for (int c = 0; c < CHUNKS; ++c) {
-            uint32_t m[VPT];
-            masks(k, c, m);
             uint32_t x = 0;
+            if ((size_t)(rank + k * G) * TILE + TILE <= n) {  // count straight from the flag bits
+                const unsigned char* f =
+                    smem_raw + (size_t)(k % STAGES) * TILE + (size_t)c * CHUNK + (size_t)warp * SEG + (size_t)lane * 4;
 #pragma unroll
-            for (int j = 0; j < VPT; ++j) x += (uint32_t)__popc(m[j]);
+                for (int j = 0; j < VPT; ++j) x += (uint32_t)__popc(nonzero_byte_bits(lds_u32(f + 128 * j)));
+            } else {
+                uint32_t m[VPT];
+                masks(k, c, m);
+#pragma unroll
+                for (int j = 0; j < VPT; ++j) x += (uint32_t)__popc(m[j]);
+            }
             x = warp_sum(x);
             if (lane == 0) s_cnt[k & 1][c * WARPS + warp] = x;
         }
@@ -742,7 +759,10 @@ k_compact_chunked(const uint32_t* keys, const uint8_t* flags, uint32_t* out, uns
                     if ((m[j] >> e) & 1u) dst[pos++] = key[j][e];
             }
         };
-#pragma unroll
+        // Not unrolled: the two-chunk body is large, and one copy of it runs faster
+        // when the flags are dense (measured at n = 2^28: 0.491 against 0.528 ms at
+        // p = 0.99; 0.223 against 0.218 ms at p = 0.01).
+#pragma unroll 1
         for (int c = 0; c < CHUNKS; c += 2) {
             masks(k, c + 1, mb);
             load_keys(k, c + 1, mb, kb);

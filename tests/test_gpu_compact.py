@@ -51,6 +51,20 @@ def test_compaction_full_size(ss, p):
     assert_equal(got, ref)
 
 
+@pytest.mark.parametrize("p", [0.0625, 0.001])
+def test_compaction_sparse_and_moderate(ss, p):
+    # Keep rates between the bench's: a few kept keys per 16-byte key vector
+    # (0.0625) and almost none (0.001), over 300 tiles of 65,536 and a ragged
+    # last one.
+    n = 300 * 65536 + 12_345
+    keys = si.uniform_u32(n, seed=33)
+    flags = si.bernoulli_flags(n, p, seed=34)
+    got, c = run_compact(ss, keys, flags)
+    ref = oracle.compact_u32(keys, flags)
+    assert c == ref.size
+    assert_equal(got, ref)
+
+
 @pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 31, 33, 511, 512, 513, 4095, 4096, 4097, 8191, 8193,
                                65535, 65536, 65537, 65536 * 3 + 1000, 100_003, 1 << 20, 152 * 65536 + 17])
 @pytest.mark.parametrize("p", [0.0, 0.3, 1.0])

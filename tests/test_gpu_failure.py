@@ -52,10 +52,11 @@ def test_scan_timeout_is_reported_and_recovered(ss, dead_tile):
     assert_equal(d_out.cpu().numpy(), oracle.scan_i32(x, True))
 
 
-def test_compaction_timeout_is_reported_and_recovered(ss):
+@pytest.mark.parametrize("p", [0.5, 0.01])
+def test_compaction_timeout_is_reported_and_recovered(ss, p):
     import torch
     n = 50 * 65536 + 17  # tile 7 exists for every compaction tile size (4096 to 65536)
-    keys, flags = si.workload_compaction(n, 0.5, seed=3)
+    keys, flags = si.workload_compaction(n, p, seed=3)
     d_k = torch.from_numpy(keys.view(np.int32)).to("cuda:0")
     d_f = torch.from_numpy(flags).to("cuda:0")
     d_o = torch.empty_like(d_k)

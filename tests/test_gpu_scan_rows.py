@@ -86,13 +86,17 @@ def test_bench_shapes(ss, shape):
     check(ss, "i32", False, rows_input("i32", *shape))
 
 
-@pytest.mark.parametrize("shape", [(9, 5000), (33, 300), (7, 2051), (5, 40000), (1001, 20), (513, 64)])
+# (333, 100), (257, 224), (300, 160), (301, 65), (129, 128): the one-step kernel with two
+# 16-byte vectors per lane (rows of 65-224 elements), whose per-vector bounds and the
+# scalar path of a misaligned base need their own cases.
+@pytest.mark.parametrize("shape", [(9, 5000), (33, 300), (7, 2051), (5, 40000), (1001, 20), (513, 64),
+                                   (333, 100), (257, 224), (301, 65), (129, 128)])
 @pytest.mark.parametrize("offset", [1, 3])
 def test_unaligned(ss, shape, offset):
     check(ss, "i32", True, rows_input("i32", *shape), offset=offset)
 
 
-@pytest.mark.parametrize("shape", [(6, 9000), (300, 64), (9, 50000)])
+@pytest.mark.parametrize("shape", [(6, 9000), (300, 64), (9, 50000), (300, 160), (257, 224), (333, 100)])
 def test_in_place(ss, shape):
     check(ss, "i32", False, rows_input("i32", *shape), inplace=True)
 
