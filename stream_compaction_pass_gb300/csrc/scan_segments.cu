@@ -235,20 +235,47 @@ k_scan_segments(const T* in, T* out, size_t n, const uint32_t* bits, uint32_t nu
         *hb_out = hb;
         T v[VPT][4];
         read_rows(k, t, v);
+        // The warp's summary: whether a segment starts in its span, and the
+        // sum from its last start on (or of the whole span).  Element order
+        // is (row, lane, element); the last start is found with one ballot
+        // per row, and each lane adds its share past it, so a single plain
+        // warp sum gives the summary (no segmented scan per row).
         SegPair<T> w{0u, T(0)};
+        int last_row = -1;
+        uint32_t last_lanes = 0u;
         if (__any_sync(kFullMask, hb != 0u)) {
 #pragma unroll
             for (int j = 0; j < VPT; ++j) {
-                const SegPair<T> row = warp_seg_scan<T>(lane_pair(v[j], (hb >> (4 * j)) & 15u), lane);
-                const SegPair<T> tot{__shfl_sync(kFullMask, row.f, 31), __shfl_sync(kFullMask, row.s, 31)};
-                w = seg_add(w, tot);
+                const uint32_t b = __ballot_sync(kFullMask, ((hb >> (4 * j)) & 15u) != 0u);
+                if (b) {
+                    last_row = j;
+                    last_lanes = b;
+                }
             }
-        } else {
-            T x = T(0);
-#pragma unroll
-            for (int j = 0; j < VPT; ++j) x += ((v[j][0] + v[j][1]) + v[j][2]) + v[j][3];
-            w.s = warp_sum(x);
         }
+        const int last_lane = last_row >= 0 ? 31 - __clz(last_lanes) : -1;
+        T x = T(0);
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const T rs = ((v[j][0] + v[j][1]) + v[j][2]) + v[j][3];
+            if (j > last_row) {
+                x += rs;
+            } else if (j == last_row) {
+                if (lane > last_lane) {
+                    x += rs;
+                } else if (lane == last_lane) {  // from this lane's last start in the row on
+                    const uint32_t h = (hb >> (4 * j)) & 15u;
+                    const int e0 = 31 - __clz(h);
+                    T r = v[j][3];
+                    if (e0 <= 2) r = v[j][2] + r;
+                    if (e0 <= 1) r = v[j][1] + r;
+                    if (e0 <= 0) r = v[j][0] + r;
+                    x += r;
+                }
+            }
+        }
+        w.s = warp_sum(x);
+        w.f = last_row >= 0 ? 1u : 0u;
         if (lane == 0) {
             s_ws[k & 1][warp] = w.s;
             s_wf[k & 1][warp] = w.f;
