@@ -9,13 +9,17 @@
 // counted on an mbarrier) fills the next STAGES-1 tiles while the CTA scans,
 // looks back and stores the current one.
 //
-// Schedule: each CTA takes a rank r from the workspace counter when it
-// starts, then processes tiles r, r + G, r + 2G, ... (G = grid size).  Ranks
-// are handed out in start order, so the CTA owning the smallest unfinished
-// tile has always started and reaches that tile after finishing its own
-// smaller ones: every look-back wait ends without relying on all CTAs being
-// resident.  Consecutive tiles belong to different CTAs and are processed at
-// about the same time, and no atomic sits inside the loop.
+// Schedule, two forms (the configuration table in scan.cu picks one):
+//  - fixed: each CTA takes a rank r from the workspace counter when it
+//    starts, then processes tiles r, r + G, r + 2G, ... (G = grid size);
+//  - claimed (the default row): each CTA claims its next tile from the
+//    counter when it starts that tile's copy, so a faster SM takes more
+//    tiles (k_scan_lookback_pipe_sb with DYN).
+// Either way tiles are handed out in start (or claim) order, so the CTA
+// owning the smallest unfinished tile has started and reaches that tile
+// after finishing its own smaller ones: every look-back wait ends without
+// relying on all CTAs being resident.  Consecutive tiles belong to
+// different CTAs and are processed at about the same time.
 //
 // The per-tile arithmetic is the same as scan.cu's (scan_body.cuh).  Reading
 // the ring back is conflict-free: lane l of a warp reads the l-th 16-byte
