@@ -44,6 +44,15 @@ __device__ __forceinline__ uint32_t nonzero_byte_bits(uint32_t w) {
 __device__ __forceinline__ uint32_t byte_keep_mask(uint32_t w) {
     return (nonzero_byte_bits(w) * 0x00204081u) >> 28;
 }
+// The keep bits of 32 consecutive flag bytes (lo: bytes 0..15, hi: 16..31),
+// bit i for byte i.
+__device__ __forceinline__ uint32_t keep_bits32(uint4 lo, uint4 hi) {
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    uint32_t m = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) m |= ((nonzero_byte_bits(w[q]) * 0x00204081u) >> (28 - 4 * q)) & (0xfu << (4 * q));
+    return m;
+}
 
 // A 16-byte key vector through the read-only path: no L1 allocation, and a
 // 256-byte L2 fetch around the miss (neighbouring vectors are usually wanted
@@ -53,6 +62,14 @@ __device__ __forceinline__ uint4 ld_key_vec(const uint4* p) {
     asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                  : "l"(p));
+    return r;
+}
+
+// One key through the read-only path, without the wider L2 fetch: with
+// sparse flags the neighbouring keys are rarely wanted.
+__device__ __forceinline__ uint32_t ld_key_u32(const uint32_t* p) {
+    uint32_t r;
+    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
     return r;
 }
 
@@ -528,13 +545,20 @@ k_compact_sel(const uint32_t* keys, const uint8_t* flags, uint32_t* out, unsigne
 //    offsets inside the tile and publishes the tile's total.
 //  - Warp 0 then looks back for tile k.  After a barrier, every warp writes
 //    its share of each chunk of tile k at
-//    prefix + offset(chunk, warp) + rank inside the warp.  Key vectors with
-//    a kept element are loaded from global memory one chunk ahead.
+//    prefix + offset(chunk, warp) + rank inside the warp, in one of two
+//    forms chosen per tile by its count:
+//      dense: key vectors with a kept element are loaded one chunk ahead,
+//        and a warp row's kept keys go to one contiguous run of the output;
+//      sparse (fewer than `sparse_below` kept keys): lane l takes elements
+//        32l .. 32l+31 of each share as one word of keep bits and loads its
+//        first few kept keys of every chunk before the next tile is counted,
+//        so they arrive during that count and the look-back; after the
+//        look-back it stores them, consecutive, with plain stores.
 //  - Counts and offsets alternate between two slots by tile parity.
 template <int THREADS, int STAGES>
 __global__ void __launch_bounds__(THREADS, 1)
 k_compact_chunked(const uint32_t* keys, const uint8_t* flags, uint32_t* out, unsigned long long* d_count,
-                  size_t n, uint32_t num_tiles, LookbackCtx ctx) {
+                  size_t n, uint32_t num_tiles, LookbackCtx ctx, uint32_t sparse_below) {
     constexpr int WARPS = THREADS / 32;
     constexpr int VPT = 8;                                // rows (16-byte key vectors) per lane per chunk
     constexpr int NW = VPT / 4;                           // packed count words per lane
@@ -542,7 +566,10 @@ k_compact_chunked(const uint32_t* keys, const uint8_t* flags, uint32_t* out, uns
     constexpr uint32_t CHUNK = SEG * WARPS;               // 16384
     constexpr int CHUNKS = 4;
     constexpr uint32_t TILE = CHUNK * CHUNKS;             // 65536
+    constexpr int kSlots = 4;                             // sparse form: kept keys per lane and chunk loaded early
     static_assert(CHUNKS * WARPS == 64, "two (chunk, warp) counts per lane of warp 0");
+    static_assert(SEG == 32u * 32u, "a lane's share of a chunk is one word of keep bits");
+    static_assert(2 * CHUNKS <= VPT && kSlots <= 4, "the sparse slots fit the dense registers");
 
     extern __shared__ __align__(128) unsigned char smem_raw[];  // STAGES x TILE flag bytes
     __shared__ __align__(8) uint64_t bars[STAGES];
@@ -604,6 +631,25 @@ k_compact_chunked(const uint32_t* keys, const uint8_t* flags, uint32_t* out, uns
                 }
             }
         }
+    };
+    // Keep bits of elements 32*lane .. 32*lane+31 of this warp's share of
+    // chunk c of tile k (bit i for element i).
+    auto lane_word = [&](uint32_t k, int c) -> uint32_t {
+        const size_t t_base = (size_t)(rank + k * G) * TILE;
+        if (t_base + TILE <= n) {
+            const unsigned char* f =
+                smem_raw + (size_t)(k % STAGES) * TILE + (size_t)c * CHUNK + (size_t)warp * SEG + 32u * lane;
+            // The two 16-byte halves in the order that puts each quarter-warp's
+            // reads on distinct banks; the halves of the result swap back.
+            const uint32_t h = (lane >> 2) & 1u;
+            const uint32_t r = keep_bits32(lds_vec(f + 16u * h), lds_vec(f + 16u * (h ^ 1u)));
+            return h ? __funnelshift_l(r, r, 16) : r;
+        }
+        const size_t seg = t_base + (size_t)c * CHUNK + (size_t)warp * SEG + 32u * lane;
+        uint32_t m = 0;
+        for (int i = 0; i < 32; ++i)
+            if (seg + i < n && flags[seg + i] != 0) m |= 1u << i;
+        return m;
     };
     // Key vectors of chunk c of tile k that hold a kept element.
     auto load_keys = [&](uint32_t k, int c, const uint32_t (&m)[VPT], uint32_t (&key)[VPT][4]) {
@@ -690,6 +736,33 @@ k_compact_chunked(const uint32_t* keys, const uint8_t* flags, uint32_t* out, uns
         if (k == 0) __syncthreads();  // tile 0's offsets and total are visible; later tiles' are by the
                                       // previous iteration's last barrier
         const uint32_t agg = s_total[k & 1];
+        const bool sparse = agg < sparse_below;  // the same in every thread
+        uint32_t ma[VPT], mb[VPT];
+        uint32_t ka[VPT][4], kb[VPT][4];
+        if (sparse) {
+            // The slots live in the dense form's registers: ka[2c][r] holds slot r
+            // of chunk c, ka[2c+1][0] the lane's count in chunk c, ma[c] its keep
+            // bits past the slots and ma[4+c] the position of its first kept key in
+            // the tile.
+#pragma unroll
+            for (int c = 0; c < CHUNKS; ++c) {
+                uint32_t m = lane_word(k, c);
+                const uint32_t cnt = (uint32_t)__popc(m);
+                const uint32_t inc = warp_inclusive_scan<uint32_t>(cnt, lane);
+                ma[4 + c] = s_cnt[k & 1][c * WARPS + warp] + inc - cnt;
+                ka[2 * c + 1][0] = cnt;
+                const uint32_t* kp = keys + (size_t)t * TILE + (size_t)c * CHUNK + (size_t)warp * SEG + 32u * lane;
+#pragma unroll
+                for (int r = 0; r < kSlots; ++r) {
+                    if (!__any_sync(kFullMask, m != 0)) break;
+                    if (m) {
+                        ka[2 * c][r] = ld_key_u32(kp + (__ffs(m) - 1));
+                        m &= m - 1;
+                    }
+                }
+                ma[c] = m;
+            }
+        }
         if (k + 1 < count && !count_publish(k + 1)) {
             failed = true;
             fail_at = k;
@@ -721,11 +794,11 @@ k_compact_chunked(const uint32_t* keys, const uint8_t* flags, uint32_t* out, uns
                 s_fail[k & 1] = lb_failed ? 1u : 0u;
             }
         }
-        // Masks and keys of chunk 0 load while warp 0 looks back.
-        uint32_t ma[VPT], mb[VPT];
-        uint32_t ka[VPT][4], kb[VPT][4];
-        masks(k, 0, ma);
-        load_keys(k, 0, ma, ka);
+        // Dense form: masks and keys of chunk 0 load while warp 0 looks back.
+        if (!sparse) {
+            masks(k, 0, ma);
+            load_keys(k, 0, ma, ka);
+        }
         __syncthreads();  // the prefix is in shared memory
         if (s_fail[k & 1]) {
             failed = true;
@@ -733,45 +806,62 @@ k_compact_chunked(const uint32_t* keys, const uint8_t* flags, uint32_t* out, uns
             break;
         }
         const uint32_t base = s_prefix[k & 1];
-        auto scatter = [&](int c, const uint32_t (&m)[VPT], const uint32_t (&key)[VPT][4]) {
-            uint32_t row_base[VPT];
-            uint32_t run = 0;
+        if (sparse) {
+            // A lane's kept keys of a chunk are consecutive in the output.
 #pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                uint32_t packed = 0;
+            for (int c = 0; c < CHUNKS; ++c) {
+                uint32_t* dst = out + (size_t)base + ma[4 + c];
+                const uint32_t cnt = ka[2 * c + 1][0];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) packed |= (uint32_t)__popc(m[4 * w + q]) << (8 * q);
-                const uint32_t inc = warp_inclusive_scan<uint32_t>(packed, lane);
-                const uint32_t exc = inc - packed;  // bytewise, no borrows (each byte <= 128)
-                const uint32_t rows = __shfl_sync(kFullMask, inc, 31);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    row_base[4 * w + q] = run + ((exc >> (8 * q)) & 0xffu);
-                    run += (rows >> (8 * q)) & 0xffu;
+                for (int r = 0; r < kSlots; ++r) {
+                    if (!__any_sync(kFullMask, cnt > (uint32_t)r)) break;
+                    if (cnt > (uint32_t)r) dst[r] = ka[2 * c][r];
                 }
+                const uint32_t* kp = keys + (size_t)t * TILE + (size_t)c * CHUNK + (size_t)warp * SEG + 32u * lane;
+                uint32_t m = ma[c];
+                for (uint32_t r = kSlots; m != 0; ++r, m &= m - 1) dst[r] = ld_key_u32(kp + (__ffs(m) - 1));
             }
-            uint32_t* dst = out + (size_t)base + s_cnt[k & 1][c * WARPS + warp];
+        } else {
+            auto scatter = [&](int c, const uint32_t (&m)[VPT], const uint32_t (&key)[VPT][4]) {
+                uint32_t row_base[VPT];
+                uint32_t run = 0;
 #pragma unroll
-            for (int j = 0; j < VPT; ++j) {
-                uint32_t pos = row_base[j];
+                for (int w = 0; w < NW; ++w) {
+                    uint32_t packed = 0;
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if ((m[j] >> e) & 1u) dst[pos++] = key[j][e];
-            }
-        };
-        // Not unrolled: the two-chunk body is large, and one copy of it runs faster
-        // when the flags are dense (measured at n = 2^28: 0.491 against 0.528 ms at
-        // p = 0.99; 0.223 against 0.218 ms at p = 0.01).
+                    for (int q = 0; q < 4; ++q) packed |= (uint32_t)__popc(m[4 * w + q]) << (8 * q);
+                    const uint32_t inc = warp_inclusive_scan<uint32_t>(packed, lane);
+                    const uint32_t exc = inc - packed;  // bytewise, no borrows (each byte <= 128)
+                    const uint32_t rows = __shfl_sync(kFullMask, inc, 31);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        row_base[4 * w + q] = run + ((exc >> (8 * q)) & 0xffu);
+                        run += (rows >> (8 * q)) & 0xffu;
+                    }
+                }
+                uint32_t* dst = out + (size_t)base + s_cnt[k & 1][c * WARPS + warp];
+#pragma unroll
+                for (int j = 0; j < VPT; ++j) {
+                    uint32_t pos = row_base[j];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if ((m[j] >> e) & 1u) dst[pos++] = key[j][e];
+                }
+            };
+            // Not unrolled: the two-chunk body is large, and one copy of it runs faster
+            // when the flags are dense (measured at n = 2^28: 0.491 against 0.528 ms at
+            // p = 0.99; 0.223 against 0.218 ms at p = 0.01).
 #pragma unroll 1
-        for (int c = 0; c < CHUNKS; c += 2) {
-            masks(k, c + 1, mb);
-            load_keys(k, c + 1, mb, kb);
-            scatter(c, ma, ka);
-            if (c + 2 < CHUNKS) {
-                masks(k, c + 2, ma);
-                load_keys(k, c + 2, ma, ka);
+            for (int c = 0; c < CHUNKS; c += 2) {
+                masks(k, c + 1, mb);
+                load_keys(k, c + 1, mb, kb);
+                scatter(c, ma, ka);
+                if (c + 2 < CHUNKS) {
+                    masks(k, c + 2, ma);
+                    load_keys(k, c + 2, ma, ka);
+                }
+                scatter(c + 1, mb, kb);
             }
-            scatter(c + 1, mb, kb);
         }
         if (t == num_tiles - 1 && threadIdx.x == 0) *d_count = (unsigned long long)base + agg;
         __syncthreads();  // tile k's flags read by everyone
@@ -814,14 +904,21 @@ static cudaError_t launch_compact_persistent(const uint32_t* keys, const uint8_t
 }
 
 // 0: bulk-copied keys and flags; 1: bulk-copied flags, selective key loads;
-// 2: the same with one look-back per 65536-element tile (the default).
+// 2: the same with one look-back per 65536-element tile (the default), each
+// tile written in the sparse or the dense form by its count; 3 and 4: the
+// chunked kernel with every tile in the dense, or the sparse, form.
 static int g_compact_kernel = 2;
+// Chunked rows 2, 3, 4: a tile keeping fewer keys than this takes the sparse
+// form.  Measured at n = 2^28 the two forms take the same time near a keep
+// rate of 0.05 (3277 keys a tile: 0.239 against 0.241 ms); at 0.03 the sparse
+// form takes 0.177 ms against 0.235, at 0.1 0.381 against 0.261.
+static const uint32_t kCompactSparseBelow[] = {3072, 0, 65537};
 
-int compact_kernel_count() { return 3; }
+int compact_kernel_count() { return 2 + (int)(sizeof(kCompactSparseBelow) / sizeof(kCompactSparseBelow[0])); }
 
 static cudaError_t launch_compact_chunked(const uint32_t* keys, const uint8_t* flags, uint32_t* out,
                                          unsigned long long* d_count, size_t n, const LookbackWs& ws,
-                                         cudaStream_t s) {
+                                         uint32_t sparse_below, cudaStream_t s) {
     constexpr int THREADS = 512, STAGES = 3;
     constexpr size_t TILE = 65536;
     constexpr size_t SMEM = STAGES * TILE;
@@ -832,7 +929,7 @@ static cudaError_t launch_compact_chunked(const uint32_t* keys, const uint8_t* f
     const uint32_t tiles = (uint32_t)((n + TILE - 1) / TILE);
     const uint32_t grid = tiles < (uint32_t)su.sms ? tiles : (uint32_t)su.sms;
     LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};
-    kern<<<grid, THREADS, SMEM, s>>>(keys, flags, out, d_count, n, tiles, ctx);
+    kern<<<grid, THREADS, SMEM, s>>>(keys, flags, out, d_count, n, tiles, ctx, sparse_below);
     return cudaGetLastError();
 }
 void set_compact_kernel(int k) { g_compact_kernel = k; }
@@ -843,8 +940,8 @@ cudaError_t launch_compact_pipe(KeepRule rule, const uint32_t* keys, const uint8
     if (rule != KeepRule::Flags) return launch_compact_pred(rule, keys, out, d_count, n, ws, s);
     if (g_compact_kernel == 0)
         return launch_compact_persistent<512, 8, 2, false>(keys, flags, out, d_count, n, ws, s);
-    if (g_compact_kernel == 2 && n > (size_t)65536)
-        return launch_compact_chunked(keys, flags, out, d_count, n, ws, s);
+    if (g_compact_kernel >= 2 && n > (size_t)65536)
+        return launch_compact_chunked(keys, flags, out, d_count, n, ws, kCompactSparseBelow[g_compact_kernel - 2], s);
     return launch_compact_persistent<512, 8, 3, true>(keys, flags, out, d_count, n, ws, s);
 }
 

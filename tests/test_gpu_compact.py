@@ -13,7 +13,7 @@ from gpu_helpers import SENTINEL, Guarded, assert_equal, compaction_input
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module", params=[2, 1, 0], ids=["chunked", "selective-keys", "bulk-keys"])
+@pytest.fixture(scope="module", params=[2, 3, 4, 1, 0], ids=["chunked", "chunked-dense", "chunked-sparse", "selective-keys", "bulk-keys"])
 def ss(request):
     import stream_compaction_pass_gb300 as m
     m.ss_set_compact_config(request.param)
@@ -59,6 +59,38 @@ def test_compaction_sparse_and_moderate(ss, p):
     n = 300 * 65536 + 12_345
     keys = si.uniform_u32(n, seed=33)
     flags = si.bernoulli_flags(n, p, seed=34)
+    got, c = run_compact(ss, keys, flags)
+    ref = oracle.compact_u32(keys, flags)
+    assert c == ref.size
+    assert_equal(got, ref)
+
+
+def test_compaction_sparse_and_dense_tiles_in_one_call(ss):
+    # A keep rate of 3072 / 65536 puts about half of the 65,536-element tiles
+    # on each side of the chunked kernel's sparse/dense switch (fewer than
+    # 3072 kept keys in the tile), interleaved across CTAs.
+    n = 200 * 65536 + 77
+    keys = si.uniform_u32(n, seed=38)
+    flags = si.bernoulli_flags(n, 3072 / 65536, seed=39)
+    got, c = run_compact(ss, keys, flags)
+    ref = oracle.compact_u32(keys, flags)
+    assert c == ref.size
+    assert_equal(got, ref)
+
+
+@pytest.mark.parametrize("run", [1, 5, 32, 33, 64, 500])
+def test_compaction_clustered_runs(ss, run):
+    # Runs of `run` consecutive kept flags at seeded positions, about 1024 kept
+    # keys per 65,536 elements: sparse tiles in which one thread's 32 elements
+    # can all be kept, so the sparse form's loads past its four slots per
+    # chunk run too.  Runs straddle threads, warps, chunks and tiles; with
+    # runs of 500 some tiles keep more than 3072 keys and take the dense form.
+    n = 97 * 65536 + 1234
+    keys = si.uniform_u32(n, seed=40)
+    starts = si.uniform_int32(max(1, n * 1024 // (65536 * run)), 0, n - 1, seed=41)
+    flags = np.zeros(n, dtype=np.uint8)
+    for st in starts.astype(np.int64):
+        flags[st: st + run] = 1
     got, c = run_compact(ss, keys, flags)
     ref = oracle.compact_u32(keys, flags)
     assert c == ref.size
