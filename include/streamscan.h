@@ -363,7 +363,7 @@ ss_status ss_set_scan_config(int config);
  *   2  (the default) as 1, with one look-back per 65536-element tile worked
  *      in four chunks, which pays a tile's fixed costs once per 65536
  *      elements (inputs of 65536 elements or fewer take 1).  A tile keeping
- *      fewer than 3072 keys is written in a sparse form: each thread loads
+ *      fewer than 3456 keys is written in a sparse form: each thread loads
  *      only its kept keys, one by one, before the tile's look-back;
  *   3  as 2 with every tile in the dense form, 4 with every tile in the
  *      sparse form.

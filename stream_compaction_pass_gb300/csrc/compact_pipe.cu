@@ -536,21 +536,24 @@ k_compact_sel(const uint32_t* keys, const uint8_t* flags, uint32_t* out, unsigne
 
 // Chunked form: one look-back per 65536-element tile, processed as four
 // 16384-element chunks.  With sparse flags the work per element is small and
-// a tile's fixed costs dominate: the wait for its flags, two barriers, and
+// a tile's fixed costs dominate: the wait for its flags, the barriers, and
 // the look-back round trips.  A tile four times larger pays them once for
 // four times the elements.
 //  - Only the flags go through the ring: three stages of 64 KB.
-//  - Counting tile k+1: every warp counts its 1024-element share of each
-//    chunk.  After a barrier, warp 0 scans the 64 (chunk, warp) counts into
-//    offsets inside the tile and publishes the tile's total.
+//  - Counting tile k+1: lane l of a warp reads elements 32l .. 32l+31 of
+//    each of its 1024-element (chunk, warp) shares and turns them into one
+//    word of keep bits.  After a barrier the words overwrite the first 8 KB
+//    of the tile's stage (its flags are no longer needed), and warp 0 scans
+//    the 64 (chunk, warp) counts into offsets inside the tile and publishes
+//    the tile's total.
 //  - Warp 0 then looks back for tile k.  After a barrier, every warp writes
 //    its share of each chunk of tile k at
-//    prefix + offset(chunk, warp) + rank inside the warp, in one of two
+//    prefix + offset(chunk, warp) + rank inside the share, in one of two
 //    forms chosen per tile by its count:
-//      dense: key vectors with a kept element are loaded one chunk ahead,
-//        and a warp row's kept keys go to one contiguous run of the output;
-//      sparse (fewer than `sparse_below` kept keys): lane l takes elements
-//        32l .. 32l+31 of each share as one word of keep bits and loads its
+//      dense: each row of 128 elements takes its keep masks from the words;
+//        key vectors with a kept element are loaded one chunk ahead, and a
+//        row's kept keys go to one contiguous run of the output;
+//      sparse (fewer than `sparse_below` kept keys): each lane loads its
 //        first few kept keys of every chunk before the next tile is counted,
 //        so they arrive during that count and the look-back; after the
 //        look-back it stores them, consecutive, with plain stores.
@@ -612,44 +615,17 @@ k_compact_chunked(const uint32_t* keys, const uint8_t* flags, uint32_t* out, uns
         }
         issued = k + 1;
     };
-    // Keep masks of this lane's rows of chunk c of tile k.
-    auto masks = [&](uint32_t k, int c, uint32_t (&m)[VPT]) {
-        const size_t seg = (size_t)(rank + k * G) * TILE + (size_t)c * CHUNK + (size_t)warp * SEG;
-        if ((size_t)(rank + k * G) * TILE + TILE <= n) {
-            const unsigned char* f =
-                smem_raw + (size_t)(k % STAGES) * TILE + (size_t)c * CHUNK + (size_t)warp * SEG + (size_t)lane * 4;
-#pragma unroll
-            for (int j = 0; j < VPT; ++j) m[j] = byte_keep_mask(lds_u32(f + 128 * j));
-        } else {
-#pragma unroll
-            for (int j = 0; j < VPT; ++j) {
-                m[j] = 0;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const size_t i = seg + (size_t)(32 * j + lane) * 4 + e;
-                    if (i < n && flags[i] != 0) m[j] |= 1u << e;
-                }
-            }
-        }
+    // The keep word of lane ln's share of chunk c, for a tile whose count has
+    // turned its stage's first 8 KB into words.
+    auto word_at = [&](uint32_t k, int c, int ln) -> uint32_t {
+        return lds_u32(smem_raw + (size_t)(k % STAGES) * TILE + 4u * ((uint32_t)(c * WARPS + warp) * 32u + (uint32_t)ln));
     };
-    // Keep bits of elements 32*lane .. 32*lane+31 of this warp's share of
-    // chunk c of tile k (bit i for element i).
-    auto lane_word = [&](uint32_t k, int c) -> uint32_t {
-        const size_t t_base = (size_t)(rank + k * G) * TILE;
-        if (t_base + TILE <= n) {
-            const unsigned char* f =
-                smem_raw + (size_t)(k % STAGES) * TILE + (size_t)c * CHUNK + (size_t)warp * SEG + 32u * lane;
-            // The two 16-byte halves in the order that puts each quarter-warp's
-            // reads on distinct banks; the halves of the result swap back.
-            const uint32_t h = (lane >> 2) & 1u;
-            const uint32_t r = keep_bits32(lds_vec(f + 16u * h), lds_vec(f + 16u * (h ^ 1u)));
-            return h ? __funnelshift_l(r, r, 16) : r;
-        }
-        const size_t seg = t_base + (size_t)c * CHUNK + (size_t)warp * SEG + 32u * lane;
-        uint32_t m = 0;
-        for (int i = 0; i < 32; ++i)
-            if (seg + i < n && flags[seg + i] != 0) m |= 1u << i;
-        return m;
+    // Keep masks of this lane's rows of chunk c: row j's four elements at lane
+    // l are elements 128j + 4l .. 128j + 4l + 3 of the share, bits 4(l mod 8)
+    // .. of the word of lane 4j + l/8.
+    auto masks = [&](uint32_t k, int c, uint32_t (&m)[VPT]) {
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) m[j] = (word_at(k, c, 4 * j + (lane >> 3)) >> (4 * (lane & 7))) & 0xfu;
     };
     // Key vectors of chunk c of tile k that hold a kept element.
     auto load_keys = [&](uint32_t k, int c, const uint32_t (&m)[VPT], uint32_t (&key)[VPT][4]) {
@@ -675,9 +651,9 @@ k_compact_chunked(const uint32_t* keys, const uint8_t* flags, uint32_t* out, uns
                 }
         }
     };
-    // Waits for tile k's flags, counts them per (chunk, warp), turns the
-    // counts into offsets and publishes the total.  False if the copy did
-    // not arrive.
+    // Waits for tile k's flags, turns them into keep words (left in the
+    // stage) and counts per (chunk, warp), turns the counts into offsets and
+    // publishes the total.  False if the copy did not arrive.
     auto count_publish = [&](uint32_t k) -> bool {
         const uint32_t t = rank + k * G;
         const bool ok = mbar_wait_bounded(&bars[k % STAGES], (k / STAGES) & 1u, ctx.max_polls, ctx.timeout_ns);
@@ -685,24 +661,33 @@ k_compact_chunked(const uint32_t* keys, const uint8_t* flags, uint32_t* out, uns
             if (threadIdx.x == 0) record_error(ctx.status, kErrBulkTimeout, t);
             return false;
         }
+        uint32_t words[CHUNKS];
+        const size_t t_base = (size_t)t * TILE;
+        unsigned char* stage = smem_raw + (size_t)(k % STAGES) * TILE;
 #pragma unroll
         for (int c = 0; c < CHUNKS; ++c) {
-            uint32_t x = 0;
-            if ((size_t)(rank + k * G) * TILE + TILE <= n) {  // count straight from the flag bits
-                const unsigned char* f =
-                    smem_raw + (size_t)(k % STAGES) * TILE + (size_t)c * CHUNK + (size_t)warp * SEG + (size_t)lane * 4;
-#pragma unroll
-                for (int j = 0; j < VPT; ++j) x += (uint32_t)__popc(nonzero_byte_bits(lds_u32(f + 128 * j)));
-            } else {
-                uint32_t m[VPT];
-                masks(k, c, m);
-#pragma unroll
-                for (int j = 0; j < VPT; ++j) x += (uint32_t)__popc(m[j]);
+            uint32_t m = 0;
+            if (t_base + TILE <= n) {
+                const unsigned char* f = stage + (size_t)c * CHUNK + (size_t)warp * SEG + 32u * lane;
+                // The two 16-byte halves in the order that puts each quarter-warp's
+                // reads on distinct banks; the halves of the result swap back.
+                const uint32_t h = (lane >> 2) & 1u;
+                const uint32_t r = keep_bits32(lds_vec(f + 16u * h), lds_vec(f + 16u * (h ^ 1u)));
+                m = h ? __funnelshift_l(r, r, 16) : r;
+            } else {  // ragged last tile: flags from global memory
+                const size_t seg = t_base + (size_t)c * CHUNK + (size_t)warp * SEG + 32u * lane;
+                for (int i = 0; i < 32; ++i)
+                    if (seg + i < n && flags[seg + i] != 0) m |= 1u << i;
             }
-            x = warp_sum(x);
+            words[c] = m;
+            const uint32_t x = warp_sum((uint32_t)__popc(m));
             if (lane == 0) s_cnt[k & 1][c * WARPS + warp] = x;
         }
-        __syncthreads();
+        __syncthreads();  // the tile's flags are read
+        uint32_t* wst = reinterpret_cast<uint32_t*>(stage);
+#pragma unroll
+        for (int c = 0; c < CHUNKS; ++c) wst[(c * WARPS + warp) * 32 + lane] = words[c];
+        fence_async_shared();  // these writes before the copy that later refills the stage
         if (warp == 0) {  // (chunk, warp) order is the elements' order
             const uint32_t a = s_cnt[k & 1][2 * lane], b = s_cnt[k & 1][2 * lane + 1];
             const uint32_t inc = warp_inclusive_scan<uint32_t>(a + b, lane);
@@ -746,7 +731,7 @@ k_compact_chunked(const uint32_t* keys, const uint8_t* flags, uint32_t* out, uns
             // the tile.
 #pragma unroll
             for (int c = 0; c < CHUNKS; ++c) {
-                uint32_t m = lane_word(k, c);
+                uint32_t m = word_at(k, c, lane);
                 const uint32_t cnt = (uint32_t)__popc(m);
                 const uint32_t inc = warp_inclusive_scan<uint32_t>(cnt, lane);
                 ma[4 + c] = s_cnt[k & 1][c * WARPS + warp] + inc - cnt;
@@ -864,7 +849,7 @@ k_compact_chunked(const uint32_t* keys, const uint8_t* flags, uint32_t* out, uns
             }
         }
         if (t == num_tiles - 1 && threadIdx.x == 0) *d_count = (unsigned long long)base + agg;
-        __syncthreads();  // tile k's flags read by everyone
+        __syncthreads();  // tile k's keep words read by everyone
         if (threadIdx.x == 0) {
             consumed = k + 1;
             if (k + STAGES < count) issue(k + STAGES);
@@ -909,10 +894,10 @@ static cudaError_t launch_compact_persistent(const uint32_t* keys, const uint8_t
 // chunked kernel with every tile in the dense, or the sparse, form.
 static int g_compact_kernel = 2;
 // Chunked rows 2, 3, 4: a tile keeping fewer keys than this takes the sparse
-// form.  Measured at n = 2^28 the two forms take the same time near a keep
-// rate of 0.05 (3277 keys a tile: 0.239 against 0.241 ms); at 0.03 the sparse
-// form takes 0.177 ms against 0.235, at 0.1 0.381 against 0.261.
-static const uint32_t kCompactSparseBelow[] = {3072, 0, 65537};
+// form.  Measured at n = 2^28 (all tiles in one form, ms): keep rate 0.01,
+// sparse 0.122 against dense 0.221; 0.03, 0.173 against 0.230; 0.05 (3277
+// keys a tile), 0.230 against 0.237; 0.1, 0.38 against 0.26.
+static const uint32_t kCompactSparseBelow[] = {3456, 0, 65537};
 
 int compact_kernel_count() { return 2 + (int)(sizeof(kCompactSparseBelow) / sizeof(kCompactSparseBelow[0])); }
 

@@ -66,12 +66,12 @@ def test_compaction_sparse_and_moderate(ss, p):
 
 
 def test_compaction_sparse_and_dense_tiles_in_one_call(ss):
-    # A keep rate of 3072 / 65536 puts about half of the 65,536-element tiles
+    # A keep rate of 3456 / 65536 puts about half of the 65,536-element tiles
     # on each side of the chunked kernel's sparse/dense switch (fewer than
-    # 3072 kept keys in the tile), interleaved across CTAs.
+    # 3456 kept keys in the tile), interleaved across CTAs.
     n = 200 * 65536 + 77
     keys = si.uniform_u32(n, seed=38)
-    flags = si.bernoulli_flags(n, 3072 / 65536, seed=39)
+    flags = si.bernoulli_flags(n, 3456 / 65536, seed=39)
     got, c = run_compact(ss, keys, flags)
     ref = oracle.compact_u32(keys, flags)
     assert c == ref.size
@@ -84,7 +84,7 @@ def test_compaction_clustered_runs(ss, run):
     # keys per 65,536 elements: sparse tiles in which one thread's 32 elements
     # can all be kept, so the sparse form's loads past its four slots per
     # chunk run too.  Runs straddle threads, warps, chunks and tiles; with
-    # runs of 500 some tiles keep more than 3072 keys and take the dense form.
+    # runs of 500 the tiles keep between 0 and 3000 keys.
     n = 97 * 65536 + 1234
     keys = si.uniform_u32(n, seed=40)
     starts = si.uniform_int32(max(1, n * 1024 // (65536 * run)), 0, n - 1, seed=41)
