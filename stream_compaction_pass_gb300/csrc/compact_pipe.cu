@@ -570,6 +570,10 @@ k_compact_chunked(const uint32_t* keys, const uint8_t* flags, uint32_t* out, uns
     constexpr int CHUNKS = 4;
     constexpr uint32_t TILE = CHUNK * CHUNKS;             // 65536
     constexpr int kSlots = 4;                             // sparse form: kept keys per lane and chunk loaded early
+    constexpr uint32_t kWordBytes = 4u * CHUNKS * WARPS * 32u;   // keep words at the start of a counted stage
+    constexpr uint32_t kStageWarpBytes = 4u * (4u * 128u + 4u);  // a warp's staging: four rows and a shift
+    static_assert(kWordBytes + WARPS * kStageWarpBytes <= TILE, "words and staging fit a stage");
+    static_assert(kStageWarpBytes % 16u == 0u && kWordBytes % 16u == 0u, "staging areas are 16-byte aligned");
     static_assert(CHUNKS * WARPS == 64, "two (chunk, warp) counts per lane of warp 0");
     static_assert(SEG == 32u * 32u, "a lane's share of a chunk is one word of keep bits");
     static_assert(2 * CHUNKS <= VPT && kSlots <= 4, "the sparse slots fit the dense registers");
@@ -807,9 +811,14 @@ k_compact_chunked(const uint32_t* keys, const uint8_t* flags, uint32_t* out, uns
                 for (uint32_t r = kSlots; m != 0; ++r, m &= m - 1) dst[r] = ld_key_u32(kp + (__ffs(m) - 1));
             }
         } else {
+            // The warp's kept keys of one share, in two halves of four rows: each half
+            // is gathered in order into this warp's staging area (in the tile's
+            // stage, past the keep words) and written out with 16-byte stores.
+            uint32_t* stg = reinterpret_cast<uint32_t*>(smem_raw + (size_t)(k % STAGES) * TILE + kWordBytes +
+                                                        (size_t)warp * kStageWarpBytes);
             auto scatter = [&](int c, const uint32_t (&m)[VPT], const uint32_t (&key)[VPT][4]) {
-                uint32_t row_base[VPT];
-                uint32_t run = 0;
+                uint32_t* dst = out + (size_t)base + s_cnt[k & 1][c * WARPS + warp];
+                uint32_t run = 0;  // kept keys of the share in the rows before this half
 #pragma unroll
                 for (int w = 0; w < NW; ++w) {
                     uint32_t packed = 0;
@@ -818,19 +827,35 @@ k_compact_chunked(const uint32_t* keys, const uint8_t* flags, uint32_t* out, uns
                     const uint32_t inc = warp_inclusive_scan<uint32_t>(packed, lane);
                     const uint32_t exc = inc - packed;  // bytewise, no borrows (each byte <= 128)
                     const uint32_t rows = __shfl_sync(kFullMask, inc, 31);
+                    // Staging index of the half's first key: its global address mod 16
+                    // bytes, so that aligned vectors of the stage are aligned in memory.
+                    uint32_t* g = dst + run;
+                    const uint32_t s0 = (uint32_t)(reinterpret_cast<uintptr_t>(g) >> 2) & 3u;
+                    uint32_t row_run = 0;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        row_base[4 * w + q] = run + ((exc >> (8 * q)) & 0xffu);
-                        run += (rows >> (8 * q)) & 0xffu;
+                        const int j = 4 * w + q;
+                        uint32_t pos = s0 + row_run + ((exc >> (8 * q)) & 0xffu);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if ((m[j] >> e) & 1u) stg[pos++] = key[j][e];
+                        row_run += (rows >> (8 * q)) & 0xffu;
                     }
-                }
-                uint32_t* dst = out + (size_t)base + s_cnt[k & 1][c * WARPS + warp];
+                    __syncwarp();
+                    uint32_t* ga = g - s0;  // 16-byte aligned; written only at [s0, s0 + row_run)
+                    const uint32_t end = s0 + row_run;
+                    for (uint32_t v = (uint32_t)lane; 4 * v < end; v += 32) {
+                        const uint32_t lo = 4 * v;
+                        if (lo >= s0 && lo + 4 <= end) {
+                            st_vec(ga + lo, lds_vec(stg + lo));
+                        } else {
 #pragma unroll
-                for (int j = 0; j < VPT; ++j) {
-                    uint32_t pos = row_base[j];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        if ((m[j] >> e) & 1u) dst[pos++] = key[j][e];
+                            for (int e = 0; e < 4; ++e)
+                                if (lo + e >= s0 && lo + e < end) ga[lo + e] = stg[lo + e];
+                        }
+                    }
+                    __syncwarp();
+                    run += row_run;
                 }
             };
             // Not unrolled: the two-chunk body is large, and one copy of it runs faster
@@ -847,6 +872,7 @@ k_compact_chunked(const uint32_t* keys, const uint8_t* flags, uint32_t* out, uns
                 }
                 scatter(c + 1, mb, kb);
             }
+            fence_async_shared();  // the staging writes before the copy that refills the stage
         }
         if (t == num_tiles - 1 && threadIdx.x == 0) *d_count = (unsigned long long)base + agg;
         __syncthreads();  // tile k's keep words read by everyone
