@@ -26,6 +26,10 @@
 //    vectors (partial vectors at the two ends element by element).  Every
 //    store instruction of a warp then covers 512 contiguous bytes, instead
 //    of one 4-byte slot in every 16 bytes.
+//  - sparse scatter: in a tile keeping fewer than 256 keys, none of whose
+//    lanes keeps more than four, each lane reads only its kept keys from the
+//    stage (before it is released) with their ranks, and stores them one by
+//    one once the offsets are in.
 // Named barriers hand each tile to the look-back warp and its offsets back.
 // Each has two ids, by tile parity; each side must pass the other's barrier
 // of tile k before it can arrive at the barrier of tile k + 2 with the same
@@ -45,6 +49,11 @@ constexpr int kPredThreads = kPredComputeThreads + 32;       // + the look-back 
 constexpr int kPredVpt = 8;                                  // 16-byte key vectors per lane per tile
 constexpr int kPredStages = 3;
 constexpr int kPredLookbackK = 1;  // descriptors per lane per look-back round
+constexpr int kPredSlots = 4;      // sparse form: the most kept keys a lane may hold in a tile
+// ... and fewer than this many in the tile.  Measured at n = 2^28 (ms): keep
+// rate 0.001, sparse 0.240 against 0.267; 0.01 (164 keys a tile), 0.251
+// against 0.272; 0.03 (492), 0.290 against 0.282.
+constexpr uint32_t kPredSparseBelow = 256;
 constexpr uint32_t kPredTile = (uint32_t)kPredComputeThreads * kPredVpt * 4;  // 16384
 constexpr uint32_t kPredStageBytes = kPredTile * 4;
 constexpr uint32_t kPredHalf = 32u * kPredVpt * 2;  // keys per staging pass: 4 rows of a warp segment
@@ -74,6 +83,21 @@ __device__ __forceinline__ uint32_t vec_elem(const uint4& v, int s) {
     return s == 0 ? v.x : s == 1 ? v.y : s == 2 ? v.z : v.w;
 }
 
+// r[j] for a j known only at run time (0..7), by selects rather than a
+// local-memory array.
+__device__ __forceinline__ uint32_t select8(const uint32_t (&r)[8], uint32_t j) {
+    const bool o = (j & 1u) != 0;
+    const uint32_t a = o ? r[1] : r[0], b = o ? r[3] : r[2], c = o ? r[5] : r[4], d = o ? r[7] : r[6];
+    const uint32_t ab = (j & 2u) ? b : a, cd = (j & 2u) ? d : c;
+    return (j & 4u) ? cd : ab;
+}
+
+__device__ __forceinline__ uint32_t lds_u32(const void* p) {
+    uint32_t r;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(smem_u32(p)) : "memory");
+    return r;
+}
+
 }  // namespace
 
 template <KeepRule RULE>
@@ -98,6 +122,9 @@ k_compact_pred(const uint32_t* keys, uint32_t* out, unsigned long long* d_count,
     // (written by the look-back warp).
     __shared__ uint32_t s_wsum[2][CW], s_base[2][CW];
     __shared__ uint32_t s_arrive[2], s_bad[2], s_agg[2], s_stop[2], s_fail[2], s_rank, s_epoch;
+    // By tile parity: a counting warp had a lane keeping more than kPredSlots
+    // keys (reset by the last of them), and the tile's form from that.
+    __shared__ uint32_t s_crowded[2], s_sparse[2];
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -110,7 +137,7 @@ k_compact_pred(const uint32_t* keys, uint32_t* out, unsigned long long* d_count,
         s_epoch = epoch;
         for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
         fence_async_shared();
-        for (int q = 0; q < 2; ++q) s_arrive[q] = s_bad[q] = s_stop[q] = s_fail[q] = 0u;
+        for (int q = 0; q < 2; ++q) s_arrive[q] = s_bad[q] = s_stop[q] = s_fail[q] = s_crowded[q] = s_sparse[q] = 0u;
     }
     __syncthreads();
     const uint32_t rank = s_rank;
@@ -263,10 +290,12 @@ k_compact_pred(const uint32_t* keys, uint32_t* out, unsigned long long* d_count,
 #pragma unroll
             for (int j = 0; j < VPT; ++j) c += (uint32_t)__popc(m[j]);
         }
+        const bool crowded = __reduce_max_sync(kFullMask, c) > (uint32_t)kPredSlots;
         c = warp_sum(c);
         uint32_t last = 0;
         if (lane == 0) {
             s_wsum[par][warp] = c;
+            if (crowded) atomicOr(&s_crowded[par], 1u);
             if (!ok) {
                 atomicOr(&s_bad[par], 1u);
                 record_error(ctx.status, kErrBulkTimeout, t);
@@ -291,6 +320,8 @@ k_compact_pred(const uint32_t* keys, uint32_t* out, unsigned long long* d_count,
                 }
                 s_agg[par] = agg;
                 s_stop[par] = bad;
+                s_sparse[par] = (!*(volatile uint32_t*)&s_crowded[par] && agg < kPredSparseBelow) ? 1u : 0u;
+                s_crowded[par] = 0u;
                 s_bad[par] = 0u;
                 s_arrive[par] = 0u;
             }
@@ -366,12 +397,10 @@ k_compact_pred(const uint32_t* keys, uint32_t* out, unsigned long long* d_count,
             bar_arrive_n(kBarAgg + ((k + 1) & 1), ALL);
         }
 
-        // Rank tile k's kept keys (masks from its count; only vectors with a
-        // kept key are read again).
+        // Rank tile k's kept keys (masks from its count).
         uint32_t key[VPT][4], m[VPT];
 #pragma unroll
         for (int j = 0; j < VPT; ++j) m[j] = m_cur[j];
-        load_kept(k, m, key);
         uint32_t row_run[VPT];
         uint32_t run = 0, c0 = 0;
 #pragma unroll
@@ -389,6 +418,37 @@ k_compact_pred(const uint32_t* keys, uint32_t* out, unsigned long long* d_count,
             }
             if (w == 0) c0 = run;
         }
+        // Sparse form, when the tile keeps fewer than kPredSparseBelow keys and
+        // no lane more than kPredSlots (a tile-wide choice, made by its count:
+        // a tile is as slow as its slowest warp): each lane reads just its kept keys from the stage now,
+        // before the stage is released, with their positions in the warp's
+        // run, and stores them once the run's offset is known.  Otherwise the
+        // vectors holding a kept key are read again for the staged scatter.
+        uint32_t packed = 0;  // bit 4j + e: element e of row j is kept
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) packed |= m[j] << (4 * j);
+        const uint32_t kept = (uint32_t)__popc(packed);
+        const bool sparse = s_sparse[k & 1] != 0;
+        uint32_t sp_key[kPredSlots], sp_pos[kPredSlots];
+        if (sparse) {
+            const size_t seg = (size_t)(rank + k * G) * TILE + (size_t)warp * SEG;
+            const unsigned char* kb = ring + (size_t)(k % STAGES) * kPredStageBytes + (size_t)warp * SEG * 4;
+            uint32_t rest = packed;
+#pragma unroll
+            for (int r = 0; r < kPredSlots; ++r) {
+                if (!__any_sync(kFullMask, rest != 0)) break;
+                if (rest) {
+                    const uint32_t b = (uint32_t)__ffs(rest) - 1u;  // row b/4, element b%4
+                    rest &= rest - 1u;
+                    const uint32_t j = b >> 2;
+                    const uint32_t elem = 128u * j + 4u * (uint32_t)lane + (b & 3u);  // index in the segment
+                    sp_pos[r] = select8(row_run, j) + (uint32_t)__popc(packed & ((1u << b) - 1u) & (0xfu << (b & ~3u)));
+                    sp_key[r] = full(k) ? lds_u32(kb + 4u * elem) : keys[seg + elem];
+                }
+            }
+        } else {
+            load_kept(k, m, key);  // only vectors with a kept key are read again
+        }
 
         bar_sync_n(kBarPre + (k & 1), ALL);  // tile k's offsets; every compute warp has read tile k
         const bool lb_failed = s_fail[k & 1] != 0;
@@ -404,7 +464,15 @@ k_compact_pred(const uint32_t* keys, uint32_t* out, unsigned long long* d_count,
             poison_from = k + 1;
             break;
         }
-        scatter(key, m, row_run, c0, run, base);
+        if (sparse) {
+#pragma unroll
+            for (int r = 0; r < kPredSlots; ++r) {
+                if (!__any_sync(kFullMask, kept > (uint32_t)r)) break;
+                if (kept > (uint32_t)r) out[(size_t)base + sp_pos[r]] = sp_key[r];
+            }
+        } else {
+            scatter(key, m, row_run, c0, run, base);
+        }
         if (next_stops) {  // tile k+1's copy did not arrive; the look-back warp stops there too
             failed = true;
             poison_from = k + 1;

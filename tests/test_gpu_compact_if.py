@@ -87,6 +87,37 @@ def test_positive_edges(ss, kind, n):
     assert_equal(got, ref)
 
 
+@pytest.mark.parametrize("kind", ["f32", "i32", "u32"])
+@pytest.mark.parametrize("p", [0.001, 0.01, 0.0155, 0.06])
+def test_positive_sparse_and_mixed_tiles(ss, kind, p):
+    # Low keep rates: tiles keeping fewer than 256 keys, none of whose threads
+    # keeps more than four, take the sparse form (at 0.001 and 0.01), the
+    # others the staged one; ragged last tile.
+    n = 150 * 16384 + 4093
+    x = positive_input(n, p, kind)
+    got, c = run_positive(ss, kind, x)
+    ref = expected_bits(kind, x)
+    assert c == ref.size
+    assert_equal(got, ref)
+
+
+@pytest.mark.parametrize("run", [3, 5, 17, 40])
+def test_positive_clustered_runs(ss, run):
+    # Runs of `run` consecutive positive values in a negative background, at
+    # seeded positions, about 128 kept keys a tile: a thread holding five or
+    # more kept keys sends its tile to the staged form while tiles without
+    # one stay sparse.
+    n = 64 * 16384 + 999
+    x = -np.abs(si.uniform_f32(n, seed=42)) - np.float32(1.0)
+    starts = si.uniform_int32(max(1, n // (128 * run)), 0, n - 1, seed=43).astype(np.int64)
+    for st in starts:
+        x[st: st + run] = np.abs(x[st: st + run])
+    got, c = run_positive(ss, "f32", x)
+    ref = expected_bits("f32", x)
+    assert c == ref.size
+    assert_equal(got, ref)
+
+
 @pytest.mark.parametrize("p", [0.0, 1.0])
 @pytest.mark.parametrize("n", [4096, 5 * 16384 + 1])
 def test_positive_none_or_all(ss, p, n):
