@@ -16,9 +16,12 @@
 //      scanned across the warp; popc of the mask below an element inside a
 //      vector);
 //   3. the stage is released and the next copy started;
-//   4. the kept keys go straight from registers to their output slots: a
-//      warp row's kept keys form one contiguous run of the output, so no
-//      shared-memory staging is needed.
+//   4. the kept keys go from registers to their output slots: a warp row's
+//      kept keys form one contiguous run of the output.
+// The default, chunked kernel (below) turns a tile's flags into words of
+// keep bits when it counts them, and then uses the rest of the tile's stage
+// to gather each warp's kept keys for 16-byte stores; tiles with few kept
+// keys skip that and load and store just those keys.
 #include <type_traits>
 
 #include "bulk.cuh"
