@@ -55,7 +55,8 @@ def check(ss, kind, inclusive, x, offsets, **kw):
     assert err <= FP32_TOL, f"normalised fp32 error {err:.3e}"
 
 
-CASES = [(1, 1.0), (5, 2.0), (4096, 3.5), (16383, 100.0), (16384, 16384.0), (16385, 1.0), (100_003, 700.0),
+CASES = [(1, 1.0), (5, 2.0), (4096, 3.5), (12287, 50.0), (12288, 12288.0), (12289, 3.0), (16383, 100.0),
+         (16384, 16384.0), (16385, 1.0), (100_003, 700.0),
          (100_003, 40_000.0), (1 << 20, 7.0), (1 << 20, 300_000.0), (3_000_017, 5000.0), (3_000_017, 1e9)]
 
 
@@ -122,6 +123,30 @@ def test_no_segments_is_one_segment(ss):
     x = seg_input("i32", n)
     got = run_segments(ss, "i32", True, x, np.array([0, n], dtype=np.uint64), num_segments=0)
     assert_equal(got, oracle.scan_i32(x, True), tile=16384)
+
+
+def test_segmented_timeout_short_segments(ss):
+    # Segments of mean length 40 take the blocked form.  A tile holding a start
+    # publishes its inclusive prefix before its look-back, but still looks
+    # back for the elements before its first start; the fault hook makes
+    # tile 7 publish nothing, so tile 8's look-back runs out.
+    import torch
+    n = 30 * 16384 + 5
+    x = seg_input("i32", n)
+    offsets = si.segment_offsets(n, 40.0, seed=101)
+    d = torch.from_numpy(x).cuda()
+    o = torch.empty_like(d)
+    d_off = torch.from_numpy(offsets.astype(np.int64)).cuda()
+    ss.ss_debug_set_lookback_fault(7, 2_000_000)
+    try:
+        ss.ss_scan_segments(ss.SS_I32, True, d, o, d_off)
+        st, tile = ss.ss_stream_status()
+    finally:
+        ss.ss_debug_set_lookback_fault(-1, 0)
+    assert st == ss.SS_ERR_LOOKBACK_TIMEOUT and tile > 7
+    ss.ss_scan_segments(ss.SS_I32, True, d, o, d_off)
+    assert ss.ss_stream_status() == (ss.SS_OK, -1)
+    assert_equal(o.cpu().numpy(), oracle.scan_segments(x, offsets, True), tile=16384)
 
 
 def test_segmented_timeout_is_reported_and_recovered(ss):
