@@ -413,6 +413,38 @@ ss_status ss_scan_noalloc(ss_dtype dtype, int inclusive, const void *in, void *o
                           ss_stream_t stream);
 
 /*
+ * Explicit-workspace form, in CUB's two-call shape ("Prefix sum and other
+ * parallel patterns", Stream compaction: the library call that first asks
+ * for its temporary storage size, then runs with the caller's buffer).
+ *
+ * ss_scan_temp_bytes: *bytes receives the device scratch, in bytes, that a
+ *   scan of n elements needs: a 256-byte header (the tile counter and the
+ *   status words) and 8 bytes per 4096 elements and per 32 tiles of them
+ *   (the tile descriptors); 0 for n = 0.  Host only; enqueues nothing.
+ *
+ * ss_scan_ws: the scan of scan_{inclusive,exclusive}_* (dtype SS_I32,
+ *   SS_U32 or SS_F32; the same kernels and the same automatic choice by n)
+ *   with `temp` as its scratch instead of the library's per-stream
+ *   workspace, so the call allocates nothing.
+ *   temp        device memory of the stream's device, 256-byte aligned, at
+ *               least ss_scan_temp_bytes(n) bytes (temp_bytes), owned by the
+ *               caller and not overlapping in or out.  Its contents on entry
+ *               do not matter: the call clears the part it uses with one
+ *               memset on `stream` before its launch.
+ *   in, out, n, stream: as for the scans above; out == in is allowed.
+ *   Calls sharing one temp must not overlap on the GPU.  Device-side
+ *   timeouts are recorded in temp's header: ss_temp_status reads them.
+ *
+ * ss_temp_status: waits for `stream`, then returns and clears the device
+ *   status held in `temp` (the values of ss_stream_status); *failing_tile
+ *   (may be NULL) receives the first tile that gave up, or -1.
+ */
+ss_status ss_scan_temp_bytes(size_t n, size_t *bytes);
+ss_status ss_scan_ws(ss_dtype dtype, int inclusive, const void *in, void *out, size_t n, void *temp,
+                     size_t temp_bytes, ss_stream_t stream);
+ss_status ss_temp_status(void *temp, ss_stream_t stream, int64_t *failing_tile);
+
+/*
  * Test hooks for ss_scan_noalloc's periodic descriptor clear: the clear runs
  * on the current device's call that makes the count of calls a multiple of
  * ss_debug_noalloc_clear_period() (2^29), before its launch.

@@ -92,6 +92,9 @@ def _declare(lib):
         "ss_debug_set_lookback_fault": [I64, U64],
         "ss_scan_noalloc": [I, I, P, P, SZ, P],
         "ss_debug_set_noalloc_calls": [U64],
+        "ss_scan_temp_bytes": [SZ, ctypes.POINTER(SZ)],
+        "ss_scan_ws": [I, I, P, P, SZ, P, SZ, P],
+        "ss_temp_status": [P, P, ctypes.POINTER(I64)],
     }
     for name, args in sigs.items():
         f = getattr(lib, name)
@@ -394,3 +397,34 @@ def ss_scan_noalloc(dtype: int, inclusive: bool, inp, out, n=None, stream=None):
                                _stream(stream, inp, out))
     if st != SS_OK:
         raise StreamScanError(st, "ss_scan_noalloc", ss_status_string(st))
+
+
+def ss_scan_temp_bytes(n: int) -> int:
+    """Device scratch bytes that ss_scan_ws needs for n elements."""
+    b = ctypes.c_size_t(0)
+    _check(lib().ss_scan_temp_bytes(n, ctypes.byref(b)), "ss_scan_temp_bytes")
+    return int(b.value)
+
+
+def ss_scan_ws(dtype: int, inclusive: bool, inp, out, temp, n=None, temp_bytes=None, stream=None):
+    """The library's scan with caller-provided scratch `temp` (device,
+    256-byte aligned, at least ss_scan_temp_bytes(n) bytes)."""
+    if n is None:
+        n = _numel(inp)
+    if temp_bytes is None:
+        temp_bytes = temp.numel() * temp.element_size()
+    st = lib().ss_scan_ws(dtype, int(bool(inclusive)), _addr(inp), _addr(out), n, _addr(temp), temp_bytes,
+                          _stream(stream, inp, out))
+    if st != SS_OK:
+        raise StreamScanError(st, "ss_scan_ws", ss_status_string(st))
+
+
+def ss_temp_status(temp, stream=None):
+    """Waits for the stream; returns (status, failing_tile) held in `temp`
+    and clears it."""
+    tile = ctypes.c_int64(-1)
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    st = lib().ss_temp_status(_addr(temp), _stream(stream), ctypes.byref(tile))
+    return st, tile.value

@@ -362,6 +362,29 @@ ss_status compact_any(ss::KeepRule rule, const void* keys_v, const uint8_t* flag
     return e == cudaSuccess ? SS_OK : cuda_fail(e, "compaction launch");
 }
 
+// The caller-provided scratch of ss_scan_ws: a 256-byte header (the tile
+// counter in word 0, the two status words in word 1), then the descriptors.
+constexpr size_t kTempHeader = 256;
+
+size_t temp_bytes_for(size_t n) { return n == 0 ? 0 : kTempHeader + scan_desc_count(n) * 8; }
+
+// Reads and clears a status pair (device) on stream s, and maps it as
+// ss_stream_status does.
+ss_status read_status_words(uint32_t* d_status, cudaStream_t s, int64_t* failing_tile) {
+    uint32_t words[2] = {0, 0};
+    cudaError_t e = cudaMemcpyAsync(words, d_status, sizeof(words), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(d_status, 0, sizeof(words), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "status read-back");
+    if (words[0] & ss::kErrCounter) return fail(SS_ERR_CUDA, "tile counter out of step with the launch");
+    if (words[0] & ss::kErrBulkTimeout) return fail(SS_ERR_CUDA, "a bulk copy into shared memory did not complete in time");
+    if (words[0] & ss::kErrLookbackTimeout) {
+        if (failing_tile) *failing_tile = words[1] ? (int64_t)words[1] - 1 : -1;
+        return fail(SS_ERR_LOOKBACK_TIMEOUT, "a look-back wait ran out");
+    }
+    return SS_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -626,6 +649,51 @@ ss_status ss_copy_u32(const uint32_t* in, uint32_t* out, size_t n, ss_stream_t s
     if (n == 0) return SS_OK;
     cudaError_t e = ss::launch_copy_probe(effective_config(n), in, out, n, (cudaStream_t)stream);
     return e == cudaSuccess ? SS_OK : cuda_fail(e, "copy launch");
+}
+
+ss_status ss_scan_temp_bytes(size_t n, size_t* bytes) {
+    if (bytes == nullptr) return fail(SS_ERR_INVALID_ARG, "bytes is null");
+    if (n > (SIZE_MAX / 8)) return fail(SS_ERR_INVALID_ARG, "n too large");
+    *bytes = temp_bytes_for(n);
+    return SS_OK;
+}
+
+ss_status ss_scan_ws(ss_dtype dtype, int inclusive, const void* in, void* out, size_t n, void* temp,
+                     size_t temp_bytes, ss_stream_t stream) {
+    if (dtype != SS_I32 && dtype != SS_U32 && dtype != SS_F32) return fail(SS_ERR_UNSUPPORTED, "unknown dtype");
+    ss_status st = check_scan_args(in, out, n, ss::kMinScanTile);
+    if (st != SS_OK) return st;
+    if (n == 0) return SS_OK;
+    const size_t need = temp_bytes_for(n);
+    if (temp == nullptr) return fail(SS_ERR_INVALID_ARG, "temp is null");
+    if (reinterpret_cast<uintptr_t>(temp) & 255u) return fail(SS_ERR_INVALID_ARG, "temp must be 256-byte aligned");
+    if (temp_bytes < need) return fail(SS_ERR_INVALID_ARG, "temp_bytes is below ss_scan_temp_bytes(n)");
+    if (overlaps(temp, need, in, n * 4) || overlaps(temp, need, out, n * 4))
+        return fail(SS_ERR_INVALID_ARG, "temp overlaps in or out");
+    cudaStream_t s = (cudaStream_t)stream;
+    // The contents on entry are whatever the caller left there: clear what
+    // this call uses (counter, status words, descriptors) on the stream.
+    cudaError_t e = cudaMemsetAsync(temp, 0, need, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    unsigned long long* base = static_cast<unsigned long long*>(temp);
+    ss::LookbackWs ws = make_ws(nullptr);
+    ws.counter = base;
+    ws.status = reinterpret_cast<uint32_t*>(base + 1);
+    ws.desc = base + kTempHeader / 8;
+    e = ss::launch_scan_lookback(to_dtype(dtype), inclusive != 0, effective_config(n), in, out, n, ws, nullptr,
+                                 nullptr, s);
+    return e == cudaSuccess ? SS_OK : cuda_fail(e, "scan launch");
+}
+
+ss_status ss_temp_status(void* temp, ss_stream_t stream, int64_t* failing_tile) {
+    if (failing_tile) *failing_tile = -1;
+    if (temp == nullptr || (reinterpret_cast<uintptr_t>(temp) & 255u))
+        return fail(SS_ERR_INVALID_ARG, "temp must be a non-null, 256-byte aligned device pointer");
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    return read_status_words(reinterpret_cast<uint32_t*>(static_cast<unsigned long long*>(temp) + 1), s,
+                             failing_tile);
 }
 
 ss_status ss_stream_status(ss_stream_t stream, int64_t* failing_tile) {

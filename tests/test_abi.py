@@ -129,6 +129,27 @@ def test_bad_enums_and_sizes(lib):
     assert lib.ss_debug_set_lookback_fault(-5, 0) == ss.SS_ERR_INVALID_ARG
 
 
+def test_explicit_workspace_arguments(lib):
+    # the CUB-shape calls: the size query is host-only; argument errors come
+    # back before anything is enqueued
+    b = ctypes.c_size_t(7)
+    assert lib.ss_scan_temp_bytes(0, ctypes.byref(b)) == ss.SS_OK and b.value == 0
+    assert lib.ss_scan_temp_bytes(5, None) == ss.SS_ERR_INVALID_ARG
+    for n in (1, 4096, 4097, 1_000_003, 100_000_000):
+        tiles = (n + 4095) // 4096
+        assert ss.ss_scan_temp_bytes(n) == 256 + 8 * (tiles + (tiles + 31) // 32)
+    need = ss.ss_scan_temp_bytes(10_000)
+    IN, OUT, TEMP = 0x100000, 0x200000, 0x300000
+    assert lib.ss_scan_ws(ss.SS_I32, 1, IN, OUT, 10_000, None, need, None) == ss.SS_ERR_INVALID_ARG
+    assert lib.ss_scan_ws(ss.SS_I32, 1, IN, OUT, 10_000, TEMP + 16, need, None) == ss.SS_ERR_INVALID_ARG
+    assert lib.ss_scan_ws(ss.SS_I32, 1, IN, OUT, 10_000, TEMP, need - 1, None) == ss.SS_ERR_INVALID_ARG
+    assert lib.ss_scan_ws(ss.SS_I32, 1, IN, OUT, 10_000, IN + 256, need, None) == ss.SS_ERR_INVALID_ARG
+    assert lib.ss_scan_ws(7, 1, IN, OUT, 10_000, TEMP, need, None) == ss.SS_ERR_UNSUPPORTED
+    assert lib.ss_scan_ws(ss.SS_F32, 0, None, None, 0, None, 0, None) == ss.SS_OK  # n = 0: nothing to do
+    t = ctypes.c_int64(0)
+    assert lib.ss_temp_status(TEMP + 8, None, ctypes.byref(t)) == ss.SS_ERR_INVALID_ARG and t.value == -1
+
+
 def test_config_table(lib):
     n = ss.ss_scan_config_count()
     tiles = []
