@@ -365,14 +365,16 @@ def row_rates(torch, ss, stream, dev, xs_d, xf_d, out_d, launch_ms_by_variant):
     # C2 at n = 1e8 and the headline variants, from the step's own per-launch events
     for (kind, incl), ms in launch_ms_by_variant.items():
         rows[f"{kind}{'i' if incl else 'x'}_1e8"] = entry(8 * N, ms)
-    # C2: fp32 inclusive and exclusive at 1e6 and 1e7 (L2 flushed)
+    # C2: fp32 inclusive and exclusive at 1e6 and 1e7: [ms and fraction with L2 flushed,
+    # ms warm (back to back, the arrays L2-resident)]
     for nf in (1_000_000, 10_000_000):
         xf_s = torch.from_numpy(si.workload_f32_unit(nf, seed=1)).to(dev)
         of_s = torch.empty_like(xf_s)
         for incl in (True, False):
             fn = (lambda: ss.scan_inclusive_f32(xf_s, of_s, stream=sh)) if incl else \
                  (lambda: ss.scan_exclusive_f32(xf_s, of_s, stream=sh))
-            rows[f"f32{'i' if incl else 'x'}_{nf:.0e}".replace("+0", "")] = entry(8 * nf, timed(fn, 8 * nf))
+            rows[f"f32{'i' if incl else 'x'}_{nf:.0e}".replace("+0", "")] = (
+                entry(8 * nf, timed(fn, 8 * nf)) + [_sig(time_region(torch, stream, fn, 20), 3)])
         del xf_s, of_s
     # C1: int32 n = 4096, an inclusive and an exclusive scan per step, per call from
     # Python and per replay of a captured graph (launch latency, not bandwidth): [us, us]
