@@ -360,13 +360,17 @@ ss_status ss_set_scan_config(int config);
  *   1  bulk-copies only the flags and loads a 16-byte key vector only where
  *      one of its four flags is set, which reads far fewer key bytes when
  *      few elements are kept; one look-back per 16384 elements;
- *   2  (the default) as 1, with one look-back per 65536-element tile worked
- *      in four chunks, which pays a tile's fixed costs once per 65536
- *      elements (inputs of 65536 elements or fewer take 1).  A tile keeping
- *      fewer than 3456 keys is written in a sparse form: each thread loads
- *      only its kept keys, one by one, before the tile's look-back;
+ *   2  (the default) as 1, with one look-back per tile of four chunks: two
+ *      256-thread CTAs per SM and 32768-element tiles, which pays a tile's
+ *      fixed costs once per 32768 elements (inputs of 32768 elements or
+ *      fewer take 1).  A tile keeping fewer than 1728 keys is written in a
+ *      sparse form: each thread loads only its kept keys, one by one, before
+ *      the tile's look-back; other tiles gather each warp's kept keys in
+ *      shared memory and write 16-byte vectors;
  *   3  as 2 with every tile in the dense form, 4 with every tile in the
- *      sparse form.
+ *      sparse form;
+ *   5, 6, 7  as 2, 3, 4 with one 512-thread CTA per SM and 65536-element
+ *      tiles (sparse below 3456 keys).
  * Results are identical. */
 ss_status ss_set_compact_config(int config);
 

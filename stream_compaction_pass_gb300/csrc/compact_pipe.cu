@@ -537,8 +537,8 @@ k_compact_sel(const uint32_t* keys, const uint8_t* flags, uint32_t* out, unsigne
     }
 }
 
-// Chunked form: one look-back per 65536-element tile, processed as four
-// 16384-element chunks.  With sparse flags the work per element is small and
+// Chunked form: one look-back per tile of four chunks (a chunk: 1024
+// elements per warp; 32768-element tiles for 256 threads, 65536 for 512).  With sparse flags the work per element is small and
 // a tile's fixed costs dominate: the wait for its flags, the barriers, and
 // the look-back round trips.  A tile four times larger pays them once for
 // four times the elements.
@@ -562,7 +562,7 @@ k_compact_sel(const uint32_t* keys, const uint8_t* flags, uint32_t* out, unsigne
 //        look-back it stores them, consecutive, with plain stores.
 //  - Counts and offsets alternate between two slots by tile parity.
 template <int THREADS, int STAGES>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS, THREADS >= 512 ? 1 : 2)
 k_compact_chunked(const uint32_t* keys, const uint8_t* flags, uint32_t* out, unsigned long long* d_count,
                   size_t n, uint32_t num_tiles, LookbackCtx ctx, uint32_t sparse_below) {
     constexpr int WARPS = THREADS / 32;
@@ -577,7 +577,8 @@ k_compact_chunked(const uint32_t* keys, const uint8_t* flags, uint32_t* out, uns
     constexpr uint32_t kStageWarpBytes = 4u * (4u * 128u + 4u);  // a warp's staging: four rows and a shift
     static_assert(kWordBytes + WARPS * kStageWarpBytes <= TILE, "words and staging fit a stage");
     static_assert(kStageWarpBytes % 16u == 0u && kWordBytes % 16u == 0u, "staging areas are 16-byte aligned");
-    static_assert(CHUNKS * WARPS == 64, "two (chunk, warp) counts per lane of warp 0");
+    constexpr int CPL = CHUNKS * WARPS / 32;  // (chunk, warp) counts per lane of warp 0
+    static_assert(CPL == 1 || CPL == 2, "one or two (chunk, warp) counts per lane of warp 0");
     static_assert(SEG == 32u * 32u, "a lane's share of a chunk is one word of keep bits");
     static_assert(2 * CHUNKS <= VPT && kSlots <= 4, "the sparse slots fit the dense registers");
 
@@ -696,10 +697,10 @@ k_compact_chunked(const uint32_t* keys, const uint8_t* flags, uint32_t* out, uns
         for (int c = 0; c < CHUNKS; ++c) wst[(c * WARPS + warp) * 32 + lane] = words[c];
         fence_async_shared();  // these writes before the copy that later refills the stage
         if (warp == 0) {  // (chunk, warp) order is the elements' order
-            const uint32_t a = s_cnt[k & 1][2 * lane], b = s_cnt[k & 1][2 * lane + 1];
+            const uint32_t a = s_cnt[k & 1][CPL * lane], b = CPL == 2 ? s_cnt[k & 1][CPL * lane + 1] : 0u;
             const uint32_t inc = warp_inclusive_scan<uint32_t>(a + b, lane);
-            s_cnt[k & 1][2 * lane] = inc - a - b;
-            s_cnt[k & 1][2 * lane + 1] = inc - b;
+            s_cnt[k & 1][CPL * lane] = inc - a - b;
+            if (CPL == 2) s_cnt[k & 1][CPL * lane + 1] = inc - b;
             const uint32_t total = __shfl_sync(kFullMask, inc, 31);
             if (lane == 0) {
                 s_total[k & 1] = total;
@@ -918,30 +919,38 @@ static cudaError_t launch_compact_persistent(const uint32_t* keys, const uint8_t
 }
 
 // 0: bulk-copied keys and flags; 1: bulk-copied flags, selective key loads;
-// 2: the same with one look-back per 65536-element tile (the default), each
-// tile written in the sparse or the dense form by its count; 3 and 4: the
-// chunked kernel with every tile in the dense, or the sparse, form.
+// 2: the chunked kernel (one look-back per tile of four chunks) with two
+// 256-thread CTAs per SM and 32768-element tiles (the default), each tile
+// written in the sparse or the dense form by its count; 3 and 4: the same
+// with every tile in the dense, or the sparse, form; 5, 6, 7: the same three
+// with one 512-thread CTA per SM and 65536-element tiles.  Measured at
+// n = 2^28 (ms at p = 0.01 / 0.5 / 0.99): two CTAs per SM 0.127 / 0.307 /
+// 0.377, one 0.122 / 0.315 / 0.388: the second CTA's warps hide the dense
+// form's key-load latency, and cost the sparse form a little.
 static int g_compact_kernel = 2;
-// Chunked rows 2, 3, 4: a tile keeping fewer keys than this takes the sparse
-// form.  Measured at n = 2^28 (all tiles in one form, ms): keep rate 0.01,
-// sparse 0.122 against dense 0.221; 0.03, 0.173 against 0.230; 0.05 (3277
-// keys a tile), 0.230 against 0.237; 0.1, 0.38 against 0.26.
-static const uint32_t kCompactSparseBelow[] = {3456, 0, 65537};
+// Chunked rows 2..7: a tile keeping fewer keys than this takes the sparse
+// form.  Measured at n = 2^28 with 65536-element tiles (all tiles in one
+// form, ms): keep rate 0.01, sparse 0.122 against dense 0.221; 0.03, 0.173
+// against 0.230; 0.05 (3277 keys a tile), 0.230 against 0.237; 0.1, 0.38
+// against 0.26.  The 32768-element tiles take half the count.
+static const uint32_t kCompactSparseBelow[] = {1728, 0, 65537, 3456, 0, 65537};
 
 int compact_kernel_count() { return 2 + (int)(sizeof(kCompactSparseBelow) / sizeof(kCompactSparseBelow[0])); }
 
+template <int THREADS>
 static cudaError_t launch_compact_chunked(const uint32_t* keys, const uint8_t* flags, uint32_t* out,
                                          unsigned long long* d_count, size_t n, const LookbackWs& ws,
                                          uint32_t sparse_below, cudaStream_t s) {
-    constexpr int THREADS = 512, STAGES = 3;
-    constexpr size_t TILE = 65536;
+    constexpr int STAGES = 3;
+    constexpr size_t TILE = (size_t)THREADS * 128;  // 65536 for 512 threads
     constexpr size_t SMEM = STAGES * TILE;
     auto kern = k_compact_chunked<THREADS, STAGES>;
     KernelSetup su;
     cudaError_t e = kernel_setup(reinterpret_cast<const void*>(kern), THREADS, SMEM, &su);
     if (e != cudaSuccess) return e;
     const uint32_t tiles = (uint32_t)((n + TILE - 1) / TILE);
-    const uint32_t grid = tiles < (uint32_t)su.sms ? tiles : (uint32_t)su.sms;
+    const uint32_t resident = (uint32_t)(su.sms * su.blocks_per_sm);
+    const uint32_t grid = tiles < resident ? tiles : resident;
     LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};
     kern<<<grid, THREADS, SMEM, s>>>(keys, flags, out, d_count, n, tiles, ctx, sparse_below);
     return cudaGetLastError();
@@ -954,8 +963,10 @@ cudaError_t launch_compact_pipe(KeepRule rule, const uint32_t* keys, const uint8
     if (rule != KeepRule::Flags) return launch_compact_pred(rule, keys, out, d_count, n, ws, s);
     if (g_compact_kernel == 0)
         return launch_compact_persistent<512, 8, 2, false>(keys, flags, out, d_count, n, ws, s);
-    if (g_compact_kernel >= 2 && n > (size_t)65536)
-        return launch_compact_chunked(keys, flags, out, d_count, n, ws, kCompactSparseBelow[g_compact_kernel - 2], s);
+    if (g_compact_kernel >= 5 && n > (size_t)65536)
+        return launch_compact_chunked<512>(keys, flags, out, d_count, n, ws, kCompactSparseBelow[g_compact_kernel - 2], s);
+    if (g_compact_kernel >= 2 && g_compact_kernel < 5 && n > (size_t)32768)
+        return launch_compact_chunked<256>(keys, flags, out, d_count, n, ws, kCompactSparseBelow[g_compact_kernel - 2], s);
     return launch_compact_persistent<512, 8, 3, true>(keys, flags, out, d_count, n, ws, s);
 }
 

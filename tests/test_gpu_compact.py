@@ -13,7 +13,9 @@ from gpu_helpers import SENTINEL, Guarded, assert_equal, compaction_input
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module", params=[2, 3, 4, 1, 0], ids=["chunked", "chunked-dense", "chunked-sparse", "selective-keys", "bulk-keys"])
+@pytest.fixture(scope="module", params=[2, 3, 4, 5, 6, 7, 1, 0],
+                ids=["chunked", "chunked-dense", "chunked-sparse", "chunked-512", "chunked-512-dense",
+                     "chunked-512-sparse", "selective-keys", "bulk-keys"])
 def ss(request):
     import stream_compaction_pass_gb300 as m
     m.ss_set_compact_config(request.param)
@@ -66,9 +68,10 @@ def test_compaction_sparse_and_moderate(ss, p):
 
 
 def test_compaction_sparse_and_dense_tiles_in_one_call(ss):
-    # A keep rate of 3456 / 65536 puts about half of the 65,536-element tiles
-    # on each side of the chunked kernel's sparse/dense switch (fewer than
-    # 3456 kept keys in the tile), interleaved across CTAs.
+    # A keep rate of 3456 / 65536 puts about half of the chunked kernel's
+    # tiles on each side of its sparse/dense switch (fewer than 1728 kept keys
+    # in a 32768-element tile, 3456 in a 65536-element one), interleaved
+    # across CTAs.
     n = 200 * 65536 + 77
     keys = si.uniform_u32(n, seed=38)
     flags = si.bernoulli_flags(n, 3456 / 65536, seed=39)
@@ -84,7 +87,7 @@ def test_compaction_clustered_runs(ss, run):
     # keys per 65,536 elements: sparse tiles in which one thread's 32 elements
     # can all be kept, so the sparse form's loads past its four slots per
     # chunk run too.  Runs straddle threads, warps, chunks and tiles; with
-    # runs of 500 the tiles keep between 0 and 3000 keys.
+    # runs of 500 some tiles take the dense form.
     n = 97 * 65536 + 1234
     keys = si.uniform_u32(n, seed=40)
     starts = si.uniform_int32(max(1, n * 1024 // (65536 * run)), 0, n - 1, seed=41)
