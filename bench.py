@@ -491,13 +491,14 @@ def row_rates(torch, ss, stream, dev, xs_d, xf_d, out_d, launch_ms_by_variant):
         rows[f"rows_{r_}x{c_}"] = entry(8 * r_ * c_, time_region(
             torch, stream, lambda: ss.ss_scan_rows(ss.SS_F32, True, xr, orr, r_, c_, stream=sh), 20))
         del xr, orr
-    # segmented fp32 inclusive scans, n = 1e8, by mean segment length, on 2n bytes
+    # segmented fp32 inclusive scans, n = 1e8, by mean segment length: [ms, frac on 2n
+    # bytes, frac on 2n bytes plus the 8-byte segment starts that the call reads]
     xs_seg = torch.from_numpy(si.uniform_f32(N, seed=96)).to(dev)
     os_seg = torch.empty_like(xs_seg)
     for mean in (128256.0, 100.0, 4.0):
         off = torch.from_numpy(si.segment_offsets(N, mean, seed=98).astype(np.int64)).to(dev)
-        rows[f"seg_mean{int(mean)}"] = entry(8 * N, time_region(
-            torch, stream, lambda: ss.ss_scan_segments(ss.SS_F32, True, xs_seg, os_seg, off, stream=sh), 20))
+        ms = time_region(torch, stream, lambda: ss.ss_scan_segments(ss.SS_F32, True, xs_seg, os_seg, off, stream=sh), 20)
+        rows[f"seg_mean{int(mean)}"] = entry(8 * N, ms) + entry(8 * N + 8 * (off.numel() - 1), ms)[1:]
         del off
     del xs_seg, os_seg, scratch
 

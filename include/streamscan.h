@@ -374,6 +374,19 @@ ss_status ss_set_scan_config(int config);
  * Results are identical. */
 ss_status ss_set_compact_config(int config);
 
+/* Selects the form of later ss_scan_segments calls in this process:
+ *   0  (the default) blocked, by mean segment length n / num_segments: 64
+ *      threads a CTA below 2048, 128 from there and for num_segments = 0;
+ *   1  row-striped: lane l of a warp holds 16-byte vectors l, l + 32, ... of
+ *      the warp's span, one 512-thread CTA per SM, 16384-element tiles;
+ *   2, 3, 4, 5  blocked: each thread owns 32 consecutive elements (one
+ *      tile row), with 256, 128, 512 or 64 threads a CTA, 512 / threads CTAs
+ *      per SM and tiles of 32 x threads elements.
+ * Integer results are identical; fp32 sums are added in another order and
+ * agree within the bound of the flat scans.  SS_ERR_INVALID_ARG for any
+ * other value. */
+ss_status ss_set_segments_config(int config);
+
 /* Frees every workspace the library allocated (all devices and streams).
  * No call may be in flight. */
 void ss_shutdown(void);

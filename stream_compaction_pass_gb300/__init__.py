@@ -89,6 +89,7 @@ def _declare(lib):
         "ss_stream_status": [P, ctypes.POINTER(I64)],
         "ss_set_scan_config": [I],
         "ss_set_compact_config": [I],
+        "ss_set_segments_config": [I],
         "ss_debug_set_lookback_fault": [I64, U64],
         "ss_scan_noalloc": [I, I, P, P, SZ, P],
         "ss_debug_set_noalloc_calls": [U64],
@@ -370,6 +371,10 @@ def ss_set_host_mode(mode: int) -> None:
 
 def ss_set_compact_config(config: int) -> None:
     _check(lib().ss_set_compact_config(config), "ss_set_compact_config")
+
+
+def ss_set_segments_config(config: int) -> None:
+    _check(lib().ss_set_segments_config(config), "ss_set_segments_config")
 
 
 def ss_shutdown() -> None:

@@ -550,7 +550,7 @@ ss_status ss_scan_segments(ss_dtype dtype, int inclusive, const void* in, void* 
     if (num_segments > ((size_t)1 << 40)) return fail(SS_ERR_INVALID_ARG, "too many segments");
     if (num_segments > 0 && overlaps(d_offsets, (num_segments + 1) * 8, out, n * 4))
         return fail(SS_ERR_INVALID_ARG, "d_offsets overlaps out");
-    const size_t tiles = (n + ss::kSegTile - 1) / ss::kSegTile;
+    const size_t tiles = (n + ss::kSegMinTile - 1) / ss::kSegMinTile;
     Workspace* w = nullptr;
     st = get_workspace(s, &w);
     if (st != SS_OK) return st;
@@ -848,6 +848,13 @@ ss_status ss_set_compact_config(int config) {
     if (config < 0 || config >= ss::compact_kernel_count())
         return fail(SS_ERR_INVALID_ARG, "no such compaction configuration");
     ss::set_compact_kernel(config);
+    return SS_OK;
+}
+
+ss_status ss_set_segments_config(int config) {
+    if (config < 0 || config >= ss::segments_config_count())
+        return fail(SS_ERR_INVALID_ARG, "no such segmented scan configuration");
+    ss::set_segments_config(config);
     return SS_OK;
 }
 

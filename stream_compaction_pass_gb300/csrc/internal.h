@@ -137,8 +137,12 @@ cudaError_t launch_scan_rows(Dtype dt, bool inclusive, const void* in, void* out
 
 // Segmented scans (scan_segments.cu): `bits` is a workspace bitmask of
 // ceil(n / 32) words that the call zeroes and fills with the segment starts
-// (offsets[0 .. num_segments-1]) before the scan.
-constexpr size_t kSegTile = 16384;
+// (offsets[0 .. num_segments-1]) before the scan.  Every form's tile is a
+// multiple of kSegMinTile elements, so a descriptor per kSegMinTile elements
+// covers any of them.
+constexpr size_t kSegMinTile = 2048;
+int segments_config_count();
+void set_segments_config(int c);
 cudaError_t launch_scan_segments(Dtype dt, bool inclusive, const void* in, void* out, size_t n,
                                  const unsigned long long* offsets, size_t num_segments, uint32_t* bits,
                                  const LookbackWs& ws, cudaStream_t s);

@@ -39,11 +39,20 @@ constexpr int kSWarps = kSThreads / 32;
 constexpr int kSVpt = 8;                                        // row-striped form: rows of 4 elements per lane
 constexpr uint32_t kSSeg = 32u * kSVpt * 4;                     // 1024 elements per warp
 constexpr int kSEpt = 32;                                       // blocked form: elements per thread, one 128-byte row
-constexpr uint32_t kSTile = (uint32_t)kSThreads * kSEpt;        // 16384, both forms
+constexpr uint32_t kSTile = (uint32_t)kSThreads * kSEpt;        // 16384, the row-striped form's tile
 constexpr int kSStages = 3;
-static_assert(kSSeg * kSWarps == kSTile, "both forms cover the same tile");
-constexpr size_t kSegBlockedBelowMean = 1024;  // segments shorter than this on average: the blocked form
-static_assert(kSTile == kSegTile, "tile size shared with the host side");
+static_assert(kSSeg * kSWarps == kSTile, "one warp segment per warp");
+// The blocked form's CTA width by mean segment length: 64 threads (eight
+// CTAs per SM) below kSegNarrowBelowMean, else 128 (four CTAs per SM).
+constexpr size_t kSegNarrowBelowMean = 2048;
+
+// Rows per tensor load of the blocked form (a tile is one row per thread).
+__host__ __device__ constexpr uint32_t blocked_box_rows(int threads) { return threads < 256 ? (uint32_t)threads : 256u; }
+
+// Which form ss_scan_segments takes: 0 by mean segment length, 1 row-striped,
+// 2 / 3 / 4 / 5 blocked with 256 / 128 / 512 / 64 threads a CTA.
+int g_seg_config = 0;
+static_assert(kSTile >= kSegMinTile, "the workspace holds a descriptor per kSegMinTile elements");
 
 template <typename T>
 struct SegPair {
@@ -131,7 +140,8 @@ __global__ void k_segment_heads(const unsigned long long* offsets, size_t num_se
 // Row-striped form (lane l of a warp holds 16-byte vector 32j + l of the
 // warp's share as its row j): each row is joined across the warp by its
 // own segmented scan, which makes it the dearer form when segments are
-// short, and the faster one when they are long (no output staging).
+// short.  It stores straight from registers, with one 512-thread CTA per SM;
+// taken only when selected (ss_set_segments_config).
 template <typename T, bool INCLUSIVE>
 __global__ void __launch_bounds__(kSThreads, 1)
 k_scan_segments_rows(const T* in, T* out, size_t n, const uint32_t* bits, uint32_t num_tiles, bool fast,
@@ -461,7 +471,8 @@ static cudaError_t launch_segments_rows(const void* in, void* out, size_t n, con
     return cudaGetLastError();
 }
 
-// Blocked form.  Each thread owns 32 consecutive elements of the tile (one
+// Blocked form, THREADS threads a CTA and 512 / THREADS CTAs per SM (tiles of
+// THREADS * 32 elements).  Each thread owns 32 consecutive elements of the tile (one
 // 128-byte row) and the tile's head word that covers exactly them, so a
 // thread's segments run through its registers in element order: its
 // summary and its outputs are sequential adds with resets at its own starts,
@@ -476,18 +487,21 @@ static cudaError_t launch_segments_rows(const void* in, void* out, size_t n, con
 //    outputs over it, and each warp stores its 32 rows with one tensor copy.
 //    The stage is refilled in the next iteration, once those stores have
 //    read it.
-template <typename T, bool INCLUSIVE>
-__global__ void __launch_bounds__(kSThreads, 1)
+template <typename T, bool INCLUSIVE, int THREADS>
+__global__ void __launch_bounds__(THREADS, 512 / THREADS)
 k_scan_segments_blocked(const T* in, T* out, size_t n, const uint32_t* bits, uint32_t num_tiles, bool fast,
                         LookbackCtx ctx, const __grid_constant__ CUtensorMap map_in,
                 const __grid_constant__ CUtensorMap map_out) {
     constexpr int STAGES = kSStages;
     constexpr int EPT = kSEpt;
-    constexpr uint32_t TILE_BYTES = kSTile * (uint32_t)sizeof(T);
-    constexpr uint32_t ROWS = kSTile / EPT;             // rows per tile, one per thread
-    constexpr uint32_t BOX_ROWS = 256;                  // rows per tensor load
-    constexpr uint32_t HEAD_WORDS = kSTile / 32;        // one head word per row
-    static_assert(sizeof(T) == 4 && ROWS == (uint32_t)kSThreads && ROWS % BOX_ROWS == 0 && HEAD_WORDS == ROWS,
+    constexpr int WARPS = THREADS / 32;
+    constexpr uint32_t TILE = (uint32_t)THREADS * EPT;
+    constexpr uint32_t TILE_BYTES = TILE * (uint32_t)sizeof(T);
+    constexpr uint32_t ROWS = TILE / EPT;                  // rows per tile, one per thread
+    constexpr uint32_t BOX_ROWS = blocked_box_rows(THREADS);  // rows per tensor load
+    constexpr uint32_t HEAD_WORDS = TILE / 32;             // one head word per row
+    static_assert(sizeof(T) == 4 && ROWS == (uint32_t)THREADS && ROWS % BOX_ROWS == 0 && HEAD_WORDS == ROWS &&
+                      TILE >= kSegMinTile,
                   "tile geometry");
 
     // The ring (1024-byte aligned for the swizzle, rounded up into the 1 KB
@@ -497,8 +511,8 @@ k_scan_segments_blocked(const T* in, T* out, size_t n, const uint32_t* bits, uin
     T* const ring = reinterpret_cast<T*>(sbase);
     uint32_t* const heads = reinterpret_cast<uint32_t*>(sbase + (size_t)STAGES * TILE_BYTES);
     __shared__ __align__(8) uint64_t bars[STAGES];
-    __shared__ T s_ws[2][kSWarps];         // warp summaries, by tile parity
-    __shared__ uint32_t s_wf[2][kSWarps];
+    __shared__ T s_ws[2][WARPS];         // warp summaries, by tile parity
+    __shared__ uint32_t s_wf[2][WARPS];
     __shared__ T s_prefix[2];
     __shared__ uint32_t s_fail[2], s_epoch;
     __shared__ uint32_t s_tile[STAGES];  // the tile in each stage, kNoTile past the last
@@ -524,7 +538,7 @@ k_scan_segments_blocked(const T* in, T* out, size_t n, const uint32_t* bits, uin
         claims_done = true;
         return kNoTile;
     };
-    auto full_tile = [&](uint32_t t) { return fast && (size_t)t * kSTile + kSTile <= n; };
+    auto full_tile = [&](uint32_t t) { return fast && (size_t)t * TILE + TILE <= n; };
     auto issue = [&](uint32_t k) {  // thread 0
         const int s = (int)(k % STAGES);
         const uint32_t t = claim_next();
@@ -536,7 +550,7 @@ k_scan_segments_blocked(const T* in, T* out, size_t n, const uint32_t* bits, uin
                 const int32_t row0 = (int32_t)((size_t)t * ROWS);
 #pragma unroll
                 for (uint32_t b = 0; b < ROWS / BOX_ROWS; ++b)
-                    tensor_load_2d(ring + (size_t)s * kSTile + (size_t)b * BOX_ROWS * EPT, &map_in, 0,
+                    tensor_load_2d(ring + (size_t)s * TILE + (size_t)b * BOX_ROWS * EPT, &map_in, 0,
                                    row0 + (int32_t)(b * BOX_ROWS), &bars[s], policy);
                 bulk_load(heads + (size_t)s * HEAD_WORDS, bits + (size_t)t * HEAD_WORDS, HEAD_WORDS * 4, &bars[s],
                           policy);
@@ -561,7 +575,7 @@ k_scan_segments_blocked(const T* in, T* out, size_t n, const uint32_t* bits, uin
     // This thread's 32 elements of slot k (tile t) and their head word.
     auto read_row = [&](uint32_t k, uint32_t t, T (&x)[EPT]) {
         if (full_tile(t)) {
-            const uint32_t row = smem_u32(ring + (size_t)(k % STAGES) * kSTile);
+            const uint32_t row = smem_u32(ring + (size_t)(k % STAGES) * TILE);
 #pragma unroll
             for (int c = 0; c < EPT / 4; ++c) {
                 const uint4 r = lds_vec_at(row + swizzle128_offset(threadIdx.x, (uint32_t)c));
@@ -571,7 +585,7 @@ k_scan_segments_blocked(const T* in, T* out, size_t n, const uint32_t* bits, uin
                 x[4 * c + 3] = from_bits<T>(r.w);
             }
         } else {
-            const size_t e0 = (size_t)t * kSTile + (size_t)threadIdx.x * EPT;
+            const size_t e0 = (size_t)t * TILE + (size_t)threadIdx.x * EPT;
 #pragma unroll
             for (int q = 0; q < EPT; ++q) x[q] = e0 + q < n ? in[e0 + q] : T(0);
         }
@@ -615,7 +629,7 @@ k_scan_segments_blocked(const T* in, T* out, size_t n, const uint32_t* bits, uin
         __syncthreads();
         SegPair<T> tp{0u, T(0)};
 #pragma unroll
-        for (int q = 0; q < kSWarps; ++q) tp = seg_add(tp, SegPair<T>{s_wf[k & 1][q], s_ws[k & 1][q]});
+        for (int q = 0; q < WARPS; ++q) tp = seg_add(tp, SegPair<T>{s_wf[k & 1][q], s_ws[k & 1][q]});
         *tile_pair = tp;
         if (threadIdx.x == 0 && (int64_t)t != ctx.fault_tile) {
             if (tp.f || t == 0) {
@@ -706,7 +720,7 @@ k_scan_segments_blocked(const T* in, T* out, size_t n, const uint32_t* bits, uin
             }
         }
         if (full_tile(t)) {  // over this thread's row of the stage, then the warp's 32 rows in one store
-            const uint32_t row = smem_u32(ring + (size_t)(k % STAGES) * kSTile);
+            const uint32_t row = smem_u32(ring + (size_t)(k % STAGES) * TILE);
 #pragma unroll
             for (int c = 0; c < EPT / 4; ++c)
                 sts_vec_at(row + swizzle128_offset(threadIdx.x, (uint32_t)c),
@@ -716,11 +730,11 @@ k_scan_segments_blocked(const T* in, T* out, size_t n, const uint32_t* bits, uin
             __syncwarp();
             if (lane == 0) {
                 tensor_store_2d(&map_out, 0, (int32_t)((size_t)t * ROWS + (size_t)warp * 32),
-                                ring + (size_t)(k % STAGES) * kSTile + (size_t)warp * 32 * EPT);
+                                ring + (size_t)(k % STAGES) * TILE + (size_t)warp * 32 * EPT);
                 bulk_commit_group();
             }
         } else {
-            const size_t e0 = (size_t)t * kSTile + (size_t)threadIdx.x * EPT;
+            const size_t e0 = (size_t)t * TILE + (size_t)threadIdx.x * EPT;
 #pragma unroll
             for (int q = 0; q < EPT; ++q)
                 if (e0 + q < n) out[e0 + q] = x[q];
@@ -749,35 +763,53 @@ k_scan_segments_blocked(const T* in, T* out, size_t n, const uint32_t* bits, uin
     if (lane == 0) bulk_wait_group0();  // this warp's output stores are complete before the CTA leaves
 }
 
-template <typename T, bool INCL>
+template <typename T, bool INCL, int THREADS>
 static cudaError_t launch_segments_blocked(const void* in, void* out, size_t n, const uint32_t* bits,
                                            const LookbackWs& ws, cudaStream_t s) {
+    constexpr size_t TILE = (size_t)THREADS * kSEpt;
     // the ring, the head words, alignment slack
-    constexpr size_t SMEM = kSStages * (size_t)kSTile * sizeof(T) + kSStages * (size_t)(kSTile / 32) * 4 + 1024;
-    auto kern = k_scan_segments_blocked<T, INCL>;
+    constexpr size_t SMEM = kSStages * TILE * sizeof(T) + kSStages * (TILE / 32) * 4 + 1024;
+    auto kern = k_scan_segments_blocked<T, INCL, THREADS>;
     KernelSetup su;
-    cudaError_t e = kernel_setup(reinterpret_cast<const void*>(kern), kSThreads, SMEM, &su);
+    cudaError_t e = kernel_setup(reinterpret_cast<const void*>(kern), THREADS, SMEM, &su);
     if (e != cudaSuccess) return e;
-    const uint32_t tiles = (uint32_t)((n + kSTile - 1) / kSTile);
-    const uint32_t grid = tiles < (uint32_t)su.sms ? tiles : (uint32_t)su.sms;
+    const uint32_t tiles = (uint32_t)((n + TILE - 1) / TILE);
+    const uint32_t resident = (uint32_t)(su.sms * su.blocks_per_sm);
+    const uint32_t grid = tiles < resident ? tiles : resident;
     // Full tiles go through the tensor copies: every buffer 16-byte aligned,
     // at least one full tile, and every row coordinate in the copies' signed
     // 32-bit range.
     const uint64_t rows = n / 32;
     const bool fast = ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out) |
                         reinterpret_cast<uintptr_t>(bits)) & 15u) == 0 &&
-                      n >= kSTile && rows <= (uint64_t)INT32_MAX;
+                      n >= TILE && rows <= (uint64_t)INT32_MAX;
     CUtensorMap map_in{}, map_out{};
     if (fast) {
-        e = encode_rows128_b32(&map_in, in, rows, 256);
+        e = encode_rows128_b32(&map_in, in, rows, blocked_box_rows(THREADS));
         if (e == cudaSuccess) e = encode_rows128_b32(&map_out, out, rows, 32);
         if (e != cudaSuccess) return e;
     }
     LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};
-    kern<<<grid, kSThreads, SMEM, s>>>(static_cast<const T*>(in), static_cast<T*>(out), n, bits, tiles, fast, ctx,
+    kern<<<grid, THREADS, SMEM, s>>>(static_cast<const T*>(in), static_cast<T*>(out), n, bits, tiles, fast, ctx,
                                        map_in, map_out);
     return cudaGetLastError();
 }
+
+template <typename T, bool INCL>
+static cudaError_t launch_segments_form(int form, const void* in, void* out, size_t n, const uint32_t* bits,
+                                        const LookbackWs& ws, cudaStream_t s) {
+    switch (form) {
+        case 1: return launch_segments_rows<T, INCL>(in, out, n, bits, ws, s);
+        case 2: return launch_segments_blocked<T, INCL, 256>(in, out, n, bits, ws, s);
+        case 3: return launch_segments_blocked<T, INCL, 128>(in, out, n, bits, ws, s);
+        case 4: return launch_segments_blocked<T, INCL, 512>(in, out, n, bits, ws, s);
+        case 5: return launch_segments_blocked<T, INCL, 64>(in, out, n, bits, ws, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+int segments_config_count() { return 6; }
+void set_segments_config(int c) { g_seg_config = c; }
 
 cudaError_t launch_scan_segments(Dtype dt, bool inclusive, const void* in, void* out, size_t n,
                                  const unsigned long long* offsets, size_t num_segments, uint32_t* bits,
@@ -789,21 +821,20 @@ cudaError_t launch_scan_segments(Dtype dt, bool inclusive, const void* in, void*
     k_segment_heads<<<grid, 256, 0, s>>>(offsets, num_segments, n, bits);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // The form by mean segment length (n / segments), measured at n = 1e8, fp32
-    // inclusive (ms, blocked against row-striped): 4, 0.218 / 0.230; 100,
-    // 0.182 / 0.196; 5000, 0.179 / 0.174; 128,256, 0.188 / 0.173.
-    const bool blocked = num_segments > 0 && n / num_segments < kSegBlockedBelowMean;
-    if (dt == Dtype::F32) {
-        if (blocked)
-            return inclusive ? launch_segments_blocked<float, true>(in, out, n, bits, ws, s)
-                             : launch_segments_blocked<float, false>(in, out, n, bits, ws, s);
-        return inclusive ? launch_segments_rows<float, true>(in, out, n, bits, ws, s)
-                         : launch_segments_rows<float, false>(in, out, n, bits, ws, s);
-    }
-    if (blocked)
-        return inclusive ? launch_segments_blocked<uint32_t, true>(in, out, n, bits, ws, s)
-                         : launch_segments_blocked<uint32_t, false>(in, out, n, bits, ws, s);
-    return inclusive ? launch_segments_rows<uint32_t, true>(in, out, n, bits, ws, s)
-                     : launch_segments_rows<uint32_t, false>(in, out, n, bits, ws, s);
+    // inclusive, start marking included (ms; blocked with 64 / 128 / 256 / 512
+    // threads a CTA, then row-striped): mean 4, 0.171 / 0.174 / 0.180 / 0.217
+    // / 0.230; 100, 0.136 / 0.138 / 0.144 / 0.182 / 0.196; 1000, 0.133 / 0.134
+    // / 0.140 / 0.178 / 0.186; 5000, 0.144 / 0.140 / 0.142 / 0.178 / 0.174;
+    // 128,256, 0.158 / 0.153 / 0.158 / 0.187 / 0.173.  Narrow CTAs keep more
+    // tiles in flight per SM; with short segments nearly every tile holds a
+    // start, so its look-back ends at its predecessor.
+    int form = g_seg_config;
+    if (form == 0) form = num_segments > 0 && n / num_segments < kSegNarrowBelowMean ? 5 : 3;
+    if (dt == Dtype::F32)
+        return inclusive ? launch_segments_form<float, true>(form, in, out, n, bits, ws, s)
+                         : launch_segments_form<float, false>(form, in, out, n, bits, ws, s);
+    return inclusive ? launch_segments_form<uint32_t, true>(form, in, out, n, bits, ws, s)
+                     : launch_segments_form<uint32_t, false>(form, in, out, n, bits, ws, s);
 }
 
 }  // namespace ss

@@ -68,6 +68,65 @@ def test_segments(ss, kind, inclusive, n, mean):
     check(ss, kind, inclusive, seg_input(kind, n), offsets)
 
 
+FORMS = {1: "rows", 2: "blocked-256", 3: "blocked-128", 4: "blocked-512", 5: "blocked-64"}
+
+
+@pytest.fixture(params=list(FORMS), ids=list(FORMS.values()))
+def form(request, ss):
+    ss.ss_set_segments_config(request.param)
+    yield request.param
+    ss.ss_set_segments_config(0)  # the library's default
+
+
+# sizes about the tiles of every form (4096, 8192, 16384) and their ragged tails
+FORM_CASES = [(1, 1.0), (4095, 3.0), (4096, 4096.0), (4097, 2.0), (8191, 20.0), (8192, 8192.0), (8193, 1.5),
+              (16385, 5.0), (49_153, 30_000.0), (100_003, 700.0), (1 << 20, 7.0), (3_000_017, 5000.0),
+              (3_000_017, 1e9)]
+
+
+@pytest.mark.parametrize("kind,inclusive", [("i32", True), ("u32", False), ("f32", True), ("f32", False)])
+@pytest.mark.parametrize("n,mean", FORM_CASES, ids=[f"{n}_{int(m)}" for n, m in FORM_CASES])
+def test_each_form(ss, form, kind, inclusive, n, mean):
+    offsets = si.segment_offsets(n, mean, seed=97, empty_frac=0.1 if mean < 50 else 0.0)
+    check(ss, kind, inclusive, seg_input(kind, n), offsets)
+
+
+@functools.lru_cache(maxsize=3)
+def full_size_case(mean: float):
+    n = 100_000_000
+    x = seg_input("i32", n)
+    offsets = si.segment_offsets(n, mean, seed=98)
+    return x, offsets, oracle.scan_segments(x, offsets, True)
+
+
+@pytest.mark.parametrize("mean", [4.0, 100.0, 128256.0])
+def test_each_form_full_size(ss, form, mean):
+    x, offsets, ref = full_size_case(mean)
+    assert_equal(run_segments(ss, "i32", True, x, offsets), ref, tile=4096)
+
+
+def test_forms_agree_bitwise_on_integers(ss):
+    n = 2_000_003
+    x = seg_input("u32", n)
+    offsets = si.segment_offsets(n, 60.0, seed=102, empty_frac=0.05)
+    outs = []
+    try:
+        for f in FORMS:
+            ss.ss_set_segments_config(f)
+            outs.append(run_segments(ss, "u32", False, x, offsets))
+    finally:
+        ss.ss_set_segments_config(0)
+    for o in outs[1:]:
+        assert_equal(o, outs[0], tile=4096)
+
+
+def test_unknown_form_is_rejected(ss):
+    with pytest.raises(ss.StreamScanError):
+        ss.ss_set_segments_config(6)
+    with pytest.raises(ss.StreamScanError):
+        ss.ss_set_segments_config(-1)
+
+
 @pytest.mark.parametrize("mean", [128256.0, 1000.0])
 def test_full_size(ss, mean):
     n = 100_000_000
@@ -125,8 +184,9 @@ def test_no_segments_is_one_segment(ss):
     assert_equal(got, oracle.scan_i32(x, True), tile=16384)
 
 
-def test_segmented_timeout_short_segments(ss):
-    # Segments of mean length 40 take the blocked form.  A tile holding a start
+@pytest.mark.parametrize("seg_form", [0, 1, 2, 3, 4, 5])
+def test_segmented_timeout_short_segments(ss, seg_form):
+    # Segments of mean length 40 (the blocked form unless one is forced).  A tile holding a start
     # publishes its inclusive prefix before its look-back, but still looks
     # back for the elements before its first start; the fault hook makes
     # tile 7 publish nothing, so tile 8's look-back runs out.
@@ -137,15 +197,18 @@ def test_segmented_timeout_short_segments(ss):
     d = torch.from_numpy(x).cuda()
     o = torch.empty_like(d)
     d_off = torch.from_numpy(offsets.astype(np.int64)).cuda()
+    ss.ss_set_segments_config(seg_form)
     ss.ss_debug_set_lookback_fault(7, 2_000_000)
     try:
         ss.ss_scan_segments(ss.SS_I32, True, d, o, d_off)
         st, tile = ss.ss_stream_status()
+        ss.ss_debug_set_lookback_fault(-1, 0)
+        assert st == ss.SS_ERR_LOOKBACK_TIMEOUT and tile > 7
+        ss.ss_scan_segments(ss.SS_I32, True, d, o, d_off)
+        assert ss.ss_stream_status() == (ss.SS_OK, -1)
     finally:
         ss.ss_debug_set_lookback_fault(-1, 0)
-    assert st == ss.SS_ERR_LOOKBACK_TIMEOUT and tile > 7
-    ss.ss_scan_segments(ss.SS_I32, True, d, o, d_off)
-    assert ss.ss_stream_status() == (ss.SS_OK, -1)
+        ss.ss_set_segments_config(0)
     assert_equal(o.cpu().numpy(), oracle.scan_segments(x, offsets, True), tile=16384)
 
 
