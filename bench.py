@@ -754,6 +754,31 @@ def profile_f64(n: int) -> None:
     print(f"fp64 scan ok at n={n}, normalised error {err:.2e}")
 
 
+def profile_wide(n: int) -> None:
+    """Two launches each of the uint32 -> uint64 inclusive scan and the int64
+    exclusive scan at n elements (seeded uniform words), for a profiler to
+    capture; checks both against the oracle."""
+    import torch
+    import seeded_inputs as si
+    import stream_compaction_pass_gb300 as ss
+    import oracle as orc
+    xu = si.uniform_u32(n, seed=60)
+    x64 = ((si.uniform_u32(n, seed=62).astype(np.uint64) << np.uint64(32)) |
+           si.uniform_u32(n, seed=63).astype(np.uint64)).view(np.int64)
+    du = torch.from_numpy(xu.view(np.int32)).cuda()
+    d64 = torch.from_numpy(x64).cuda()
+    o = torch.empty(n, dtype=torch.int64, device="cuda")
+    for _ in range(2):
+        ss.ss_scan_wide(ss.SS_WIDE_U32_U64, True, du, o)
+    torch.cuda.synchronize()
+    assert np.array_equal(o.cpu().numpy().view(np.uint64), orc.scan_u32_u64(xu, True)), "uint32 -> uint64 mismatch"
+    for _ in range(2):
+        ss.ss_scan_wide(ss.SS_WIDE_I64, False, d64, o)
+    torch.cuda.synchronize()
+    assert np.array_equal(o.cpu().numpy(), orc.scan_i64(x64, False)), "int64 mismatch"
+    print(f"64-bit sum scans ok at n={n}")
+
+
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -779,7 +804,12 @@ def main() -> None:
     ap.add_argument("--mean", type=float, default=128256.0, help="mean segment length for --profile-segments")
     ap.add_argument("--profile-f64", type=int, default=0, metavar="N",
                     help="only run the fp64 inclusive scan twice at n=N (for a profiler) and exit")
+    ap.add_argument("--profile-wide", type=int, default=0, metavar="N",
+                    help="only run the uint32 -> uint64 and int64 scans twice each at n=N (for a profiler) and exit")
     args = ap.parse_args()
+    if args.profile_wide:
+        profile_wide(args.profile_wide)
+        return
     if args.profile_segments:
         profile_segments(args.profile_segments, args.mean)
         return

@@ -116,10 +116,11 @@ cudaError_t launch_compact_unordered(KeepRule rule, const uint32_t* keys, const 
 
 // Scans with 64-bit sums (scan_wide.cu): uint32 -> uint64, int32 -> int64,
 // int64 (modulo 2^64; uint64 is the same bits) and fp64.  Descriptors are 16
-// bytes, two 64-bit words per tile: kWideTile elements for the integer
-// types, kWideTileF64 for fp64.
+// bytes, two 64-bit words per tile: the workspace holds one per kWideTile
+// elements for the integer types (the smallest of their tiles), per
+// kWideTileF64 for fp64.
 enum class WideType : int { U32toU64 = 0, I32toI64 = 1, I64 = 2, F64 = 3 };
-constexpr size_t kWideTile = 8192;
+constexpr size_t kWideTile = 4096;
 constexpr size_t kWideTileF64 = 4096;
 cudaError_t launch_scan_wide(WideType type, bool inclusive, const void* in, void* out, size_t n,
                              const LookbackWs& ws, cudaStream_t s);

@@ -15,8 +15,9 @@
 //   - tile k is read again from the ring, scanned in registers and stored.
 // The descriptors are 16 bytes (lookback_wide.cuh).
 //
-// A tile is 64 KB of input: 16384 elements of a 32-bit input, 8192 of a
-// 64-bit one.  Each of the 512 threads takes rows of 2 elements (16 rows or
+// A tile is 128 bytes of input per thread: 4096 elements of a 32-bit input
+// in a 128-thread CTA (four per SM), 8192 of a 64-bit one in a 512-thread
+// CTA (one per SM).  Each thread takes rows of 2 elements (16 rows or
 // 8).  Warp w owns a contiguous segment; row j of it is 64 consecutive
 // elements and lane l holds elements 2l and 2l+1.  So the scan order inside a
 // warp is (row, lane, element), every output store of a warp is 512
@@ -39,15 +40,24 @@ namespace ss {
 
 namespace {
 
-constexpr int kWThreads = 512;
-constexpr int kWWarps = kWThreads / 32;
-// 64 KB of input per tile: 16384 elements of a 32-bit input, 8192 of a
-// 64-bit one.  The host sizes the descriptors for the smaller tile.
+// Threads per CTA by input width, and 512 / threads CTAs per SM.  A tile is
+// 128 bytes of input per thread: 4096 elements of a 32-bit input in 128
+// threads, 8192 of a 64-bit one in 512.  Measured at n = 1e8 (fraction of
+// the measured copy bandwidth; 512 / 256 / 128 threads): uint32 -> uint64
+// inclusive 0.78 / 0.86 / 0.87, int64 exclusive 0.81 / 0.79 / 0.78.  The
+// narrow CTAs hide each other's look-back when the input tile is small next
+// to its output; a 64-bit input's tile, read whole into registers, gains
+// nothing from them.
 template <typename TI>
-constexpr uint32_t wide_tile() {
-    return 65536u / (uint32_t)sizeof(TI);
+__host__ __device__ constexpr int wide_threads() {
+    return sizeof(TI) == 4 ? 128 : 512;
 }
-static_assert(wide_tile<double>() == kWideTile, "tile size shared with the host side");
+template <typename TI>
+__host__ __device__ constexpr uint32_t wide_tile() {
+    return (uint32_t)wide_threads<TI>() * 128u / (uint32_t)sizeof(TI);
+}
+static_assert(wide_tile<uint32_t>() == kWideTile && wide_tile<double>() >= kWideTile,
+              "the host sizes the descriptors for the smallest tile");
 
 template <typename TI, typename TA> __device__ __forceinline__ TA widen(TI x);
 template <> __device__ __forceinline__ unsigned long long widen<uint32_t, unsigned long long>(uint32_t x) {
@@ -89,24 +99,26 @@ __device__ __forceinline__ void st_v2_u64(void* p, unsigned long long a, unsigne
 }  // namespace
 
 template <typename TI, typename TA, bool INCLUSIVE>
-__global__ void __launch_bounds__(kWThreads, 1)
+__global__ void __launch_bounds__(wide_threads<TI>(), 512 / wide_threads<TI>())
 k_scan_wide(const TI* in, TA* out, size_t n, uint32_t num_tiles, bool fast, LookbackCtx ctx) {
     constexpr int STAGES = 3;
-    constexpr uint32_t TILE = wide_tile<TI>();
+    constexpr int THREADS = wide_threads<TI>();
+    constexpr int WARPS = THREADS / 32;
+    constexpr uint32_t TILE = (uint32_t)THREADS * 128u / (uint32_t)sizeof(TI);
     constexpr int EPV = 2;                                 // elements per lane per row
-    constexpr int VPT = (int)TILE / (kWThreads * EPV);     // rows per lane
+    constexpr int VPT = (int)TILE / (THREADS * EPV);     // rows per lane
     constexpr int GRP = sizeof(TI) == 8 ? VPT : 4;         // rows handled together
     static_assert(VPT % GRP == 0, "rows come in groups");
     constexpr uint32_t SEG = 32u * VPT * EPV;              // elements per warp segment
     constexpr uint32_t IN_BYTES = TILE * (uint32_t)sizeof(TI);
-    static_assert(SEG * kWWarps == TILE, "tile geometry");
+    static_assert(SEG * WARPS == TILE, "tile geometry");
 
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bars[STAGES];
     // Warp totals, prefix and failure flag alternate between two slots by
     // tile parity, so a slot is never rewritten while a slower warp may still
     // read it.
-    __shared__ TA s_warp[2][kWWarps];
+    __shared__ TA s_warp[2][WARPS];
     __shared__ TA s_prefix[2];
     __shared__ uint32_t s_fail[2], s_rank, s_epoch;
 
@@ -191,10 +203,10 @@ k_scan_wide(const TI* in, TA* out, size_t n, uint32_t num_tiles, bool fast, Look
         if (lane == 0) s_warp[k & 1][warp] = x;
         __syncthreads();
         // The warp totals scanned across the lanes of every warp (5 adds, not 16).
-        const TA inc = warp_inclusive_scan<TA>(lane < kWWarps ? s_warp[k & 1][lane] : TA(0), lane);
+        const TA inc = warp_inclusive_scan<TA>(lane < WARPS ? s_warp[k & 1][lane] : TA(0), lane);
         const TA w = __shfl_sync(kFullMask, inc, warp > 0 ? warp - 1 : 0);
         *wp = warp > 0 ? w : TA(0);
-        *agg = __shfl_sync(kFullMask, inc, kWWarps - 1);
+        *agg = __shfl_sync(kFullMask, inc, WARPS - 1);
         const TA b = *agg;
         if (threadIdx.x == 0 && (int64_t)t != ctx.fault_tile) {
             if (t == 0) {
@@ -322,17 +334,19 @@ k_scan_wide(const TI* in, TA* out, size_t n, uint32_t num_tiles, bool fast, Look
 
 template <typename TI, typename TA, bool INCL>
 static cudaError_t launch_wide(const void* in, void* out, size_t n, const LookbackWs& ws, cudaStream_t s) {
-    constexpr uint32_t TILE = wide_tile<TI>();
+    constexpr int THREADS = wide_threads<TI>();
+    constexpr uint32_t TILE = (uint32_t)THREADS * 128u / (uint32_t)sizeof(TI);
     constexpr size_t SMEM = 3 * (size_t)TILE * sizeof(TI);
     auto kern = k_scan_wide<TI, TA, INCL>;
     KernelSetup su;
-    cudaError_t e = kernel_setup(reinterpret_cast<const void*>(kern), kWThreads, SMEM, &su);
+    cudaError_t e = kernel_setup(reinterpret_cast<const void*>(kern), THREADS, SMEM, &su);
     if (e != cudaSuccess) return e;
     const uint32_t tiles = (uint32_t)((n + TILE - 1) / TILE);
-    const uint32_t grid = tiles < (uint32_t)su.sms ? tiles : (uint32_t)su.sms;
+    const uint32_t resident = (uint32_t)(su.sms * su.blocks_per_sm);
+    const uint32_t grid = tiles < resident ? tiles : resident;
     const bool fast = ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) & 15u) == 0;
     LookbackCtx ctx{ws.desc, ws.counter, ws.status, ws.timeout_ns, ws.max_polls, ws.fault_tile};
-    kern<<<grid, kWThreads, SMEM, s>>>(static_cast<const TI*>(in), static_cast<TA*>(out), n, tiles, fast, ctx);
+    kern<<<grid, THREADS, SMEM, s>>>(static_cast<const TI*>(in), static_cast<TA*>(out), n, tiles, fast, ctx);
     return cudaGetLastError();
 }
 
