@@ -18,7 +18,8 @@ from gpu_helpers import SENTINEL, Guarded, assert_equal
 
 pytestmark = pytest.mark.gpu
 
-TILE = 8192      # integer kinds
+TILE = 8192      # integer kinds: 8192-element tiles of a 64-bit input (one 512-thread CTA per SM)
+TILE_W32 = 4096  # ... and 4096 of a 32-bit one (four 128-thread CTAs per SM)
 TILE_F64 = 4096  # fp64: two 256-thread CTAs per SM, 16 elements per lane
 U = 2.0 ** -53
 
@@ -96,7 +97,9 @@ def check(ss, kind, inclusive, x, **kw):
 @pytest.mark.parametrize("inclusive", [True, False])
 @pytest.mark.parametrize("n", [1, 2, 3, 7, 4095, 4096, 4097, 8191, 8192, 8193, 16383, 16384, 16385, 3 * 8192 + 5,
                                152 * 8192,
-                               152 * 8192 + 1, 152 * 16384 + 3, 1_000_003])
+                               152 * 8192 + 1, 152 * 16384 + 3, 1_000_003,
+                               # a whole round of 608 CTAs on 4096-element tiles, and ragged ones
+                               608 * TILE_W32, 608 * TILE_W32 + 1, 3 * 608 * TILE_W32 + TILE_W32 - 1])
 def test_sizes(ss, kind, inclusive, n):
     check(ss, kind, inclusive, wide_input(kind, n))
 
