@@ -22,6 +22,7 @@
 // keep bits when it counts them, and then uses the rest of the tile's stage
 // to gather each warp's kept keys for 16-byte stores; tiles with few kept
 // keys skip that and load and store just those keys.
+#include <atomic>
 #include <type_traits>
 
 #include "bulk.cuh"
@@ -927,7 +928,7 @@ static cudaError_t launch_compact_persistent(const uint32_t* keys, const uint8_t
 // n = 2^28 (ms at p = 0.01 / 0.5 / 0.99): two CTAs per SM 0.127 / 0.307 /
 // 0.377, one 0.122 / 0.315 / 0.388: the second CTA's warps hide the dense
 // form's key-load latency, and cost the sparse form a little.
-static int g_compact_kernel = 2;
+static std::atomic<int> g_compact_kernel{2};  // read once per call; set from any thread
 // Chunked rows 2..7: a tile keeping fewer keys than this takes the sparse
 // form.  Measured at n = 2^28 with 65536-element tiles (all tiles in one
 // form, ms): keep rate 0.01, sparse 0.122 against dense 0.221; 0.03, 0.173
@@ -955,18 +956,19 @@ static cudaError_t launch_compact_chunked(const uint32_t* keys, const uint8_t* f
     kern<<<grid, THREADS, SMEM, s>>>(keys, flags, out, d_count, n, tiles, ctx, sparse_below);
     return cudaGetLastError();
 }
-void set_compact_kernel(int k) { g_compact_kernel = k; }
+void set_compact_kernel(int k) { g_compact_kernel.store(k, std::memory_order_relaxed); }
 
 cudaError_t launch_compact_pipe(KeepRule rule, const uint32_t* keys, const uint8_t* flags, uint32_t* out,
                                 unsigned long long* d_count, size_t n, const LookbackWs& ws, cudaStream_t s) {
     // A predicate needs every key: its own kernel streams them all through the ring.
     if (rule != KeepRule::Flags) return launch_compact_pred(rule, keys, out, d_count, n, ws, s);
-    if (g_compact_kernel == 0)
+    const int cfg = g_compact_kernel.load(std::memory_order_relaxed);
+    if (cfg == 0)
         return launch_compact_persistent<512, 8, 2, false>(keys, flags, out, d_count, n, ws, s);
-    if (g_compact_kernel >= 5 && n > (size_t)65536)
-        return launch_compact_chunked<512>(keys, flags, out, d_count, n, ws, kCompactSparseBelow[g_compact_kernel - 2], s);
-    if (g_compact_kernel >= 2 && g_compact_kernel < 5 && n > (size_t)32768)
-        return launch_compact_chunked<256>(keys, flags, out, d_count, n, ws, kCompactSparseBelow[g_compact_kernel - 2], s);
+    if (cfg >= 5 && n > (size_t)65536)
+        return launch_compact_chunked<512>(keys, flags, out, d_count, n, ws, kCompactSparseBelow[cfg - 2], s);
+    if (cfg >= 2 && cfg < 5 && n > (size_t)32768)
+        return launch_compact_chunked<256>(keys, flags, out, d_count, n, ws, kCompactSparseBelow[cfg - 2], s);
     return launch_compact_persistent<512, 8, 3, true>(keys, flags, out, d_count, n, ws, s);
 }
 

@@ -25,6 +25,8 @@
 //      prefix found by the look-back applies only up to the tile's first
 //      start.
 // The array's first element always starts a segment.
+#include <atomic>
+
 #include "bulk.cuh"
 #include "internal.h"
 #include "tensor_copy.cuh"
@@ -51,7 +53,7 @@ __host__ __device__ constexpr uint32_t blocked_box_rows(int threads) { return th
 
 // Which form ss_scan_segments takes: 0 by mean segment length, 1 row-striped,
 // 2 / 3 / 4 / 5 blocked with 256 / 128 / 512 / 64 threads a CTA.
-int g_seg_config = 0;
+std::atomic<int> g_seg_config{0};  // read once per call; set from any thread
 static_assert(kSTile >= kSegMinTile, "the workspace holds a descriptor per kSegMinTile elements");
 
 template <typename T>
@@ -809,7 +811,7 @@ static cudaError_t launch_segments_form(int form, const void* in, void* out, siz
 }
 
 int segments_config_count() { return 6; }
-void set_segments_config(int c) { g_seg_config = c; }
+void set_segments_config(int c) { g_seg_config.store(c, std::memory_order_relaxed); }
 
 cudaError_t launch_scan_segments(Dtype dt, bool inclusive, const void* in, void* out, size_t n,
                                  const unsigned long long* offsets, size_t num_segments, uint32_t* bits,
@@ -828,7 +830,7 @@ cudaError_t launch_scan_segments(Dtype dt, bool inclusive, const void* in, void*
     // 128,256, 0.158 / 0.153 / 0.158 / 0.187 / 0.173.  Narrow CTAs keep more
     // tiles in flight per SM; with short segments nearly every tile holds a
     // start, so its look-back ends at its predecessor.
-    int form = g_seg_config;
+    int form = g_seg_config.load(std::memory_order_relaxed);
     if (form == 0) form = num_segments > 0 && n / num_segments < kSegNarrowBelowMean ? 5 : 3;
     if (dt == Dtype::F32)
         return inclusive ? launch_segments_form<float, true>(form, in, out, n, bits, ws, s)
