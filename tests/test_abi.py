@@ -129,6 +129,20 @@ def test_bad_enums_and_sizes(lib):
     assert lib.ss_debug_set_lookback_fault(-5, 0) == ss.SS_ERR_INVALID_ARG
 
 
+def test_form_switches(lib):
+    # host-only: each switch takes exactly its documented values
+    for c in range(8):
+        assert lib.ss_set_compact_config(c) == ss.SS_OK
+    assert lib.ss_set_compact_config(8) == ss.SS_ERR_INVALID_ARG
+    assert lib.ss_set_compact_config(-1) == ss.SS_ERR_INVALID_ARG
+    assert lib.ss_set_compact_config(2) == ss.SS_OK  # the default
+    for c in range(6):
+        assert lib.ss_set_segments_config(c) == ss.SS_OK
+    assert lib.ss_set_segments_config(6) == ss.SS_ERR_INVALID_ARG
+    assert lib.ss_set_segments_config(-1) == ss.SS_ERR_INVALID_ARG
+    assert lib.ss_set_segments_config(0) == ss.SS_OK  # the default
+
+
 def test_explicit_workspace_arguments(lib):
     # the CUB-shape calls: the size query is host-only; argument errors come
     # back before anything is enqueued
